@@ -1,0 +1,340 @@
+"""Pins for the fp64 oracle: each check ties it to something other than itself.
+
+Closed forms, library special cases (torch CPU float64 SDPA and autograd,
+scipy's Hadamard, torch's e4m3 cast), an independent scalar-loop
+implementation, and central finite differences.  CPU only.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import scipy.linalg
+import torch
+
+from oracle import attn64 as A
+from oracle import brute
+import attn_inputs as gen
+
+
+def _rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+def _docs(B, N, seed):
+    rng = np.random.default_rng(seed)
+    out = np.zeros((B, N), dtype=np.int32)
+    for b in range(B):
+        cuts = np.sort(rng.choice(np.arange(1, N), size=2, replace=False))
+        out[b] = np.searchsorted(cuts, np.arange(N), side="right")
+    return out
+
+
+MOD_CASES = {
+    "none": dict(),
+    "causal": dict(causal=True),
+    "window": dict(window=3),
+    "causal_window": dict(causal=True, window=3),
+    "doc": dict(doc=True),
+    "causal_doc": dict(causal=True, doc=True),
+    "softcap": dict(softcap=2.0),
+    "alibi": dict(alibi=True),
+    "all": dict(causal=True, window=4, doc=True, softcap=2.0, alibi=True),
+}
+
+
+def _mods(case, B, N, seed=7):
+    c = MOD_CASES[case]
+    return A.Mods(causal=c.get("causal", False), window=c.get("window"),
+                  doc_ids=_docs(B, N, seed) if c.get("doc") else None,
+                  softcap=c.get("softcap"), alibi=c.get("alibi", False))
+
+
+# ---------------------------------------------------------------- forward pins
+
+@pytest.mark.parametrize("case", list(MOD_CASES))
+def test_forward_matches_scalar_loops(case):
+    B, Hq, Hkv, N, d = 2, 4, 2, 9, 4
+    q, k, v = _rand((B, Hq, N, d), 1), _rand((B, Hkv, N, d), 2), _rand((B, Hkv, N, d), 3)
+    mods = _mods(case, B, N)
+    scale = 0.7
+    O, L = A.forward(q, k, v, scale, mods)
+    slopes = list(A.alibi_slopes(Hq)) if mods.alibi else None
+    Ob, Lb = brute.forward(q, k, v, scale, causal=mods.causal, window=mods.window,
+                           doc=mods.doc_ids, softcap=mods.softcap, slopes=slopes)
+    np.testing.assert_allclose(O, np.array(Ob), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(L, np.array(Lb), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("case", list(MOD_CASES))
+def test_softmax_rows_sum_to_one(case):
+    B, Hq, Hkv, N, d = 1, 2, 1, 11, 5
+    q, k, v = _rand((B, Hq, N, d), 4), _rand((B, Hkv, N, d), 5), _rand((B, Hkv, N, d), 6)
+    mods = _mods(case, B, N)
+    for h in range(Hq):
+        _, lse, P = A.head_forward(q, k, v, 0.5, mods, 0, h, return_p=True)
+        np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+        assert (P >= 0).all()
+        m = A.allowed(mods, 0, np.arange(N), np.arange(N))
+        assert (P[~m] == 0).all()
+
+
+@pytest.mark.parametrize("case", list(MOD_CASES))
+def test_constant_v_returns_v(case):
+    B, Hq, Hkv, N, d = 1, 2, 2, 10, 3
+    q, k = _rand((B, Hq, N, d), 7), _rand((B, Hkv, N, d), 8)
+    row = np.array([0.25, -1.5, 3.0])
+    v = np.broadcast_to(row, (B, Hkv, N, d)).copy()
+    O, _ = A.forward(q, k, v, 0.9, _mods(case, B, N))
+    np.testing.assert_allclose(O, np.broadcast_to(row, O.shape), rtol=0, atol=1e-13)
+
+
+def test_causal_row_zero_and_single_key():
+    B, Hq, N, d = 1, 3, 6, 4
+    q, k, v = _rand((B, Hq, N, d), 9), _rand((B, Hq, N, d), 10), _rand((B, Hq, N, d), 11)
+    scale = 0.3
+    O, L = A.forward(q, k, v, scale, A.Mods(causal=True))
+    for h in range(Hq):
+        np.testing.assert_allclose(O[0, h, 0], v[0, h, 0], rtol=0, atol=1e-15)
+        assert L[0, h, 0] == pytest.approx(scale * float(q[0, h, 0] @ k[0, h, 0]), abs=1e-14)
+    # N = 1: the only key is attended with weight 1.
+    q1, k1, v1 = q[:, :, :1], k[:, :, :1], v[:, :, :1]
+    O1, L1 = A.forward(q1, k1, v1, scale)
+    np.testing.assert_allclose(O1, v1, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(L1[..., 0], scale * np.einsum("bhd,bhd->bh", q1[:, :, 0], k1[:, :, 0]),
+                               atol=1e-14)
+
+
+def _sdpa64(q, k, v, scale, mask=None, bias=None, causal=False):
+    Hq, Hkv = q.shape[1], k.shape[1]
+    rep = Hq // Hkv
+    Q = torch.from_numpy(np.ascontiguousarray(q))
+    K = torch.from_numpy(np.repeat(k, rep, axis=1))
+    V = torch.from_numpy(np.repeat(v, rep, axis=1))
+    am = None
+    if mask is not None or bias is not None:
+        am = torch.zeros(q.shape[0], Hq, q.shape[2], k.shape[2], dtype=torch.float64)
+        if bias is not None:
+            am = am + torch.from_numpy(bias)
+        if mask is not None:
+            am = am.masked_fill(~torch.from_numpy(mask), float("-inf"))
+    return torch.nn.functional.scaled_dot_product_attention(
+        Q, K, V, attn_mask=am, is_causal=causal, scale=scale).numpy()
+
+
+def test_matches_torch_sdpa_float64():
+    B, Hq, Hkv, N, d = 2, 4, 2, 33, 8
+    q, k, v = _rand((B, Hq, N, d), 12), _rand((B, Hkv, N, d), 13), _rand((B, Hkv, N, d), 14)
+    s = 1 / math.sqrt(d)
+    O, _ = A.forward(q, k, v, s)
+    np.testing.assert_allclose(O, _sdpa64(q, k, v, s), rtol=1e-12, atol=1e-12)
+    O, _ = A.forward(q, k, v, s, A.Mods(causal=True))
+    np.testing.assert_allclose(O, _sdpa64(q, k, v, s, causal=True), rtol=1e-12, atol=1e-12)
+    # ALiBi as an additive bias and window/doc as a boolean mask, built by hand here.
+    docs = _docs(B, N, 3)
+    i = np.arange(N)[:, None]
+    j = np.arange(N)[None, :]
+    slopes = 2.0 ** (-8.0 * (np.arange(Hq) + 1) / Hq)
+    bias = -slopes[None, :, None, None] * (i - j)[None, None]
+    bias = np.broadcast_to(bias, (B, Hq, N, N)).copy()
+    mask = np.broadcast_to(((j <= i) & (i - j < 7))[None, None], (B, Hq, N, N)).copy()
+    mask &= (docs[:, None, :, None] == docs[:, None, None, :])
+    O, _ = A.forward(q, k, v, s, A.Mods(causal=True, window=7, doc_ids=docs, alibi=True))
+    np.testing.assert_allclose(O, _sdpa64(q, k, v, s, mask=mask, bias=bias), rtol=1e-12, atol=1e-12)
+
+
+def test_mod_reductions():
+    B, Hq, Hkv, N, d = 2, 2, 1, 12, 4
+    q, k, v = _rand((B, Hq, N, d), 15), _rand((B, Hkv, N, d), 16), _rand((B, Hkv, N, d), 17)
+    causal = A.forward(q, k, v, 0.8, A.Mods(causal=True))
+    plain = A.forward(q, k, v, 0.8)
+    # A window at least N wide changes nothing.
+    for ref, mods in [(causal, A.Mods(causal=True, window=N)), (plain, A.Mods(window=N + 5))]:
+        got = A.forward(q, k, v, 0.8, mods)
+        np.testing.assert_array_equal(got[0], ref[0])
+    # One document is no mask.
+    got = A.forward(q, k, v, 0.8, A.Mods(causal=True, doc_ids=np.zeros((B, N), np.int32)))
+    np.testing.assert_array_equal(got[0], causal[0])
+    # A huge soft-cap is the identity.
+    got = A.forward(q, k, v, 0.8, A.Mods(softcap=1e12))
+    np.testing.assert_allclose(got[0], plain[0], rtol=1e-12, atol=1e-12)
+    # ALiBi with zero slopes is no bias.
+    got = A.forward(q, k, v, 0.8, A.Mods(alibi=True, alibi_slopes=np.zeros(Hq)))
+    np.testing.assert_array_equal(got[0], plain[0])
+
+
+def test_gqa_equals_repeated_kv():
+    B, Hq, Hkv, N, d = 1, 6, 2, 8, 4
+    q, k, v, do = (_rand((B, Hq, N, d), 18), _rand((B, Hkv, N, d), 19),
+                   _rand((B, Hkv, N, d), 20), _rand((B, Hq, N, d), 21))
+    mods = A.Mods(causal=True, softcap=3.0)
+    kr, vr = np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1)
+    O, L = A.forward(q, k, v, 0.6, mods)
+    Or, Lr = A.forward(q, kr, vr, 0.6, mods)
+    np.testing.assert_allclose(O, Or, atol=1e-14)
+    np.testing.assert_allclose(L, Lr, atol=1e-14)
+    dq, dk, dv = A.backward(q, k, v, do, 0.6, mods)
+    dqr, dkr, dvr = A.backward(q, kr, vr, do, 0.6, mods)
+    np.testing.assert_allclose(dq, dqr, atol=1e-13)
+    np.testing.assert_allclose(dk, dkr.reshape(B, Hkv, 3, N, d).sum(axis=2), atol=1e-13)
+    np.testing.assert_allclose(dv, dvr.reshape(B, Hkv, 3, N, d).sum(axis=2), atol=1e-13)
+
+
+# --------------------------------------------------------------- backward pins
+
+@pytest.mark.parametrize("case", ["none", "causal", "causal_window", "doc", "softcap",
+                                  "alibi", "all"])
+def test_backward_finite_differences(case):
+    B, Hq, Hkv, N, d = 1, 2, 1, 6, 3
+    q, k, v, do = (_rand((B, Hq, N, d), 22), _rand((B, Hkv, N, d), 23),
+                   _rand((B, Hkv, N, d), 24), _rand((B, Hq, N, d), 25))
+    mods = _mods(case, B, N)
+    scale = 1.3
+
+    def loss(qq, kk, vv):
+        return float((A.forward(qq, kk, vv, scale, mods)[0] * do).sum())
+
+    dq, dk, dv = A.backward(q, k, v, do, scale, mods)
+    h = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in itertools.product(*[range(s) for s in x.shape]):
+            old = x[idx]
+            x[idx] = old + h
+            lp = loss(q, k, v)
+            x[idx] = old - h
+            lm = loss(q, k, v)
+            x[idx] = old
+            num[idx] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8)
+
+
+def test_backward_matches_torch_autograd_sdpa():
+    B, Hq, Hkv, N, d = 2, 4, 2, 17, 8
+    q, k, v, do = (_rand((B, Hq, N, d), 26), _rand((B, Hkv, N, d), 27),
+                   _rand((B, Hkv, N, d), 28), _rand((B, Hq, N, d), 29))
+    s = 1 / math.sqrt(d)
+    Q = torch.from_numpy(q.copy()).requires_grad_()
+    K = torch.from_numpy(k.copy()).requires_grad_()
+    V = torch.from_numpy(v.copy()).requires_grad_()
+    O = torch.nn.functional.scaled_dot_product_attention(
+        Q, K.repeat_interleave(2, dim=1), V.repeat_interleave(2, dim=1), is_causal=True, scale=s)
+    O.backward(torch.from_numpy(do))
+    dq, dk, dv = A.backward(q, k, v, do, s, A.Mods(causal=True))
+    np.testing.assert_allclose(dq, Q.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, K.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, V.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_delta_identity():
+    """rowsum(dO * O) equals rowsum(P * dP): the preprocessing shortcut is exact."""
+    B, Hq, N, d = 1, 1, 9, 5
+    q, k, v, do = (_rand((B, Hq, N, d), s) for s in (30, 31, 32, 33))
+    mods = A.Mods(causal=True, softcap=2.5, alibi=True)
+    O, lse, P = A.head_forward(q, k, v, 0.7, mods, 0, 0, return_p=True)
+    dP = do[0, 0] @ v[0, 0].T
+    np.testing.assert_allclose((do[0, 0] * O).sum(1), (P * dP).sum(1), rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------- block map pins
+
+@pytest.mark.parametrize("case", ["none", "causal", "window", "causal_window", "doc", "all"])
+@pytest.mark.parametrize("N", [8, 13, 16])
+def test_block_map_brute_force(case, N):
+    B = 2
+    mods = _mods(case, B, N, seed=N)
+    got = A.block_map(mods, B, N, tile=4)
+    ref = brute.tile_class(B, N, 4, causal=mods.causal, window=mods.window, doc=mods.doc_ids)
+    np.testing.assert_array_equal(got, np.array(ref, dtype=np.uint8))
+
+
+def test_block_map_closed_forms():
+    N, T = 1000, 128
+    nT = 8
+    causal = A.block_map(A.Mods(causal=True), 1, N, T)[0]
+    I, J = np.meshgrid(np.arange(nT), np.arange(nT), indexing="ij")
+    expect = np.where(J < I, 2, np.where(J == I, 1, 0))
+    np.testing.assert_array_equal(causal, expect)
+    plain = A.block_map(A.Mods(), 1, N, T)[0]
+    np.testing.assert_array_equal(plain, np.where(J == nT - 1, 1, 2))  # ragged last column
+    full = A.block_map(A.Mods(), 1, 1024, T)[0]
+    assert (full == 2).all()
+
+
+def test_flop_pairs_causal():
+    assert A.flop_pairs(A.Mods(causal=True), 3, 50) == 3 * 50 * 51 // 2
+    assert A.flop_pairs(A.Mods(), 1, 50) == 2500
+
+
+# ------------------------------------------------------------------- FP8 pins
+
+def test_hadamard_is_scipy_and_rotation_orthogonal():
+    np.testing.assert_array_equal(A.sylvester_hadamard(128), scipy.linalg.hadamard(128))
+    s = gen.hadamard_signs(1, 128, 3)[0]
+    M = A.rotation(s)
+    np.testing.assert_allclose(M @ M.T, np.eye(128), atol=1e-13)
+    x = _rand(128, 5)
+    fw = np.array(brute.fwht(x * s)) / math.sqrt(128)
+    np.testing.assert_allclose(x @ M, fw, atol=1e-12)
+
+
+def test_rotation_leaves_attention_unchanged():
+    B, Hq, Hkv, N, d = 1, 4, 2, 20, 128
+    q, k, v = _rand((B, Hq, N, d), 40), _rand((B, Hkv, N, d), 41), _rand((B, Hkv, N, d), 42)
+    signs = gen.hadamard_signs(Hkv, d, 43)
+    qr, kr = A.rotate_heads(q, signs, Hkv), A.rotate_heads(k, signs, Hkv)
+    for mods in (A.Mods(), A.Mods(causal=True)):
+        O, L = A.forward(q, k, v, 0.1, mods)
+        Or, Lr = A.forward(qr, kr, v, 0.1, mods)
+        np.testing.assert_allclose(Or, O, atol=1e-12)
+        np.testing.assert_allclose(Lr, L, atol=1e-12)
+
+
+def test_e4m3_round_matches_torch_cast():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(20000) * 30, rng.standard_normal(5000) * 1e-2,
+                        np.linspace(-448, 448, 4001)])
+    ref = torch.from_numpy(x).to(torch.float32).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    # torch's fp32 round trip could differ from fp64 only at exact fp32 ties; x is fp64 here,
+    # so compare on values exactly representable in fp32.
+    x32 = x.astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(x32).to(torch.float32).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(A.e4m3_round(x32), ref)
+    # saturation and ties to even
+    assert A.e4m3_round(np.array([500.0, -1e9]))[0] == 448.0
+    assert A.e4m3_round(np.array([-1e9]))[0] == -448.0
+    assert A.e4m3_round(np.array([1.0625]))[0] == 1.0     # tie between 1.0 and 1.125 -> even
+    assert A.e4m3_round(np.array([1.1875]))[0] == 1.25    # tie between 1.125 and 1.25 -> even
+    assert A.e4m3_round(np.array([2.0 ** -10]))[0] == 0.0  # half of the smallest subnormal
+
+
+def test_fp8_prologue_scales_and_range():
+    B, H, N, d = 1, 2, 64, 128
+    q, k, v = _rand((B, H, N, d), 50), _rand((B, H, N, d), 51), _rand((B, H, N, d), 52)
+    signs = gen.hadamard_signs(H, d, 53)
+    q8, k8, v8, sc = A.fp8_prologue(q, k, v, signs, H)
+    qr = A.rotate_heads(q, signs, H)
+    np.testing.assert_allclose(sc[0], np.abs(qr).max(axis=(2, 3)) / 448.0)
+    assert np.abs(q8).max() == 448.0 and np.abs(k8).max() == 448.0 and np.abs(v8).max() == 448.0
+    # dequantised values sit within half an e4m3 step of the rotated inputs
+    deq = q8 * sc[0][:, :, None, None]
+    rel = np.abs(deq - qr) / np.maximum(np.abs(qr), 2.0 ** -6 * sc[0].max())
+    assert rel.max() <= 2.0 ** -4 + 1e-12
+
+
+# ---------------------------------------------------------- input recipe pins
+
+def test_doc_lengths_recipe():
+    for seed in range(20):
+        lens = gen.doc_lengths(4096, seed)
+        assert sum(lens) == 4096
+        assert all(128 <= n <= 2048 for n in lens[:-1])
+        assert 1 <= lens[-1] <= 2048
+    ids = gen.doc_ids(3, 4096, 10)
+    assert ids.shape == (3, 4096) and (np.diff(ids, axis=1) >= 0).all()
+
+
+def test_outlier_recipe():
+    x = torch.ones(1000, 100)
+    y = gen.with_outliers(x, 1e-3, 50.0, 1)
+    assert int((y == 50.0).sum()) == 100 and int((y == 1.0).sum()) == 100000 - 100
