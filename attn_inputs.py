@@ -69,11 +69,11 @@ def doc_lengths(N: int, seed: int, lo: int = DOC_LEN_MIN, hi: int = DOC_LEN_MAX)
     return lens
 
 
-def doc_ids(B: int, N: int, seed: int) -> np.ndarray:
+def doc_ids(B: int, N: int, seed: int, lo: int = DOC_LEN_MIN, hi: int = DOC_LEN_MAX) -> np.ndarray:
     """int32 [B, N]: document index (0, 1, 2, ...) of every position, per batch row."""
     out = np.empty((B, N), dtype=np.int32)
     for b in range(B):
-        lens = doc_lengths(N, seed + b)
+        lens = doc_lengths(N, seed + b, lo, hi)
         out[b] = np.repeat(np.arange(len(lens), dtype=np.int32), lens)
     return out
 

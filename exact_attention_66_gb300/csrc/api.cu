@@ -1,0 +1,354 @@
+// C ABI of the attention library (declared in include/attn.h): argument
+// validation, workspace carve-up, TMA descriptor encoding and kernel launch.
+// Every argument check runs before the first CUDA call, so a bad call returns
+// its status without touching the device.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include "../../include/attn.h"
+#include "launch.h"
+
+namespace attn {
+__device__ int g_status;  // device status word (DEV_OK / DEV_ERR_*)
+}
+
+using namespace attn;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int n_tiles(int N) { return (N + TILE - 1) / TILE; }
+
+uint32_t mod_flags(const attn_mods_t* m) { return m ? m->flags : 0u; }
+
+bool needs_map(uint32_t flags) { return (flags & (ATTN_MOD_WINDOW | ATTN_MOD_DOC)) != 0; }
+
+size_t map_bytes(int B, int N) { return round_up((size_t)B * n_tiles(N) * n_tiles(N), 256); }
+
+attn_status_t check_mods(const attn_mods_t* m) {
+  if (!m) return ATTN_OK;
+  const uint32_t known = ATTN_MOD_CAUSAL | ATTN_MOD_WINDOW | ATTN_MOD_DOC | ATTN_MOD_SOFTCAP |
+                         ATTN_MOD_ALIBI;
+  if (m->flags & ~known) return ATTN_ERR_INVALID_ARG;
+  if ((m->flags & ATTN_MOD_WINDOW) && m->window < 1) return ATTN_ERR_INVALID_ARG;
+  if ((m->flags & ATTN_MOD_DOC) && (m->doc_ids == nullptr || !aligned(m->doc_ids, 4)))
+    return ATTN_ERR_INVALID_ARG;
+  if ((m->flags & ATTN_MOD_SOFTCAP) && !(std::isfinite(m->softcap) && m->softcap > 0.f))
+    return ATTN_ERR_INVALID_ARG;
+  if ((m->flags & ATTN_MOD_ALIBI) && m->alibi_slopes && !aligned(m->alibi_slopes, 4))
+    return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+attn_status_t check_shape(int B, int Hq, int Hkv, int N, int d, bool fp8) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_UNSUPPORTED;
+  if (fp8 ? d != 128 : (d != 64 && d != 128)) return ATTN_ERR_UNSUPPORTED;
+  const long long planes = (long long)B * (Hq > Hkv ? Hq : Hkv);
+  if (planes * N >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+attn_status_t check_tensors(std::initializer_list<const void*> ps) {
+  for (const void* p : ps) {
+    if (p == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(p, 16)) return ATTN_ERR_UNSUPPORTED;
+  }
+  return ATTN_OK;
+}
+
+attn_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (need == 0) return ATTN_OK;
+  if (ws == nullptr || ws_bytes < need || !aligned(ws, 256)) return ATTN_ERR_WORKSPACE;
+  return ATTN_OK;
+}
+
+// ---- device state: sm_103 check, status word address (per device) --------
+struct DevState {
+  int checked = 0;  // 0 unknown, 1 ok, -1 unsupported
+  int* status = nullptr;
+};
+DevState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+attn_status_t device_state(int** status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState& s = g_dev[dev];
+  if (s.checked == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (major != 10 || minor != 3) {
+      s.checked = -1;
+    } else {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return ATTN_ERR_CUDA;
+      s.status = static_cast<int*>(p);
+      s.checked = 1;
+    }
+  }
+  if (s.checked < 0) return ATTN_ERR_DEVICE;
+  *status = s.status;
+  return ATTN_OK;
+}
+
+// ---- TMA descriptors -------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// [planes, N, d] contiguous tensor; box = 128 rows x 128 bytes, 128-B swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, bool e4m3, int d, int N, long long planes) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const int es = e4m3 ? 1 : 2;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)d * es, (cuuint64_t)N * d * es};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / es), (cuuint32_t)TILE, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+AttnParams make_params(int B, int Hq, int Hkv, int N, float scale, const attn_mods_t* mods,
+                       int* status) {
+  AttnParams p{};
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.nT = n_tiles(N);
+  p.n_qblk = (N + 2 * TILE - 1) / (2 * TILE);
+  p.scale = scale;
+  p.scale_log2 = scale * LOG2E;
+  p.flags = mod_flags(mods);
+  p.window = mods ? mods->window : 0;
+  p.softcap = (mods && (mods->flags & ATTN_MOD_SOFTCAP)) ? mods->softcap : 1.0f;
+  p.doc_ids = (mods && (mods->flags & ATTN_MOD_DOC)) ? mods->doc_ids : nullptr;
+  p.slopes = (mods && (mods->flags & ATTN_MOD_ALIBI)) ? mods->alibi_slopes : nullptr;
+  p.map = nullptr;
+  p.status = status;
+  return p;
+}
+
+bool has_score_mods(uint32_t flags) {
+  return (flags & (ATTN_MOD_WINDOW | ATTN_MOD_DOC | ATTN_MOD_SOFTCAP | ATTN_MOD_ALIBI)) != 0;
+}
+
+attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int N, int d, const attn_mods_t* mods) {
+  if (check_shape(B, Hq, Hkv, N, d, op == ATTN_OP_FWD_FP8 || op == ATTN_OP_QUANT_FP8) != ATTN_OK ||
+      check_mods(mods) != ATTN_OK)
+    return 0;
+  const uint32_t f = mod_flags(mods);
+  switch (op) {
+    case ATTN_OP_FWD:
+    case ATTN_OP_FWD_FP8:
+      return needs_map(f) ? map_bytes(B, N) : 0;
+    case ATTN_OP_BWD:
+      return round_up((size_t)B * Hq * N * sizeof(float), 256) + (needs_map(f) ? map_bytes(B, N) : 0);
+    case ATTN_OP_QUANT_FP8:
+      return round_up((size_t)(B * Hq + 2 * B * Hkv) * sizeof(unsigned), 256);
+    default:
+      return 0;
+  }
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int N, int d, float scale, const attn_mods_t* mods,
+                       void* ws, size_t ws_bytes, void* stream) {
+  attn_status_t st;
+  if ((st = check_shape(B, Hq, Hkv, N, d, false)) != ATTN_OK) return st;
+  if ((st = check_tensors({q, k, v, o})) != ATTN_OK) return st;
+  if (lse == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(lse, 4)) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if ((st = check_mods(mods)) != ATTN_OK) return st;
+  const size_t need = attn_workspace_size(ATTN_OP_FWD, B, Hq, Hkv, N, d, mods);
+  if ((st = check_ws(ws, ws_bytes, need)) != ATTN_OK) return st;
+  int* status = nullptr;
+  if ((st = device_state(&status)) != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  FwdLaunch L{};
+  L.p = make_params(B, Hq, Hkv, N, scale, mods, status);
+  if (!make_map(&L.tq, q, false, d, N, (long long)B * Hq) ||
+      !make_map(&L.tk, k, false, d, N, (long long)B * Hkv) ||
+      !make_map(&L.tv, v, false, d, N, (long long)B * Hkv))
+    return ATTN_ERR_CUDA;
+  L.o = o;
+  L.lse = lse;
+  if (needs_map(L.p.flags)) {
+    uint8_t* map = static_cast<uint8_t*>(ws);
+    if ((st = cuda_status(launch_block_map(L.p, map, s))) != ATTN_OK) return st;
+    L.p.map = map;
+  }
+  return cuda_status(launch_fwd_bf16(L, d, has_score_mods(L.p.flags), s));
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int Hq, int Hkv, int N, int d, float scale, const attn_mods_t* mods,
+                       void* ws, size_t ws_bytes, void* stream) {
+  attn_status_t st;
+  if ((st = check_shape(B, Hq, Hkv, N, d, false)) != ATTN_OK) return st;
+  if (N > BWD_MAX_N) return ATTN_ERR_UNSUPPORTED;
+  if ((st = check_tensors({q, k, v, o, dout, dq, dk, dv})) != ATTN_OK) return st;
+  if (lse == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(lse, 4)) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if ((st = check_mods(mods)) != ATTN_OK) return st;
+  const size_t need = attn_workspace_size(ATTN_OP_BWD, B, Hq, Hkv, N, d, mods);
+  if ((st = check_ws(ws, ws_bytes, need)) != ATTN_OK) return st;
+  int* status = nullptr;
+  if ((st = device_state(&status)) != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  BwdLaunch L{};
+  L.p = make_params(B, Hq, Hkv, N, scale, mods, status);
+  if (!make_map(&L.tq, q, false, d, N, (long long)B * Hq) ||
+      !make_map(&L.tk, k, false, d, N, (long long)B * Hkv) ||
+      !make_map(&L.tv, v, false, d, N, (long long)B * Hkv) ||
+      !make_map(&L.tdo, dout, false, d, N, (long long)B * Hq))
+    return ATTN_ERR_CUDA;
+  L.o = o;
+  L.dout = dout;
+  L.lse = lse;
+  L.dq = dq;
+  L.dk = dk;
+  L.dv = dv;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  L.delta = reinterpret_cast<float*>(wsb);
+  if (needs_map(L.p.flags)) {
+    uint8_t* map = wsb + round_up((size_t)B * Hq * N * sizeof(float), 256);
+    if ((st = cuda_status(launch_block_map(L.p, map, s))) != ATTN_OK) return st;
+    L.p.map = map;
+  }
+  return cuda_status(launch_bwd(L, d, has_score_mods(L.p.flags), s));
+}
+
+attn_status_t attn_hadamard_quant_fp8(const void* q, const void* k, const void* v, void* q8,
+                                      void* k8, void* v8, float* scales, const int8_t* signs,
+                                      int B, int Hq, int Hkv, int N, int d, void* ws,
+                                      size_t ws_bytes, void* stream) {
+  attn_status_t st;
+  if ((st = check_shape(B, Hq, Hkv, N, d, true)) != ATTN_OK) return st;
+  if ((st = check_tensors({q, k, v, q8, k8, v8})) != ATTN_OK) return st;
+  if (scales == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(scales, 4)) return ATTN_ERR_UNSUPPORTED;
+  const size_t need = attn_workspace_size(ATTN_OP_QUANT_FP8, B, Hq, Hkv, N, d, nullptr);
+  if ((st = check_ws(ws, ws_bytes, need)) != ATTN_OK) return st;
+  int* status = nullptr;
+  if ((st = device_state(&status)) != ATTN_OK) return st;
+  return cuda_status(launch_hadamard_quant(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N,
+                                           static_cast<unsigned*>(ws),
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* scales,
+                           void* o, float* lse, int B, int Hq, int Hkv, int N, int d, float scale,
+                           const attn_mods_t* mods, void* ws, size_t ws_bytes, void* stream) {
+  attn_status_t st;
+  if ((st = check_shape(B, Hq, Hkv, N, d, true)) != ATTN_OK) return st;
+  if ((st = check_tensors({q8, k8, v8, o})) != ATTN_OK) return st;
+  if (lse == nullptr || scales == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(lse, 4) || !aligned(scales, 4)) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if ((st = check_mods(mods)) != ATTN_OK) return st;
+  const size_t need = attn_workspace_size(ATTN_OP_FWD_FP8, B, Hq, Hkv, N, d, mods);
+  if ((st = check_ws(ws, ws_bytes, need)) != ATTN_OK) return st;
+  int* status = nullptr;
+  if ((st = device_state(&status)) != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  Fp8Launch L{};
+  L.p = make_params(B, Hq, Hkv, N, scale, mods, status);
+  if (!make_map(&L.tq, q8, true, d, N, (long long)B * Hq) ||
+      !make_map(&L.tk, k8, true, d, N, (long long)B * Hkv) ||
+      !make_map(&L.tv, v8, true, d, N, (long long)B * Hkv))
+    return ATTN_ERR_CUDA;
+  L.scales = scales;
+  L.o = o;
+  L.lse = lse;
+  if (needs_map(L.p.flags)) {
+    uint8_t* map = static_cast<uint8_t*>(ws);
+    if ((st = cuda_status(launch_block_map(L.p, map, s))) != ATTN_OK) return st;
+    L.p.map = map;
+  }
+  return cuda_status(launch_fwd_fp8(L, has_score_mods(L.p.flags), s));
+}
+
+attn_status_t attn_block_map(const attn_mods_t* mods, int B, int N, uint8_t* map, void* stream) {
+  attn_status_t st;
+  if (B < 1 || N < 1 || map == nullptr) return ATTN_ERR_INVALID_ARG;
+  if ((st = check_mods(mods)) != ATTN_OK) return st;
+  if ((long long)B * n_tiles(N) * n_tiles(N) >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  int* status = nullptr;
+  if ((st = device_state(&status)) != ATTN_OK) return st;
+  AttnParams p = make_params(B, 1, 1, N, 1.0f, mods, status);
+  return cuda_status(launch_block_map(p, map, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_status(void* stream) {
+  int* status = nullptr;
+  attn_status_t st = device_state(&status);
+  if (st != ATTN_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  switch (h) {
+    case 0: return ATTN_OK;
+    case DEV_ERR_TIMEOUT: return ATTN_ERR_TIMEOUT;
+    default: return ATTN_ERR_BOUNDS;
+  }
+}
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported shape, head size or alignment";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case ATTN_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    case ATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case ATTN_ERR_BOUNDS: return "device index check failed";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// Block-sparsity map: every 128 x 128 tile (b, I, J) is classified as skip /
+// partial / full by testing each of its (i, j) pairs against the mask
+// (FlexAttention/FA4 page, "Limitations actuelles": block sparsity; tile
+// size 128 as named there).  Tiles that the causal or window bound rules out
+// as a whole are classified without the element test (every pair of such a
+// tile fails the same condition, so the result is the same).
+#include "common.cuh"
+#include "launch.h"
+
+namespace attn {
+
+__global__ void __launch_bounds__(256) block_map_kernel(const AttnParams p, uint8_t* __restrict__ map) {
+  const int J = blockIdx.x, I = blockIdx.y, b = blockIdx.z;
+  const bool causal = (p.flags & MOD_CAUSAL) != 0;
+  const bool win = (p.flags & MOD_WINDOW) != 0;
+  const bool doc = (p.flags & MOD_DOC) != 0;
+  uint8_t* out = map + ((size_t)b * p.nT + I) * p.nT + J;
+  const int i_lo = I * TILE, j_lo = J * TILE;
+  const int i_hi = min(i_lo + TILE, p.N) - 1;  // last real row
+  // Whole-tile rejections: all pairs have j > i, or all have i - j >= window.
+  if ((causal && j_lo > i_hi) || (win && i_lo - (j_lo + TILE - 1) >= p.window)) {
+    if (threadIdx.x == 0) *out = CLS_SKIP;
+    return;
+  }
+  const int r = threadIdx.x & (TILE - 1);
+  const int half = threadIdx.x >> 7;
+  const int i = i_lo + r;
+  bool any_ok = false, all_ok = true;
+  if (i < p.N) {
+    const int di = doc ? p.doc_ids[(size_t)b * p.N + i] : 0;
+#pragma unroll 4
+    for (int c = 0; c < TILE / 2; ++c) {
+      const int j = j_lo + half * (TILE / 2) + c;
+      bool ok = j < p.N;
+      if (ok && causal) ok = j <= i;
+      if (ok && win) ok = (i - j) < p.window;
+      if (ok && doc) ok = p.doc_ids[(size_t)b * p.N + j] == di;
+      any_ok |= ok;
+      all_ok &= ok;
+    }
+  }
+  any_ok = __syncthreads_or(any_ok);
+  all_ok = __syncthreads_and(all_ok);
+  if (threadIdx.x == 0) {
+    int c = !any_ok ? CLS_SKIP : ((all_ok && j_lo + TILE <= p.N) ? CLS_FULL : CLS_PARTIAL);
+    *out = (uint8_t)c;
+  }
+}
+
+cudaError_t launch_block_map(const AttnParams& p, uint8_t* map, cudaStream_t st) {
+  const dim3 grid(p.nT, p.nT, p.B);
+  block_map_kernel<<<grid, 256, 0, st>>>(p, map);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,441 @@
+// Forward pass of exact tiled attention, bf16 in, fp32 accumulate, for sm_103a.
+//
+// Method (FlashAttention-3 digest, "Rappel du fonctionnement de FlashAttention"
+// and "Chevauchement de GEMM et softmax grâce à l'asynchronisme"; FlashAttention-2
+// (FR), "Architecture technique et principes de fonctionnement"): Q is split in
+// tiles of 128 rows, K/V are streamed in tiles of 128 rows, and for every tile
+// pair the two GEMMs S = Q K^T and O += P V run on the tensor cores while a
+// running row max m and row sum l rescale the partial output, so the N x N
+// score matrix is never stored and the result is exact.
+//
+// GB300 design (not a translation of the pages' Hopper/Ampere kernels):
+//  * one CTA = two Q tiles (256 rows) of one (batch, query head); both tiles
+//    share every K/V tile that TMA brings into shared memory;
+//  * warp 0 issues TMA loads (Q once, K/V through two-stage rings guarded by
+//    mbarriers); warp 1 issues tcgen05 MMAs from a single thread; warps 4-7
+//    and 8-11 are the softmax warpgroups of Q tile 0 and Q tile 1;
+//  * S lives in TMEM (fp32, 128 columns per tile), the softmax warpgroup
+//    writes P back over S as packed bf16, and P V reads P straight from TMEM
+//    (A operand in tensor memory), so P never touches shared memory;
+//  * the MMA order S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ... hides each
+//    warpgroup's exponentials behind the other tile's GEMMs (the pages'
+//    ping-pong idea, expressed with tcgen05 commits instead of named barriers);
+//  * O is rescaled in TMEM only when a row max grows by more than 2^8
+//    (lazy rescale, exact after the final division by l);
+//  * on partial (masked) tiles P is split into bf16 hi + lo parts and both
+//    are multiplied by V, which removes the bf16 rounding of P where few keys
+//    carry the whole row (the first rows of a causal context);
+//  * fully masked tiles are skipped (block-sparsity map, FlexAttention/FA4
+//    page, "Limitations actuelles").
+#include "common.cuh"
+#include "launch.h"
+
+namespace attn {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int CH = D / 64;                 // 128-byte column chunks per row
+  static constexpr int TILE_BYTES = TILE * D * 2;   // one bf16 tile of 128 rows
+  static constexpr int KST = (D == 128) ? 2 : 3;    // K ring stages
+  static constexpr int VST = (D == 128) ? 2 : 3;    // V ring stages
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
+  static constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
+  static constexpr int BAR_OFF = V_OFF + VST * TILE_BYTES;
+  static constexpr int SMEM_BYTES = smem_one_cta(BAR_OFF + 512 + 1024);  // + alignment slack
+  static constexpr uint32_t O_COL = 256;            // TMEM: S0 @0, S1 @128, O0 @256, O1 @256+D
+  static constexpr int THREADS = 384;
+};
+
+struct FwdBars {
+  uint64_t q_full;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t mma_drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Next kv tile >= J that at least one of the CTA's two Q tiles needs.
+__device__ __forceinline__ int union_next(const AttnParams& p, int b, int I0, int J, int J_end) {
+  while (J < J_end && tile_class(p, b, I0, J) == CLS_SKIP && tile_class(p, b, I0 + 1, J) == CLS_SKIP)
+    ++J;
+  return J;
+}
+
+template <int D>
+__device__ __forceinline__ void issue_S(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t id = idesc_bf16(128, 128, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+    mma_f16_ss(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024),
+               id, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_PV(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool first, bool with_lo) {
+  constexpr uint32_t id = idesc_bf16(128, D, false, true);
+#pragma unroll
+  for (int kk = 0; kk < TILE / 16; ++kk) {
+    const uint64_t bd = sdesc_sw128(v_smem + kk * 16 * 128, 16384, 1024);
+    mma_f16_ts(o_tmem, p_tmem + kk * 8, bd, id, (first && kk == 0) ? 0u : 1u);
+  }
+  if (with_lo) {
+#pragma unroll
+    for (int kk = 0; kk < TILE / 16; ++kk) {
+      const uint64_t bd = sdesc_sw128(v_smem + kk * 16 * 128, 16384, 1024);
+      mma_f16_ts(o_tmem, p_tmem + 64 + kk * 8, bd, id, 1u);
+    }
+  }
+}
+
+// P = 2^(x - mu) for the 128 columns of this thread's row, packed to bf16 and
+// written over S in TMEM (columns 0..63); with LO the rounding residual
+// p - bf16(p) goes to columns 64..127.  Returns the row sum of P (fp32).
+template <bool LO>
+__device__ __forceinline__ float store_p(const uint32_t (&s)[128], float mu, uint32_t tS) {
+  float sum = 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t ph[32];
+    uint32_t pl[32];
+#pragma unroll
+    for (int w = 0; w < 32; ++w) {
+      const int c = h * 64 + 2 * w;
+      const float p0 = ex2(__uint_as_float(s[c]) - mu);
+      const float p1 = ex2(__uint_as_float(s[c + 1]) - mu);
+      sum += p0 + p1;
+      ph[w] = pack_bf16(p0, p1);
+      if (LO) pl[w] = pack_bf16(p0 - bf16lo_f32(ph[w]), p1 - bf16hi_f32(ph[w]));
+    }
+    tmem_st32(tS + h * 32, ph);
+    if (LO) tmem_st32(tS + 64 + h * 32, pl);
+  }
+  return sum;
+}
+
+template <int D, bool MODS>
+__global__ void __launch_bounds__(384, 1)
+    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
+                    float* __restrict__ lse, const AttnParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  FwdBars& S = *reinterpret_cast<FwdBars*>(smem + C::BAR_OFF);
+  const Abort ab{&S.abort, p.status};
+  const int warp = warp_id(), lane = lane_id();
+
+  // Work item, heaviest Q blocks first (longest-processing-time order).
+  const int BH = p.B * p.Hq;
+  const int qblk = p.n_qblk - 1 - (int)(blockIdx.x / BH);
+  const int bh = (int)(blockIdx.x % BH);
+  const int b = bh / p.Hq, hq = bh - b * p.Hq;
+  const int hk = hq / (p.Hq / p.Hkv);
+  const int I0 = 2 * qblk;
+  const int J_end = (p.flags & MOD_CAUSAL) ? min(p.nT, I0 + 2) : p.nT;
+
+  if (threadIdx.x == 0) {
+    S.abort = 0;
+    mbar_init(&S.q_full, 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&S.k_full[s], 1);
+      mbar_init(&S.k_empty[s], 1);
+      mbar_init(&S.v_full[s], 1);
+      mbar_init(&S.v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&S.s_full[t], 1);
+      mbar_init(&S.p_full[t], 128);
+      mbar_init(&S.o_full[t], 1);
+    }
+    mbar_init(&S.mma_drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&S.tmem_base, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  const uint32_t sQ = smem_u32(smem + C::Q_OFF);
+  const uint32_t sK = smem_u32(smem + C::K_OFF);
+  const uint32_t sV = smem_u32(smem + C::V_OFF);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      mbar_arrive_tx(&S.q_full, 2 * C::TILE_BYTES);
+      for (int t = 0; t < 2; ++t)
+        for (int ch = 0; ch < C::CH; ++ch)
+          tma_load_3d(smem + C::Q_OFF + t * C::TILE_BYTES + ch * 16384, &tq, &S.q_full, ch * 64,
+                      (I0 + t) * TILE, b * p.Hq + hq);
+      int kit = 0, vit = 0;
+      for (int J = union_next(p, b, I0, 0, J_end); J < J_end; J = union_next(p, b, I0, J + 1, J_end)) {
+        const int ks = kit % C::KST;
+        if (!mbar_wait(&S.k_empty[ks], ((kit / C::KST) & 1) ^ 1, ab)) break;
+        mbar_arrive_tx(&S.k_full[ks], C::TILE_BYTES);
+        for (int ch = 0; ch < C::CH; ++ch)
+          tma_load_3d(smem + C::K_OFF + ks * C::TILE_BYTES + ch * 16384, &tk, &S.k_full[ks],
+                      ch * 64, J * TILE, b * p.Hkv + hk);
+        ++kit;
+        const int vs = vit % C::VST;
+        if (!mbar_wait(&S.v_empty[vs], ((vit / C::VST) & 1) ^ 1, ab)) break;
+        mbar_arrive_tx(&S.v_full[vs], C::TILE_BYTES);
+        for (int ch = 0; ch < C::CH; ++ch)
+          tma_load_3d(smem + C::V_OFF + vs * C::TILE_BYTES + ch * 16384, &tv, &S.v_full[vs],
+                      ch * 64, J * TILE, b * p.Hkv + hk);
+        ++vit;
+      }
+      // Let every copy this thread issued land before the CTA can exit: the
+      // last load into each stage completes phase ((n_loads - 1) & 1).
+      mbar_wait_drain(&S.q_full, 0);
+      for (int s = 0; s < C::KST; ++s)
+        if (kit > s) mbar_wait_drain(&S.k_full[s], ((kit - 1 - s) / C::KST) & 1);
+      for (int s = 0; s < C::VST; ++s)
+        if (vit > s) mbar_wait_drain(&S.v_full[s], ((vit - 1 - s) / C::VST) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int npv[2] = {0, 0};
+      bool ok = mbar_wait(&S.q_full, 0, ab);
+      tc_fence_after();
+      int J = union_next(p, b, I0, 0, J_end);
+      int c0 = 0, c1 = 0;
+      if (ok && J < J_end) {
+        c0 = tile_class(p, b, I0, J);
+        c1 = tile_class(p, b, I0 + 1, J);
+        ok = mbar_wait(&S.k_full[0], 0, ab);
+        tc_fence_after();
+        if (ok) {
+          if (c0 != CLS_SKIP) { issue_S<D>(tmem + 0, sQ, sK); mma_commit(&S.s_full[0]); }
+          if (c1 != CLS_SKIP) { issue_S<D>(tmem + 128, sQ + C::TILE_BYTES, sK); mma_commit(&S.s_full[1]); }
+          mma_commit(&S.k_empty[0]);
+        }
+      }
+      int it = 0;
+      while (ok && J < J_end) {
+        const int Jn = union_next(p, b, I0, J + 1, J_end);
+        const bool has_next = Jn < J_end;
+        const int n0 = has_next ? tile_class(p, b, I0, Jn) : CLS_SKIP;
+        const int n1 = has_next ? tile_class(p, b, I0 + 1, Jn) : CLS_SKIP;
+        const int vs = it % C::VST;
+        const int ksn = (it + 1) % C::KST;
+        const uint32_t vsm = sV + vs * C::TILE_BYTES;
+        const uint32_t ksm = sK + ksn * C::TILE_BYTES;
+        if (!(ok = mbar_wait(&S.v_full[vs], (it / C::VST) & 1, ab))) break;
+        bool k_ready = false;
+        if (c0 != CLS_SKIP) {
+          if (!(ok = mbar_wait(&S.p_full[0], npv[0] & 1, ab))) break;
+          tc_fence_after();
+          issue_PV<D>(tmem + C::O_COL, tmem + 0, vsm, npv[0] == 0, c0 == CLS_PARTIAL);
+          mma_commit(&S.o_full[0]);
+          ++npv[0];
+        }
+        if (n0 != CLS_SKIP) {
+          if (!(ok = mbar_wait(&S.k_full[ksn], ((it + 1) / C::KST) & 1, ab))) break;
+          k_ready = true;
+          tc_fence_after();
+          issue_S<D>(tmem + 0, sQ, ksm);
+          mma_commit(&S.s_full[0]);
+        }
+        if (c1 != CLS_SKIP) {
+          if (!(ok = mbar_wait(&S.p_full[1], npv[1] & 1, ab))) break;
+          tc_fence_after();
+          issue_PV<D>(tmem + C::O_COL + D, tmem + 128, vsm, npv[1] == 0, c1 == CLS_PARTIAL);
+          mma_commit(&S.o_full[1]);
+          ++npv[1];
+        }
+        if (n1 != CLS_SKIP) {
+          if (!k_ready) {
+            if (!(ok = mbar_wait(&S.k_full[ksn], ((it + 1) / C::KST) & 1, ab))) break;
+            tc_fence_after();
+          }
+          issue_S<D>(tmem + 128, sQ + C::TILE_BYTES, ksm);
+          mma_commit(&S.s_full[1]);
+        }
+        if (has_next) mma_commit(&S.k_empty[ksn]);
+        mma_commit(&S.v_empty[vs]);
+        J = Jn;
+        c0 = n0;
+        c1 = n1;
+        ++it;
+      }
+      // Every MMA this thread issued completes before TMEM can be released.
+      mma_commit(&S.mma_drain);
+      mbar_wait_drain(&S.mma_drain, 0);
+    }
+  } else if (warp >= 4) {
+    // -------------------------------------------------------------- softmax
+    const int t = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int I = I0 + t;
+    const int i = I * TILE + r;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (uint32_t)t * 128;
+    const uint32_t tO = tmem + lane_off + C::O_COL + (uint32_t)t * D;
+    const bool causal = (p.flags & MOD_CAUSAL) != 0;
+    RowMods rm{};
+    if (MODS) {
+      rm.sc_in = p.scale / p.softcap;
+      rm.sc_out = p.softcap * LOG2E;
+      rm.alibi_l2 = (p.flags & MOD_ALIBI) ? alibi_slope(p, hq) * LOG2E : 0.f;
+      rm.doc_i = ((p.flags & MOD_DOC) && i < p.N) ? p.doc_ids[(size_t)b * p.N + i] : 0;
+    }
+    float m = -INFINITY, l = 0.f;
+    int ns = 0;
+    bool ok = true;
+    for (int J = 0; J < J_end; ++J) {
+      const int cls = tile_class(p, b, I, J);
+      if (cls == CLS_SKIP) continue;
+      if (!(ok = wait_warp(&S.s_full[t], ns & 1, ab))) break;
+      tc_fence_after();
+      uint32_t s[128];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        tmem_ld32(tS + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[q4 * 32]));
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(&s[q4 * 32]));
+
+      // Scores in log2 units, masked on partial tiles.
+      const int j0 = J * TILE;
+      const int hi_lim = min(causal ? i : 0x7fffffff, p.N - 1) - j0;  // valid iff c <= hi_lim
+      float mt = -INFINITY;
+      if (!MODS) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          float x = __uint_as_float(s[c]) * p.scale_log2;
+          if (cls == CLS_PARTIAL && c > hi_lim) x = -INFINITY;
+          s[c] = __float_as_uint(x);
+          mt = fmaxf(mt, x);
+        }
+      } else {
+        const bool sc = (p.flags & MOD_SOFTCAP) != 0;
+        const bool al = (p.flags & MOD_ALIBI) != 0;
+        const bool win = (p.flags & MOD_WINDOW) != 0;
+        const bool doc = (p.flags & MOD_DOC) != 0;
+        const float al_row = rm.alibi_l2 * (float)(j0 - i);
+        const int lo_lim = win ? (i - p.window - j0) : -0x7fffffff;  // valid iff c > lo_lim
+        const int* drow = doc ? p.doc_ids + (size_t)b * p.N + j0 : nullptr;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          float x = __uint_as_float(s[c]);
+          x = sc ? tanh_exp(x * rm.sc_in) * rm.sc_out : x * p.scale_log2;
+          if (al) x = fmaf(rm.alibi_l2, (float)c, x + al_row);
+          if (cls == CLS_PARTIAL) {
+            bool valid = (c <= hi_lim) && (c > lo_lim);
+            if (doc && valid) valid = (__ldg(drow + c) == rm.doc_i);
+            if (!valid) x = -INFINITY;
+          }
+          s[c] = __float_as_uint(x);
+          mt = fmaxf(mt, x);
+        }
+      }
+
+      // Running max; O is rescaled only when some row's max grew by > 2^8.
+      const float mn = fmaxf(m, mt);
+      if (ns == 0) {
+        m = mn;
+      } else {
+        const bool need = mn > m + RESCALE_THRESHOLD;
+        if (__any_sync(0xffffffffu, need)) {
+          if (!(ok = wait_warp(&S.o_full[t], (ns - 1) & 1, ab))) break;
+          tc_fence_after();
+          const float alpha = need ? ex2(m - mn) : 1.0f;
+          if (need) {
+            l *= alpha;
+            m = mn;
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < D / 32; ++q4) {
+            uint32_t ov[32];
+            tmem_ld32(tO + q4 * 32, ov);
+            tmem_wait_ld(ov);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+            tmem_st32(tO + q4 * 32, ov);
+          }
+          tmem_wait_st();
+        }
+      }
+      const float mu = (m == -INFINITY) ? 0.f : m;
+
+      // P = 2^(x - m) as bf16 (hi, plus lo on partial tiles) over S in TMEM.
+      if (cls == CLS_PARTIAL)
+        l += store_p<true>(s, mu, tS);
+      else
+        l += store_p<false>(s, mu, tS);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&S.p_full[t]);
+      ++ns;
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (ok && ns > 0) {
+      ok = wait_warp(&S.o_full[t], (ns - 1) & 1, ab);
+      tc_fence_after();
+    }
+    if (ok) {
+      const float inv = l > 0.f ? 1.0f / l : 0.f;
+      __nv_bfloat16* orow = o + (((size_t)b * p.Hq + hq) * p.N + i) * D;
+#pragma unroll
+      for (int q4 = 0; q4 < D / 32; ++q4) {
+        uint32_t ov[32];
+        if (ns > 0) {
+          tmem_ld32(tO + q4 * 32, ov);
+          tmem_wait_ld(ov);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int w = 0; w < 16; ++w)
+          pk[w] = pack_bf16(__uint_as_float(ov[2 * w]) * inv, __uint_as_float(ov[2 * w + 1]) * inv);
+        if (i < p.N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + q4 * 32);
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+        }
+      }
+      if (i < p.N)
+        lse[((size_t)b * p.Hq + hq) * p.N + i] = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool MODS>
+static cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  auto kern = fwd_bf16_kernel<D, MODS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)(L.p.n_qblk * L.p.B * L.p.Hq));
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(L.tq, L.tk, L.tv, (__nv_bfloat16*)L.o, L.lse, L.p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_bf16(const FwdLaunch& L, int d, bool mods, cudaStream_t st) {
+  if (d == 128) return mods ? launch_fwd_t<128, true>(L, st) : launch_fwd_t<128, false>(L, st);
+  return mods ? launch_fwd_t<64, true>(L, st) : launch_fwd_t<64, false>(L, st);
+}
+
+}  // namespace attn

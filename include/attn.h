@@ -1,0 +1,185 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact tiled attention library.
+ *
+ * What the library computes.  Exact softmax attention, in tiles, without ever
+ * storing the N x N score matrix:
+ *   O = softmax(mods(scale * Q K^T), masked) V,   LSE = log sum exp of each row.
+ * The tiled method reaches the plain definition exactly (up to rounding
+ * order): "FlashAttention-2 (FR)", opening paragraph and section "Contexte"
+ * (tiles in on-chip SRAM, linear memory, identical result); the FlashAttention-3
+ * digest, section "Rappel du fonctionnement de FlashAttention" (tiling plus
+ * softmax rescaling gives the exact output; the backward recomputes instead of
+ * storing).  The mods are the FlexAttention variants named on the
+ * FlexAttention/FA4 page (ALiBi, sliding window, document masking,
+ * soft-capping), here a fixed set of flags with runtime scalars in place of a
+ * Python JIT, and GQA as in the Hacker News thread of the FlashAttention-3
+ * digest.  The FP8 forward with Hadamard incoherent processing follows the
+ * same digest, section "Basse précision FP8 et incoherent processing".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Layout   : contiguous [B, H, N, d] row-major; Q/O/dO/dQ have H = Hq heads,
+ *            K/V/dK/dV have H = Hkv heads; query head hq reads KV head
+ *            hq / (Hq / Hkv).  LSE is fp32 [B, Hq, N], natural log.
+ * Types    : Q, K, V, O, dO, dQ, dK, dV are bf16; FP8 tensors are e4m3.
+ * Sizes    : d in {64, 128} (FP8: d = 128); N >= 1 (backward: N <= 131072); Hq % Hkv == 0;
+ *            B * max(Hq, Hkv) * N < 2^31.
+ * Pointers : device pointers, 16-byte aligned.  The caller owns every
+ *            buffer, including the workspace; the library allocates nothing
+ *            per call (it keeps only a device status word).
+ * Streams  : every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *            the legacy default stream).  The device current for the calling
+ *            thread must own the buffers.
+ * Errors   : argument problems are reported synchronously, before anything is
+ *            launched (ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
+ *            ATTN_ERR_WORKSPACE); a failed launch gives ATTN_ERR_CUDA.  Errors
+ *            found on the device (a pipeline wait that timed out, a bounds
+ *            check) are recorded in the status word and returned by
+ *            attn_status().  There is no fallback path of any kind.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, bad mod scalar */
+  ATTN_ERR_UNSUPPORTED = 2,  /* d not supported, Hq % Hkv != 0, misaligned pointer */
+  ATTN_ERR_WORKSPACE = 3,    /* workspace missing or smaller than attn_workspace_size() */
+  ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call or a launch failed */
+  ATTN_ERR_DEVICE = 5,       /* the current device is not an sm_103 GPU */
+  ATTN_ERR_TIMEOUT = 6,      /* (device) a pipeline wait gave up after its time limit */
+  ATTN_ERR_BOUNDS = 7        /* (device) an index check failed */
+} attn_status_t;
+
+/* Mod flags.  The mask is the AND of the enabled parts. */
+enum {
+  ATTN_MOD_CAUSAL = 1u << 0,  /* allowed iff j <= i */
+  ATTN_MOD_WINDOW = 1u << 1,  /* allowed iff i - j < window */
+  ATTN_MOD_DOC = 1u << 2,     /* allowed iff doc_ids[b][i] == doc_ids[b][j] */
+  ATTN_MOD_SOFTCAP = 1u << 3, /* score x -> softcap * tanh(x / softcap), applied to scale*q.k */
+  ATTN_MOD_ALIBI = 1u << 4    /* score x -> x - slope[hq] * (i - j), after the soft-cap */
+};
+
+/* FlexAttention variants as a fixed set of flags plus runtime scalars
+ * (FlexAttention/FA4 page, opening paragraphs and "Limitations actuelles":
+ * no recompilation when a scalar changes). */
+typedef struct {
+  uint32_t flags;             /* OR of ATTN_MOD_* */
+  int32_t window;             /* ATTN_MOD_WINDOW: >= 1 */
+  float softcap;              /* ATTN_MOD_SOFTCAP: > 0 */
+  const int32_t* doc_ids;     /* ATTN_MOD_DOC: device int32 [B, N] */
+  const float* alibi_slopes;  /* ATTN_MOD_ALIBI: device fp32 [Hq], or NULL for 2^(-8(h+1)/Hq) */
+} attn_mods_t;
+
+/* Operations for attn_workspace_size(). */
+enum { ATTN_OP_FWD = 0, ATTN_OP_BWD = 1, ATTN_OP_FWD_FP8 = 2, ATTN_OP_QUANT_FP8 = 3 };
+
+/* Block-map tile classes (128 x 128 tiles). */
+enum { ATTN_TILE_SKIP = 0, ATTN_TILE_PARTIAL = 1, ATTN_TILE_FULL = 2 };
+
+/*
+ * Bytes of caller-provided workspace an operation needs (0 when none).
+ * mods may be NULL (no mods).  Returns 0 for invalid arguments as well; the
+ * operation itself then reports the argument error.
+ */
+size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int N, int d, const attn_mods_t* mods);
+
+/*
+ * Forward pass: O (bf16 [B,Hq,N,d]) and LSE (fp32 [B,Hq,N]) from Q, K, V.
+ * The method: the FlashAttention-3 digest, "Rappel du fonctionnement de
+ * FlashAttention" (tiles, online softmax rescale, never materialising S) and
+ * "Chevauchement de GEMM et softmax grâce à l'asynchronisme" (GEMMs on the
+ * tensor cores overlapped with the exponentials).  Rows with no allowed key
+ * get O = 0 and LSE = -inf.  Fully masked 128 x 128 tiles are skipped
+ * (block sparsity, FlexAttention/FA4 page, "Limitations actuelles").
+ * scale : multiplier of q.k (typically 1/sqrt(d)), finite.
+ * ws    : workspace of attn_workspace_size(ATTN_OP_FWD, ...) bytes (may be
+ *         NULL when that size is 0).
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int Hq, int Hkv, int N, int d, float scale,
+                       const attn_mods_t* mods, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Backward pass: dQ (bf16 [B,Hq,N,d]), dK and dV (bf16 [B,Hkv,N,d]) from Q, K,
+ * V, the forward's O and LSE, and dO.  P is recomputed from LSE (the
+ * FlashAttention-3 digest, "Rappel du fonctionnement": tiling and
+ * recomputation).  The result is bitwise reproducible from run to run: no
+ * floating-point atomics; every dQ, dK and dV tile is accumulated by one CTA
+ * over its partner tiles in ascending order (contrast the FlexAttention/FA4
+ * page, "Limitations actuelles": nondeterministic backward with block
+ * sparsity).  dK/dV of a KV head sum over its query heads (GQA).
+ * ws : workspace of attn_workspace_size(ATTN_OP_BWD, ...) bytes (row sums
+ *      D = rowsum(dO * O) and, with window/document mods, the block map).
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       int B, int Hq, int Hkv, int N, int d, float scale,
+                       const attn_mods_t* mods, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * FP8 prologue (FlashAttention-3 digest, "Basse précision FP8 et incoherent
+ * processing"): every row of Q and K is multiplied by diag(s) H / sqrt(d),
+ * H the natural-order Sylvester Hadamard matrix of order d and s the +-1
+ * sign vector of the row's KV head (query head hq uses signs[hq/(Hq/Hkv)]);
+ * V is not rotated.  Each (b, head) tensor is then scaled by 448/amax and
+ * rounded to e4m3 (nearest even, saturating).
+ * signs  : device int8 [Hkv, d] of +-1, or NULL to skip the rotation (the
+ *          plain-FP8 variant).
+ * q8     : e4m3 [B,Hq,N,d];  k8, v8 : e4m3 [B,Hkv,N,d].
+ * scales : device fp32, B*Hq + 2*B*Hkv entries: the dequantisation scales
+ *          amax/448 of Q [B,Hq], then K [B,Hkv], then V [B,Hkv] (1 where a
+ *          head is all zero).
+ * ws     : workspace of attn_workspace_size(ATTN_OP_QUANT_FP8, ...) bytes.
+ * d must be 128.
+ */
+attn_status_t attn_hadamard_quant_fp8(const void* q, const void* k, const void* v, void* q8,
+                                      void* k8, void* v8, float* scales, const int8_t* signs,
+                                      int B, int Hq, int Hkv, int N, int d, void* ws,
+                                      size_t ws_bytes, void* stream);
+
+/*
+ * FP8 forward: O (bf16) and LSE (fp32, of the dequantised scores) from the
+ * e4m3 tensors and scales written by attn_hadamard_quant_fp8.  Q K^T runs in
+ * e4m3 with fp32 accumulation, P is rounded to e4m3 for P V, and the
+ * dequantisation factors are folded into the softmax scale (Q, K) and the
+ * epilogue (V).  Same mods, workspace rule and errors as attn_fwd; d = 128.
+ */
+attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* scales,
+                           void* o, float* lse, int B, int Hq, int Hkv, int N, int d,
+                           float scale, const attn_mods_t* mods, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/*
+ * Block-sparsity map of the mask in mods (FlexAttention/FA4 page, "Limitations
+ * actuelles": block sparsity; 128 x 128 tiles as named there).  map is device
+ * uint8 [B, nT, nT], nT = ceil(N/128); entry (b, I, J) classifies rows
+ * [128I, 128I+128) x columns [128J, 128J+128), counting only rows i < N:
+ * ATTN_TILE_SKIP when no pair with j < N is allowed, ATTN_TILE_FULL when the
+ * column range lies inside [0, N) and every pair is allowed, else
+ * ATTN_TILE_PARTIAL.  Only the mask flags of mods matter.
+ */
+attn_status_t attn_block_map(const attn_mods_t* mods, int B, int N, uint8_t* map, void* stream);
+
+/*
+ * Synchronise `stream`, then return and clear the device status word
+ * (ATTN_OK, ATTN_ERR_TIMEOUT or ATTN_ERR_BOUNDS), or ATTN_ERR_CUDA when the
+ * synchronisation itself failed.
+ */
+attn_status_t attn_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* attn_status_string(attn_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

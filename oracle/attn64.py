@@ -192,6 +192,47 @@ def group_backward(q, k, v, do, scale: float, mods: Mods, b: int, hk: int):
     return heads, dQ, dK, dV
 
 
+def sampled_backward(q, k, v, do, scale: float, mods: Mods, b: int, hk: int,
+                     q_rows=None, kv_rows=None):
+    """Selected outputs of the backward for KV head ``hk`` of batch row ``b``.
+
+    Returns (dQ [G, len(q_rows), d], dK [len(kv_rows), d], dV [len(kv_rows), d])
+    for the query heads of the group, computed from the same definitions as
+    ``group_backward``: each query head's full score matrix gives P and D, and
+    only the requested rows of dQ and columns of P / dS are reduced.
+    """
+    Hq, Hkv = q.shape[1], k.shape[1]
+    G = Hq // Hkv
+    K = _f64(k[b, hk])
+    V = _f64(v[b, hk])
+    N, d = K.shape
+    idx = np.arange(N)
+    qr = idx if q_rows is None else np.asarray(q_rows)
+    kr = idx if kv_rows is None else np.asarray(kv_rows)
+    m = allowed(mods, b, idx, idx)
+    dQ = np.zeros((G, qr.size, d))
+    dK = np.zeros((kr.size, d))
+    dV = np.zeros((kr.size, d))
+    for g in range(G):
+        hq = hk * G + g
+        Q = _f64(q[b, hq])
+        dO = _f64(do[b, hq])
+        z, x = logits(Q, K, scale, mods, hq, Hq, idx, idx)
+        P, _ = _softmax_rows(x, m)
+        dP = dO @ V.T
+        D = (P * dP).sum(axis=1)
+        dX = P * (dP - D[:, None])
+        if mods.softcap is not None:
+            c = float(mods.softcap)
+            dZ = dX * (1.0 - np.tanh(z / c) ** 2)
+        else:
+            dZ = dX
+        dQ[g] = scale * (dZ[qr] @ K)
+        dK += scale * (dZ[:, kr].T @ Q)
+        dV += P[:, kr].T @ dO
+    return dQ, dK, dV
+
+
 def backward(q, k, v, do, scale: float, mods: Mods = None):
     """dQ [B, Hq, N, d], dK and dV [B, Hkv, N, d] in fp64."""
     mods = mods or Mods()

@@ -8,3 +8,10 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a GB300 (sm_103a) GPU and the built CUDA library")
+
+
+def pytest_sessionstart(session):
+    """GPU runs build the CUDA library first (it is never shipped prebuilt)."""
+    if session.config.getoption("-m", default="") == "gpu":
+        import __graft_entry__
+        __graft_entry__.build()

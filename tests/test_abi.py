@@ -1,0 +1,109 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+include/attn.h declares, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    from exact_attention_66_gb300 import _lib
+    return _lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_bwd", "attn_fwd_fp8", "attn_hadamard_quant_fp8", "attn_block_map",
+              "attn_workspace_size", "attn_status", "attn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    so = ctypes.CDLL(L.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(so, n), n
+    assert set(L.EXPORTS) <= set(declared_functions())
+
+
+A = 0x10000  # an aligned, never-dereferenced address
+
+
+def fwd(L, q=A, k=A, v=A, o=A, lse=A, B=1, Hq=2, Hkv=2, N=128, d=128, scale=0.1, mods=None,
+        ws=None, nws=0):
+    return L.lib().attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale,
+                            ctypes.byref(mods) if mods else None, ws, nws, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), 1), (dict(N=0), 1), (dict(Hq=0), 1), (dict(q=None), 1), (dict(lse=None), 1),
+    (dict(d=96), 2), (dict(d=256), 2), (dict(Hq=3, Hkv=2), 2), (dict(q=A + 8), 2),
+    (dict(lse=A + 2), 2), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+])
+def test_fwd_argument_errors(L, kw, code):
+    assert fwd(L, **kw) == code
+
+
+def test_mod_argument_errors(L):
+    m = L.make_mods(window=0)
+    assert fwd(L, mods=m) == 1
+    m = L.make_mods(causal=True)
+    m.flags |= 1 << 7
+    assert fwd(L, mods=m) == 1
+    m = L.make_mods(softcap=-1.0)
+    assert fwd(L, mods=m) == 1
+    m = L.Mods()
+    m.flags = L.MOD_DOC
+    assert fwd(L, mods=m) == 1  # document mask without ids
+    # window/doc masks need the block-map workspace
+    m = L.make_mods(causal=True, window=64)
+    assert fwd(L, mods=m) == 3
+    need = L.attn_workspace_size(L.OP_FWD, 1, 2, 2, 128, 128, m)
+    assert fwd(L, mods=m, ws=A + 16, nws=need) == 3  # misaligned workspace
+
+
+def test_other_entry_points_validate(L):
+    so = L.lib()
+    # backward: null dq
+    assert so.attn_bwd(A, A, A, A, A, A, None, A, A, 1, 2, 2, 64, 128, 0.1, None, A, 1 << 20, None) == 1
+    # backward: workspace too small
+    assert so.attn_bwd(A, A, A, A, A, A, A, A, A, 1, 2, 2, 64, 128, 0.1, None, A, 16, None) == 3
+    # FP8 needs d = 128
+    assert so.attn_fwd_fp8(A, A, A, A, A, A, 1, 2, 2, 64, 64, 0.1, None, None, 0, None) == 2
+    assert so.attn_hadamard_quant_fp8(A, A, A, A, A, A, A, None, 1, 2, 2, 64, 64, A, 4096, None) == 2
+    assert so.attn_hadamard_quant_fp8(A, A, A, A, A, A, None, None, 1, 2, 2, 64, 128, A, 4096, None) == 1
+    assert so.attn_block_map(None, 1, 100, None, None) == 1
+
+
+def test_workspace_sizes(L):
+    ws = L.attn_workspace_size
+    assert ws(L.OP_FWD, 1, 2, 2, 1000, 128, L.make_mods(causal=True)) == 0
+    m = L.make_mods(causal=True, window=64)
+    assert ws(L.OP_FWD, 4, 16, 16, 4096, 128, m) == 4 * 32 * 32
+    assert ws(L.OP_BWD, 1, 64, 8, 8192, 128, L.make_mods(causal=True)) == 64 * 8192 * 4
+    assert ws(L.OP_BWD, 2, 2, 2, 1000, 64, m) == 256 * ((2 * 2 * 1000 * 4 + 255) // 256) + 256
+    assert ws(L.OP_QUANT_FP8, 2, 16, 16, 16384, 128, None) == 512  # 96 fp32 amax words
+    assert ws(L.OP_FWD, 1, 3, 2, 128, 128, None) == 0  # invalid shape -> 0
+
+
+def test_status_strings(L):
+    for c in range(8):
+        assert L.status_string(c)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
+def test_valid_call_without_gpu_reports_cuda_error(L):
+    assert fwd(L) == 4  # ATTN_ERR_CUDA: no silent CPU path

@@ -226,6 +226,19 @@ def test_backward_matches_torch_autograd_sdpa():
     np.testing.assert_allclose(dv, V.grad.numpy(), rtol=1e-10, atol=1e-12)
 
 
+def test_sampled_backward_matches_full():
+    B, Hq, Hkv, N, d = 2, 4, 2, 12, 4
+    q, k, v, do = (_rand((B, Hq, N, d), 60), _rand((B, Hkv, N, d), 61),
+                   _rand((B, Hkv, N, d), 62), _rand((B, Hq, N, d), 63))
+    mods = _mods("all", B, N)
+    dq, dk, dv = A.backward(q, k, v, do, 0.9, mods)
+    rows, cols = np.array([0, 5, 11]), np.array([1, 2, 10])
+    gq, gk, gv = A.sampled_backward(q, k, v, do, 0.9, mods, 1, 1, rows, cols)
+    np.testing.assert_allclose(gq, dq[1, 2:4][:, rows], atol=1e-13)
+    np.testing.assert_allclose(gk, dk[1, 1, cols], atol=1e-13)
+    np.testing.assert_allclose(gv, dv[1, 1, cols], atol=1e-13)
+
+
 def test_delta_identity():
     """rowsum(dO * O) equals rowsum(P * dP): the preprocessing shortcut is exact."""
     B, Hq, N, d = 1, 1, 9, 5
