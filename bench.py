@@ -1,0 +1,397 @@
+#!/usr/bin/env python3
+"""Benchmark: exact attention forward + backward on the GQA causal 8K workload.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+attn_fwd (O, LSE) then attn_bwd (row sums D, dK/dV kernel, dQ kernel) on
+B=1, Hq=64, Hkv=8, N=8192, d=128, causal, bf16 (the Llama-3-70B attention
+shape).  Throughput counts algorithmic FLOPs: 4*B*Hq*d*(allowed pairs) for
+the forward and 2.5x that for the backward.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle (the reference arm of this build) on bounded row slices of the same
+workload.  Under torchrun each rank runs an independent replica (weak
+scaling, no data-path collective; the process group only carries the
+timing barrier and max).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import attn_inputs as gen  # noqa: E402
+
+WORKLOAD = "gqa_causal_8k"
+METRIC = "attention TFLOPS fwd/bwd (bf16 causal N=8K d=128) & % of GB300 dense peak"
+UNIT = "TFLOP/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def causal_pairs(N: int) -> int:
+    return N * (N + 1) // 2
+
+
+def flops(cfg):
+    fwd = 4.0 * cfg["B"] * cfg["Hq"] * cfg["d"] * causal_pairs(cfg["N"])
+    return fwd, 2.5 * fwd
+
+
+# ---------------------------------------------------------------- clocks ----
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------- distributed ----
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allmax(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------- oracle baseline ----
+def oracle_sample(cfg, x, budget_s: float, rows_per_slice: int):
+    """Time the fp64 oracle on row slices of query heads of the workload.
+
+    Runs slices (forward rows + their backward contributions) until
+    ``budget_s`` seconds have passed (at least one).  Returns (TFLOP/s,
+    seconds, description)."""
+    from oracle import attn64
+    mods = attn64.Mods(causal=True)
+    scale = 1.0 / math.sqrt(cfg["d"])
+    N, d = cfg["N"], cfg["d"]
+    done_flops, t0, n = 0.0, time.perf_counter(), 0
+    starts = list(range(N - rows_per_slice, -1, -rows_per_slice))
+    while True:
+        hq = n % cfg["Hq"]
+        r0 = starts[n % len(starts)]
+        rows = np.arange(r0, r0 + rows_per_slice)
+        attn64.head_forward(x["q"], x["k"], x["v"], scale, mods, 0, hq, rows=rows)
+        attn64.head_rows_backward(x["q"], x["k"], x["v"], x["do"], scale, mods, 0, hq, rows)
+        done_flops += 3.5 * 4.0 * d * float((rows + 1).sum())
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    desc = (f"{n} slices of {rows_per_slice} query rows (forward + their backward "
+            f"contributions, fp64 numpy) of {WORKLOAD}; {done_flops:.3e} algorithmic FLOP")
+    return done_flops / el / 1e12, el, desc
+
+
+def cpu_info():
+    cores = os.cpu_count() or 1
+    return cores
+
+
+# ---------------------------------------------------------------- ours -----
+def traffic_record(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source is unchanged since it was captured (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "exact_attention_66_gb300", "csrc", rec["source"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return rec["bytes_per_launch"] if h == rec.get("source_sha") else None
+
+
+def run_ours(args, world, rank, local):
+    import exact_attention_66_gb300 as ea
+
+    cfg = dict(gen.WORKLOADS[WORKLOAD])
+    B, Hq, Hkv, N, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"]
+    scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = gen.make_inputs(B, Hq, Hkv, N, d, seed=cfg["seed"] + 97 * rank)
+    host = {k: x[k].pin_memory() for k in ("q", "k", "v", "do")}
+    q, k, v, do = (host[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    mods = ea.make_mods(causal=True)
+    nws = ea.attn_workspace_size(ea.OP_BWD, B, Hq, Hkv, N, d, mods)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def mk_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)  # create the handles before passing them to the library
+        return evs
+
+    def step(ev=None):
+        if ev is None:
+            ea.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, mods, None, 0, stream)
+            ea.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods, ws, nws, stream)
+        else:
+            ev[0].record(stream)
+            ea.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, mods, None, 0, stream)
+            ev[1].record(stream)
+            ea.attn_bwd_profiled(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods,
+                                 ws, nws, stream, ev[2:6])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ea.attn_status(stream)
+
+    evs = [mk_events(6) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier(world)
+    ea.attn_status(stream)
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = allmax(world, total_ms)
+    k_fwd = [e[0].elapsed_time(e[1]) for e in evs]
+    k_pre = [e[2].elapsed_time(e[3]) for e in evs]
+    k_kv = [e[3].elapsed_time(e[4]) for e in evs]
+    k_dq = [e[4].elapsed_time(e[5]) for e in evs]
+    mean = lambda a: sum(a) / len(a)  # noqa: E731
+
+    # end to end through the public API: pinned host inputs in, results out
+    out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    h2d = sum(host[n].numel() * host[n].element_size() for n in host)
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for n, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
+            dst.copy_(host[n], non_blocking=True)
+        fo, fl = ea.forward(q, k, v, scale, mods, out=o, lse=lse, stream=stream)
+        ea.attn_bwd(q, k, v, fo, do, fl, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods, ws, nws, stream)
+        for n, src in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            out_host[n].copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = allmax(world, e0.elapsed_time(e1)) / e2e_steps
+    ea.attn_status(stream)
+
+    fwd_f, bwd_f = flops(cfg)
+    ms = total_ms / args.steps
+    value = world * (fwd_f + bwd_f) / (ms * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    sustained = peaks["bf16_tflops_sustained"]
+    burst = peaks["bf16_tflops"]
+    fwd_t = fwd_f / (mean(k_fwd) * 1e-3) / 1e12
+    bwd_ms = mean(k_pre) + mean(k_kv) + mean(k_dq)
+    bwd_t = bwd_f / (bwd_ms * 1e-3) / 1e12
+    # dominant kernel: the dK/dV kernel; its algorithmic work is 4 of the 5
+    # backward GEMMs (S recompute, dP, dV, dK) = 2x the forward FLOPs.
+    kernels = {"fwd_bf16": (mean(k_fwd), fwd_f), "bwd_dkdv": (mean(k_kv), 0.8 * bwd_f),
+               "bwd_dq": (mean(k_dq), 0.2 * bwd_f), "bwd_pre": (mean(k_pre), 0.0)}
+    dom = max(kernels, key=lambda n: kernels[n][0])
+    dom_ms, dom_flops = kernels[dom]
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
+                   "mask": "causal", "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (Q/O/dO/dQ 128 MiB each, step working set ~700 MiB)"},
+        "fwd_tflops": round(fwd_t, 1), "bwd_tflops": round(bwd_t, 1),
+        "fwd_frac_peak": round(fwd_t / sustained, 4), "bwd_frac_peak": round(bwd_t / sustained, 4),
+        "fwd_frac_burst_peak": round(fwd_t / burst, 4), "bwd_frac_burst_peak": round(bwd_t / burst, 4),
+        "kernel_ms": {n: round(t, 4) for n, (t, _) in kernels.items()},
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": sustained, "unit": "TFLOP/s", "frac": round(achieved / sustained, 4),
+                     "traffic": traffic_record(dom),
+                     "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside back-to-back steps)"},
+        "e2e": {"value": round(world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, el, desc = oracle_sample(cfg, x, args.cpu_seconds, 512)
+        line["cpu_baseline"] = {"value": round(tf, 5), "unit": UNIT, "cores": cpu_info(),
+                                "kind": "oracle", "sample": desc, "seconds": round(el, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle as the reference arm, on bounded slices per step."""
+    if rank != 0:
+        return
+    cfg = dict(gen.WORKLOADS[WORKLOAD])
+    x = gen.make_inputs(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"], seed=cfg["seed"])
+    # size each step's slice so the whole run stays within about two minutes
+    per_step = max(0.05, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    t0 = time.perf_counter()
+    oracle_sample(cfg, x, 0.0, 64)
+    t64 = time.perf_counter() - t0
+    rows = int(max(16, min(2048, 64 * per_step / max(t64, 1e-3))) // 16 * 16)
+    for _ in range(args.warmup):
+        oracle_sample(cfg, x, 0.0, rows)
+    tf_all, el_all = [], 0.0
+    for _ in range(args.steps):
+        tf, el, desc = oracle_sample(cfg, x, 0.0, rows)
+        tf_all.append(tf)
+        el_all += el
+    value = statistics.mean(tf_all)
+    ms = 1e3 * el_all / args.steps
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": cfg["B"], "Hq": cfg["Hq"], "Hkv": cfg["Hkv"],
+                   "N": cfg["N"], "d": cfg["d"], "mask": "causal"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cpu_info(), "kind": "oracle",
+                         "sample": f"per step: one slice of {rows} query rows (forward + their "
+                                   f"backward contributions) of {WORKLOAD}"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="time budget of the oracle CPU baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup()
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

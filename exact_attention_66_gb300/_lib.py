@@ -25,7 +25,7 @@ OP_FWD, OP_BWD, OP_FWD_FP8, OP_QUANT_FP8 = 0, 1, 2, 3
 TILE_SKIP, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 
 # Exported symbols, in the order include/attn.h declares them.
-EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_hadamard_quant_fp8",
+EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_hadamard_quant_fp8",
            "attn_fwd_fp8", "attn_block_map", "attn_status", "attn_status_string")
 
 
@@ -44,7 +44,7 @@ class Mods(ctypes.Structure):
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError(
-            f"{path} is missing: build the CUDA library first (python -m exact_attention_66_gb300.build)")
+            f"{path} is missing: build the CUDA library first (python exact_attention_66_gb300/build.py)")
     lib = ctypes.CDLL(path)
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     mp = ctypes.POINTER(Mods)
@@ -52,13 +52,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_workspace_size.restype = sz
     lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
+    lib.attn_bwd_profiled.argtypes = lib.attn_bwd.argtypes + [ctypes.POINTER(ctypes.c_void_p)]
     lib.attn_hadamard_quant_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp]
     lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_block_map.argtypes = [mp, i, i, vp, vp]
     lib.attn_status.argtypes = [vp]
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
-    for name in ("attn_fwd", "attn_bwd", "attn_hadamard_quant_fp8", "attn_fwd_fp8",
+    for name in ("attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_hadamard_quant_fp8", "attn_fwd_fp8",
                  "attn_block_map", "attn_status"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
@@ -131,6 +132,16 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods=No
     _check(_lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
                          _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, float(scale), _mods_ref(mods),
                          _ptr(ws), int(ws_bytes), _stream(stream)), "attn_bwd")
+
+
+def attn_bwd_profiled(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods, ws,
+                      ws_bytes, stream, events):
+    """attn_bwd recording four torch.cuda.Event objects around its kernels (see attn.h)."""
+    arr = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
+    _check(_lib.attn_bwd_profiled(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, float(scale),
+                                  _mods_ref(mods), _ptr(ws), int(ws_bytes), _stream(stream), arr),
+           "attn_bwd_profiled")
 
 
 def attn_hadamard_quant_fp8(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N, d, ws=None,

@@ -215,10 +215,11 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   return cuda_status(launch_fwd_bf16(L, d, has_score_mods(L.p.flags), s));
 }
 
-attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
-                       int Hq, int Hkv, int N, int d, float scale, const attn_mods_t* mods,
-                       void* ws, size_t ws_bytes, void* stream) {
+static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                              int B, int Hq, int Hkv, int N, int d, float scale,
+                              const attn_mods_t* mods, void* ws, size_t ws_bytes, void* stream,
+                              void* const* events) {
   attn_status_t st;
   if ((st = check_shape(B, Hq, Hkv, N, d, false)) != ATTN_OK) return st;
   if (N > BWD_MAX_N) return ATTN_ERR_UNSUPPORTED;
@@ -253,7 +254,29 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
     if ((st = cuda_status(launch_block_map(L.p, map, s))) != ATTN_OK) return st;
     L.p.map = map;
   }
+  if (events != nullptr)
+    for (int e = 0; e < 4; ++e) L.events[e] = static_cast<cudaEvent_t>(events[e]);
   return cuda_status(launch_bwd(L, d, has_score_mods(L.p.flags), s));
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int Hq, int Hkv, int N, int d, float scale, const attn_mods_t* mods,
+                       void* ws, size_t ws_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods, ws, ws_bytes,
+                  stream, nullptr);
+}
+
+attn_status_t attn_bwd_profiled(const void* q, const void* k, const void* v, const void* o,
+                                const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                int B, int Hq, int Hkv, int N, int d, float scale,
+                                const attn_mods_t* mods, void* ws, size_t ws_bytes, void* stream,
+                                void* const* events) {
+  if (events == nullptr) return ATTN_ERR_INVALID_ARG;
+  for (int e = 0; e < 4; ++e)
+    if (events[e] == nullptr) return ATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods, ws, ws_bytes,
+                  stream, events);
 }
 
 attn_status_t attn_hadamard_quant_fp8(const void* q, const void* k, const void* v, void* q8,

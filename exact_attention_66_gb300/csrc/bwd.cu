@@ -580,6 +580,7 @@ static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
   const AttnParams& p = L.p;
   const long long rows = (long long)p.B * p.Hq * p.N;
   const long long threads = rows * (D / 8);
+  if (L.events[0]) cudaEventRecord(L.events[0], st);
   bwd_pre_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
       (const __nv_bfloat16*)L.o, (const __nv_bfloat16*)L.dout, L.delta, rows);
   cudaError_t e = cudaGetLastError();
@@ -589,6 +590,7 @@ static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
   if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::SMEM_BYTES)) !=
       cudaSuccess)
     return e;
+  if (L.events[1]) cudaEventRecord(L.events[1], st);
   kv<<<(unsigned)(p.nT * p.B * p.Hkv), 256, KvCfg<D>::SMEM_BYTES, st>>>(
       L.tq, L.tk, L.tv, L.tdo, L.lse, L.delta, (__nv_bfloat16*)L.dk, (__nv_bfloat16*)L.dv, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -597,8 +599,11 @@ static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
   if ((e = cudaFuncSetAttribute(dqk, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM_BYTES)) !=
       cudaSuccess)
     return e;
+  if (L.events[2]) cudaEventRecord(L.events[2], st);
   dqk<<<(unsigned)(p.nT * p.B * p.Hq), 256, DqCfg<D>::SMEM_BYTES, st>>>(
       L.tq, L.tk, L.tv, L.tdo, L.lse, L.delta, (__nv_bfloat16*)L.dq, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (L.events[3]) cudaEventRecord(L.events[3], st);
   return cudaGetLastError();
 }
 

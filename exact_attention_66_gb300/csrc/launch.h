@@ -34,6 +34,7 @@ struct BwdLaunch {
   void* dk;
   void* dv;
   AttnParams p;
+  cudaEvent_t events[4];  // optional: recorded before pre / dkdv / dq and after dq
 };
 cudaError_t launch_bwd(const BwdLaunch& L, int d, bool mods, cudaStream_t st);
 

@@ -125,6 +125,21 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        const attn_mods_t* mods, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * attn_bwd, plus timing: events[0..3] are cudaEvent_t handles created by the
+ * caller; events[0] is recorded on `stream` before the row-sum kernel,
+ * events[1] before the dK/dV kernel, events[2] before the dQ kernel and
+ * events[3] after it (the block-map kernel, when the mods need one, runs
+ * before events[0]).  Measurement aid for "profiler l'exécution" (the kernel
+ * fusion page, "Fusion et CUDA Graphs avec torch.compile"); results are
+ * identical to attn_bwd.  events must not be NULL.
+ */
+attn_status_t attn_bwd_profiled(const void* q, const void* k, const void* v, const void* o,
+                                const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                int B, int Hq, int Hkv, int N, int d, float scale,
+                                const attn_mods_t* mods, void* ws, size_t ws_bytes, void* stream,
+                                void* const* events);
+
+/*
  * FP8 prologue (FlashAttention-3 digest, "Basse précision FP8 et incoherent
  * processing"): every row of Q and K is multiplied by diag(s) H / sqrt(d),
  * H the natural-order Sylvester Hadamard matrix of order d and s the +-1

@@ -233,6 +233,36 @@ def sampled_backward(q, k, v, do, scale: float, mods: Mods, b: int, hk: int,
     return dQ, dK, dV
 
 
+def head_rows_backward(q, k, v, do, scale: float, mods: Mods, b: int, hq: int, rows):
+    """What query rows ``rows`` of head ``hq`` contribute to the backward.
+
+    Returns (dQ[rows] [R, d], dK part [N, d], dV part [N, d]); the full dK/dV
+    of a KV head are the sums of these parts over all rows of every query head
+    of its group (the sums over i in dK = scale dZ^T Q and dV = P^T dO split
+    by rows).  Used to time the oracle on a bounded slice of a workload.
+    """
+    Hq, Hkv = q.shape[1], k.shape[1]
+    hk = hq // (Hq // Hkv)
+    K = _f64(k[b, hk])
+    V = _f64(v[b, hk])
+    N = K.shape[0]
+    rows = np.asarray(rows)
+    idx = np.arange(N)
+    Q = _f64(q[b, hq])[rows]
+    dO = _f64(do[b, hq])[rows]
+    z, x = logits(_f64(q[b, hq]), K, scale, mods, hq, Hq, rows, idx)
+    P, _ = _softmax_rows(x, allowed(mods, b, rows, idx))
+    dP = dO @ V.T
+    D = (P * dP).sum(axis=1)
+    dX = P * (dP - D[:, None])
+    if mods.softcap is not None:
+        c = float(mods.softcap)
+        dZ = dX * (1.0 - np.tanh(z / c) ** 2)
+    else:
+        dZ = dX
+    return scale * (dZ @ K), scale * (dZ.T @ Q), P.T @ dO
+
+
 def backward(q, k, v, do, scale: float, mods: Mods = None):
     """dQ [B, Hq, N, d], dK and dV [B, Hkv, N, d] in fp64."""
     mods = mods or Mods()

@@ -239,6 +239,25 @@ def test_sampled_backward_matches_full():
     np.testing.assert_allclose(gv, dv[1, 1, cols], atol=1e-13)
 
 
+def test_row_slices_sum_to_full_backward():
+    B, Hq, Hkv, N, d = 1, 4, 2, 11, 3
+    q, k, v, do = (_rand((B, Hq, N, d), 64), _rand((B, Hkv, N, d), 65),
+                   _rand((B, Hkv, N, d), 66), _rand((B, Hq, N, d), 67))
+    mods = _mods("all", B, N)
+    dq, dk, dv = A.backward(q, k, v, do, 0.8, mods)
+    for hk in range(Hkv):
+        gk = np.zeros((N, d))
+        gv = np.zeros((N, d))
+        for hq in (2 * hk, 2 * hk + 1):
+            for rows in (np.arange(0, 4), np.arange(4, 11)):
+                a, b_, c = A.head_rows_backward(q, k, v, do, 0.8, mods, 0, hq, rows)
+                np.testing.assert_allclose(a, dq[0, hq, rows], atol=1e-13)
+                gk += b_
+                gv += c
+        np.testing.assert_allclose(gk, dk[0, hk], atol=1e-13)
+        np.testing.assert_allclose(gv, dv[0, hk], atol=1e-13)
+
+
 def test_delta_identity():
     """rowsum(dO * O) equals rowsum(P * dP): the preprocessing shortcut is exact."""
     B, Hq, N, d = 1, 1, 9, 5
