@@ -14,14 +14,14 @@ import math
 from ._lib import (  # noqa: F401
     AttnError, Mods, EXPORTS, MOD_ALIBI, MOD_CAUSAL, MOD_DOC, MOD_SOFTCAP, MOD_WINDOW, OP_BWD,
     OP_FWD, OP_FWD_FP8, OP_QUANT_FP8, TILE_FULL, TILE_PARTIAL, TILE_SKIP, attn_block_map, attn_bwd,
-    attn_bwd_profiled,
+    attn_bwd_profiled, attn_bwd_noalloc, NOALLOC_SCRATCH_BYTES,
     attn_fwd, attn_fwd_fp8, attn_hadamard_quant_fp8, attn_status, attn_workspace_size, lib,
     make_mods, status_string,
 )
 
 __all__ = [
     "forward", "backward", "hadamard_quant_fp8", "forward_fp8", "block_map", "make_mods",
-    "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_hadamard_quant_fp8", "attn_fwd_fp8", "attn_block_map",
+    "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc", "attn_hadamard_quant_fp8", "attn_fwd_fp8", "attn_block_map",
     "attn_status", "attn_workspace_size", "AttnError",
 ]
 

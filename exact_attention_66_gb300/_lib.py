@@ -25,7 +25,8 @@ OP_FWD, OP_BWD, OP_FWD_FP8, OP_QUANT_FP8 = 0, 1, 2, 3
 TILE_SKIP, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 
 # Exported symbols, in the order include/attn.h declares them.
-EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_hadamard_quant_fp8",
+EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc",
+           "attn_hadamard_quant_fp8",
            "attn_fwd_fp8", "attn_block_map", "attn_status", "attn_status_string")
 
 
@@ -53,13 +54,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_bwd_profiled.argtypes = lib.attn_bwd.argtypes + [ctypes.POINTER(ctypes.c_void_p)]
+    lib.attn_bwd_noalloc.argtypes = lib.attn_bwd.argtypes[:16] + [vp]  # no ws, ws_bytes
     lib.attn_hadamard_quant_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp]
     lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_block_map.argtypes = [mp, i, i, vp, vp]
     lib.attn_status.argtypes = [vp]
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
-    for name in ("attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_hadamard_quant_fp8", "attn_fwd_fp8",
+    for name in ("attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc", "attn_hadamard_quant_fp8", "attn_fwd_fp8",
                  "attn_block_map", "attn_status"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
@@ -142,6 +144,21 @@ def attn_bwd_profiled(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale
                                   _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, float(scale),
                                   _mods_ref(mods), _ptr(ws), int(ws_bytes), _stream(stream), arr),
            "attn_bwd_profiled")
+
+
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024  # ATTN_NOALLOC_SCRATCH_BYTES
+
+
+def attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods=None,
+                     stream=None):
+    """attn_bwd without a workspace, for callers that cannot allocate device
+    memory (memory owned by a framework allocator or a fixed arena, or no
+    cudaMalloc/cudaFree allowed because they synchronise the device).  The
+    library's fixed scratch array stands in for the workspace: the work must
+    fit in NOALLOC_SCRATCH_BYTES, and calls that overlap on the GPU race."""
+    _check(_lib.attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, float(scale),
+                                 _mods_ref(mods), _stream(stream)), "attn_bwd_noalloc")
 
 
 def attn_hadamard_quant_fp8(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N, d, ws=None,

@@ -139,6 +139,42 @@ attn_status_t attn_bwd_profiled(const void* q, const void* k, const void* v, con
                                 const attn_mods_t* mods, void* ws, size_t ws_bytes, void* stream,
                                 void* const* events);
 
+/* Capacity, in bytes, of the fixed device scratch array of attn_bwd_noalloc. */
+#define ATTN_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * attn_bwd for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point: it is a library addition.
+ *
+ * Who needs it: code whose device memory is owned by someone else -- a host
+ * framework with its own caching allocator, or a fixed arena that other code
+ * must not allocate around -- and code that must not call cudaMalloc/cudaFree
+ * because those calls synchronise the device.  Such callers can still pass Q,
+ * K, V, O, dO, LSE and the dQ/dK/dV outputs, but not the workspace attn_bwd
+ * takes.  This variant uses instead a scratch array compiled into the library
+ * (a file-scope device array of ATTN_NOALLOC_SCRATCH_BYTES, held by every GPU
+ * that loads the library until the process exits).  It calls no cudaMalloc,
+ * cudaFree or any other allocating routine.
+ *
+ * Arguments, layout and errors are those of attn_bwd, without ws/ws_bytes.
+ * Limit: the workspace attn_bwd would need, attn_workspace_size(ATTN_OP_BWD,
+ * ...) = 4*B*Hq*N bytes rounded up to 256, plus the block map with window or
+ * document mods, must fit in ATTN_NOALLOC_SCRATCH_BYTES; otherwise the call
+ * returns ATTN_ERR_WORKSPACE before touching the device.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.
+ * Sharing: every call uses the same array, which keeps the last call's
+ * contents.  Each call overwrites all of the scratch it reads (nothing there
+ * has to start at zero), so consecutive calls are fine; calls that overlap on
+ * the GPU (different streams, or host threads without ordering) race on the
+ * array and give wrong results.
+ */
+attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                               int B, int Hq, int Hkv, int N, int d, float scale,
+                               const attn_mods_t* mods, void* stream);
+
 /*
  * FP8 prologue (FlashAttention-3 digest, "Basse précision FP8 et incoherent
  * processing"): every row of Q and K is multiplied by diag(s) H / sqrt(d),
