@@ -1,4 +1,5 @@
-// Forward pass of exact tiled attention, bf16 in, fp32 accumulate, for sm_103a.
+// Forward pass of exact tiled attention for sm_103a: bf16 or e4m3 operands,
+// fp32 accumulation and softmax.
 //
 // Method (FlashAttention-3 digest, "Rappel du fonctionnement de FlashAttention"
 // and "Chevauchement de GEMM et softmax grâce à l'asynchronisme"; FlashAttention-2
@@ -26,18 +27,26 @@
 //    are multiplied by V, which removes the bf16 rounding of P where few keys
 //    carry the whole row (the first rows of a causal context);
 //  * fully masked tiles are skipped (block-sparsity map, FlexAttention/FA4
-//    page, "Limitations actuelles").
+//    page, "Limitations actuelles");
+//  * the FP8 variant (FlashAttention-3 digest, "Basse précision FP8 et
+//    incoherent processing") runs the same pipeline on e4m3 Q/K/V with
+//    tcgen05.mma kind::f8f6f4 (twice the bf16 rate), rounds P to e4m3 for
+//    P V, and folds the per-(batch, head) dequantisation scales into the
+//    softmax scale (Q, K) and the epilogue (V).
 #include "common.cuh"
 #include "launch.h"
 
 namespace attn {
 
-template <int D>
+template <int D, bool FP8>
 struct FwdCfg {
-  static constexpr int CH = D / 64;                 // 128-byte column chunks per row
-  static constexpr int TILE_BYTES = TILE * D * 2;   // one bf16 tile of 128 rows
-  static constexpr int KST = (D == 128) ? 2 : 3;    // K ring stages
-  static constexpr int VST = (D == 128) ? 2 : 3;    // V ring stages
+  static constexpr int ESZ = FP8 ? 1 : 2;              // bytes per element
+  static constexpr int ROW_BYTES = D * ESZ;
+  static constexpr int CH = ROW_BYTES / 128;            // 128-byte column chunks per row
+  static constexpr int BOX = 128 / ESZ;                 // elements per TMA box row
+  static constexpr int TILE_BYTES = TILE * ROW_BYTES;   // one tile of 128 rows
+  static constexpr int KST = TILE_BYTES >= 32768 ? 2 : (FP8 ? 4 : 3);  // K ring stages
+  static constexpr int VST = KST;                       // V ring stages
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
@@ -63,27 +72,38 @@ __device__ __forceinline__ int union_next(const AttnParams& p, int b, int I0, in
   return J;
 }
 
-template <int D>
+// S = Q K^T over d: every MMA consumes 32 bytes of each row (16 bf16 or 32
+// e4m3 elements), stepping through the 128-byte swizzled chunks.
+template <int D, bool FP8>
 __device__ __forceinline__ void issue_S(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
-  constexpr uint32_t id = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t id = FP8 ? idesc_e4m3(128, 128, false, false) : idesc_bf16(128, 128, false, false);
+  constexpr int KSTEPS = FwdCfg<D, FP8>::ROW_BYTES / 32;
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
+  for (int kk = 0; kk < KSTEPS; ++kk) {
     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-    mma_f16_ss(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024),
-               id, kk > 0 ? 1u : 0u);
+    const uint64_t a = sdesc_sw128(q_smem + off, 16, 1024), b = sdesc_sw128(k_smem + off, 16, 1024);
+    if (FP8)
+      mma_f8_ss(d_tmem, a, b, id, kk > 0 ? 1u : 0u);
+    else
+      mma_f16_ss(d_tmem, a, b, id, kk > 0 ? 1u : 0u);
   }
 }
 
-template <int D>
+// O += P V with P from TMEM (8 columns = 16 bf16 or 32 e4m3 keys per MMA).
+template <int D, bool FP8>
 __device__ __forceinline__ void issue_PV(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
                                          bool first, bool with_lo) {
-  constexpr uint32_t id = idesc_bf16(128, D, false, true);
+  constexpr uint32_t id = FP8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
+  constexpr int KV = FP8 ? 32 : 16;
 #pragma unroll
-  for (int kk = 0; kk < TILE / 16; ++kk) {
-    const uint64_t bd = sdesc_sw128(v_smem + kk * 16 * 128, 16384, 1024);
-    mma_f16_ts(o_tmem, p_tmem + kk * 8, bd, id, (first && kk == 0) ? 0u : 1u);
+  for (int kk = 0; kk < TILE / KV; ++kk) {
+    const uint64_t bd = sdesc_sw128(v_smem + kk * KV * 128, 16384, 1024);
+    if (FP8)
+      mma_f8_ts(o_tmem, p_tmem + kk * 8, bd, id, (first && kk == 0) ? 0u : 1u);
+    else
+      mma_f16_ts(o_tmem, p_tmem + kk * 8, bd, id, (first && kk == 0) ? 0u : 1u);
   }
-  if (with_lo) {
+  if (!FP8 && with_lo) {
 #pragma unroll
     for (int kk = 0; kk < TILE / 16; ++kk) {
       const uint64_t bd = sdesc_sw128(v_smem + kk * 16 * 128, 16384, 1024);
@@ -117,12 +137,30 @@ __device__ __forceinline__ float store_p(const uint32_t (&s)[128], float mu, uin
   return sum;
 }
 
-template <int D, bool MODS>
+// P = 2^(x - mu) rounded to e4m3 (nearest even, saturating), four per TMEM
+// column, over S (columns 0..31).  Returns the row sum of the fp32 P.
+__device__ __forceinline__ float store_p_e4m3(const uint32_t (&s)[128], float mu, uint32_t tS) {
+  float sum = 0.f;
+  uint32_t pw[32];
+#pragma unroll
+  for (int w = 0; w < 32; ++w) {
+    const float p0 = ex2(__uint_as_float(s[4 * w]) - mu);
+    const float p1 = ex2(__uint_as_float(s[4 * w + 1]) - mu);
+    const float p2 = ex2(__uint_as_float(s[4 * w + 2]) - mu);
+    const float p3 = ex2(__uint_as_float(s[4 * w + 3]) - mu);
+    sum += (p0 + p1) + (p2 + p3);
+    pw[w] = pack_e4m3x4(p0, p1, p2, p3);
+  }
+  tmem_st32(tS, pw);
+  return sum;
+}
+
+template <int D, bool MODS, bool FP8>
 __global__ void __launch_bounds__(384, 1)
-    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
-                    float* __restrict__ lse, const AttnParams p) {
-  using C = FwdCfg<D>;
+    fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
+               float* __restrict__ lse, const float* __restrict__ scales, const AttnParams p) {
+  using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   FwdBars& S = *reinterpret_cast<FwdBars*>(smem + C::BAR_OFF);
@@ -175,7 +213,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_arrive_tx(&S.q_full, 2 * C::TILE_BYTES);
       for (int t = 0; t < 2; ++t)
         for (int ch = 0; ch < C::CH; ++ch)
-          tma_load_3d(smem + C::Q_OFF + t * C::TILE_BYTES + ch * 16384, &tq, &S.q_full, ch * 64,
+          tma_load_3d(smem + C::Q_OFF + t * C::TILE_BYTES + ch * 16384, &tq, &S.q_full, ch * C::BOX,
                       (I0 + t) * TILE, b * p.Hq + hq);
       int kit = 0, vit = 0;
       for (int J = union_next(p, b, I0, 0, J_end); J < J_end; J = union_next(p, b, I0, J + 1, J_end)) {
@@ -184,14 +222,14 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive_tx(&S.k_full[ks], C::TILE_BYTES);
         for (int ch = 0; ch < C::CH; ++ch)
           tma_load_3d(smem + C::K_OFF + ks * C::TILE_BYTES + ch * 16384, &tk, &S.k_full[ks],
-                      ch * 64, J * TILE, b * p.Hkv + hk);
+                      ch * C::BOX, J * TILE, b * p.Hkv + hk);
         ++kit;
         const int vs = vit % C::VST;
         if (!mbar_wait(&S.v_empty[vs], ((vit / C::VST) & 1) ^ 1, ab)) break;
         mbar_arrive_tx(&S.v_full[vs], C::TILE_BYTES);
         for (int ch = 0; ch < C::CH; ++ch)
           tma_load_3d(smem + C::V_OFF + vs * C::TILE_BYTES + ch * 16384, &tv, &S.v_full[vs],
-                      ch * 64, J * TILE, b * p.Hkv + hk);
+                      ch * C::BOX, J * TILE, b * p.Hkv + hk);
         ++vit;
       }
       // Let every copy this thread issued land before the CTA can exit: the
@@ -216,8 +254,8 @@ __global__ void __launch_bounds__(384, 1)
         ok = mbar_wait(&S.k_full[0], 0, ab);
         tc_fence_after();
         if (ok) {
-          if (c0 != CLS_SKIP) { issue_S<D>(tmem + 0, sQ, sK); mma_commit(&S.s_full[0]); }
-          if (c1 != CLS_SKIP) { issue_S<D>(tmem + 128, sQ + C::TILE_BYTES, sK); mma_commit(&S.s_full[1]); }
+          if (c0 != CLS_SKIP) { issue_S<D, FP8>(tmem + 0, sQ, sK); mma_commit(&S.s_full[0]); }
+          if (c1 != CLS_SKIP) { issue_S<D, FP8>(tmem + 128, sQ + C::TILE_BYTES, sK); mma_commit(&S.s_full[1]); }
           mma_commit(&S.k_empty[0]);
         }
       }
@@ -236,7 +274,7 @@ __global__ void __launch_bounds__(384, 1)
         if (c0 != CLS_SKIP) {
           if (!(ok = mbar_wait(&S.p_full[0], npv[0] & 1, ab))) break;
           tc_fence_after();
-          issue_PV<D>(tmem + C::O_COL, tmem + 0, vsm, npv[0] == 0, c0 == CLS_PARTIAL);
+          issue_PV<D, FP8>(tmem + C::O_COL, tmem + 0, vsm, npv[0] == 0, c0 == CLS_PARTIAL);
           mma_commit(&S.o_full[0]);
           ++npv[0];
         }
@@ -244,13 +282,13 @@ __global__ void __launch_bounds__(384, 1)
           if (!(ok = mbar_wait(&S.k_full[ksn], ((it + 1) / C::KST) & 1, ab))) break;
           k_ready = true;
           tc_fence_after();
-          issue_S<D>(tmem + 0, sQ, ksm);
+          issue_S<D, FP8>(tmem + 0, sQ, ksm);
           mma_commit(&S.s_full[0]);
         }
         if (c1 != CLS_SKIP) {
           if (!(ok = mbar_wait(&S.p_full[1], npv[1] & 1, ab))) break;
           tc_fence_after();
-          issue_PV<D>(tmem + C::O_COL + D, tmem + 128, vsm, npv[1] == 0, c1 == CLS_PARTIAL);
+          issue_PV<D, FP8>(tmem + C::O_COL + D, tmem + 128, vsm, npv[1] == 0, c1 == CLS_PARTIAL);
           mma_commit(&S.o_full[1]);
           ++npv[1];
         }
@@ -259,7 +297,7 @@ __global__ void __launch_bounds__(384, 1)
             if (!(ok = mbar_wait(&S.k_full[ksn], ((it + 1) / C::KST) & 1, ab))) break;
             tc_fence_after();
           }
-          issue_S<D>(tmem + 128, sQ + C::TILE_BYTES, ksm);
+          issue_S<D, FP8>(tmem + 128, sQ + C::TILE_BYTES, ksm);
           mma_commit(&S.s_full[1]);
         }
         if (has_next) mma_commit(&S.k_empty[ksn]);
@@ -284,9 +322,13 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tmem + lane_off + (uint32_t)t * 128;
     const uint32_t tO = tmem + lane_off + C::O_COL + (uint32_t)t * D;
     const bool causal = (p.flags & MOD_CAUSAL) != 0;
+    // FP8: the scores are q8.k8 and need the Q and K dequantisation scales.
+    const float qk_scale = FP8 ? p.scale * scales[b * p.Hq + hq] * scales[p.B * p.Hq + b * p.Hkv + hk]
+                               : p.scale;
+    const float scale_log2 = qk_scale * LOG2E;
     RowMods rm{};
     if (MODS) {
-      rm.sc_in = p.scale / p.softcap;
+      rm.sc_in = qk_scale / p.softcap;
       rm.sc_out = p.softcap * LOG2E;
       rm.alibi_l2 = (p.flags & MOD_ALIBI) ? alibi_slope(p, hq) * LOG2E : 0.f;
       rm.doc_i = ((p.flags & MOD_DOC) && i < p.N) ? p.doc_ids[(size_t)b * p.N + i] : 0;
@@ -313,7 +355,7 @@ __global__ void __launch_bounds__(384, 1)
       if (!MODS) {
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
-          float x = __uint_as_float(s[c]) * p.scale_log2;
+          float x = __uint_as_float(s[c]) * scale_log2;
           if (cls == CLS_PARTIAL && c > hi_lim) x = -INFINITY;
           s[c] = __float_as_uint(x);
           mt = fmaxf(mt, x);
@@ -329,7 +371,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
           float x = __uint_as_float(s[c]);
-          x = sc ? tanh_exp(x * rm.sc_in) * rm.sc_out : x * p.scale_log2;
+          x = sc ? tanh_exp(x * rm.sc_in) * rm.sc_out : x * scale_log2;
           if (al) x = fmaf(rm.alibi_l2, (float)c, x + al_row);
           if (cls == CLS_PARTIAL) {
             bool valid = (c <= hi_lim) && (c > lo_lim);
@@ -370,7 +412,9 @@ __global__ void __launch_bounds__(384, 1)
       const float mu = (m == -INFINITY) ? 0.f : m;
 
       // P = 2^(x - m) as bf16 (hi, plus lo on partial tiles) over S in TMEM.
-      if (cls == CLS_PARTIAL)
+      if (FP8)
+        l += store_p_e4m3(s, mu, tS);
+      else if (cls == CLS_PARTIAL)
         l += store_p<true>(s, mu, tS);
       else
         l += store_p<false>(s, mu, tS);
@@ -386,7 +430,8 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
     }
     if (ok) {
-      const float inv = l > 0.f ? 1.0f / l : 0.f;
+      const float vscale = FP8 ? scales[p.B * p.Hq + p.B * p.Hkv + b * p.Hkv + hk] : 1.0f;
+      const float inv = l > 0.f ? vscale / l : 0.f;
       __nv_bfloat16* orow = o + (((size_t)b * p.Hq + hq) * p.N + i) * D;
 #pragma unroll
       for (int q4 = 0; q4 < D / 32; ++q4) {
@@ -422,20 +467,30 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool MODS>
-static cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t st) {
-  using C = FwdCfg<D>;
-  auto kern = fwd_bf16_kernel<D, MODS>;
+template <int D, bool MODS, bool FP8>
+static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                void* o, float* lse, const float* scales, const AttnParams& p,
+                                cudaStream_t st) {
+  using C = FwdCfg<D, FP8>;
+  auto kern = fwd_kernel<D, MODS, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)(L.p.n_qblk * L.p.B * L.p.Hq));
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(L.tq, L.tk, L.tv, (__nv_bfloat16*)L.o, L.lse, L.p);
+  const dim3 grid((unsigned)(p.n_qblk * p.B * p.Hq));
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, (__nv_bfloat16*)o, lse, scales, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_bf16(const FwdLaunch& L, int d, bool mods, cudaStream_t st) {
-  if (d == 128) return mods ? launch_fwd_t<128, true>(L, st) : launch_fwd_t<128, false>(L, st);
-  return mods ? launch_fwd_t<64, true>(L, st) : launch_fwd_t<64, false>(L, st);
+  if (d == 128)
+    return mods ? launch_fwd_t<128, true, false>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st)
+                : launch_fwd_t<128, false, false>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st);
+  return mods ? launch_fwd_t<64, true, false>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st)
+              : launch_fwd_t<64, false, false>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st);
+}
+
+cudaError_t launch_fwd_fp8(const Fp8Launch& L, bool mods, cudaStream_t st) {
+  return mods ? launch_fwd_t<128, true, true>(L.tq, L.tk, L.tv, L.o, L.lse, L.scales, L.p, st)
+              : launch_fwd_t<128, false, true>(L.tq, L.tk, L.tv, L.o, L.lse, L.scales, L.p, st);
 }
 
 }  // namespace attn
