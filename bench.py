@@ -201,6 +201,8 @@ def run_ours(args, world, rank, local):
     import exact_attention_66_gb300 as ea
 
     cfg = dict(gen.WORKLOADS[WORKLOAD])
+    if args.heads:  # smaller case of the same shape family (profiling); 8 query heads per KV head
+        cfg["Hq"], cfg["Hkv"] = args.heads, max(1, args.heads // 8)
     B, Hq, Hkv, N, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"]
     scale = 1.0 / math.sqrt(d)
     dev = torch.device("cuda", local)
@@ -267,7 +269,7 @@ def run_ours(args, world, rank, local):
                 for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
     h2d = sum(host[n].numel() * host[n].element_size() for n in host)
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
-    e2e_steps = max(3, min(args.steps, 20))
+    e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
 
     def e2e_step():
         for n, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
@@ -277,17 +279,19 @@ def run_ours(args, world, rank, local):
         for n, src in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
             out_host[n].copy_(src, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = allmax(world, e0.elapsed_time(e1)) / e2e_steps
+    e2e_ms = float("nan")
+    if e2e_steps:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = allmax(world, e0.elapsed_time(e1)) / e2e_steps
     ea.attn_status(stream)
 
     fwd_f, bwd_f = flops(cfg)
@@ -374,12 +378,15 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="time budget of the oracle CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host copies) leg")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="query heads (8 per KV head) for a smaller profiling case; default: the workload's 64")
     args = ap.parse_args()
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))

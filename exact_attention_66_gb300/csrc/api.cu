@@ -191,7 +191,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   if ((st = check_tensors({q, k, v, o})) != ATTN_OK) return st;
   if (lse == nullptr) return ATTN_ERR_INVALID_ARG;
   if (!aligned(lse, 4)) return ATTN_ERR_UNSUPPORTED;
-  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if ((st = check_mods(mods)) != ATTN_OK) return st;
   const size_t need = attn_workspace_size(ATTN_OP_FWD, B, Hq, Hkv, N, d, mods);
   if ((st = check_ws(ws, ws_bytes, need)) != ATTN_OK) return st;
@@ -226,7 +226,7 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   if ((st = check_tensors({q, k, v, o, dout, dq, dk, dv})) != ATTN_OK) return st;
   if (lse == nullptr) return ATTN_ERR_INVALID_ARG;
   if (!aligned(lse, 4)) return ATTN_ERR_UNSUPPORTED;
-  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if ((st = check_mods(mods)) != ATTN_OK) return st;
   const size_t need = attn_workspace_size(ATTN_OP_BWD, B, Hq, Hkv, N, d, mods);
   if ((st = check_ws(ws, ws_bytes, need)) != ATTN_OK) return st;
@@ -305,7 +305,7 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const
   if ((st = check_tensors({q8, k8, v8, o})) != ATTN_OK) return st;
   if (lse == nullptr || scales == nullptr) return ATTN_ERR_INVALID_ARG;
   if (!aligned(lse, 4) || !aligned(scales, 4)) return ATTN_ERR_UNSUPPORTED;
-  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if ((st = check_mods(mods)) != ATTN_OK) return st;
   const size_t need = attn_workspace_size(ATTN_OP_FWD_FP8, B, Hq, Hkv, N, d, mods);
   if ((st = check_ws(ws, ws_bytes, need)) != ATTN_OK) return st;

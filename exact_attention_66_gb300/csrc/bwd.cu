@@ -73,11 +73,11 @@ __device__ __forceinline__ void pack64(const float (&v)[64], uint32_t (&w)[32]) 
 template <int D>
 __device__ __forceinline__ void issue_half_nt(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
   constexpr uint32_t id = idesc_bf16(128, 64, false, false);
+  const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-    mma_f16_ss(d_tmem, sdesc_sw128(a_smem + off, 16, 1024), sdesc_sw128(b_smem + off, 16, 1024), id,
-               kk > 0 ? 1u : 0u);
+    mma_f16_ss(d_tmem, sdesc_add(ad, off), sdesc_add(bd, off), id, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -86,10 +86,10 @@ template <int D>
 __device__ __forceinline__ void issue_half_acc(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
                                                bool first) {
   constexpr uint32_t id = idesc_bf16(128, D, false, true);
+  const uint64_t bd = sdesc_sw128(b_smem, 16384, 1024);
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk)
-    mma_f16_ts(d_tmem, a_tmem + kk * 8, sdesc_sw128(b_smem + kk * 16 * 128, 16384, 1024), id,
-               (first && kk == 0) ? 0u : 1u);
+    mma_f16_ts(d_tmem, a_tmem + kk * 8, sdesc_add(bd, kk * 16 * 128), id, (first && kk == 0) ? 0u : 1u);
 }
 
 // Write a 128-column-or-less fp32 TMEM row (D columns at t_col) to a bf16 row, times mul.

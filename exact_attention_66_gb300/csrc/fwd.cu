@@ -54,7 +54,12 @@ struct FwdCfg {
   static constexpr int SMEM_BYTES = smem_one_cta(BAR_OFF + 512 + 1024);  // + alignment slack
   static constexpr uint32_t O_COL = 256;            // TMEM: S0 @0, S1 @128, O0 @256, O1 @256+D
   static constexpr int THREADS = 384;
+  // Register split: launched at 168 per thread (65536 / 384, rounded down to
+  // a multiple of 8); warpgroup 0 (TMA, MMA, two idle warps) gives up
+  // registers to the two softmax warpgroups: 128 * 56 + 256 * 224 = 384 * 168.
+  static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_HIGH = 224;
 };
+static_assert(128 * 56 + 256 * 224 <= 384 * 168, "register split exceeds the launch allocation");
 
 struct FwdBars {
   uint64_t q_full;
@@ -78,10 +83,11 @@ template <int D, bool FP8>
 __device__ __forceinline__ void issue_S(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
   constexpr uint32_t id = FP8 ? idesc_e4m3(128, 128, false, false) : idesc_bf16(128, 128, false, false);
   constexpr int KSTEPS = FwdCfg<D, FP8>::ROW_BYTES / 32;
-#pragma unroll
+  const uint64_t qd = sdesc_sw128(q_smem, 16, 1024), kd = sdesc_sw128(k_smem, 16, 1024);
+#pragma unroll 1
   for (int kk = 0; kk < KSTEPS; ++kk) {
     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-    const uint64_t a = sdesc_sw128(q_smem + off, 16, 1024), b = sdesc_sw128(k_smem + off, 16, 1024);
+    const uint64_t a = sdesc_add(qd, off), b = sdesc_add(kd, off);
     if (FP8)
       mma_f8_ss(d_tmem, a, b, id, kk > 0 ? 1u : 0u);
     else
@@ -95,29 +101,55 @@ __device__ __forceinline__ void issue_PV(uint32_t o_tmem, uint32_t p_tmem, uint3
                                          bool first, bool with_lo) {
   constexpr uint32_t id = FP8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
   constexpr int KV = FP8 ? 32 : 16;
-#pragma unroll
+  const uint64_t vd = sdesc_sw128(v_smem, 16384, 1024);
+#pragma unroll 1
   for (int kk = 0; kk < TILE / KV; ++kk) {
-    const uint64_t bd = sdesc_sw128(v_smem + kk * KV * 128, 16384, 1024);
+    const uint64_t bd = sdesc_add(vd, kk * KV * 128);
     if (FP8)
       mma_f8_ts(o_tmem, p_tmem + kk * 8, bd, id, (first && kk == 0) ? 0u : 1u);
     else
       mma_f16_ts(o_tmem, p_tmem + kk * 8, bd, id, (first && kk == 0) ? 0u : 1u);
   }
   if (!FP8 && with_lo) {
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < TILE / 16; ++kk) {
-      const uint64_t bd = sdesc_sw128(v_smem + kk * 16 * 128, 16384, 1024);
+      const uint64_t bd = sdesc_add(vd, kk * 16 * 128);
       mma_f16_ts(o_tmem, p_tmem + 64 + kk * 8, bd, id, 1u);
     }
   }
 }
 
-// P = 2^(x - mu) for the 128 columns of this thread's row, packed to bf16 and
-// written over S in TMEM (columns 0..63); with LO the rounding residual
-// p - bf16(p) goes to columns 64..127.  Returns the row sum of P (fp32).
+// Maximum of a 128-column row: eight independent chains of three-input max.
+__device__ __forceinline__ float row_max128(const uint32_t (&s)[128]) {
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = fmaxf(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1]));
+#pragma unroll
+  for (int c = 16; c < 128; c += 16)
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      m[k] = max3(m[k], __uint_as_float(s[c + 2 * k]), __uint_as_float(s[c + 2 * k + 1]));
+  return max3(max3(m[0], m[1], m[2]), max3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
+// Row sum of four packed partial sums.
+__device__ __forceinline__ float sum_acc(const uint64_t (&acc)[4]) {
+  float a0, a1, b0, b1, c0, c1, d0, d1;
+  f2_unpack(acc[0], a0, a1);
+  f2_unpack(acc[1], b0, b1);
+  f2_unpack(acc[2], c0, c1);
+  f2_unpack(acc[3], d0, d1);
+  return ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+}
+
+// P = 2^(mul * s - mu) for the 128 columns of this thread's row (mul folds
+// the softmax scale in; 1 when s already holds log2-unit logits), packed to
+// bf16 and written over S in TMEM (columns 0..63); with LO the rounding
+// residual p - bf16(p) goes to columns 64..127.  Returns the row sum of P.
 template <bool LO>
-__device__ __forceinline__ float store_p(const uint32_t (&s)[128], float mu, uint32_t tS) {
-  float sum = 0.f;
+__device__ __forceinline__ float store_p(const uint32_t (&s)[128], float mul, float mu, uint32_t tS) {
+  const uint64_t mul2 = f2_pack(mul, mul), nmu2 = f2_pack(-mu, -mu);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t ph[32];
@@ -125,34 +157,37 @@ __device__ __forceinline__ float store_p(const uint32_t (&s)[128], float mu, uin
 #pragma unroll
     for (int w = 0; w < 32; ++w) {
       const int c = h * 64 + 2 * w;
-      const float p0 = ex2(__uint_as_float(s[c]) - mu);
-      const float p1 = ex2(__uint_as_float(s[c + 1]) - mu);
-      sum += p0 + p1;
+      float y0, y1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), mul2, nmu2), y0, y1);
+      const float p0 = ex2(y0), p1 = ex2(y1);
+      acc[w & 3] = f2_add(acc[w & 3], f2_pack(p0, p1));
       ph[w] = pack_bf16(p0, p1);
       if (LO) pl[w] = pack_bf16(p0 - bf16lo_f32(ph[w]), p1 - bf16hi_f32(ph[w]));
     }
     tmem_st32(tS + h * 32, ph);
     if (LO) tmem_st32(tS + 64 + h * 32, pl);
   }
-  return sum;
+  return sum_acc(acc);
 }
 
-// P = 2^(x - mu) rounded to e4m3 (nearest even, saturating), four per TMEM
-// column, over S (columns 0..31).  Returns the row sum of the fp32 P.
-__device__ __forceinline__ float store_p_e4m3(const uint32_t (&s)[128], float mu, uint32_t tS) {
-  float sum = 0.f;
+// P = 2^(mul * s - mu) rounded to e4m3 (nearest even, saturating), four per
+// TMEM column, over S (columns 0..31).  Returns the row sum of the fp32 P.
+__device__ __forceinline__ float store_p_e4m3(const uint32_t (&s)[128], float mul, float mu, uint32_t tS) {
+  const uint64_t mul2 = f2_pack(mul, mul), nmu2 = f2_pack(-mu, -mu);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
   uint32_t pw[32];
 #pragma unroll
   for (int w = 0; w < 32; ++w) {
-    const float p0 = ex2(__uint_as_float(s[4 * w]) - mu);
-    const float p1 = ex2(__uint_as_float(s[4 * w + 1]) - mu);
-    const float p2 = ex2(__uint_as_float(s[4 * w + 2]) - mu);
-    const float p3 = ex2(__uint_as_float(s[4 * w + 3]) - mu);
-    sum += (p0 + p1) + (p2 + p3);
+    float y0, y1, y2, y3;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * w]), __uint_as_float(s[4 * w + 1])), mul2, nmu2), y0, y1);
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * w + 2]), __uint_as_float(s[4 * w + 3])), mul2, nmu2), y2, y3);
+    const float p0 = ex2(y0), p1 = ex2(y1), p2 = ex2(y2), p3 = ex2(y3);
+    acc[(2 * w) & 3] = f2_add(acc[(2 * w) & 3], f2_pack(p0, p1));
+    acc[(2 * w + 1) & 3] = f2_add(acc[(2 * w + 1) & 3], f2_pack(p2, p3));
     pw[w] = pack_e4m3x4(p0, p1, p2, p3);
   }
   tmem_st32(tS, pw);
-  return sum;
+  return sum_acc(acc);
 }
 
 template <int D, bool MODS, bool FP8>
@@ -204,6 +239,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sK = smem_u32(smem + C::K_OFF);
   const uint32_t sV = smem_u32(smem + C::V_OFF);
 
+  if (warp < 4) regs_dec<C::REGS_LOW>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -313,6 +349,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp >= 4) {
     // -------------------------------------------------------------- softmax
+    regs_inc<C::REGS_HIGH>();
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
@@ -351,16 +388,20 @@ __global__ void __launch_bounds__(384, 1)
       // Scores in log2 units, masked on partial tiles.
       const int j0 = J * TILE;
       const int hi_lim = min(causal ? i : 0x7fffffff, p.N - 1) - j0;  // valid iff c <= hi_lim
-      float mt = -INFINITY;
+      float mt;   // tile row max in log2 units
+      float mul;  // factor still to apply to s inside the exponential
       if (!MODS) {
+        // Raw scores: the scale is positive, so it commutes with the max and
+        // is folded into the exponential's FMA.
+        if (cls == CLS_PARTIAL) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          float x = __uint_as_float(s[c]) * scale_log2;
-          if (cls == CLS_PARTIAL && c > hi_lim) x = -INFINITY;
-          s[c] = __float_as_uint(x);
-          mt = fmaxf(mt, x);
+          for (int c = 0; c < 128; ++c)
+            if (c > hi_lim) s[c] = __float_as_uint(-INFINITY);
         }
+        mt = row_max128(s) * scale_log2;
+        mul = scale_log2;
       } else {
+        mul = 1.0f;
         const bool sc = (p.flags & MOD_SOFTCAP) != 0;
         const bool al = (p.flags & MOD_ALIBI) != 0;
         const bool win = (p.flags & MOD_WINDOW) != 0;
@@ -379,8 +420,8 @@ __global__ void __launch_bounds__(384, 1)
             if (!valid) x = -INFINITY;
           }
           s[c] = __float_as_uint(x);
-          mt = fmaxf(mt, x);
         }
+        mt = row_max128(s);
       }
 
       // Running max; O is rescaled only when some row's max grew by > 2^8.
@@ -413,11 +454,11 @@ __global__ void __launch_bounds__(384, 1)
 
       // P = 2^(x - m) as bf16 (hi, plus lo on partial tiles) over S in TMEM.
       if (FP8)
-        l += store_p_e4m3(s, mu, tS);
+        l += store_p_e4m3(s, mul, mu, tS);
       else if (cls == CLS_PARTIAL)
-        l += store_p<true>(s, mu, tS);
+        l += store_p<true>(s, mul, mu, tS);
       else
-        l += store_p<false>(s, mu, tS);
+        l += store_p<false>(s, mul, mu, tS);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&S.p_full[t]);
@@ -473,6 +514,15 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
                                 cudaStream_t st) {
   using C = FwdCfg<D, FP8>;
   auto kern = fwd_kernel<D, MODS, FP8>;
+  // The register split inside the kernel assumes exactly LAUNCH_REGS per
+  // thread at launch; refuse to launch any other build of it.
+  static int regs = -1;
+  if (regs < 0) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return cudaErrorInvalidDeviceFunction;
+    regs = fa.numRegs;
+  }
+  if (regs != C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)(p.n_qblk * p.B * p.Hq));

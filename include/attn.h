@@ -99,7 +99,7 @@ size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int N, int d, const a
  * tensor cores overlapped with the exponentials).  Rows with no allowed key
  * get O = 0 and LSE = -inf.  Fully masked 128 x 128 tiles are skipped
  * (block sparsity, FlexAttention/FA4 page, "Limitations actuelles").
- * scale : multiplier of q.k (typically 1/sqrt(d)), finite.
+ * scale : multiplier of q.k (typically 1/sqrt(d)), finite and > 0.
  * ws    : workspace of attn_workspace_size(ATTN_OP_FWD, ...) bytes (may be
  *         NULL when that size is 0).
  */

@@ -52,6 +52,7 @@ def fwd(L, q=A, k=A, v=A, o=A, lse=A, B=1, Hq=2, Hkv=2, N=128, d=128, scale=0.1,
     (dict(B=0), 1), (dict(N=0), 1), (dict(Hq=0), 1), (dict(q=None), 1), (dict(lse=None), 1),
     (dict(d=96), 2), (dict(d=256), 2), (dict(Hq=3, Hkv=2), 2), (dict(q=A + 8), 2),
     (dict(lse=A + 2), 2), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(scale=0.0), 1), (dict(scale=-0.1), 1),
 ])
 def test_fwd_argument_errors(L, kw, code):
     assert fwd(L, **kw) == code
