@@ -326,8 +326,9 @@ def run_ours(args, world, rank, local):
                      "peak": sustained, "unit": "TFLOP/s", "frac": round(achieved / sustained, 4),
                      "traffic": traffic_record(dom),
                      "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside back-to-back steps)"},
-        "e2e": {"value": round(world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "e2e": None if not e2e_steps else {
+            "value": round(world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": 4 * args.steps,
         "clocks": clk,
     }

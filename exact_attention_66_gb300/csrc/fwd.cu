@@ -12,20 +12,26 @@
 // GB300 design (not a translation of the pages' Hopper/Ampere kernels):
 //  * one CTA = two Q tiles (256 rows) of one (batch, query head); both tiles
 //    share every K/V tile that TMA brings into shared memory;
-//  * warp 0 issues TMA loads (Q once, K/V through two-stage rings guarded by
-//    mbarriers); warp 1 issues tcgen05 MMAs from a single thread; warps 4-7
-//    and 8-11 are the softmax warpgroups of Q tile 0 and Q tile 1;
-//  * S lives in TMEM (fp32, 128 columns per tile), the softmax warpgroup
-//    writes P back over S as packed bf16, and P V reads P straight from TMEM
-//    (A operand in tensor memory), so P never touches shared memory;
-//  * the MMA order S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ... hides each
-//    warpgroup's exponentials behind the other tile's GEMMs (the pages'
-//    ping-pong idea, expressed with tcgen05 commits instead of named barriers);
-//  * O is rescaled in TMEM only when a row max grows by more than 2^8
-//    (lazy rescale, exact after the final division by l);
-//  * on partial (masked) tiles P is split into bf16 hi + lo parts and both
-//    are multiplied by V, which removes the bf16 rounding of P where few keys
-//    carry the whole row (the first rows of a causal context);
+//  * warp 0 issues TMA loads (Q once; K and V through one 3-stage ring in the
+//    order the MMAs consume them); warps 1 and 2 each issue the tcgen05 MMAs
+//    of one Q tile from a single thread (the tensor pipe queues few MMAs, so
+//    one issuer waiting on a barrier would leave it idle); warps 4-7 and 8-11
+//    are the softmax warpgroups of Q tile 0 / 1;
+//  * S and O live in TMEM (S0, S1, O0, O1: all 512 columns).  A softmax thread
+//    (one row) copies its S row to registers and immediately hands the TMEM
+//    columns back, so the MMA computes S(j+1) while the softmax of tile j is
+//    still running; P is written to shared memory (128-byte swizzled K-major
+//    tile) and P V is a shared-memory MMA.  The tensor pipe therefore never
+//    waits for an exponential unless the softmax is slower than the GEMMs
+//    (the FA3 digest's overlap of softmax and GEMM, done here with tcgen05's
+//    asynchronous MMAs instead of warpgroup ping-pong);
+//  * O is rescaled in TMEM only when a row max grows by more than 2^8 (lazy
+//    rescale, exact after the final division by l), after the previous P V
+//    has completed;
+//  * on partial (masked) bf16 tiles P is split into bf16 hi + lo parts and both
+//    are multiplied by V (lo read from TMEM), which removes the bf16 rounding
+//    of P where few keys carry the whole row (the first rows of a causal
+//    context); for those tiles S(j+1) is issued after P V;
 //  * fully masked tiles are skipped (block-sparsity map, FlexAttention/FA4
 //    page, "Limitations actuelles");
 //  * the FP8 variant (FlashAttention-3 digest, "Basse précision FP8 et
@@ -41,18 +47,18 @@ namespace attn {
 template <int D, bool FP8>
 struct FwdCfg {
   static constexpr int ESZ = FP8 ? 1 : 2;              // bytes per element
-  static constexpr int ROW_BYTES = D * ESZ;
+  static constexpr int ROW_BYTES = D * ESZ;             // one Q/K/V row
   static constexpr int CH = ROW_BYTES / 128;            // 128-byte column chunks per row
   static constexpr int BOX = 128 / ESZ;                 // elements per TMA box row
-  static constexpr int TILE_BYTES = TILE * ROW_BYTES;   // one tile of 128 rows
-  static constexpr int KST = TILE_BYTES >= 32768 ? 2 : (FP8 ? 4 : 3);  // K ring stages
-  static constexpr int VST = KST;                       // V ring stages
+  static constexpr int TILE_BYTES = TILE * ROW_BYTES;   // one Q/K/V tile of 128 rows
+  static constexpr int P_BYTES = TILE * TILE * ESZ;     // one P tile (128 x 128)
+  static constexpr int RST = TILE_BYTES >= 32768 ? 3 : 4;  // K/V ring stages
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
-  static constexpr int V_OFF = K_OFF + KST * TILE_BYTES;
-  static constexpr int BAR_OFF = V_OFF + VST * TILE_BYTES;
-  static constexpr int SMEM_BYTES = smem_one_cta(BAR_OFF + 512 + 1024);  // + alignment slack
-  static constexpr uint32_t O_COL = 256;            // TMEM: S0 @0, S1 @128, O0 @256, O1 @256+D
+  static constexpr int R_OFF = Q_OFF + 2 * TILE_BYTES;
+  static constexpr int P_OFF = R_OFF + RST * TILE_BYTES;
+  static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
+  static constexpr int SMEM_BYTES = smem_one_cta(BAR_OFF + 256 + 1024);  // + alignment slack
+  static constexpr uint32_t O_COL = 256;  // TMEM: S0 @0, S1 @128, O0 @256, O1 @256+D
   static constexpr int THREADS = 384;
   // Register split: launched at 168 per thread (65536 / 384, rounded down to
   // a multiple of 8); warpgroup 0 (TMA, MMA, two idle warps) gives up
@@ -60,15 +66,20 @@ struct FwdCfg {
   static constexpr int LAUNCH_REGS = 168, REGS_LOW = 56, REGS_HIGH = 224;
 };
 static_assert(128 * 56 + 256 * 224 <= 384 * 168, "register split exceeds the launch allocation");
+static_assert(FwdCfg<128, false>::SMEM_BYTES <= 232448, "forward shared memory exceeds 227 KB");
 
 struct FwdBars {
   uint64_t q_full;
-  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], p_full[2], o_full[2];
-  uint64_t mma_drain;
+  uint64_t full[4], empty[4];  // K/V ring
+  uint64_t s_full[2];          // S_t computed (MMA commit)
+  uint64_t s_free[2];          // S_t copied out of TMEM by the softmax (128 arrivals)
+  uint64_t p_full[2];          // P_t written (128 arrivals)
+  uint64_t o_full[2];          // P_t V done (MMA commit)
+  uint64_t mma_drain[2];
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(FwdBars) <= 256, "barrier block");
 
 // Next kv tile >= J that at least one of the CTA's two Q tiles needs.
 __device__ __forceinline__ int union_next(const AttnParams& p, int b, int I0, int J, int J_end) {
@@ -77,45 +88,49 @@ __device__ __forceinline__ int union_next(const AttnParams& p, int b, int I0, in
   return J;
 }
 
-// S = Q K^T over d: every MMA consumes 32 bytes of each row (16 bf16 or 32
-// e4m3 elements), stepping through the 128-byte swizzled chunks.
-template <int D, bool FP8>
-__device__ __forceinline__ void issue_S(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
-  constexpr uint32_t id = FP8 ? idesc_e4m3(128, 128, false, false) : idesc_bf16(128, 128, false, false);
-  constexpr int KSTEPS = FwdCfg<D, FP8>::ROW_BYTES / 32;
-  const uint64_t qd = sdesc_sw128(q_smem, 16, 1024), kd = sdesc_sw128(k_smem, 16, 1024);
+// D(tmem) = A B^T with A and B K-major 128-byte swizzled tiles in shared
+// memory of `row_bytes` per row; every MMA consumes 32 bytes of each row (16
+// bf16 or 32 e4m3 elements), stepping through the 16 KB column chunks.
+template <bool FP8, int N>
+__device__ __forceinline__ void issue_nt(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
+                                         int row_bytes, bool accumulate_first) {
+  constexpr uint32_t id = FP8 ? idesc_e4m3(128, N, false, false) : idesc_bf16(128, N, false, false);
+  const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, 16, 1024);
+  const int ksteps = row_bytes / 32;
 #pragma unroll 1
-  for (int kk = 0; kk < KSTEPS; ++kk) {
+  for (int kk = 0; kk < ksteps; ++kk) {
     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-    const uint64_t a = sdesc_add(qd, off), b = sdesc_add(kd, off);
+    const uint32_t acc = (kk > 0 || accumulate_first) ? 1u : 0u;
     if (FP8)
-      mma_f8_ss(d_tmem, a, b, id, kk > 0 ? 1u : 0u);
+      mma_f8_ss(d_tmem, sdesc_add(ad, off), sdesc_add(bd, off), id, acc);
     else
-      mma_f16_ss(d_tmem, a, b, id, kk > 0 ? 1u : 0u);
+      mma_f16_ss(d_tmem, sdesc_add(ad, off), sdesc_add(bd, off), id, acc);
   }
 }
 
-// O += P V with P from TMEM (8 columns = 16 bf16 or 32 e4m3 keys per MMA).
+// O(tmem) += P V: P (shared memory, K-major, 128 keys) times V (shared
+// memory, 128 keys x D, MN-major).  With LO (bf16 partial tiles) the rounding
+// residual of P, packed in TMEM at lo_tmem, is added with A read from TMEM.
 template <int D, bool FP8>
-__device__ __forceinline__ void issue_PV(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
-                                         bool first, bool with_lo) {
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_smem, uint32_t v_smem,
+                                         bool first, bool with_lo, uint32_t lo_tmem) {
   constexpr uint32_t id = FP8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
-  constexpr int KV = FP8 ? 32 : 16;
-  const uint64_t vd = sdesc_sw128(v_smem, 16384, 1024);
+  constexpr int KV = FP8 ? 32 : 16;  // keys per MMA
+  const uint64_t pd = sdesc_sw128(p_smem, 16, 1024), vd = sdesc_sw128(v_smem, 16384, 1024);
 #pragma unroll 1
   for (int kk = 0; kk < TILE / KV; ++kk) {
+    const uint32_t poff = (kk / 4) * 16384 + (kk % 4) * 32;
     const uint64_t bd = sdesc_add(vd, kk * KV * 128);
+    const uint32_t acc = (first && kk == 0) ? 0u : 1u;
     if (FP8)
-      mma_f8_ts(o_tmem, p_tmem + kk * 8, bd, id, (first && kk == 0) ? 0u : 1u);
+      mma_f8_ss(o_tmem, sdesc_add(pd, poff), bd, id, acc);
     else
-      mma_f16_ts(o_tmem, p_tmem + kk * 8, bd, id, (first && kk == 0) ? 0u : 1u);
+      mma_f16_ss(o_tmem, sdesc_add(pd, poff), bd, id, acc);
   }
   if (!FP8 && with_lo) {
 #pragma unroll 1
-    for (int kk = 0; kk < TILE / 16; ++kk) {
-      const uint64_t bd = sdesc_add(vd, kk * 16 * 128);
-      mma_f16_ts(o_tmem, p_tmem + 64 + kk * 8, bd, id, 1u);
-    }
+    for (int kk = 0; kk < TILE / 16; ++kk)
+      mma_f16_ts(o_tmem, lo_tmem + kk * 8, sdesc_add(vd, kk * 16 * 128), id, 1u);
   }
 }
 
@@ -143,51 +158,54 @@ __device__ __forceinline__ float sum_acc(const uint64_t (&acc)[4]) {
 }
 
 // P = 2^(mul * s - mu) for the 128 columns of this thread's row (mul folds
-// the softmax scale in; 1 when s already holds log2-unit logits), packed to
-// bf16 and written over S in TMEM (columns 0..63); with LO the rounding
-// residual p - bf16(p) goes to columns 64..127.  Returns the row sum of P.
+// the softmax scale in; 1 when s already holds log2-unit logits), as packed
+// bf16 written in place into s[0..63] (s[k] = columns 2k, 2k+1; step k reads
+// only s[2k], s[2k+1], so no unread score is overwritten) and, with LO, the
+// rounding residual p - bf16(p) in lo[0..63].  Returns the row sum of P.
 template <bool LO>
-__device__ __forceinline__ float store_p(const uint32_t (&s)[128], float mul, float mu, uint32_t tS) {
+__device__ __forceinline__ float exp_bf16(uint32_t (&s)[128], uint32_t (&lo)[64], float mul, float mu) {
   const uint64_t mul2 = f2_pack(mul, mul), nmu2 = f2_pack(-mu, -mu);
   uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t ph[32];
-    uint32_t pl[32];
-#pragma unroll
-    for (int w = 0; w < 32; ++w) {
-      const int c = h * 64 + 2 * w;
-      float y0, y1;
-      f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), mul2, nmu2), y0, y1);
-      const float p0 = ex2(y0), p1 = ex2(y1);
-      acc[w & 3] = f2_add(acc[w & 3], f2_pack(p0, p1));
-      ph[w] = pack_bf16(p0, p1);
-      if (LO) pl[w] = pack_bf16(p0 - bf16lo_f32(ph[w]), p1 - bf16hi_f32(ph[w]));
-    }
-    tmem_st32(tS + h * 32, ph);
-    if (LO) tmem_st32(tS + 64 + h * 32, pl);
+  for (int k = 0; k < 64; ++k) {
+    float y0, y1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1])), mul2, nmu2), y0, y1);
+    const float p0 = ex2(y0), p1 = ex2(y1);
+    acc[k & 3] = f2_add(acc[k & 3], f2_pack(p0, p1));
+    const uint32_t hi = pack_bf16(p0, p1);
+    s[k] = hi;
+    if (LO) lo[k] = pack_bf16(p0 - bf16lo_f32(hi), p1 - bf16hi_f32(hi));
   }
   return sum_acc(acc);
 }
 
-// P = 2^(mul * s - mu) rounded to e4m3 (nearest even, saturating), four per
-// TMEM column, over S (columns 0..31).  Returns the row sum of the fp32 P.
-__device__ __forceinline__ float store_p_e4m3(const uint32_t (&s)[128], float mul, float mu, uint32_t tS) {
+// Same for e4m3 P, in place: s[k] holds the codes of columns 4k..4k+3.
+__device__ __forceinline__ float exp_e4m3(uint32_t (&s)[128], float mul, float mu) {
   const uint64_t mul2 = f2_pack(mul, mul), nmu2 = f2_pack(-mu, -mu);
   uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-  uint32_t pw[32];
 #pragma unroll
-  for (int w = 0; w < 32; ++w) {
+  for (int k = 0; k < 32; ++k) {
     float y0, y1, y2, y3;
-    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * w]), __uint_as_float(s[4 * w + 1])), mul2, nmu2), y0, y1);
-    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * w + 2]), __uint_as_float(s[4 * w + 3])), mul2, nmu2), y2, y3);
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * k]), __uint_as_float(s[4 * k + 1])), mul2, nmu2), y0, y1);
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * k + 2]), __uint_as_float(s[4 * k + 3])), mul2, nmu2), y2, y3);
     const float p0 = ex2(y0), p1 = ex2(y1), p2 = ex2(y2), p3 = ex2(y3);
-    acc[(2 * w) & 3] = f2_add(acc[(2 * w) & 3], f2_pack(p0, p1));
-    acc[(2 * w + 1) & 3] = f2_add(acc[(2 * w + 1) & 3], f2_pack(p2, p3));
-    pw[w] = pack_e4m3x4(p0, p1, p2, p3);
+    acc[(2 * k) & 3] = f2_add(acc[(2 * k) & 3], f2_pack(p0, p1));
+    acc[(2 * k + 1) & 3] = f2_add(acc[(2 * k + 1) & 3], f2_pack(p2, p3));
+    s[k] = pack_e4m3x4(p0, p1, p2, p3);
   }
-  tmem_st32(tS, pw);
   return sum_acc(acc);
+}
+
+// Store this thread's P row (row r, `row_bytes` = 256 for bf16, 128 for e4m3)
+// into the 128-byte swizzled K-major tile: 16-byte granule g of the row goes
+// to chunk g / 8, row r, slot (g % 8) ^ (r % 8).
+template <int NWORDS>
+__device__ __forceinline__ void store_p_smem(uint8_t* tile, int r, const uint32_t (&w)[128]) {
+#pragma unroll
+  for (int g = 0; g < NWORDS / 4; ++g) {
+    const uint32_t addr = (uint32_t)((g >> 3) * 16384 + r * 128 + (((g & 7) ^ (r & 7)) << 4));
+    *reinterpret_cast<uint4*>(tile + addr) = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+  }
 }
 
 template <int D, bool MODS, bool FP8>
@@ -215,17 +233,17 @@ __global__ void __launch_bounds__(384, 1)
     S.abort = 0;
     mbar_init(&S.q_full, 1);
     for (int s = 0; s < 4; ++s) {
-      mbar_init(&S.k_full[s], 1);
-      mbar_init(&S.k_empty[s], 1);
-      mbar_init(&S.v_full[s], 1);
-      mbar_init(&S.v_empty[s], 1);
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 2);  // one commit from each MMA issuer
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&S.s_full[t], 1);
+      mbar_init(&S.s_free[t], 128);
       mbar_init(&S.p_full[t], 128);
       mbar_init(&S.o_full[t], 1);
     }
-    mbar_init(&S.mma_drain, 1);
+    mbar_init(&S.mma_drain[0], 1);
+    mbar_init(&S.mma_drain[1], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -236,12 +254,14 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   const uint32_t sQ = smem_u32(smem + C::Q_OFF);
-  const uint32_t sK = smem_u32(smem + C::K_OFF);
-  const uint32_t sV = smem_u32(smem + C::V_OFF);
+  const uint32_t sR = smem_u32(smem + C::R_OFF);
+  const uint32_t sP = smem_u32(smem + C::P_OFF);
 
   if (warp < 4) regs_dec<C::REGS_LOW>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // Ring order = consumption order: K(J0), then per union tile J:
+    // K(next J) before V(J).
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
@@ -251,101 +271,113 @@ __global__ void __launch_bounds__(384, 1)
         for (int ch = 0; ch < C::CH; ++ch)
           tma_load_3d(smem + C::Q_OFF + t * C::TILE_BYTES + ch * 16384, &tq, &S.q_full, ch * C::BOX,
                       (I0 + t) * TILE, b * p.Hq + hq);
-      int kit = 0, vit = 0;
-      for (int J = union_next(p, b, I0, 0, J_end); J < J_end; J = union_next(p, b, I0, J + 1, J_end)) {
-        const int ks = kit % C::KST;
-        if (!mbar_wait(&S.k_empty[ks], ((kit / C::KST) & 1) ^ 1, ab)) break;
-        mbar_arrive_tx(&S.k_full[ks], C::TILE_BYTES);
+      int r = 0;
+      auto load = [&](const CUtensorMap* map, int J) -> bool {
+        const int st = r % C::RST;
+        if (!mbar_wait(&S.empty[st], ((r / C::RST) & 1) ^ 1, ab)) return false;
+        mbar_arrive_tx(&S.full[st], C::TILE_BYTES);
         for (int ch = 0; ch < C::CH; ++ch)
-          tma_load_3d(smem + C::K_OFF + ks * C::TILE_BYTES + ch * 16384, &tk, &S.k_full[ks],
-                      ch * C::BOX, J * TILE, b * p.Hkv + hk);
-        ++kit;
-        const int vs = vit % C::VST;
-        if (!mbar_wait(&S.v_empty[vs], ((vit / C::VST) & 1) ^ 1, ab)) break;
-        mbar_arrive_tx(&S.v_full[vs], C::TILE_BYTES);
-        for (int ch = 0; ch < C::CH; ++ch)
-          tma_load_3d(smem + C::V_OFF + vs * C::TILE_BYTES + ch * 16384, &tv, &S.v_full[vs],
-                      ch * C::BOX, J * TILE, b * p.Hkv + hk);
-        ++vit;
+          tma_load_3d(smem + C::R_OFF + st * C::TILE_BYTES + ch * 16384, map, &S.full[st], ch * C::BOX,
+                      J * TILE, b * p.Hkv + hk);
+        ++r;
+        return true;
+      };
+      int J = union_next(p, b, I0, 0, J_end);
+      bool ok = J >= J_end || load(&tk, J);
+      while (ok && J < J_end) {
+        const int Jn = union_next(p, b, I0, J + 1, J_end);
+        if (Jn < J_end && !(ok = load(&tk, Jn))) break;
+        if (!(ok = load(&tv, J))) break;
+        J = Jn;
       }
       // Let every copy this thread issued land before the CTA can exit: the
-      // last load into each stage completes phase ((n_loads - 1) & 1).
+      // last load into each stage completes phase ((loads into it - 1) & 1).
       mbar_wait_drain(&S.q_full, 0);
-      for (int s = 0; s < C::KST; ++s)
-        if (kit > s) mbar_wait_drain(&S.k_full[s], ((kit - 1 - s) / C::KST) & 1);
-      for (int s = 0; s < C::VST; ++s)
-        if (vit > s) mbar_wait_drain(&S.v_full[s], ((vit - 1 - s) / C::VST) & 1);
+      for (int s = 0; s < C::RST; ++s)
+        if (r > s) mbar_wait_drain(&S.full[s], ((r - 1 - s) / C::RST) & 1);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ---------------------------------------------------------- MMA issuers
+    // One issuing thread per Q tile (warp 1: tile 0, warp 2: tile 1).  The
+    // tensor pipe queues few MMAs, so a thread that waits on a barrier leaves
+    // it idle; two independent issuers keep it fed while either one waits.
     if (lane == 0) {
-      int npv[2] = {0, 0};
+      const int t = warp - 1;
+      const int I = I0 + t;
+      const uint32_t s_tm = tmem + (uint32_t)t * 128;
+      const uint32_t o_tm = tmem + C::O_COL + (uint32_t)t * D;
+      const uint32_t q_sm = sQ + t * C::TILE_BYTES;
+      const uint32_t p_sm = sP + t * C::P_BYTES;
       bool ok = mbar_wait(&S.q_full, 0, ab);
       tc_fence_after();
-      int J = union_next(p, b, I0, 0, J_end);
-      int c0 = 0, c1 = 0;
-      if (ok && J < J_end) {
-        c0 = tile_class(p, b, I0, J);
-        c1 = tile_class(p, b, I0 + 1, J);
-        ok = mbar_wait(&S.k_full[0], 0, ab);
+      int r = 0;    // ring slots consumed
+      int nk = 0;   // S tiles issued
+      int npv = 0;  // P V issued
+      auto slot = [&](int& st) -> bool {  // wait for the next ring slot
+        st = r % C::RST;
+        const bool good = mbar_wait(&S.full[st], (r / C::RST) & 1, ab);
+        ++r;
         tc_fence_after();
+        return good;
+      };
+      auto issue_S = [&](uint32_t k_sm) {
+        issue_nt<FP8, 128>(s_tm, q_sm, k_sm, C::ROW_BYTES, false);
+        mma_commit(&S.s_full[t]);
+        ++nk;
+      };
+      int J = union_next(p, b, I0, 0, J_end);
+      int c = CLS_SKIP;
+      if (ok && J < J_end) {
+        int ks;
+        ok = slot(ks);
+        c = tile_class(p, b, I, J);
         if (ok) {
-          if (c0 != CLS_SKIP) { issue_S<D, FP8>(tmem + 0, sQ, sK); mma_commit(&S.s_full[0]); }
-          if (c1 != CLS_SKIP) { issue_S<D, FP8>(tmem + 128, sQ + C::TILE_BYTES, sK); mma_commit(&S.s_full[1]); }
-          mma_commit(&S.k_empty[0]);
+          if (c != CLS_SKIP) issue_S(sR + ks * C::TILE_BYTES);
+          mma_commit(&S.empty[ks]);
         }
       }
-      int it = 0;
       while (ok && J < J_end) {
         const int Jn = union_next(p, b, I0, J + 1, J_end);
         const bool has_next = Jn < J_end;
-        const int n0 = has_next ? tile_class(p, b, I0, Jn) : CLS_SKIP;
-        const int n1 = has_next ? tile_class(p, b, I0 + 1, Jn) : CLS_SKIP;
-        const int vs = it % C::VST;
-        const int ksn = (it + 1) % C::KST;
-        const uint32_t vsm = sV + vs * C::TILE_BYTES;
-        const uint32_t ksm = sK + ksn * C::TILE_BYTES;
-        if (!(ok = mbar_wait(&S.v_full[vs], (it / C::VST) & 1, ab))) break;
-        bool k_ready = false;
-        if (c0 != CLS_SKIP) {
-          if (!(ok = mbar_wait(&S.p_full[0], npv[0] & 1, ab))) break;
-          tc_fence_after();
-          issue_PV<D, FP8>(tmem + C::O_COL, tmem + 0, vsm, npv[0] == 0, c0 == CLS_PARTIAL);
-          mma_commit(&S.o_full[0]);
-          ++npv[0];
-        }
-        if (n0 != CLS_SKIP) {
-          if (!(ok = mbar_wait(&S.k_full[ksn], ((it + 1) / C::KST) & 1, ab))) break;
-          k_ready = true;
-          tc_fence_after();
-          issue_S<D, FP8>(tmem + 0, sQ, ksm);
-          mma_commit(&S.s_full[0]);
-        }
-        if (c1 != CLS_SKIP) {
-          if (!(ok = mbar_wait(&S.p_full[1], npv[1] & 1, ab))) break;
-          tc_fence_after();
-          issue_PV<D, FP8>(tmem + C::O_COL + D, tmem + 128, vsm, npv[1] == 0, c1 == CLS_PARTIAL);
-          mma_commit(&S.o_full[1]);
-          ++npv[1];
-        }
-        if (n1 != CLS_SKIP) {
-          if (!k_ready) {
-            if (!(ok = mbar_wait(&S.k_full[ksn], ((it + 1) / C::KST) & 1, ab))) break;
-            tc_fence_after();
+        const int n = has_next ? tile_class(p, b, I, Jn) : CLS_SKIP;
+        // Partial bf16 tiles keep their P residual in the S columns: their
+        // S(Jn) goes after P V.
+        const bool late = !FP8 && c == CLS_PARTIAL;
+        int ks = 0, vs = 0;
+        if (has_next) {
+          if (!(ok = slot(ks))) break;
+          // Early S(Jn): the S columns are free once the softmax copied S(J)
+          // out (at once if this tile skipped J).
+          if (n != CLS_SKIP && !late) {
+            if (c != CLS_SKIP) {
+              if (!(ok = mbar_wait(&S.s_free[t], (nk - 1) & 1, ab))) break;
+              tc_fence_after();
+            }
+            issue_S(sR + ks * C::TILE_BYTES);
           }
-          issue_S<D, FP8>(tmem + 128, sQ + C::TILE_BYTES, ksm);
-          mma_commit(&S.s_full[1]);
+          if (!late) mma_commit(&S.empty[ks]);
         }
-        if (has_next) mma_commit(&S.k_empty[ksn]);
-        mma_commit(&S.v_empty[vs]);
+        if (!(ok = slot(vs))) break;
+        if (c != CLS_SKIP) {
+          if (!(ok = mbar_wait(&S.p_full[t], npv & 1, ab))) break;
+          tc_fence_after();
+          issue_pv<D, FP8>(o_tm, p_sm, sR + vs * C::TILE_BYTES, npv == 0, c == CLS_PARTIAL, s_tm);
+          mma_commit(&S.o_full[t]);
+          ++npv;
+          if (late && n != CLS_SKIP) {
+            if (!(ok = mbar_wait(&S.s_free[t], (nk - 1) & 1, ab))) break;
+            tc_fence_after();
+            issue_S(sR + ks * C::TILE_BYTES);
+          }
+        }
+        if (has_next && late) mma_commit(&S.empty[ks]);
+        mma_commit(&S.empty[vs]);
         J = Jn;
-        c0 = n0;
-        c1 = n1;
-        ++it;
+        c = n;
       }
       // Every MMA this thread issued completes before TMEM can be released.
-      mma_commit(&S.mma_drain);
-      mbar_wait_drain(&S.mma_drain, 0);
+      mma_commit(&S.mma_drain[t]);
+      mbar_wait_drain(&S.mma_drain[t], 0);
     }
   } else if (warp >= 4) {
     // -------------------------------------------------------------- softmax
@@ -358,6 +390,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + (uint32_t)t * 128;
     const uint32_t tO = tmem + lane_off + C::O_COL + (uint32_t)t * D;
+    uint8_t* p_tile = smem + C::P_OFF + t * C::P_BYTES;
     const bool causal = (p.flags & MOD_CAUSAL) != 0;
     // FP8: the scores are q8.k8 and need the Q and K dequantisation scales.
     const float qk_scale = FP8 ? p.scale * scales[b * p.Hq + hq] * scales[p.B * p.Hq + b * p.Hkv + hk]
@@ -376,6 +409,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int J = 0; J < J_end; ++J) {
       const int cls = tile_class(p, b, I, J);
       if (cls == CLS_SKIP) continue;
+      const bool partial = cls == CLS_PARTIAL;
       if (!(ok = wait_warp(&S.s_full[t], ns & 1, ab))) break;
       tc_fence_after();
       uint32_t s[128];
@@ -384,6 +418,10 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld32(tS + q4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[q4 * 32]));
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(&s[q4 * 32]));
+      if (!partial || FP8) {  // S is in registers: hand the columns back to the MMA
+        tc_fence_before();
+        mbar_arrive(&S.s_free[t]);
+      }
 
       // Scores in log2 units, masked on partial tiles.
       const int j0 = J * TILE;
@@ -393,7 +431,7 @@ __global__ void __launch_bounds__(384, 1)
       if (!MODS) {
         // Raw scores: the scale is positive, so it commutes with the max and
         // is folded into the exponential's FMA.
-        if (cls == CLS_PARTIAL) {
+        if (partial) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c > hi_lim) s[c] = __float_as_uint(-INFINITY);
@@ -414,7 +452,7 @@ __global__ void __launch_bounds__(384, 1)
           float x = __uint_as_float(s[c]);
           x = sc ? tanh_exp(x * rm.sc_in) * rm.sc_out : x * scale_log2;
           if (al) x = fmaf(rm.alibi_l2, (float)c, x + al_row);
-          if (cls == CLS_PARTIAL) {
+          if (partial) {
             bool valid = (c <= hi_lim) && (c > lo_lim);
             if (doc && valid) valid = (__ldg(drow + c) == rm.doc_i);
             if (!valid) x = -INFINITY;
@@ -424,20 +462,36 @@ __global__ void __launch_bounds__(384, 1)
         mt = row_max128(s);
       }
 
-      // Running max; O is rescaled only when some row's max grew by > 2^8.
+      // Running max: it moves only when some row's max grew by > 2^8.
       const float mn = fmaxf(m, mt);
+      bool need = false;
+      float alpha = 1.0f;
       if (ns == 0) {
         m = mn;
       } else {
-        const bool need = mn > m + RESCALE_THRESHOLD;
+        need = mn > m + RESCALE_THRESHOLD;
+        if (need) {
+          alpha = ex2(m - mn);
+          l *= alpha;
+          m = mn;
+        }
+      }
+      const float mu = (m == -INFINITY) ? 0.f : m;
+
+      // P into registers (the previous P V may still be reading P's buffer).
+      uint32_t lo[64];
+      if (FP8)
+        l += exp_e4m3(s, mul, mu);
+      else if (partial)
+        l += exp_bf16<true>(s, lo, mul, mu);
+      else
+        l += exp_bf16<false>(s, lo, mul, mu);
+
+      // The previous P V must be done before O is rescaled or P overwritten.
+      if (ns > 0) {
+        if (!(ok = wait_warp(&S.o_full[t], (ns - 1) & 1, ab))) break;
+        tc_fence_after();
         if (__any_sync(0xffffffffu, need)) {
-          if (!(ok = wait_warp(&S.o_full[t], (ns - 1) & 1, ab))) break;
-          tc_fence_after();
-          const float alpha = need ? ex2(m - mn) : 1.0f;
-          if (need) {
-            l *= alpha;
-            m = mn;
-          }
 #pragma unroll
           for (int q4 = 0; q4 < D / 32; ++q4) {
             uint32_t ov[32];
@@ -447,20 +501,21 @@ __global__ void __launch_bounds__(384, 1)
             for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
             tmem_st32(tO + q4 * 32, ov);
           }
-          tmem_wait_st();
         }
       }
-      const float mu = (m == -INFINITY) ? 0.f : m;
-
-      // P = 2^(x - m) as bf16 (hi, plus lo on partial tiles) over S in TMEM.
-      if (FP8)
-        l += store_p_e4m3(s, mul, mu, tS);
-      else if (cls == CLS_PARTIAL)
-        l += store_p<true>(s, mul, mu, tS);
-      else
-        l += store_p<false>(s, mul, mu, tS);
+      if (FP8) {
+        store_p_smem<32>(p_tile, r, s);
+      } else {
+        store_p_smem<64>(p_tile, r, s);
+        if (partial) {  // residual of P into the (now unused) S columns, for the TS MMA
+          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&lo[0]));
+          tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&lo[32]));
+        }
+      }
       tmem_wait_st();
+      fence_async_smem();
       tc_fence_before();
+      if (partial && !FP8) mbar_arrive(&S.s_free[t]);
       mbar_arrive(&S.p_full[t]);
       ++ns;
     }
