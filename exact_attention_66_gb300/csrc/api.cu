@@ -159,6 +159,12 @@ bool has_score_mods(uint32_t flags) {
   return (flags & (ATTN_MOD_WINDOW | ATTN_MOD_DOC | ATTN_MOD_SOFTCAP | ATTN_MOD_ALIBI)) != 0;
 }
 
+// Backward row statistics: one {LSE * log2(e), D} pair per query row, rows
+// padded to whole 128-row tiles so that every tile's pairs are 16-byte aligned.
+size_t bwd_rowstat_bytes(int B, int Hq, int N) {
+  return round_up((size_t)B * Hq * ((N + 127) / 128) * 128 * sizeof(float2), 256);
+}
+
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
 }  // namespace
@@ -175,7 +181,7 @@ size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int N, int d, const a
     case ATTN_OP_FWD_FP8:
       return needs_map(f) ? map_bytes(B, N) : 0;
     case ATTN_OP_BWD:
-      return round_up((size_t)B * Hq * N * sizeof(float), 256) + (needs_map(f) ? map_bytes(B, N) : 0);
+      return bwd_rowstat_bytes(B, Hq, N) + (needs_map(f) ? map_bytes(B, N) : 0);
     case ATTN_OP_QUANT_FP8:
       return round_up((size_t)(B * Hq + 2 * B * Hkv) * sizeof(unsigned), 256);
     default:
@@ -248,9 +254,9 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   L.dk = dk;
   L.dv = dv;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
-  L.delta = reinterpret_cast<float*>(wsb);
+  L.rowstat = reinterpret_cast<float2*>(wsb);
   if (needs_map(L.p.flags)) {
-    uint8_t* map = wsb + round_up((size_t)B * Hq * N * sizeof(float), 256);
+    uint8_t* map = wsb + bwd_rowstat_bytes(B, Hq, N);
     if ((st = cuda_status(launch_block_map(L.p, map, s))) != ATTN_OK) return st;
     L.p.map = map;
   }

@@ -33,18 +33,28 @@
 namespace attn {
 
 // ------------------------------------------------------------------ bwd_pre
+// Row statistics of the backward, one pair per query row, rows padded to whole
+// 128-row tiles: {LSE * log2(e), D = rowsum(dO * O)}.  Padding rows and rows
+// with no allowed key get +inf (so that P = exp2(x - inf) = 0) and D = 0.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dout,
-                                                      float* __restrict__ delta, long long rows) {
+                                                      const float* __restrict__ lse,
+                                                      float2* __restrict__ rowstat, int N,
+                                                      long long rows_padded) {
   constexpr int TPR = D / 8;  // threads per row, 8 bf16 each
   const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = gt / TPR;
   const int part = (int)(gt % TPR);
+  const long long np = (long long)((N + TILE - 1) / TILE) * TILE;
+  const long long bh = row / np;
+  const int i = (int)(row - bh * np);
+  const bool real = row < rows_padded && i < N;
   float acc = 0.f;
-  if (row < rows) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * D) + part);
-    const uint4 g = __ldg(reinterpret_cast<const uint4*>(dout + row * D) + part);
+  if (real) {
+    const long long src = bh * N + i;
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + src * D) + part);
+    const uint4 g = __ldg(reinterpret_cast<const uint4*>(dout + src * D) + part);
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
     const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
@@ -55,23 +65,26 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   }
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && part == 0) delta[row] = acc;
-}
-
-// log2-unit LSE of a row; +inf (so that P = 0) past N or for rows with no key.
-__device__ __forceinline__ float lse_log2(const float* lse, size_t idx, bool in_range) {
-  if (!in_range) return INFINITY;
-  const float v = lse[idx];
-  return v == -INFINITY ? INFINITY : v * LOG2E;
+  if (row < rows_padded && part == 0) {
+    float l2 = INFINITY;
+    if (real) {
+      const float v = lse[bh * N + i];
+      l2 = v == -INFINITY ? INFINITY : v * LOG2E;
+    }
+    rowstat[row] = make_float2(l2, acc);
+  }
 }
 
 // D(tmem, 128 x 128) = A B^T, A and B K-major 128-byte swizzled tiles of
-// `row_bytes` per row (16 KB column chunks), one MMA per 32 bytes of a row.
-__device__ __forceinline__ void issue_nt(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, int row_bytes) {
+// ROW_BYTES per row (16 KB column chunks), one MMA per 32 bytes of a row.
+// Issue loops are unrolled: the tensor pipe queues few MMAs, and a rolled
+// loop's per-iteration overhead in the issuing thread leaves it idle.
+template <int ROW_BYTES>
+__device__ __forceinline__ void issue_nt(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
   constexpr uint32_t id = idesc_bf16(128, 128, false, false);
   const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, 16, 1024);
-#pragma unroll 1
-  for (int kk = 0; kk < row_bytes / 32; ++kk) {
+#pragma unroll
+  for (int kk = 0; kk < ROW_BYTES / 32; ++kk) {
     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
     mma_f16_ss(d_tmem, sdesc_add(ad, off), sdesc_add(bd, off), id, kk > 0 ? 1u : 0u);
   }
@@ -83,7 +96,7 @@ template <int D>
 __device__ __forceinline__ void issue_nt_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem) {
   constexpr uint32_t id = idesc_bf16(128, 128, false, false);
   const uint64_t bd = sdesc_sw128(b_smem, 16, 1024);
-#pragma unroll 1
+#pragma unroll
   for (int kk = 0; kk < D / 16; ++kk)
     mma_f16_ts(d_tmem, a_tmem + kk * 8, sdesc_add(bd, (kk / 4) * 16384 + (kk % 4) * 32), id,
                kk > 0 ? 1u : 0u);
@@ -109,18 +122,18 @@ __device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int r, uin
 }
 
 // D(tmem, 128 x D) += A(128 x 128 keys) B(128 keys x D, MN-major in shared
-// memory).  A is a K-major shared-memory tile (a_tmem == 0) or packed bf16 in
-// TMEM (a_smem ignored).
-template <int D>
+// memory).  A is a K-major shared-memory tile (A_TMEM false; a_tmem ignored)
+// or packed bf16 in TMEM (A_TMEM true; a_smem ignored).
+template <int D, bool A_TMEM>
 __device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_smem, uint32_t a_tmem,
                                           uint32_t b_smem, bool first) {
   constexpr uint32_t id = idesc_bf16(128, D, false, true);
   const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, 16384, 1024);
-#pragma unroll 1
+#pragma unroll
   for (int kk = 0; kk < TILE / 16; ++kk) {
     const uint32_t acc = (first && kk == 0) ? 0u : 1u;
     const uint64_t b = sdesc_add(bd, kk * 16 * 128);
-    if (a_tmem)
+    if (A_TMEM)
       mma_f16_ts(d_tmem, a_tmem + kk * 8, b, id, acc);
     else
       mma_f16_ss(d_tmem, sdesc_add(ad, (kk / 4) * 16384 + (kk % 4) * 32), b, id, acc);
@@ -177,8 +190,8 @@ __device__ __forceinline__ void tmem_wait64(uint32_t (&v)[64]) {
 
 struct BwdBars {
   uint64_t in_full;              // resident tiles
-  uint64_t full[2], empty[2];    // streamed stages (dkdv: Q+dO; dq: K)
-  uint64_t vfull[2], vempty[2];  // dq: V stages
+  uint64_t full[3], empty[3];    // streamed stages (dkdv: Q+dO, 2 used; dq: K)
+  uint64_t vfull[3], vempty[3];  // dq: V stages
   uint64_t s_full, s_free, p_full, acc_done;
   uint64_t a_ready;              // dq: Q and dO copied into TMEM
   uint64_t fin[2];               // per issuer: all its MMAs done
@@ -190,6 +203,14 @@ constexpr int BWD_LAUNCH_REGS = 168, BWD_REGS_LOW = 56, BWD_REGS_HIGH = 224;
 static_assert(128 * BWD_REGS_LOW + 256 * BWD_REGS_HIGH <= 384 * BWD_LAUNCH_REGS, "register split");
 
 // ================================================================== dK, dV
+// Shared memory: K_J, V_J and two stages of (Q_I, dO_I).  TMEM (512 columns):
+//   X   [0, 128)        S^T(n), then dP^T(n) once the softmax has copied S^T out
+//   P^T [128, 192)      packed bf16, A operand of dV += P^T dO
+//   dS^T [192, 256)     packed bf16, A operand of dK += dS^T Q
+//   dV  [256, 256 + D), dK [256 + D, 256 + 2D)  fp32 accumulators
+// Sharing X between S^T and dP^T leaves room for P^T and dS^T in TMEM, so no
+// GEMM of the next step waits for an accumulation of this one, and dV / dK
+// read their A operand from TMEM instead of shared memory.
 template <int D>
 struct KvCfg {
   static constexpr int CH = D / 64;
@@ -197,11 +218,26 @@ struct KvCfg {
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = TB;
   static constexpr int ST_OFF = 2 * TB;  // stage s: Q tile at +0, dO tile at +TB
-  static constexpr int PT_OFF = ST_OFF + 2 * 2 * TB;  // P^T tile, 128 x 128 bf16
-  static constexpr int BAR_OFF = PT_OFF + TILE * TILE * 2;
+  static constexpr int BAR_OFF = ST_OFF + 2 * 2 * TB;
   static constexpr int SMEM_BYTES = smem_one_cta(BAR_OFF + 256 + 1024);
 };
 static_assert(KvCfg<128>::SMEM_BYTES <= 232448, "dK/dV shared memory exceeds 227 KB");
+
+struct KvBars {
+  uint64_t in_full;            // K_J, V_J
+  uint64_t full[2], empty[2];  // Q/dO stages
+  uint64_t s_full;             // S^T(n) in X                (MMA commit)
+  uint64_t xs_free;            // S^T(n) copied out of X     (256 softmax threads)
+  uint64_t dp_full;            // dP^T(n) in X               (MMA commit)
+  uint64_t xd_free;            // dP^T(n) copied out of X    (256)
+  uint64_t p_full;             // P^T(n) stored in TMEM      (256)
+  uint64_t pt_free;            // dV(n) done reading P^T     (MMA commit)
+  uint64_t ds_full;            // dS^T(n) stored in TMEM     (256)
+  uint64_t ds_free;            // dK(n) done reading dS^T    (MMA commit)
+  uint64_t fin;                // every MMA done
+  uint32_t tmem_base;
+  int abort;
+};
 
 // Steps of a dK/dV CTA: query head g of the group (outer), non-skipped Q tile
 // I (inner, ascending).
@@ -225,12 +261,12 @@ template <int D, bool MODS>
 __global__ void __launch_bounds__(384, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                    const float* __restrict__ lse, const float* __restrict__ delta,
-                    __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, const AttnParams p) {
+                    const float2* __restrict__ rowstat, __nv_bfloat16* __restrict__ dk,
+                    __nv_bfloat16* __restrict__ dv, const AttnParams p) {
   using C = KvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  BwdBars& S = *reinterpret_cast<BwdBars*>(smem + C::BAR_OFF);
+  KvBars& S = *reinterpret_cast<KvBars*>(smem + C::BAR_OFF);
   const Abort ab{&S.abort, p.status};
   const int warp = warp_id(), lane = lane_id();
 
@@ -249,14 +285,17 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&S.in_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 2);  // dV issuer and dK issuer
+      mbar_init(&S.empty[s], 1);
     }
-    mbar_init(&S.s_full, 2);      // S^T (issuer A) and dP^T (issuer B)
-    mbar_init(&S.s_free, 256);
+    mbar_init(&S.s_full, 1);
+    mbar_init(&S.xs_free, 256);
+    mbar_init(&S.dp_full, 1);
+    mbar_init(&S.xd_free, 256);
     mbar_init(&S.p_full, 256);
-    mbar_init(&S.acc_done, 1);    // dV(n) done: P^T buffer free
-    mbar_init(&S.fin[0], 1);
-    mbar_init(&S.fin[1], 1);
+    mbar_init(&S.pt_free, 1);
+    mbar_init(&S.ds_full, 256);
+    mbar_init(&S.ds_free, 1);
+    mbar_init(&S.fin, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -269,9 +308,8 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sK = smem_u32(smem + C::K_OFF);
   const uint32_t sV = smem_u32(smem + C::V_OFF);
   const uint32_t sST = smem_u32(smem + C::ST_OFF);
-  const uint32_t sPT = smem_u32(smem + C::PT_OFF);
-  // TMEM: S^T [0,128), dP^T / dS^T [128,256), dV [256, 256+D), dK [256+D, 256+2D).
-  const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+  const uint32_t tX = tmem, tPT = tmem + 128, tDS = tmem + 192;
+  const uint32_t tdV = tmem + 256, tdK = tmem + 256 + D;
 
   if (warp < 4) regs_dec<BWD_REGS_LOW>();
   if (warp == 0) {
@@ -302,12 +340,11 @@ __global__ void __launch_bounds__(384, 1)
       for (int s = 0; s < 2; ++s)
         if (n > s) mbar_wait_drain(&S.full[s], ((n - 1 - s) >> 1) & 1);
     }
-  } else if (warp == 1 || warp == 2) {
-    // ---------------------------------------------------------- MMA issuers
-    // Issuer A (warp 1): S^T = K Q^T and dV += P^T dO.
-    // Issuer B (warp 2): dP^T = V dO^T and dK += dS^T Q.
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // Program order per step n follows the order in which the softmax frees
+    // and fills its buffers: dP(n), dV(n), S(n+1), dK(n).
     if (lane == 0) {
-      const bool A = warp == 1;
       bool ok = mbar_wait(&S.in_full, 0, ab);
       tc_fence_after();
       if (ok && any) {
@@ -315,10 +352,7 @@ __global__ void __launch_bounds__(384, 1)
         ok = mbar_wait(&S.full[0], 0, ab);
         tc_fence_after();
         if (ok) {
-          if (A)
-            issue_nt(tS, sK, sST, D * 2);
-          else
-            issue_nt(tdP, sV, sST + C::TB, D * 2);
+          issue_nt<D * 2>(tX, sK, sST);  // S^T(0) = K Q(0)^T
           mma_commit(&S.s_full);
         }
         while (ok) {
@@ -326,39 +360,38 @@ __global__ void __launch_bounds__(384, 1)
           const uint32_t do_sm = q_sm + C::TB;
           int g2 = g, I2 = I;
           const bool has_next = steps.advance(p, b, g2, I2);
-          const uint32_t qn_sm = sST + ((n + 1) & 1) * 2 * C::TB;
-          if (A && has_next) {
-            // S^T(n+1) as soon as the softmax copied S^T(n) out.
-            if (!(ok = mbar_wait(&S.full[(n + 1) & 1], ((n + 1) >> 1) & 1, ab))) break;
-            if (!(ok = mbar_wait(&S.s_free, n & 1, ab))) break;
-            tc_fence_after();
-            issue_nt(tS, sK, qn_sm, D * 2);
-            mma_commit(&S.s_full);
-          }
+          // dP^T(n) = V dO(n)^T into X once S^T(n) has been copied out.
+          if (!(ok = mbar_wait(&S.xs_free, n & 1, ab))) break;
+          tc_fence_after();
+          issue_nt<D * 2>(tX, sV, do_sm);
+          mma_commit(&S.dp_full);
+          // dV += P^T(n) dO(n).
           if (!(ok = mbar_wait(&S.p_full, n & 1, ab))) break;
           tc_fence_after();
-          if (A) {
-            issue_acc<D>(tdV, sPT, 0, do_sm, n == 0);
-            mma_commit(&S.acc_done);
-          } else {
-            issue_acc<D>(tdK, 0, tdP, q_sm, n == 0);
-          }
-          mma_commit(&S.empty[n & 1]);
-          if (!A && has_next) {
-            // dP^T(n+1) after dK(n) has read dS^T(n) (same columns, in order).
+          issue_acc<D, true>(tdV, 0, tPT, do_sm, n == 0);
+          mma_commit(&S.pt_free);
+          // S^T(n+1) into X once dP^T(n) has been copied out.
+          if (has_next) {
+            if (!(ok = mbar_wait(&S.xd_free, n & 1, ab))) break;
             if (!(ok = mbar_wait(&S.full[(n + 1) & 1], ((n + 1) >> 1) & 1, ab))) break;
             tc_fence_after();
-            issue_nt(tdP, sV, qn_sm + C::TB, D * 2);
+            issue_nt<D * 2>(tX, sK, sST + ((n + 1) & 1) * 2 * C::TB);
             mma_commit(&S.s_full);
           }
+          // dK += dS^T(n) Q(n); the stage is free after it (and dV(n)).
+          if (!(ok = mbar_wait(&S.ds_full, n & 1, ab))) break;
+          tc_fence_after();
+          issue_acc<D, true>(tdK, 0, tDS, q_sm, n == 0);
+          mma_commit(&S.ds_free);
+          mma_commit(&S.empty[n & 1]);
           if (!has_next) break;
           g = g2;
           I = I2;
           ++n;
         }
       }
-      mma_commit(&S.fin[A ? 0 : 1]);
-      mbar_wait_drain(&S.fin[A ? 0 : 1], 0);
+      mma_commit(&S.fin);
+      mbar_wait_drain(&S.fin, 0);
     }
   } else if (warp >= 4) {
     // ---------------------------------------------- softmax / dS warpgroups
@@ -374,7 +407,6 @@ __global__ void __launch_bounds__(384, 1)
     const bool doc = MODS && (p.flags & MOD_DOC);
     const float sc_in = p.scale / p.softcap, sc_out = p.softcap * LOG2E;
     const int doc_j = (doc && j < p.N) ? p.doc_ids[(size_t)b * p.N + j] : 0;
-    uint8_t* pt_tile = smem + C::PT_OFF;
     bool ok = true;
     if (any) {
       int g = 0, I = steps.I_first, n = 0;
@@ -382,89 +414,101 @@ __global__ void __launch_bounds__(384, 1)
         const int hq = hk * G + g;
         const int cls = tile_class(p, b, I, J);
         const float al2 = al ? alibi_slope(p, hq) * LOG2E : 0.f;
-        // LSE (log2 units) and D of this warpgroup's 64 query rows: lane k
-        // holds rows k and 32 + k; loaded before the wait, broadcast below.
+        // {LSE log2, D} of this warpgroup's 64 query rows (columns): lane k
+        // holds rows k and 32 + k, broadcast by shuffles where used.
         const int i0 = I * TILE + 64 * w;  // query row of column 0
-        const size_t rbase = ((size_t)b * p.Hq + hq) * p.N;
-        float my_l2[2], my_dd[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int ii = i0 + 32 * h + lane;
-          my_l2[h] = lse_log2(lse, rbase + ii, ii < p.N);
-          my_dd[h] = ii < p.N ? delta[rbase + ii] : 0.f;
-        }
+        const float2* rs = rowstat + ((size_t)b * p.Hq + hq) * ((size_t)p.nT * TILE) + i0;
+        const float2 rs0 = rs[lane], rs1 = rs[32 + lane];
+        const float my_l2[2] = {rs0.x, rs1.x}, my_dd[2] = {rs0.y, rs1.y};
+
+        // S^T(n) -> registers, X back to the MMA pipe.
         if (!(ok = wait_warp(&S.s_full, n & 1, ab))) break;
         tc_fence_after();
-        uint32_t s[64], dp[64];
-        tmem_ld64(tS + lane_off + 64 * w, s);
-        tmem_ld64(tdP + lane_off + 64 * w, dp);
+        uint32_t s[64];
+        tmem_ld64(tX + lane_off + 64 * w, s);
         tmem_wait64(s);
-        tmem_wait64(dp);
         tc_fence_before();
-        mbar_arrive(&S.s_free);
+        mbar_arrive(&S.xs_free);
 
+        // P = exp2(x - LSE) (0 where masked); s[] keeps P (times the
+        // soft-cap derivative) for dS.
         const int lo = causal ? j - i0 : -0x7fffffff;   // valid iff c >= lo
         const int hi = win ? p.window + j - i0 : 0x7fffffff;  // valid iff c < hi
         const float al_base = al2 * (float)(j - i0);
-        uint32_t pw[32], dw[32];
+        uint32_t pk[32];
 #pragma unroll
-        for (int c4 = 0; c4 < 64; c4 += 16) {
-          float l2[16], dd[16];
+        for (int c = 0; c < 64; c += 2) {
+          float pe[2];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            l2[k] = __shfl_sync(0xffffffffu, my_l2[(c4 + k) >> 5], (c4 + k) & 31);
-            dd[k] = __shfl_sync(0xffffffffu, my_dd[(c4 + k) >> 5], (c4 + k) & 31);
-          }
-#pragma unroll
-          for (int k = 0; k < 16; k += 2) {
-            float pe[2], ds[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int c = c4 + k + e;
-              const float sv = __uint_as_float(s[c]);
-              float x, dmul = 1.f;
-              if (sc) {
-                const float t = tanh_exp(sv * sc_in);
-                x = t * sc_out;
-                dmul = fmaf(-t, t, 1.f);
-              } else {
-                x = sv * p.scale_log2;
-              }
-              if (al) x = fmaf(-al2, (float)c, x + al_base);
-              float pv = ex2(x - l2[k + e]);
-              if (cls == CLS_PARTIAL) {
-                bool valid = (c >= lo) && (c < hi);
-                if (doc && valid)
-                  valid = (i0 + c < p.N) && (__ldg(p.doc_ids + (size_t)b * p.N + i0 + c) == doc_j);
-                if (!valid) pv = 0.f;
-              }
-              pe[e] = pv;
-              ds[e] = pv * (__uint_as_float(dp[c]) - dd[k + e]) * dmul;
+          for (int e = 0; e < 2; ++e) {
+            const int cc = c + e;
+            const float l2 = __shfl_sync(0xffffffffu, my_l2[cc >> 5], cc & 31);
+            const float sv = __uint_as_float(s[cc]);
+            float x, dmul = 1.f;
+            if (sc) {
+              const float t = tanh_exp(sv * sc_in);
+              x = t * sc_out;
+              dmul = fmaf(-t, t, 1.f);
+            } else {
+              x = sv * p.scale_log2;
             }
-            pw[(c4 + k) / 2] = pack_bf16(pe[0], pe[1]);
-            dw[(c4 + k) / 2] = pack_bf16(ds[0], ds[1]);
+            if (al) x = fmaf(-al2, (float)cc, x + al_base);
+            float pv = ex2(x - l2);
+            if (cls == CLS_PARTIAL) {
+              bool valid = (cc >= lo) && (cc < hi);
+              if (doc && valid)
+                valid = (i0 + cc < p.N) && (__ldg(p.doc_ids + (size_t)b * p.N + i0 + cc) == doc_j);
+              if (!valid) pv = 0.f;
+            }
+            pe[e] = pv;
+            s[cc] = __float_as_uint(pv * dmul);
           }
+          pk[c / 2] = pack_bf16(pe[0], pe[1]);
         }
-        // dS^T over dP^T in TMEM (A operand of dK += dS^T Q), packed into the
-        // first 64 columns of dP^T -- which the other warpgroup reads: wait
-        // until all 256 softmax threads have copied dP^T(n) out.
-        if (!(ok = wait_warp(&S.s_free, n & 1, ab))) break;
-        tc_fence_after();
-        tmem_st32(tdP + lane_off + 32 * w, dw);
-        // P^T to shared memory once dV(n-1) has read the previous one.
+        // P^T(n) into TMEM once dV(n-1) has read P^T(n-1).
         if (n > 0) {
-          if (!(ok = wait_warp(&S.acc_done, (n - 1) & 1, ab))) break;
+          if (!(ok = wait_warp(&S.pt_free, (n - 1) & 1, ab))) break;
           tc_fence_after();
         }
-        store_half_row(pt_tile, r, w, pw);
+        tmem_st32(tPT + lane_off + 32 * w, pk);
         tmem_wait_st();
-        fence_async_smem();
         tc_fence_before();
         mbar_arrive(&S.p_full);
+
+        // dP^T(n) -> registers, X back to the MMA pipe.
+        if (!(ok = wait_warp(&S.dp_full, n & 1, ab))) break;
+        tc_fence_after();
+        uint32_t dp[64];
+        tmem_ld64(tX + lane_off + 64 * w, dp);
+        tmem_wait64(dp);
+        tc_fence_before();
+        mbar_arrive(&S.xd_free);
+
+        // dS = P (dP - D) (times the soft-cap derivative).
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int cc = c + e;
+            const float dd = __shfl_sync(0xffffffffu, my_dd[cc >> 5], cc & 31);
+            ds[e] = __uint_as_float(s[cc]) * (__uint_as_float(dp[cc]) - dd);
+          }
+          pk[c / 2] = pack_bf16(ds[0], ds[1]);
+        }
+        // dS^T(n) into TMEM once dK(n-1) has read dS^T(n-1).
+        if (n > 0) {
+          if (!(ok = wait_warp(&S.ds_free, (n - 1) & 1, ab))) break;
+          tc_fence_after();
+        }
+        tmem_st32(tDS + lane_off + 32 * w, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&S.ds_full);
         ++n;
       } while (steps.advance(p, b, g, I));
     }
-    if (ok) ok = wait_warp(&S.fin[0], 0, ab) && wait_warp(&S.fin[1], 0, ab);
+    if (ok) ok = wait_warp(&S.fin, 0, ab);
     tc_fence_after();
     if (ok) {
       const size_t row = ((size_t)b * p.Hkv + hk) * p.N + j;
@@ -482,17 +526,22 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ======================================================================= dQ
+// Shared memory: six 128 x D bf16 slots and the dS tile.  K/V tile pair n sits
+// in slots (2 (n mod 3), 2 (n mod 3) + 1); Q and dO are first loaded into
+// slots 4 and 5, copied into TMEM by the softmax warpgroups, and their slots
+// then join the ring as its third stage.
 template <int D>
 struct DqCfg {
   static constexpr int CH = D / 64;
   static constexpr int TB = TILE * D * 2;
-  static constexpr int Q_OFF = 0;
-  static constexpr int DO_OFF = TB;
-  static constexpr int K_OFF = 2 * TB;  // 2 K stages
-  static constexpr int V_OFF = 4 * TB;  // 2 V stages
-  static constexpr int DS_OFF = 6 * TB; // dS tile, 128 x 128 bf16
+  static constexpr int STAGES = 3;
+  static constexpr int Q_OFF = 4 * TB;
+  static constexpr int DO_OFF = 5 * TB;
+  static constexpr int DS_OFF = 6 * TB;  // dS tile, 128 x 128 bf16
   static constexpr int BAR_OFF = DS_OFF + TILE * TILE * 2;
   static constexpr int SMEM_BYTES = smem_one_cta(BAR_OFF + 256 + 1024);
+  __host__ __device__ static constexpr int k_off(int st) { return 2 * st * TB; }
+  __host__ __device__ static constexpr int v_off(int st) { return (2 * st + 1) * TB; }
 };
 static_assert(DqCfg<128>::SMEM_BYTES <= 232448, "dQ shared memory exceeds 227 KB");
 
@@ -500,8 +549,8 @@ template <int D, bool MODS>
 __global__ void __launch_bounds__(384, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                  const float* __restrict__ lse, const float* __restrict__ delta,
-                  __nv_bfloat16* __restrict__ dq, const AttnParams p) {
+                  const float2* __restrict__ rowstat, __nv_bfloat16* __restrict__ dq,
+                  const AttnParams p) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -525,7 +574,7 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     S.abort = 0;
     mbar_init(&S.in_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 2);   // K: read by S (A) and dQ (B)
       mbar_init(&S.vfull[s], 1);
@@ -535,7 +584,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&S.s_free, 256);
     mbar_init(&S.p_full, 256);
     mbar_init(&S.acc_done, 1);     // dQ(n) done: dS buffer free
-    mbar_init(&S.a_ready, 256);    // Q / dO in TMEM
+    mbar_init(&S.a_ready, 256);    // Q / dO in TMEM: slots 4 and 5 free
     mbar_init(&S.fin[0], 1);
     mbar_init(&S.fin[1], 1);
     fence_mbar_init();
@@ -547,10 +596,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
-  const uint32_t sQ = smem_u32(smem + C::Q_OFF);
-  const uint32_t sDO = smem_u32(smem + C::DO_OFF);
-  const uint32_t sK = smem_u32(smem + C::K_OFF);
-  const uint32_t sV = smem_u32(smem + C::V_OFF);
+  const uint32_t sbase = smem_u32(smem);
   const uint32_t sDS = smem_u32(smem + C::DS_OFF);
   // TMEM: S [0,128), dP [128,256), dQ [256, 256+D), then Q and dO as packed
   // bf16 A operands (D / 2 columns each): the recompute GEMMs S = Q K^T and
@@ -566,26 +612,29 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_3d(smem + C::Q_OFF + ch * 16384, &tq, &S.in_full, ch * 64, I * TILE, b * p.Hq + hq);
         tma_load_3d(smem + C::DO_OFF + ch * 16384, &tdo, &S.in_full, ch * 64, I * TILE, b * p.Hq + hq);
       }
-      int nk = 0, nv = 0;
+      int nk = 0, nv = 0;  // K / V loads issued
       for (int J = J_first; J < J_end; J = next_J(J + 1)) {
-        const int st = nk & 1;
-        if (!mbar_wait(&S.empty[st], ((nk >> 1) & 1) ^ 1, ab)) break;
+        const int st = nk % C::STAGES;
+        const uint32_t ph = ((nk / C::STAGES) & 1) ^ 1;
+        if (nk == C::STAGES - 1 && !mbar_wait(&S.a_ready, 0, ab)) break;
+        if (!mbar_wait(&S.empty[st], ph, ab)) break;
         mbar_arrive_tx(&S.full[st], C::TB);
         for (int ch = 0; ch < C::CH; ++ch)
-          tma_load_3d(smem + C::K_OFF + st * C::TB + ch * 16384, &tk, &S.full[st], ch * 64, J * TILE,
+          tma_load_3d(smem + C::k_off(st) + ch * 16384, &tk, &S.full[st], ch * 64, J * TILE,
                       b * p.Hkv + hk);
         ++nk;
-        if (!mbar_wait(&S.vempty[st], ((nv >> 1) & 1) ^ 1, ab)) break;
+        if (!mbar_wait(&S.vempty[st], ph, ab)) break;
         mbar_arrive_tx(&S.vfull[st], C::TB);
         for (int ch = 0; ch < C::CH; ++ch)
-          tma_load_3d(smem + C::V_OFF + st * C::TB + ch * 16384, &tv, &S.vfull[st], ch * 64, J * TILE,
+          tma_load_3d(smem + C::v_off(st) + ch * 16384, &tv, &S.vfull[st], ch * 64, J * TILE,
                       b * p.Hkv + hk);
         ++nv;
       }
+      // Loads still in flight must land before the CTA exits.
       mbar_wait_drain(&S.in_full, 0);
-      for (int s = 0; s < 2; ++s) {
-        if (nk > s) mbar_wait_drain(&S.full[s], ((nk - 1 - s) >> 1) & 1);
-        if (nv > s) mbar_wait_drain(&S.vfull[s], ((nv - 1 - s) >> 1) & 1);
+      for (int s = 0; s < C::STAGES; ++s) {
+        if (nk > s) mbar_wait_drain(&S.full[s], ((nk - 1 - s) / C::STAGES) & 1);
+        if (nv > s) mbar_wait_drain(&S.vfull[s], ((nv - 1 - s) / C::STAGES) & 1);
       }
     }
   } else if (warp == 1 || warp == 2) {
@@ -596,22 +645,24 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       int n = 0;
       for (int J = J_first; ok && J < J_end; J = next_J(J + 1), ++n) {
-        const int st = n & 1;
-        if (!(ok = mbar_wait(&S.full[st], (n >> 1) & 1, ab))) break;
+        const int st = n % C::STAGES;
+        const uint32_t ph = (n / C::STAGES) & 1;
+        const uint32_t k_sm = sbase + C::k_off(st), v_sm = sbase + C::v_off(st);
+        if (!(ok = mbar_wait(&S.full[st], ph, ab))) break;
         if (A) {
-          if (!(ok = mbar_wait(&S.vfull[st], (n >> 1) & 1, ab))) break;
+          if (!(ok = mbar_wait(&S.vfull[st], ph, ab))) break;
           if (n == 0 && !(ok = mbar_wait(&S.a_ready, 0, ab))) break;
           if (n > 0 && !(ok = mbar_wait(&S.s_free, (n - 1) & 1, ab))) break;
           tc_fence_after();
-          issue_nt_tmem_a<D>(tS, tQa, sK + st * C::TB);
-          issue_nt_tmem_a<D>(tdP, tDOa, sV + st * C::TB);
+          issue_nt_tmem_a<D>(tS, tQa, k_sm);
+          issue_nt_tmem_a<D>(tdP, tDOa, v_sm);
           mma_commit(&S.s_full);
           mma_commit(&S.vempty[st]);
           mma_commit(&S.empty[st]);
         } else {
           if (!(ok = mbar_wait(&S.p_full, n & 1, ab))) break;
           tc_fence_after();
-          issue_acc<D>(tdQ, sDS, 0, sK + st * C::TB, n == 0);
+          issue_acc<D, false>(tdQ, sDS, 0, k_sm, n == 0);
           mma_commit(&S.acc_done);
           mma_commit(&S.empty[st]);
         }
@@ -633,8 +684,8 @@ __global__ void __launch_bounds__(384, 1)
     const float sc_in = p.scale / p.softcap, sc_out = p.softcap * LOG2E;
     const float al2 = al ? alibi_slope(p, hq) * LOG2E : 0.f;
     const size_t row = ((size_t)b * p.Hq + hq) * p.N + i;
-    const float lse2 = lse_log2(lse, row, i < p.N);
-    const float dd = i < p.N ? delta[row] : 0.f;
+    const float2 rs = rowstat[((size_t)b * p.Hq + hq) * ((size_t)p.nT * TILE) + i];
+    const float lse2 = rs.x, dd = rs.y;
     const int doc_i = (doc && i < p.N) ? p.doc_ids[(size_t)b * p.N + i] : 0;
     uint8_t* ds_tile = smem + C::DS_OFF;
     bool ok = wait_warp(&S.in_full, 0, ab);
@@ -725,11 +776,11 @@ static cudaError_t check_regs(K kern, int& cached) {
 template <int D, bool MODS>
 static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
   const AttnParams& p = L.p;
-  const long long rows = (long long)p.B * p.Hq * p.N;
+  const long long rows = (long long)p.B * p.Hq * p.nT * TILE;
   const long long threads = rows * (D / 8);
   if (L.events[0]) cudaEventRecord(L.events[0], st);
   bwd_pre_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
-      (const __nv_bfloat16*)L.o, (const __nv_bfloat16*)L.dout, L.delta, rows);
+      (const __nv_bfloat16*)L.o, (const __nv_bfloat16*)L.dout, L.lse, L.rowstat, p.N, rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -741,7 +792,7 @@ static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
     return e;
   if (L.events[1]) cudaEventRecord(L.events[1], st);
   kv<<<(unsigned)(p.nT * p.B * p.Hkv), 384, KvCfg<D>::SMEM_BYTES, st>>>(
-      L.tq, L.tk, L.tv, L.tdo, L.lse, L.delta, (__nv_bfloat16*)L.dk, (__nv_bfloat16*)L.dv, p);
+      L.tq, L.tk, L.tv, L.tdo, L.rowstat, (__nv_bfloat16*)L.dk, (__nv_bfloat16*)L.dv, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   auto dqk = bwd_dq_kernel<D, MODS>;
@@ -751,7 +802,7 @@ static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
     return e;
   if (L.events[2]) cudaEventRecord(L.events[2], st);
   dqk<<<(unsigned)(p.nT * p.B * p.Hq), 384, DqCfg<D>::SMEM_BYTES, st>>>(
-      L.tq, L.tk, L.tv, L.tdo, L.lse, L.delta, (__nv_bfloat16*)L.dq, p);
+      L.tq, L.tk, L.tv, L.tdo, L.rowstat, (__nv_bfloat16*)L.dq, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (L.events[3]) cudaEventRecord(L.events[3], st);
   return cudaGetLastError();

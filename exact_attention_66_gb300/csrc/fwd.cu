@@ -91,14 +91,13 @@ __device__ __forceinline__ int union_next(const AttnParams& p, int b, int I0, in
 // D(tmem) = A B^T with A and B K-major 128-byte swizzled tiles in shared
 // memory of `row_bytes` per row; every MMA consumes 32 bytes of each row (16
 // bf16 or 32 e4m3 elements), stepping through the 16 KB column chunks.
-template <bool FP8, int N>
+template <bool FP8, int N, int ROW_BYTES>
 __device__ __forceinline__ void issue_nt(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
-                                         int row_bytes, bool accumulate_first) {
+                                         bool accumulate_first) {
   constexpr uint32_t id = FP8 ? idesc_e4m3(128, N, false, false) : idesc_bf16(128, N, false, false);
   const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, 16, 1024);
-  const int ksteps = row_bytes / 32;
-#pragma unroll 1
-  for (int kk = 0; kk < ksteps; ++kk) {
+#pragma unroll
+  for (int kk = 0; kk < ROW_BYTES / 32; ++kk) {
     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
     const uint32_t acc = (kk > 0 || accumulate_first) ? 1u : 0u;
     if (FP8)
@@ -117,7 +116,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_smem, uint3
   constexpr uint32_t id = FP8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
   constexpr int KV = FP8 ? 32 : 16;  // keys per MMA
   const uint64_t pd = sdesc_sw128(p_smem, 16, 1024), vd = sdesc_sw128(v_smem, 16384, 1024);
-#pragma unroll 1
+#pragma unroll
   for (int kk = 0; kk < TILE / KV; ++kk) {
     const uint32_t poff = (kk / 4) * 16384 + (kk % 4) * 32;
     const uint64_t bd = sdesc_add(vd, kk * KV * 128);
@@ -128,7 +127,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_smem, uint3
       mma_f16_ss(o_tmem, sdesc_add(pd, poff), bd, id, acc);
   }
   if (!FP8 && with_lo) {
-#pragma unroll 1
+#pragma unroll
     for (int kk = 0; kk < TILE / 16; ++kk)
       mma_f16_ts(o_tmem, lo_tmem + kk * 8, sdesc_add(vd, kk * 16 * 128), id, 1u);
   }
@@ -321,7 +320,7 @@ __global__ void __launch_bounds__(384, 1)
         return good;
       };
       auto issue_S = [&](uint32_t k_sm) {
-        issue_nt<FP8, 128>(s_tm, q_sm, k_sm, C::ROW_BYTES, false);
+        issue_nt<FP8, 128, C::ROW_BYTES>(s_tm, q_sm, k_sm, false);
         mma_commit(&S.s_full[t]);
         ++nk;
       };

@@ -29,7 +29,7 @@ struct BwdLaunch {
   const void* o;
   const void* dout;
   const float* lse;
-  float* delta;  // [B, Hq, N] workspace
+  float2* rowstat;  // [B, Hq, nT*128] workspace: {LSE * log2(e) (+inf: no P), D = rowsum(dO*O)}
   void* dq;
   void* dk;
   void* dv;

@@ -94,8 +94,9 @@ def test_workspace_sizes(L):
     assert ws(L.OP_FWD, 1, 2, 2, 1000, 128, L.make_mods(causal=True)) == 0
     m = L.make_mods(causal=True, window=64)
     assert ws(L.OP_FWD, 4, 16, 16, 4096, 128, m) == 4 * 32 * 32
-    assert ws(L.OP_BWD, 1, 64, 8, 8192, 128, L.make_mods(causal=True)) == 64 * 8192 * 4
-    assert ws(L.OP_BWD, 2, 2, 2, 1000, 64, m) == 256 * ((2 * 2 * 1000 * 4 + 255) // 256) + 256
+    # one {LSE, D} float pair per query row, rows padded to whole 128-row tiles
+    assert ws(L.OP_BWD, 1, 64, 8, 8192, 128, L.make_mods(causal=True)) == 64 * 8192 * 8
+    assert ws(L.OP_BWD, 2, 2, 2, 1000, 64, m) == 2 * 2 * 1024 * 8 + 256
     assert ws(L.OP_QUANT_FP8, 2, 16, 16, 16384, 128, None) == 512  # 96 fp32 amax words
     assert ws(L.OP_FWD, 1, 3, 2, 128, 128, None) == 0  # invalid shape -> 0
 

@@ -49,7 +49,7 @@ def test_noalloc_matches_attn_bwd_on_consecutive_calls(case):
 def test_noalloc_rejects_work_beyond_its_scratch():
     ea = lib()
     A = 0x10000  # aligned placeholder address, never dereferenced: the size check comes first
-    B, Hq, Hkv, N, d = 1, 64, 8, 65536, 128  # 16 MiB of row sums > 8 MiB of scratch
+    B, Hq, Hkv, N, d = 1, 64, 8, 65536, 128  # 32 MiB of row statistics > 8 MiB of scratch
     assert ea.attn_workspace_size(ea.OP_BWD, B, Hq, Hkv, N, d, None) > ea.NOALLOC_SCRATCH_BYTES
     st = ea.lib().attn_bwd_noalloc(A, A, A, A, A, A, A, A, A, B, Hq, Hkv, N, d, 0.1, None, None)
     assert st == 3  # ATTN_ERR_WORKSPACE
