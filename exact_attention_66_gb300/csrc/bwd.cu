@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 template <int ROW_BYTES>
 __device__ __forceinline__ void issue_nt(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
   constexpr uint32_t id = idesc_bf16(128, 128, false, false);
-  const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, 16, 1024);
+  const uint64_t ad = opaque(sdesc_sw128(a_smem, 16, 1024)), bd = opaque(sdesc_sw128(b_smem, 16, 1024));
 #pragma unroll
   for (int kk = 0; kk < ROW_BYTES / 32; ++kk) {
     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
@@ -95,7 +95,7 @@ __device__ __forceinline__ void issue_nt(uint32_t d_tmem, uint32_t a_smem, uint3
 template <int D>
 __device__ __forceinline__ void issue_nt_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem) {
   constexpr uint32_t id = idesc_bf16(128, 128, false, false);
-  const uint64_t bd = sdesc_sw128(b_smem, 16, 1024);
+  const uint64_t bd = opaque(sdesc_sw128(b_smem, 16, 1024));
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk)
     mma_f16_ts(d_tmem, a_tmem + kk * 8, sdesc_add(bd, (kk / 4) * 16384 + (kk % 4) * 32), id,
@@ -128,7 +128,7 @@ template <int D, bool A_TMEM>
 __device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_smem, uint32_t a_tmem,
                                           uint32_t b_smem, bool first) {
   constexpr uint32_t id = idesc_bf16(128, D, false, true);
-  const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, 16384, 1024);
+  const uint64_t ad = opaque(sdesc_sw128(a_smem, 16, 1024)), bd = opaque(sdesc_sw128(b_smem, 16384, 1024));
 #pragma unroll
   for (int kk = 0; kk < TILE / 16; ++kk) {
     const uint32_t acc = (first && kk == 0) ? 0u : 1u;

@@ -95,7 +95,7 @@ template <bool FP8, int N, int ROW_BYTES>
 __device__ __forceinline__ void issue_nt(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
                                          bool accumulate_first) {
   constexpr uint32_t id = FP8 ? idesc_e4m3(128, N, false, false) : idesc_bf16(128, N, false, false);
-  const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, 16, 1024);
+  const uint64_t ad = opaque(sdesc_sw128(a_smem, 16, 1024)), bd = opaque(sdesc_sw128(b_smem, 16, 1024));
 #pragma unroll
   for (int kk = 0; kk < ROW_BYTES / 32; ++kk) {
     const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
@@ -115,7 +115,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_smem, uint3
                                          bool first, bool with_lo, uint32_t lo_tmem) {
   constexpr uint32_t id = FP8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
   constexpr int KV = FP8 ? 32 : 16;  // keys per MMA
-  const uint64_t pd = sdesc_sw128(p_smem, 16, 1024), vd = sdesc_sw128(v_smem, 16384, 1024);
+  const uint64_t pd = opaque(sdesc_sw128(p_smem, 16, 1024)), vd = opaque(sdesc_sw128(v_smem, 16384, 1024));
 #pragma unroll
   for (int kk = 0; kk < TILE / KV; ++kk) {
     const uint32_t poff = (kk / 4) * 16384 + (kk % 4) * 32;

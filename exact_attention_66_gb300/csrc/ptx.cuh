@@ -272,6 +272,15 @@ __device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
   return desc + (uint64_t)(bytes >> 4);
 }
 
+// An optimisation barrier on a descriptor: arithmetic on the result stays
+// after this point, so the compiler cannot hoist the per-MMA descriptors of an
+// unrolled issue loop out of the caller's loops and keep them all live in the
+// issuing thread's small register budget.
+__device__ __forceinline__ uint64_t opaque(uint64_t x) {
+  asm volatile("" : "+l"(x));
+  return x;
+}
+
 // ------------------------------------------------- TMEM <-> register moves --
 #define ATTN_R8(a, o) a[o + 0], a[o + 1], a[o + 2], a[o + 3], a[o + 4], a[o + 5], a[o + 6], a[o + 7]
 #define ATTN_OUT8(a, o)                                                                      \
