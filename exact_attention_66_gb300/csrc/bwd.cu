@@ -188,18 +188,7 @@ __device__ __forceinline__ void tmem_wait64(uint32_t (&v)[64]) {
   tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(&v[32]));
 }
 
-struct BwdBars {
-  uint64_t in_full;              // resident tiles
-  uint64_t full[3], empty[3];    // streamed stages (dkdv: Q+dO, 2 used; dq: K)
-  uint64_t vfull[3], vempty[3];  // dq: V stages
-  uint64_t s_full, s_free, p_full, acc_done;
-  uint64_t a_ready;              // dq: Q and dO copied into TMEM
-  uint64_t fin[2];               // per issuer: all its MMAs done
-  uint32_t tmem_base;
-  int abort;
-};
-
-constexpr int BWD_LAUNCH_REGS = 168, BWD_REGS_LOW = 56, BWD_REGS_HIGH = 224;
+constexpr int BWD_LAUNCH_REGS = 168, BWD_REGS_LOW = 80, BWD_REGS_HIGH = 208;
 static_assert(128 * BWD_REGS_LOW + 256 * BWD_REGS_HIGH <= 384 * BWD_LAUNCH_REGS, "register split");
 
 // ================================================================== dK, dV
@@ -217,15 +206,23 @@ struct KvCfg {
   static constexpr int TB = TILE * D * 2;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = TB;
-  static constexpr int ST_OFF = 2 * TB;  // stage s: Q tile at +0, dO tile at +TB
-  static constexpr int BAR_OFF = ST_OFF + 2 * 2 * TB;
+  // Q tiles in a 3-slot ring (last read by dK, the step's final GEMM) and dO
+  // tiles in a 2-slot ring (last read by dV): the load of Q(n+1) never waits
+  // for dK(n-1), which runs late in step n.
+  static constexpr int QS = 3, DOS = 2;
+  static constexpr int Q_OFF = 2 * TB;
+  static constexpr int DO_OFF = Q_OFF + QS * TB;
+  static constexpr int BAR_OFF = DO_OFF + DOS * TB;
   static constexpr int SMEM_BYTES = smem_one_cta(BAR_OFF + 256 + 1024);
 };
 static_assert(KvCfg<128>::SMEM_BYTES <= 232448, "dK/dV shared memory exceeds 227 KB");
 
+constexpr bool KV_X_FIRST = false;
+
 struct KvBars {
-  uint64_t in_full;            // K_J, V_J
-  uint64_t full[2], empty[2];  // Q/dO stages
+  uint64_t in_full;              // K_J, V_J
+  uint64_t qfull[3], qempty[3];  // Q ring
+  uint64_t dfull[2], dempty[2];  // dO ring
   uint64_t s_full;             // S^T(n) in X                (MMA commit)
   uint64_t xs_free;            // S^T(n) copied out of X     (256 softmax threads)
   uint64_t dp_full;            // dP^T(n) in X               (MMA commit)
@@ -283,9 +280,13 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     S.abort = 0;
     mbar_init(&S.in_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 1);
+    for (int s = 0; s < C::QS; ++s) {
+      mbar_init(&S.qfull[s], 1);
+      mbar_init(&S.qempty[s], 1);
+    }
+    for (int s = 0; s < C::DOS; ++s) {
+      mbar_init(&S.dfull[s], 1);
+      mbar_init(&S.dempty[s], 1);
     }
     mbar_init(&S.s_full, 1);
     mbar_init(&S.xs_free, 256);
@@ -307,7 +308,8 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = S.tmem_base;
   const uint32_t sK = smem_u32(smem + C::K_OFF);
   const uint32_t sV = smem_u32(smem + C::V_OFF);
-  const uint32_t sST = smem_u32(smem + C::ST_OFF);
+  const uint32_t sQ = smem_u32(smem + C::Q_OFF);
+  const uint32_t sDO = smem_u32(smem + C::DO_OFF);
   const uint32_t tX = tmem, tPT = tmem + 128, tDS = tmem + 192;
   const uint32_t tdV = tmem + 256, tdK = tmem + 256 + D;
 
@@ -320,70 +322,86 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_3d(smem + C::K_OFF + ch * 16384, &tk, &S.in_full, ch * 64, J * TILE, b * p.Hkv + hk);
         tma_load_3d(smem + C::V_OFF + ch * 16384, &tv, &S.in_full, ch * 64, J * TILE, b * p.Hkv + hk);
       }
-      int n = 0;
+      int nq = 0, nd = 0;  // Q / dO loads issued
       if (any) {
         int g = 0, I = steps.I_first;
         do {
-          const int st = n & 1;
-          if (!mbar_wait(&S.empty[st], ((n >> 1) & 1) ^ 1, ab)) break;
           const int hq = hk * G + g;
-          mbar_arrive_tx(&S.full[st], 2 * C::TB);
-          uint8_t* dst = smem + C::ST_OFF + st * 2 * C::TB;
-          for (int ch = 0; ch < C::CH; ++ch) {
-            tma_load_3d(dst + ch * 16384, &tq, &S.full[st], ch * 64, I * TILE, b * p.Hq + hq);
-            tma_load_3d(dst + C::TB + ch * 16384, &tdo, &S.full[st], ch * 64, I * TILE, b * p.Hq + hq);
-          }
-          ++n;
+          const int qs = nq % C::QS, ds = nd % C::DOS;
+          if (!mbar_wait(&S.qempty[qs], ((nq / C::QS) & 1) ^ 1, ab)) break;
+          mbar_arrive_tx(&S.qfull[qs], C::TB);
+          for (int ch = 0; ch < C::CH; ++ch)
+            tma_load_3d(smem + C::Q_OFF + qs * C::TB + ch * 16384, &tq, &S.qfull[qs], ch * 64, I * TILE,
+                        b * p.Hq + hq);
+          ++nq;
+          if (!mbar_wait(&S.dempty[ds], ((nd / C::DOS) & 1) ^ 1, ab)) break;
+          mbar_arrive_tx(&S.dfull[ds], C::TB);
+          for (int ch = 0; ch < C::CH; ++ch)
+            tma_load_3d(smem + C::DO_OFF + ds * C::TB + ch * 16384, &tdo, &S.dfull[ds], ch * 64, I * TILE,
+                        b * p.Hq + hq);
+          ++nd;
         } while (steps.advance(p, b, g, I));
       }
+      // Loads still in flight must land before the CTA exits.
       mbar_wait_drain(&S.in_full, 0);
-      for (int s = 0; s < 2; ++s)
-        if (n > s) mbar_wait_drain(&S.full[s], ((n - 1 - s) >> 1) & 1);
+      for (int s = 0; s < C::QS; ++s)
+        if (nq > s) mbar_wait_drain(&S.qfull[s], ((nq - 1 - s) / C::QS) & 1);
+      for (int s = 0; s < C::DOS; ++s)
+        if (nd > s) mbar_wait_drain(&S.dfull[s], ((nd - 1 - s) / C::DOS) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // Program order per step n follows the order in which the softmax frees
-    // and fills its buffers: dP(n), dV(n), S(n+1), dK(n).
+    // One thread issues every GEMM, in the order in which the softmax releases
+    // X and fills P^T / dS^T, so it never waits on an event that comes after
+    // one it could already act on.  KV_X_FIRST: per step n, S(n+1), dV(n),
+    // dP(n+1), dK(n) (the X chain ahead of the accumulations); otherwise
+    // dP(n), dV(n), S(n+1), dK(n).
     if (lane == 0) {
       bool ok = mbar_wait(&S.in_full, 0, ab);
       tc_fence_after();
       if (ok && any) {
         int g = 0, I = steps.I_first, n = 0;
-        ok = mbar_wait(&S.full[0], 0, ab);
-        tc_fence_after();
-        if (ok) {
-          issue_nt<D * 2>(tX, sK, sST);  // S^T(0) = K Q(0)^T
+        auto q_at = [&](int m) { return sQ + (uint32_t)((m % C::QS) * C::TB); };
+        auto do_at = [&](int m) { return sDO + (uint32_t)((m % C::DOS) * C::TB); };
+        // S^T(m) = K Q(m)^T into X once dP^T(m-1) has been copied out.
+        auto issue_s = [&](int m) -> bool {
+          if (m > 0 && !mbar_wait(&S.xd_free, (m - 1) & 1, ab)) return false;
+          if (!mbar_wait(&S.qfull[m % C::QS], (m / C::QS) & 1, ab)) return false;
+          tc_fence_after();
+          issue_nt<D * 2>(tX, sK, q_at(m));
           mma_commit(&S.s_full);
-        }
+          return true;
+        };
+        // dP^T(m) = V dO(m)^T into X once S^T(m) has been copied out.
+        auto issue_dp = [&](int m) -> bool {
+          if (!mbar_wait(&S.xs_free, m & 1, ab)) return false;
+          if (!mbar_wait(&S.dfull[m % C::DOS], (m / C::DOS) & 1, ab)) return false;
+          tc_fence_after();
+          issue_nt<D * 2>(tX, sV, do_at(m));
+          mma_commit(&S.dp_full);
+          return true;
+        };
+        ok = issue_s(0);
+        if (KV_X_FIRST && ok) ok = issue_dp(0);
         while (ok) {
-          const uint32_t q_sm = sST + (n & 1) * 2 * C::TB;
-          const uint32_t do_sm = q_sm + C::TB;
           int g2 = g, I2 = I;
           const bool has_next = steps.advance(p, b, g2, I2);
-          // dP^T(n) = V dO(n)^T into X once S^T(n) has been copied out.
-          if (!(ok = mbar_wait(&S.xs_free, n & 1, ab))) break;
-          tc_fence_after();
-          issue_nt<D * 2>(tX, sV, do_sm);
-          mma_commit(&S.dp_full);
-          // dV += P^T(n) dO(n).
+          if (!KV_X_FIRST && !(ok = issue_dp(n))) break;
+          if (KV_X_FIRST && has_next && !(ok = issue_s(n + 1))) break;
+          // dV += P^T(n) dO(n); dO(n) is free after it.
           if (!(ok = mbar_wait(&S.p_full, n & 1, ab))) break;
           tc_fence_after();
-          issue_acc<D, true>(tdV, 0, tPT, do_sm, n == 0);
+          issue_acc<D, true>(tdV, 0, tPT, do_at(n), n == 0);
           mma_commit(&S.pt_free);
-          // S^T(n+1) into X once dP^T(n) has been copied out.
-          if (has_next) {
-            if (!(ok = mbar_wait(&S.xd_free, n & 1, ab))) break;
-            if (!(ok = mbar_wait(&S.full[(n + 1) & 1], ((n + 1) >> 1) & 1, ab))) break;
-            tc_fence_after();
-            issue_nt<D * 2>(tX, sK, sST + ((n + 1) & 1) * 2 * C::TB);
-            mma_commit(&S.s_full);
-          }
-          // dK += dS^T(n) Q(n); the stage is free after it (and dV(n)).
+          mma_commit(&S.dempty[n % C::DOS]);
+          if (KV_X_FIRST && has_next && !(ok = issue_dp(n + 1))) break;
+          if (!KV_X_FIRST && has_next && !(ok = issue_s(n + 1))) break;
+          // dK += dS^T(n) Q(n); Q(n) is free after it.
           if (!(ok = mbar_wait(&S.ds_full, n & 1, ab))) break;
           tc_fence_after();
-          issue_acc<D, true>(tdK, 0, tDS, q_sm, n == 0);
+          issue_acc<D, true>(tdK, 0, tDS, q_at(n), n == 0);
           mma_commit(&S.ds_free);
-          mma_commit(&S.empty[n & 1]);
+          mma_commit(&S.qempty[n % C::QS]);
           if (!has_next) break;
           g = g2;
           I = I2;
@@ -415,11 +433,11 @@ __global__ void __launch_bounds__(384, 1)
         const int cls = tile_class(p, b, I, J);
         const float al2 = al ? alibi_slope(p, hq) * LOG2E : 0.f;
         // {LSE log2, D} of this warpgroup's 64 query rows (columns): lane k
-        // holds rows k and 32 + k, broadcast by shuffles where used.
+        // holds rows k and 32 + k (negated), broadcast by shuffles where used.
         const int i0 = I * TILE + 64 * w;  // query row of column 0
         const float2* rs = rowstat + ((size_t)b * p.Hq + hq) * ((size_t)p.nT * TILE) + i0;
         const float2 rs0 = rs[lane], rs1 = rs[32 + lane];
-        const float my_l2[2] = {rs0.x, rs1.x}, my_dd[2] = {rs0.y, rs1.y};
+        const float my_nl2[2] = {-rs0.x, -rs1.x}, my_ndd[2] = {-rs0.y, -rs1.y};
 
         // S^T(n) -> registers, X back to the MMA pipe.
         if (!(ok = wait_warp(&S.s_full, n & 1, ab))) break;
@@ -431,39 +449,60 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(&S.xs_free);
 
         // P = exp2(x - LSE) (0 where masked); s[] keeps P (times the
-        // soft-cap derivative) for dS.
+        // soft-cap derivative) for dS.  fp32 arithmetic in pairs.
         const int lo = causal ? j - i0 : -0x7fffffff;   // valid iff c >= lo
         const int hi = win ? p.window + j - i0 : 0x7fffffff;  // valid iff c < hi
         const float al_base = al2 * (float)(j - i0);
+        const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          float pe[2];
+          const uint64_t nl2 = f2_pack(__shfl_sync(0xffffffffu, my_nl2[c >> 5], c & 31),
+                                       __shfl_sync(0xffffffffu, my_nl2[(c + 1) >> 5], (c + 1) & 31));
+          const float s0 = __uint_as_float(s[c]), s1 = __uint_as_float(s[c + 1]);
+          uint64_t x2, dmul2 = 0;
+          if (sc || al) {
+            float x[2], dm[2] = {1.f, 1.f};
+            const float sv[2] = {s0, s1};
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cc = c + e;
-            const float l2 = __shfl_sync(0xffffffffu, my_l2[cc >> 5], cc & 31);
-            const float sv = __uint_as_float(s[cc]);
-            float x, dmul = 1.f;
-            if (sc) {
-              const float t = tanh_exp(sv * sc_in);
-              x = t * sc_out;
-              dmul = fmaf(-t, t, 1.f);
-            } else {
-              x = sv * p.scale_log2;
+            for (int e = 0; e < 2; ++e) {
+              if (sc) {
+                const float t = tanh_exp(sv[e] * sc_in);
+                x[e] = t * sc_out;
+                dm[e] = fmaf(-t, t, 1.f);
+              } else {
+                x[e] = sv[e] * p.scale_log2;
+              }
+              if (al) x[e] = fmaf(-al2, (float)(c + e), x[e] + al_base);
             }
-            if (al) x = fmaf(-al2, (float)cc, x + al_base);
-            float pv = ex2(x - l2);
-            if (cls == CLS_PARTIAL) {
+            x2 = f2_add(f2_pack(x[0], x[1]), nl2);
+            dmul2 = f2_pack(dm[0], dm[1]);
+          } else {
+            x2 = f2_fma(f2_pack(s0, s1), sl2, nl2);
+          }
+          float x0, x1;
+          f2_unpack(x2, x0, x1);
+          float pe[2] = {ex2(x0), ex2(x1)};
+          if (cls == CLS_PARTIAL) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int cc = c + e;
               bool valid = (cc >= lo) && (cc < hi);
               if (doc && valid)
                 valid = (i0 + cc < p.N) && (__ldg(p.doc_ids + (size_t)b * p.N + i0 + cc) == doc_j);
-              if (!valid) pv = 0.f;
+              if (!valid) pe[e] = 0.f;
             }
-            pe[e] = pv;
-            s[cc] = __float_as_uint(pv * dmul);
           }
           pk[c / 2] = pack_bf16(pe[0], pe[1]);
+          if (sc) {
+            float q0, q1;
+            f2_unpack(f2_mul(f2_pack(pe[0], pe[1]), dmul2), q0, q1);
+            s[c] = __float_as_uint(q0);
+            s[c + 1] = __float_as_uint(q1);
+          } else {
+            s[c] = __float_as_uint(pe[0]);
+            s[c + 1] = __float_as_uint(pe[1]);
+          }
         }
         // P^T(n) into TMEM once dV(n-1) has read P^T(n-1).
         if (n > 0) {
@@ -484,17 +523,15 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_before();
         mbar_arrive(&S.xd_free);
 
-        // dS = P (dP - D) (times the soft-cap derivative).
+        // dS = P (dP - D) (times the soft-cap derivative), in pairs.
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          float ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int cc = c + e;
-            const float dd = __shfl_sync(0xffffffffu, my_dd[cc >> 5], cc & 31);
-            ds[e] = __uint_as_float(s[cc]) * (__uint_as_float(dp[cc]) - dd);
-          }
-          pk[c / 2] = pack_bf16(ds[0], ds[1]);
+          const uint64_t ndd = f2_pack(__shfl_sync(0xffffffffu, my_ndd[c >> 5], c & 31),
+                                       __shfl_sync(0xffffffffu, my_ndd[(c + 1) >> 5], (c + 1) & 31));
+          const uint64_t g2 = f2_add(f2_pack(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), ndd);
+          float ds0, ds1;
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), g2), ds0, ds1);
+          pk[c / 2] = pack_bf16(ds0, ds1);
         }
         // dS^T(n) into TMEM once dK(n-1) has read dS^T(n-1).
         if (n > 0) {
@@ -526,24 +563,35 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ======================================================================= dQ
-// Shared memory: six 128 x D bf16 slots and the dS tile.  K/V tile pair n sits
-// in slots (2 (n mod 3), 2 (n mod 3) + 1); Q and dO are first loaded into
-// slots 4 and 5, copied into TMEM by the softmax warpgroups, and their slots
-// then join the ring as its third stage.
+// Shared memory: K tiles in a 4-slot ring (read by S and, at the end of the
+// step, by dQ), V tiles in a 2-slot ring (read only by dP, early), and the dS
+// tile.  Q and dO are first loaded into K slot 3 and V slot 1, copied into
+// TMEM by the softmax warpgroups, and those slots then join their rings.
 template <int D>
 struct DqCfg {
   static constexpr int CH = D / 64;
   static constexpr int TB = TILE * D * 2;
-  static constexpr int STAGES = 3;
-  static constexpr int Q_OFF = 4 * TB;
-  static constexpr int DO_OFF = 5 * TB;
-  static constexpr int DS_OFF = 6 * TB;  // dS tile, 128 x 128 bf16
+  static constexpr int KS = 4, VS = 2;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = KS * TB;
+  static constexpr int Q_OFF = K_OFF + 3 * TB;   // K slot 3
+  static constexpr int DO_OFF = V_OFF + 1 * TB;  // V slot 1
+  static constexpr int DS_OFF = V_OFF + VS * TB;  // dS tile, 128 x 128 bf16
   static constexpr int BAR_OFF = DS_OFF + TILE * TILE * 2;
   static constexpr int SMEM_BYTES = smem_one_cta(BAR_OFF + 256 + 1024);
-  __host__ __device__ static constexpr int k_off(int st) { return 2 * st * TB; }
-  __host__ __device__ static constexpr int v_off(int st) { return (2 * st + 1) * TB; }
 };
 static_assert(DqCfg<128>::SMEM_BYTES <= 232448, "dQ shared memory exceeds 227 KB");
+
+struct DqBars {
+  uint64_t in_full;              // Q, dO
+  uint64_t kfull[4], kempty[4];  // K ring
+  uint64_t vfull[2], vempty[2];  // V ring
+  uint64_t s_full, s_free, p_full, acc_done;
+  uint64_t a_ready;              // Q and dO copied into TMEM: their slots are free
+  uint64_t fin[2];               // per issuer: all its MMAs done
+  uint32_t tmem_base;
+  int abort;
+};
 
 template <int D, bool MODS>
 __global__ void __launch_bounds__(384, 1)
@@ -554,7 +602,7 @@ __global__ void __launch_bounds__(384, 1)
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  BwdBars& S = *reinterpret_cast<BwdBars*>(smem + C::BAR_OFF);
+  DqBars& S = *reinterpret_cast<DqBars*>(smem + C::BAR_OFF);
   const Abort ab{&S.abort, p.status};
   const int warp = warp_id(), lane = lane_id();
 
@@ -574,11 +622,13 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     S.abort = 0;
     mbar_init(&S.in_full, 1);
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 2);   // K: read by S (A) and dQ (B)
+    for (int s = 0; s < C::KS; ++s) {
+      mbar_init(&S.kfull[s], 1);
+      mbar_init(&S.kempty[s], 2);  // read by S (issuer A) and dQ (issuer B)
+    }
+    for (int s = 0; s < C::VS; ++s) {
       mbar_init(&S.vfull[s], 1);
-      mbar_init(&S.vempty[s], 1);  // V: read by dP (A)
+      mbar_init(&S.vempty[s], 1);  // read by dP (issuer A)
     }
     mbar_init(&S.s_full, 1);
     mbar_init(&S.s_free, 256);
@@ -596,7 +646,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
-  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sKr = smem_u32(smem + C::K_OFF), sVr = smem_u32(smem + C::V_OFF);
   const uint32_t sDS = smem_u32(smem + C::DS_OFF);
   // TMEM: S [0,128), dP [128,256), dQ [256, 256+D), then Q and dO as packed
   // bf16 A operands (D / 2 columns each): the recompute GEMMs S = Q K^T and
@@ -614,28 +664,29 @@ __global__ void __launch_bounds__(384, 1)
       }
       int nk = 0, nv = 0;  // K / V loads issued
       for (int J = J_first; J < J_end; J = next_J(J + 1)) {
-        const int st = nk % C::STAGES;
-        const uint32_t ph = ((nk / C::STAGES) & 1) ^ 1;
-        if (nk == C::STAGES - 1 && !mbar_wait(&S.a_ready, 0, ab)) break;
-        if (!mbar_wait(&S.empty[st], ph, ab)) break;
-        mbar_arrive_tx(&S.full[st], C::TB);
+        const int ks = nk % C::KS, vs = nv % C::VS;
+        // K slot 3 and V slot 1 hold Q and dO until the softmax copied them.
+        if (nk == 3 && !mbar_wait(&S.a_ready, 0, ab)) break;
+        if (!mbar_wait(&S.kempty[ks], ((nk / C::KS) & 1) ^ 1, ab)) break;
+        mbar_arrive_tx(&S.kfull[ks], C::TB);
         for (int ch = 0; ch < C::CH; ++ch)
-          tma_load_3d(smem + C::k_off(st) + ch * 16384, &tk, &S.full[st], ch * 64, J * TILE,
+          tma_load_3d(smem + C::K_OFF + ks * C::TB + ch * 16384, &tk, &S.kfull[ks], ch * 64, J * TILE,
                       b * p.Hkv + hk);
         ++nk;
-        if (!mbar_wait(&S.vempty[st], ph, ab)) break;
-        mbar_arrive_tx(&S.vfull[st], C::TB);
+        if (nv == 1 && !mbar_wait(&S.a_ready, 0, ab)) break;
+        if (!mbar_wait(&S.vempty[vs], ((nv / C::VS) & 1) ^ 1, ab)) break;
+        mbar_arrive_tx(&S.vfull[vs], C::TB);
         for (int ch = 0; ch < C::CH; ++ch)
-          tma_load_3d(smem + C::v_off(st) + ch * 16384, &tv, &S.vfull[st], ch * 64, J * TILE,
+          tma_load_3d(smem + C::V_OFF + vs * C::TB + ch * 16384, &tv, &S.vfull[vs], ch * 64, J * TILE,
                       b * p.Hkv + hk);
         ++nv;
       }
       // Loads still in flight must land before the CTA exits.
       mbar_wait_drain(&S.in_full, 0);
-      for (int s = 0; s < C::STAGES; ++s) {
-        if (nk > s) mbar_wait_drain(&S.full[s], ((nk - 1 - s) / C::STAGES) & 1);
-        if (nv > s) mbar_wait_drain(&S.vfull[s], ((nv - 1 - s) / C::STAGES) & 1);
-      }
+      for (int s = 0; s < C::KS; ++s)
+        if (nk > s) mbar_wait_drain(&S.kfull[s], ((nk - 1 - s) / C::KS) & 1);
+      for (int s = 0; s < C::VS; ++s)
+        if (nv > s) mbar_wait_drain(&S.vfull[s], ((nv - 1 - s) / C::VS) & 1);
     }
   } else if (warp == 1 || warp == 2) {
     // Issuer A (warp 1): S = Q K^T and dP = dO V^T.  Issuer B (warp 2): dQ += dS K.
@@ -645,26 +696,25 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       int n = 0;
       for (int J = J_first; ok && J < J_end; J = next_J(J + 1), ++n) {
-        const int st = n % C::STAGES;
-        const uint32_t ph = (n / C::STAGES) & 1;
-        const uint32_t k_sm = sbase + C::k_off(st), v_sm = sbase + C::v_off(st);
-        if (!(ok = mbar_wait(&S.full[st], ph, ab))) break;
+        const int ks = n % C::KS, vs = n % C::VS;
+        const uint32_t k_sm = sKr + ks * C::TB, v_sm = sVr + vs * C::TB;
+        if (!(ok = mbar_wait(&S.kfull[ks], (n / C::KS) & 1, ab))) break;
         if (A) {
-          if (!(ok = mbar_wait(&S.vfull[st], ph, ab))) break;
+          if (!(ok = mbar_wait(&S.vfull[vs], (n / C::VS) & 1, ab))) break;
           if (n == 0 && !(ok = mbar_wait(&S.a_ready, 0, ab))) break;
           if (n > 0 && !(ok = mbar_wait(&S.s_free, (n - 1) & 1, ab))) break;
           tc_fence_after();
           issue_nt_tmem_a<D>(tS, tQa, k_sm);
           issue_nt_tmem_a<D>(tdP, tDOa, v_sm);
           mma_commit(&S.s_full);
-          mma_commit(&S.vempty[st]);
-          mma_commit(&S.empty[st]);
+          mma_commit(&S.vempty[vs]);
+          mma_commit(&S.kempty[ks]);
         } else {
           if (!(ok = mbar_wait(&S.p_full, n & 1, ab))) break;
           tc_fence_after();
           issue_acc<D, false>(tdQ, sDS, 0, k_sm, n == 0);
           mma_commit(&S.acc_done);
-          mma_commit(&S.empty[st]);
+          mma_commit(&S.kempty[ks]);
         }
       }
       mma_commit(&S.fin[A ? 0 : 1]);
@@ -685,7 +735,8 @@ __global__ void __launch_bounds__(384, 1)
     const float al2 = al ? alibi_slope(p, hq) * LOG2E : 0.f;
     const size_t row = ((size_t)b * p.Hq + hq) * p.N + i;
     const float2 rs = rowstat[((size_t)b * p.Hq + hq) * ((size_t)p.nT * TILE) + i];
-    const float lse2 = rs.x, dd = rs.y;
+    const uint64_t nl2 = f2_pack(-rs.x, -rs.x), ndd = f2_pack(-rs.y, -rs.y);
+    const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
     const int doc_i = (doc && i < p.N) ? p.doc_ids[(size_t)b * p.N + i] : 0;
     uint8_t* ds_tile = smem + C::DS_OFF;
     bool ok = wait_warp(&S.in_full, 0, ab);
@@ -715,29 +766,45 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t dw[32];
 #pragma unroll
       for (int k = 0; k < 64; k += 2) {
-        float ds[2];
+        const float s0 = __uint_as_float(s[k]), s1 = __uint_as_float(s[k + 1]);
+        uint64_t x2, dmul2 = 0;
+        if (sc || al) {
+          float x[2], dm[2] = {1.f, 1.f};
+          const float sv[2] = {s0, s1};
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int c = k + e;
-          const float sv = __uint_as_float(s[c]);
-          float x, dmul = 1.f;
-          if (sc) {
-            const float t = tanh_exp(sv * sc_in);
-            x = t * sc_out;
-            dmul = fmaf(-t, t, 1.f);
-          } else {
-            x = sv * p.scale_log2;
+          for (int e = 0; e < 2; ++e) {
+            if (sc) {
+              const float t = tanh_exp(sv[e] * sc_in);
+              x[e] = t * sc_out;
+              dm[e] = fmaf(-t, t, 1.f);
+            } else {
+              x[e] = sv[e] * p.scale_log2;
+            }
+            if (al) x[e] = fmaf(al2, (float)(k + e), x[e] + al_base);
           }
-          if (al) x = fmaf(al2, (float)c, x + al_base);
-          float pe = ex2(x - lse2);
-          if (cls == CLS_PARTIAL) {
+          x2 = f2_add(f2_pack(x[0], x[1]), nl2);
+          dmul2 = f2_pack(dm[0], dm[1]);
+        } else {
+          x2 = f2_fma(f2_pack(s0, s1), sl2, nl2);
+        }
+        float x0, x1;
+        f2_unpack(x2, x0, x1);
+        float pe[2] = {ex2(x0), ex2(x1)};
+        if (cls == CLS_PARTIAL) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = k + e;
             bool valid = (c <= hi_lim) && (c > lo_lim);
             if (doc && valid) valid = (__ldg(p.doc_ids + (size_t)b * p.N + j0 + c) == doc_i);
-            if (!valid) pe = 0.f;
+            if (!valid) pe[e] = 0.f;
           }
-          ds[e] = pe * (__uint_as_float(dp[c]) - dd) * dmul;
         }
-        dw[k / 2] = pack_bf16(ds[0], ds[1]);
+        uint64_t pp = f2_pack(pe[0], pe[1]);
+        if (sc) pp = f2_mul(pp, dmul2);
+        const uint64_t g2 = f2_add(f2_pack(__uint_as_float(dp[k]), __uint_as_float(dp[k + 1])), ndd);
+        float ds0, ds1;
+        f2_unpack(f2_mul(pp, g2), ds0, ds1);
+        dw[k / 2] = pack_bf16(ds0, ds1);
       }
       if (n > 0) {
         if (!(ok = wait_warp(&S.acc_done, (n - 1) & 1, ab))) break;

@@ -386,6 +386,15 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Scalar fp32 add / mul / fma on the warps beside an MMA stream slow the
+// tensor pipe several-fold on this part, while the two-wide forms above do
+// not: the hot loops next to the MMAs do their fp32 arithmetic in pairs.
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
