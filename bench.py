@@ -8,8 +8,12 @@ shape).  Throughput counts algorithmic FLOPs: 4*B*Hq*d*(allowed pairs) for
 the forward and 2.5x that for the backward.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+  python bench.py --workload causal_mha_2k|flex_mods_4k|tiny_mha|fp8_outliers_16k
 
-Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+Prints ONE JSON line (rank 0); the default workload is the one the metric is
+quoted on, the others are the smaller parity workloads timed the same way
+(tiny_mha: forward only; fp8_outliers_16k: Hadamard + e4m3 prologue and the
+e4m3 forward).  ``--impl reference`` times the fp64 CPU
 oracle (the reference arm of this build) on bounded row slices of the same
 workload.  Under torchrun each rank runs an independent replica (weak
 scaling, no data-path collective; the process group only carries the
@@ -56,8 +60,26 @@ def causal_pairs(N: int) -> int:
     return N * (N + 1) // 2
 
 
-def flops(cfg):
-    fwd = 4.0 * cfg["B"] * cfg["Hq"] * cfg["d"] * causal_pairs(cfg["N"])
+def allowed_pairs(cfg, doc_ids=None) -> int:
+    """Number of (query, key) pairs the workload's mask allows, summed over the
+    batch (the FLOP count's unmasked fraction times N^2 times B)."""
+    N, B = cfg["N"], cfg["B"]
+    causal, W = cfg.get("causal", False), cfg.get("window")
+    if doc_ids is None and W is None:
+        return B * (causal_pairs(N) if causal else N * N)
+    if not causal:
+        raise ValueError("pair count implemented for causal masks with window / documents")
+    total = 0
+    for b in range(B):
+        lens = np.bincount(doc_ids[b]) if doc_ids is not None else np.array([N])
+        for L in lens.tolist():
+            i = np.arange(L, dtype=np.int64)
+            total += int(np.minimum(i + 1, W if W is not None else L).sum())
+    return total
+
+
+def flops(cfg, doc_ids=None):
+    fwd = 4.0 * cfg["Hq"] * cfg["d"] * allowed_pairs(cfg, doc_ids)
     return fwd, 2.5 * fwd
 
 
@@ -144,31 +166,51 @@ def allmax(world, x: float) -> float:
 
 
 # ------------------------------------------------------- oracle baseline ----
-def oracle_sample(cfg, x, budget_s: float, rows_per_slice: int):
+def row_pairs(cfg, doc_ids, b, rows):
+    """Allowed keys of each query row in ``rows`` (of batch entry b)."""
+    N = cfg["N"]
+    rows = np.asarray(rows, np.int64)
+    cnt = rows + 1 if cfg.get("causal") else np.full(rows.shape, N, np.int64)
+    if cfg.get("window") is not None:
+        cnt = np.minimum(cnt, cfg["window"])
+    if doc_ids is not None:
+        start = np.searchsorted(doc_ids[b], doc_ids[b][rows], side="left")
+        cnt = np.minimum(cnt, rows - start + 1)
+    return cnt
+
+
+def oracle_sample(cfg, x, budget_s: float, rows_per_slice: int, fwd_only=False):
     """Time the fp64 oracle on row slices of query heads of the workload.
 
     Runs slices (forward rows + their backward contributions) until
     ``budget_s`` seconds have passed (at least one).  Returns (TFLOP/s,
     seconds, description)."""
     from oracle import attn64
-    mods = attn64.Mods(causal=True)
+    docs = x.get("doc_ids")
+    mods = attn64.Mods(causal=cfg.get("causal", False), window=cfg.get("window"), doc_ids=docs,
+                       softcap=cfg.get("softcap"), alibi=cfg.get("alibi", False))
     scale = 1.0 / math.sqrt(cfg["d"])
     N, d = cfg["N"], cfg["d"]
+    rows_per_slice = min(rows_per_slice, N)
+    per_pair = (1.0 if fwd_only else 3.5) * 4.0 * d
     done_flops, t0, n = 0.0, time.perf_counter(), 0
     starts = list(range(N - rows_per_slice, -1, -rows_per_slice))
     while True:
+        b = (n // cfg["Hq"]) % cfg["B"]
         hq = n % cfg["Hq"]
         r0 = starts[n % len(starts)]
         rows = np.arange(r0, r0 + rows_per_slice)
-        attn64.head_forward(x["q"], x["k"], x["v"], scale, mods, 0, hq, rows=rows)
-        attn64.head_rows_backward(x["q"], x["k"], x["v"], x["do"], scale, mods, 0, hq, rows)
-        done_flops += 3.5 * 4.0 * d * float((rows + 1).sum())
+        attn64.head_forward(x["q"], x["k"], x["v"], scale, mods, b, hq, rows=rows)
+        if not fwd_only:
+            attn64.head_rows_backward(x["q"], x["k"], x["v"], x["do"], scale, mods, b, hq, rows)
+        done_flops += per_pair * float(row_pairs(cfg, docs, b, rows).sum())
         n += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    desc = (f"{n} slices of {rows_per_slice} query rows (forward + their backward "
-            f"contributions, fp64 numpy) of {WORKLOAD}; {done_flops:.3e} algorithmic FLOP")
+    what = "forward" if fwd_only else "forward + their backward contributions"
+    desc = (f"{n} slices of {rows_per_slice} query rows ({what}, fp64 numpy) of "
+            f"{cfg.get('name', WORKLOAD)}; {done_flops:.3e} algorithmic FLOP")
     return done_flops / el / 1e12, el, desc
 
 
@@ -197,26 +239,53 @@ def traffic_record(kernel: str):
     return rec["bytes_per_launch"] if h == rec.get("source_sha") else None
 
 
+def workload_mods(ea, cfg, x, dev):
+    docs = x.get("doc_ids")
+    ddocs = torch.from_numpy(docs).to(dev) if docs is not None else None
+    m = ea.make_mods(causal=cfg.get("causal", False), window=cfg.get("window"), doc_ids=ddocs,
+                     softcap=cfg.get("softcap"), alibi=cfg.get("alibi", False))
+    return m, docs
+
+
+def mods_label(cfg):
+    parts = [k for k in ("causal", "window", "doc", "softcap", "alibi") if cfg.get(k)]
+    return "+".join(parts) or "none"
+
+
+def l2_note(cfg):
+    q_bytes = cfg["B"] * cfg["Hq"] * cfg["N"] * cfg["d"] * 2
+    if q_bytes * 4 > 130 * 2**20:
+        return f"inputs larger than L2 (Q/O/dO/dQ {q_bytes / 2**20:.0f} MiB each)"
+    return f"inputs fit in L2 (Q {q_bytes / 2**10:.0f} KiB): warm-cache timing"
+
+
 def run_ours(args, world, rank, local):
     import exact_attention_66_gb300 as ea
 
-    cfg = dict(gen.WORKLOADS[WORKLOAD])
+    if args.workload == "fp8_outliers_16k":
+        return run_fp8(args, world, rank, local)
+    name = args.workload
+    cfg = dict(gen.WORKLOADS[name])
     if args.heads:  # smaller case of the same shape family (profiling); 8 query heads per KV head
         cfg["Hq"], cfg["Hkv"] = args.heads, max(1, args.heads // 8)
     B, Hq, Hkv, N, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"]
+    fwd_only = name == "tiny_mha"
     scale = 1.0 / math.sqrt(d)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    x = gen.make_inputs(B, Hq, Hkv, N, d, seed=cfg["seed"] + 97 * rank)
+    x = gen.make_inputs(**dict(cfg, seed=cfg["seed"] + 97 * rank))
     host = {k: x[k].pin_memory() for k in ("q", "k", "v", "do")}
     q, k, v, do = (host[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    mods = ea.make_mods(causal=True)
+    mods, docs = workload_mods(ea, cfg, x, dev)
+    nws_f = ea.attn_workspace_size(ea.OP_FWD, B, Hq, Hkv, N, d, mods)
+    ws_f = torch.empty(max(nws_f, 1), dtype=torch.uint8, device=dev)
     nws = ea.attn_workspace_size(ea.OP_BWD, B, Hq, Hkv, N, d, mods)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    with_map = bool(cfg.get("window") or cfg.get("doc"))
 
     def mk_events(n):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -224,16 +293,21 @@ def run_ours(args, world, rank, local):
             e.record(stream)  # create the handles before passing them to the library
         return evs
 
+    def fwd():
+        ea.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, mods, ws_f if nws_f else None, nws_f, stream)
+
     def step(ev=None):
         if ev is None:
-            ea.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, mods, None, 0, stream)
-            ea.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods, ws, nws, stream)
+            fwd()
+            if not fwd_only:
+                ea.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods, ws, nws, stream)
         else:
             ev[0].record(stream)
-            ea.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, mods, None, 0, stream)
+            fwd()
             ev[1].record(stream)
-            ea.attn_bwd_profiled(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods,
-                                 ws, nws, stream, ev[2:6])
+            if not fwd_only:
+                ea.attn_bwd_profiled(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods,
+                                     ws, nws, stream, ev[2:6])
 
     for _ in range(args.warmup):
         step()
@@ -258,25 +332,31 @@ def run_ours(args, world, rank, local):
     ea.attn_status(stream)
     total_ms = t_start.elapsed_time(t_end)
     total_ms = allmax(world, total_ms)
-    k_fwd = [e[0].elapsed_time(e[1]) for e in evs]
-    k_pre = [e[2].elapsed_time(e[3]) for e in evs]
-    k_kv = [e[3].elapsed_time(e[4]) for e in evs]
-    k_dq = [e[4].elapsed_time(e[5]) for e in evs]
     mean = lambda a: sum(a) / len(a)  # noqa: E731
+    k_fwd = [e[0].elapsed_time(e[1]) for e in evs]
+    if fwd_only:
+        k_pre = k_kv = k_dq = [0.0]
+    else:
+        k_pre = [e[2].elapsed_time(e[3]) for e in evs]
+        k_kv = [e[3].elapsed_time(e[4]) for e in evs]
+        k_dq = [e[4].elapsed_time(e[5]) for e in evs]
 
     # end to end through the public API: pinned host inputs in, results out
-    out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
-    h2d = sum(host[n].numel() * host[n].element_size() for n in host)
+    outs = (("o", o), ("lse", lse)) if fwd_only else (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))
+    ins = ("q", "k", "v") if fwd_only else ("q", "k", "v", "do")
+    out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs}
+    h2d = sum(host[n].numel() * host[n].element_size() for n in ins)
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
     e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
 
     def e2e_step():
         for n, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
-            dst.copy_(host[n], non_blocking=True)
+            if n in ins:
+                dst.copy_(host[n], non_blocking=True)
         fo, fl = ea.forward(q, k, v, scale, mods, out=o, lse=lse, stream=stream)
-        ea.attn_bwd(q, k, v, fo, do, fl, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods, ws, nws, stream)
-        for n, src in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+        if not fwd_only:
+            ea.attn_bwd(q, k, v, fo, do, fl, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods, ws, nws, stream)
+        for n, src in outs:
             out_host[n].copy_(src, non_blocking=True)
 
     e2e_ms = float("nan")
@@ -294,7 +374,9 @@ def run_ours(args, world, rank, local):
         e2e_ms = allmax(world, e0.elapsed_time(e1)) / e2e_steps
     ea.attn_status(stream)
 
-    fwd_f, bwd_f = flops(cfg)
+    fwd_f, bwd_f = flops(cfg, docs)
+    if fwd_only:
+        bwd_f = 0.0
     ms = total_ms / args.steps
     value = world * (fwd_f + bwd_f) / (ms * 1e-3) / 1e12
     peaks, src = load_peaks()
@@ -302,40 +384,136 @@ def run_ours(args, world, rank, local):
     burst = peaks["bf16_tflops"]
     fwd_t = fwd_f / (mean(k_fwd) * 1e-3) / 1e12
     bwd_ms = mean(k_pre) + mean(k_kv) + mean(k_dq)
-    bwd_t = bwd_f / (bwd_ms * 1e-3) / 1e12
+    bwd_t = bwd_f / (bwd_ms * 1e-3) / 1e12 if not fwd_only else 0.0
     # dominant kernel: the dK/dV kernel; its algorithmic work is 4 of the 5
     # backward GEMMs (S recompute, dP, dV, dK) = 2x the forward FLOPs.
-    kernels = {"fwd_bf16": (mean(k_fwd), fwd_f), "bwd_dkdv": (mean(k_kv), 0.8 * bwd_f),
-               "bwd_dq": (mean(k_dq), 0.2 * bwd_f), "bwd_pre": (mean(k_pre), 0.0)}
+    kernels = {"fwd_bf16": (mean(k_fwd), fwd_f)}
+    if not fwd_only:
+        kernels.update({"bwd_dkdv": (mean(k_kv), 0.8 * bwd_f), "bwd_dq": (mean(k_dq), 0.2 * bwd_f),
+                        "bwd_pre": (mean(k_pre), 0.0)})
     dom = max(kernels, key=lambda n: kernels[n][0])
     dom_ms, dom_flops = kernels[dom]
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1),
+                "peak": sustained, "unit": "TFLOP/s", "frac": round(achieved / sustained, 4),
+                "traffic": traffic_record(dom) if name == WORKLOAD and not args.heads else None,
+                "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside back-to-back steps)"}
+    if fwd_only:
+        # a forward this small is latency / HBM bound: bytes Q+K+V in, O + LSE out
+        nbytes = 2 * (B * Hq * N * d + 2 * B * Hkv * N * d + B * Hq * N * d) + 4 * B * Hq * N
+        gbs = nbytes / (mean(k_fwd) * 1e-3) / 1e9
+        roofline = {"kernel": "fwd_bf16", "bound": "hbm", "achieved": round(gbs, 1),
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 5),
+                    "traffic": None, "bytes_per_launch": nbytes,
+                    "peak_source": f"{src} hbm_gbs (inputs stay in L2 between steps: warm)"}
+    launches = (2 if with_map else 1) + (0 if fwd_only else (4 if with_map else 3))
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC if name == WORKLOAD else f"attention TFLOPS fwd{'' if fwd_only else '/bwd'} ({name})",
+        "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
-                   "mask": "causal", "parallelism": f"replicas{world}" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (Q/O/dO/dQ 128 MiB each, step working set ~700 MiB)"},
+        "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
+                   "mask": mods_label(cfg), "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": l2_note(cfg)},
         "fwd_tflops": round(fwd_t, 1), "bwd_tflops": round(bwd_t, 1),
         "fwd_frac_peak": round(fwd_t / sustained, 4), "bwd_frac_peak": round(bwd_t / sustained, 4),
         "fwd_frac_burst_peak": round(fwd_t / burst, 4), "bwd_frac_burst_peak": round(bwd_t / burst, 4),
         "kernel_ms": {n: round(t, 4) for n, (t, _) in kernels.items()},
-        "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1),
-                     "peak": sustained, "unit": "TFLOP/s", "frac": round(achieved / sustained, 4),
-                     "traffic": traffic_record(dom),
-                     "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside back-to-back steps)"},
+        "roofline": roofline,
         "e2e": None if not e2e_steps else {
             "value": round(world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tf, el, desc = oracle_sample(cfg, x, args.cpu_seconds, 512)
+        tf, el, desc = oracle_sample(dict(cfg, name=name), x, args.cpu_seconds, 512, fwd_only)
         line["cpu_baseline"] = {"value": round(tf, 5), "unit": UNIT, "cores": cpu_info(),
                                 "kind": "oracle", "sample": desc, "seconds": round(el, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_fp8(args, world, rank, local):
+    """The FP8 workload: signed-Hadamard + e4m3 prologue, then the e4m3
+    forward (non-causal), timed per kernel group with CUDA events."""
+    import exact_attention_66_gb300 as ea
+
+    name = args.workload
+    cfg = dict(gen.WORKLOADS[name])
+    B, Hq, Hkv, N, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"]
+    scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = gen.make_inputs(**dict(cfg, seed=cfg["seed"] + 97 * rank, need_do=False))
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    signs = torch.from_numpy(gen.hadamard_signs(Hkv, d, cfg["seed"] + 20)).to(dev)
+    q8 = torch.empty(q.shape, dtype=torch.uint8, device=dev)
+    k8 = torch.empty(k.shape, dtype=torch.uint8, device=dev)
+    v8 = torch.empty(v.shape, dtype=torch.uint8, device=dev)
+    sc = torch.empty(B * Hq + 2 * B * Hkv, dtype=torch.float32, device=dev)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    nq = ea.attn_workspace_size(ea.OP_QUANT_FP8, B, Hq, Hkv, N, d, None)
+    wq = torch.empty(nq, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ea.attn_hadamard_quant_fp8(q, k, v, q8, k8, v8, sc, signs, B, Hq, Hkv, N, d, wq, nq, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ea.attn_fwd_fp8(q8, k8, v8, sc, o, lse, B, Hq, Hkv, N, d, scale, None, None, 0, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ea.attn_status(stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    t0.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier(world)
+    ea.attn_status(stream)
+    ms = allmax(world, t0.elapsed_time(t1)) / args.steps
+    k_pro = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    k_fwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    peaks, src = load_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]  # dense e4m3 = 2x bf16 (nominal ratio)
+    fwd_f = 4.0 * Hq * d * allowed_pairs(cfg)
+    fwd_t = fwd_f / (k_fwd * 1e-3) / 1e12
+    rows = B * Hq * N + 2 * B * Hkv * N
+    pro_bytes = rows * (2 * 2 * d + d)  # bf16 row read by each of the two passes, e4m3 row written
+    pro_gbs = pro_bytes / (k_pro * 1e-3) / 1e9
+    line = {
+        "metric": f"attention TFLOPS fwd ({name}, e4m3)", "value": round(world * fwd_f / (ms * 1e-3) / 1e12, 2),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3", "data": "synthetic (0.1 % of entries x50)",
+        "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "mask": "none",
+                   "parallelism": "single" if world == 1 else f"replicas{world}", "l2": l2_note(cfg)},
+        "fwd_tflops": round(fwd_t, 1), "fwd_frac_fp8_peak": round(fwd_t / fp8_peak, 4),
+        "kernel_ms": {"hadamard_quant": round(k_pro, 4), "fwd_fp8": round(k_fwd, 4)},
+        "roofline": {"kernel": "fwd_fp8", "bound": "tensor", "achieved": round(fwd_t, 1), "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": round(fwd_t / fp8_peak, 4), "traffic": None,
+                     "peak_source": f"{src} bf16_tflops_sustained x 2 (nominal e4m3/bf16 ratio)"},
+        "prologue": {"achieved": round(pro_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(pro_gbs / peaks["hbm_gbs"], 4), "bytes": pro_bytes},
+        "e2e": None, "gpu_launches": 4 * args.steps, "clocks": clk,
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -386,6 +564,8 @@ def main():
                     help="time budget of the oracle CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host copies) leg")
+    ap.add_argument("--workload", choices=sorted(gen.WORKLOADS), default=WORKLOAD,
+                    help="workload to time; the default is the one the metric is quoted on")
     ap.add_argument("--heads", type=int, default=0,
                     help="query heads (8 per KV head) for a smaller profiling case; default: the workload's 64")
     args = ap.parse_args()

@@ -34,6 +34,14 @@ bool needs_map(uint32_t flags) { return (flags & (ATTN_MOD_WINDOW | ATTN_MOD_DOC
 
 size_t map_bytes(int B, int N) { return round_up((size_t)B * n_tiles(N) * n_tiles(N), 256); }
 
+// Workspace of the window / document mods: the block map, then (documents)
+// the run bounds of every position and the "ids not sorted" flag.
+size_t doc_bytes(int B, int N) { return round_up((size_t)B * N * sizeof(int2), 256) + 256; }
+size_t mods_bytes(int B, int N, uint32_t flags) {
+  if (!needs_map(flags)) return 0;
+  return map_bytes(B, N) + ((flags & ATTN_MOD_DOC) ? doc_bytes(B, N) : 0);
+}
+
 attn_status_t check_mods(const attn_mods_t* m) {
   if (!m) return ATTN_OK;
   const uint32_t known = ATTN_MOD_CAUSAL | ATTN_MOD_WINDOW | ATTN_MOD_DOC | ATTN_MOD_SOFTCAP |
@@ -151,6 +159,8 @@ AttnParams make_params(int B, int Hq, int Hkv, int N, float scale, const attn_mo
   p.doc_ids = (mods && (mods->flags & ATTN_MOD_DOC)) ? mods->doc_ids : nullptr;
   p.slopes = (mods && (mods->flags & ATTN_MOD_ALIBI)) ? mods->alibi_slopes : nullptr;
   p.map = nullptr;
+  p.doc_bounds = nullptr;
+  p.doc_unsorted = nullptr;
   p.status = status;
   return p;
 }
@@ -167,6 +177,22 @@ size_t bwd_rowstat_bytes(int B, int Hq, int N) {
 
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
+// Fill the mods workspace (block map, document runs) and point p at it.
+attn_status_t prepare_mods(AttnParams& p, uint8_t* region, cudaStream_t s) {
+  if (!needs_map(p.flags)) return ATTN_OK;
+  attn_status_t st;
+  if ((st = cuda_status(launch_block_map(p, region, s))) != ATTN_OK) return st;
+  p.map = region;
+  if (p.flags & ATTN_MOD_DOC) {
+    int2* bounds = reinterpret_cast<int2*>(region + map_bytes(p.B, p.N));
+    int* unsorted = reinterpret_cast<int*>(region + map_bytes(p.B, p.N) + doc_bytes(p.B, p.N) - 256);
+    if ((st = cuda_status(launch_doc_bounds(p, bounds, unsorted, s))) != ATTN_OK) return st;
+    p.doc_bounds = bounds;
+    p.doc_unsorted = unsorted;
+  }
+  return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -179,9 +205,9 @@ size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int N, int d, const a
   switch (op) {
     case ATTN_OP_FWD:
     case ATTN_OP_FWD_FP8:
-      return needs_map(f) ? map_bytes(B, N) : 0;
+      return mods_bytes(B, N, f);
     case ATTN_OP_BWD:
-      return bwd_rowstat_bytes(B, Hq, N) + (needs_map(f) ? map_bytes(B, N) : 0);
+      return bwd_rowstat_bytes(B, Hq, N) + mods_bytes(B, N, f);
     case ATTN_OP_QUANT_FP8:
       return round_up((size_t)(B * Hq + 2 * B * Hkv) * sizeof(unsigned), 256);
     default:
@@ -213,11 +239,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
     return ATTN_ERR_CUDA;
   L.o = o;
   L.lse = lse;
-  if (needs_map(L.p.flags)) {
-    uint8_t* map = static_cast<uint8_t*>(ws);
-    if ((st = cuda_status(launch_block_map(L.p, map, s))) != ATTN_OK) return st;
-    L.p.map = map;
-  }
+  if ((st = prepare_mods(L.p, static_cast<uint8_t*>(ws), s)) != ATTN_OK) return st;
   return cuda_status(launch_fwd_bf16(L, d, has_score_mods(L.p.flags), s));
 }
 
@@ -255,11 +277,7 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   L.dv = dv;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   L.rowstat = reinterpret_cast<float2*>(wsb);
-  if (needs_map(L.p.flags)) {
-    uint8_t* map = wsb + bwd_rowstat_bytes(B, Hq, N);
-    if ((st = cuda_status(launch_block_map(L.p, map, s))) != ATTN_OK) return st;
-    L.p.map = map;
-  }
+  if ((st = prepare_mods(L.p, wsb + bwd_rowstat_bytes(B, Hq, N), s)) != ATTN_OK) return st;
   if (events != nullptr)
     for (int e = 0; e < 4; ++e) L.events[e] = static_cast<cudaEvent_t>(events[e]);
   return cuda_status(launch_bwd(L, d, has_score_mods(L.p.flags), s));
@@ -328,11 +346,7 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const
   L.scales = scales;
   L.o = o;
   L.lse = lse;
-  if (needs_map(L.p.flags)) {
-    uint8_t* map = static_cast<uint8_t*>(ws);
-    if ((st = cuda_status(launch_block_map(L.p, map, s))) != ATTN_OK) return st;
-    L.p.map = map;
-  }
+  if ((st = prepare_mods(L.p, static_cast<uint8_t*>(ws), s)) != ATTN_OK) return st;
   return cuda_status(launch_fwd_fp8(L, has_score_mods(L.p.flags), s));
 }
 

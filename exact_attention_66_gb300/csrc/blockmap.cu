@@ -47,9 +47,44 @@ __global__ void __launch_bounds__(256) block_map_kernel(const AttnParams p, uint
   }
 }
 
+// Runs of equal document ids: for every position, the [start, end) of the run
+// holding it, by binary search on the ids of its batch row (which assumes
+// they do not decrease along N), and a flag set when some id does decrease
+// (the kernels then test ids element by element instead).
+__global__ void __launch_bounds__(256) doc_bounds_kernel(const int* __restrict__ doc, int B, int N,
+                                                         int2* __restrict__ bounds, int* __restrict__ unsorted) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= (long long)B * N) return;
+  const int b = (int)(t / N), pos = (int)(t - (long long)b * N);
+  const int* d = doc + (size_t)b * N;
+  const int id = d[pos];
+  if (pos + 1 < N && d[pos + 1] < id) atomicOr(unsorted, 1);
+  int lo = 0, hi = pos;  // first index whose id is >= id
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (d[mid] < id) lo = mid + 1; else hi = mid;
+  }
+  const int start = lo;
+  lo = pos + 1;
+  hi = N;  // first index whose id is > id
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (d[mid] <= id) lo = mid + 1; else hi = mid;
+  }
+  bounds[t] = make_int2(start, lo);
+}
+
 cudaError_t launch_block_map(const AttnParams& p, uint8_t* map, cudaStream_t st) {
   const dim3 grid(p.nT, p.nT, p.B);
   block_map_kernel<<<grid, 256, 0, st>>>(p, map);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_doc_bounds(const AttnParams& p, int2* bounds, int* unsorted, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(unsorted, 0, sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  const long long n = (long long)p.B * p.N;
+  doc_bounds_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(p.doc_ids, p.B, p.N, bounds, unsorted);
   return cudaGetLastError();
 }
 

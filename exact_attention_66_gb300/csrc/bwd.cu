@@ -425,6 +425,11 @@ __global__ void __launch_bounds__(384, 1)
     const bool doc = MODS && (p.flags & MOD_DOC);
     const float sc_in = p.scale / p.softcap, sc_out = p.softcap * LOG2E;
     const int doc_j = (doc && j < p.N) ? p.doc_ids[(size_t)b * p.N + j] : 0;
+    bool doc_runs = false;
+    const int2 run_j = doc ? doc_run(p, b, j, doc_runs) : make_int2(0, p.N);
+    const bool doc_each = doc && !doc_runs;  // ids tested element by element
+    const uint64_t sc_in2 = f2_pack(sc_in, sc_in), sc_out2 = f2_pack(sc_out, sc_out);
+    const uint64_t one2 = f2_pack(1.f, 1.f);
     bool ok = true;
     if (any) {
       int g = 0, I = steps.I_first, n = 0;
@@ -450,9 +455,14 @@ __global__ void __launch_bounds__(384, 1)
 
         // P = exp2(x - LSE) (0 where masked); s[] keeps P (times the
         // soft-cap derivative) for dS.  fp32 arithmetic in pairs.
-        const int lo = causal ? j - i0 : -0x7fffffff;   // valid iff c >= lo
-        const int hi = win ? p.window + j - i0 : 0x7fffffff;  // valid iff c < hi
+        int lo = causal ? j - i0 : -0x7fffffff;   // valid iff c >= lo
+        int hi = win ? p.window + j - i0 : 0x7fffffff;  // valid iff c < hi
+        if (doc_runs) {  // the query rows of this KV row's document: one interval
+          lo = max(lo, run_j.x - i0);
+          hi = min(hi, run_j.y - i0);
+        }
         const float al_base = al2 * (float)(j - i0);
+        const uint64_t al_base2 = f2_pack(al_base, al_base), nal2 = f2_pack(-al2, -al2);
         const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
         uint32_t pk[32];
 #pragma unroll
@@ -462,21 +472,16 @@ __global__ void __launch_bounds__(384, 1)
           const float s0 = __uint_as_float(s[c]), s1 = __uint_as_float(s[c + 1]);
           uint64_t x2, dmul2 = 0;
           if (sc || al) {
-            float x[2], dm[2] = {1.f, 1.f};
-            const float sv[2] = {s0, s1};
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              if (sc) {
-                const float t = tanh_exp(sv[e] * sc_in);
-                x[e] = t * sc_out;
-                dm[e] = fmaf(-t, t, 1.f);
-              } else {
-                x[e] = sv[e] * p.scale_log2;
-              }
-              if (al) x[e] = fmaf(-al2, (float)(c + e), x[e] + al_base);
+            uint64_t y2 = f2_pack(s0, s1);
+            if (sc) {
+              const uint64_t t2 = tanh2_exp(f2_mul(y2, sc_in2));
+              y2 = f2_mul(t2, sc_out2);
+              dmul2 = f2_fma(t2, f2_neg(t2), one2);  // 1 - t^2
+            } else {
+              y2 = f2_mul(y2, sl2);
             }
-            x2 = f2_add(f2_pack(x[0], x[1]), nl2);
-            dmul2 = f2_pack(dm[0], dm[1]);
+            if (al) y2 = f2_fma(f2_pack((float)c, (float)(c + 1)), nal2, f2_add(y2, al_base2));
+            x2 = f2_add(y2, nl2);
           } else {
             x2 = f2_fma(f2_pack(s0, s1), sl2, nl2);
           }
@@ -488,7 +493,7 @@ __global__ void __launch_bounds__(384, 1)
             for (int e = 0; e < 2; ++e) {
               const int cc = c + e;
               bool valid = (cc >= lo) && (cc < hi);
-              if (doc && valid)
+              if (doc_each && valid)
                 valid = (i0 + cc < p.N) && (__ldg(p.doc_ids + (size_t)b * p.N + i0 + cc) == doc_j);
               if (!valid) pe[e] = 0.f;
             }
@@ -738,6 +743,11 @@ __global__ void __launch_bounds__(384, 1)
     const uint64_t nl2 = f2_pack(-rs.x, -rs.x), ndd = f2_pack(-rs.y, -rs.y);
     const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
     const int doc_i = (doc && i < p.N) ? p.doc_ids[(size_t)b * p.N + i] : 0;
+    bool doc_runs = false;
+    const int2 run_i = doc ? doc_run(p, b, i, doc_runs) : make_int2(0, p.N);
+    const bool doc_each = doc && !doc_runs;  // ids tested element by element
+    const uint64_t sc_in2 = f2_pack(sc_in, sc_in), sc_out2 = f2_pack(sc_out, sc_out);
+    const uint64_t one2 = f2_pack(1.f, 1.f), al2x = f2_pack(al2, al2);
     uint8_t* ds_tile = smem + C::DS_OFF;
     bool ok = wait_warp(&S.in_full, 0, ab);
     if (ok) {  // warpgroup 0 copies Q, warpgroup 1 copies dO into TMEM
@@ -760,8 +770,12 @@ __global__ void __launch_bounds__(384, 1)
       mbar_arrive(&S.s_free);
 
       const int j0 = J * TILE + 64 * w;  // key row of column 0
-      const int hi_lim = min(causal ? i : 0x7fffffff, p.N - 1) - j0;  // valid iff c <= hi_lim
-      const int lo_lim = win ? i - p.window - j0 : -0x7fffffff;        // valid iff c > lo_lim
+      int hi_lim = min(causal ? i : 0x7fffffff, p.N - 1) - j0;  // valid iff c <= hi_lim
+      int lo_lim = win ? i - p.window - j0 : -0x7fffffff;        // valid iff c > lo_lim
+      if (doc_runs) {  // the keys of this query row's document: one interval
+        hi_lim = min(hi_lim, run_i.y - 1 - j0);
+        lo_lim = max(lo_lim, run_i.x - 1 - j0);
+      }
       const float al_base = al2 * (float)(j0 - i);
       uint32_t dw[32];
 #pragma unroll
@@ -769,21 +783,16 @@ __global__ void __launch_bounds__(384, 1)
         const float s0 = __uint_as_float(s[k]), s1 = __uint_as_float(s[k + 1]);
         uint64_t x2, dmul2 = 0;
         if (sc || al) {
-          float x[2], dm[2] = {1.f, 1.f};
-          const float sv[2] = {s0, s1};
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            if (sc) {
-              const float t = tanh_exp(sv[e] * sc_in);
-              x[e] = t * sc_out;
-              dm[e] = fmaf(-t, t, 1.f);
-            } else {
-              x[e] = sv[e] * p.scale_log2;
-            }
-            if (al) x[e] = fmaf(al2, (float)(k + e), x[e] + al_base);
+          uint64_t y2 = f2_pack(s0, s1);
+          if (sc) {
+            const uint64_t t2 = tanh2_exp(f2_mul(y2, sc_in2));
+            y2 = f2_mul(t2, sc_out2);
+            dmul2 = f2_fma(t2, f2_neg(t2), one2);  // 1 - t^2
+          } else {
+            y2 = f2_mul(y2, sl2);
           }
-          x2 = f2_add(f2_pack(x[0], x[1]), nl2);
-          dmul2 = f2_pack(dm[0], dm[1]);
+          if (al) y2 = f2_fma(f2_pack((float)k, (float)(k + 1)), al2x, f2_add(y2, f2_pack(al_base, al_base)));
+          x2 = f2_add(y2, nl2);
         } else {
           x2 = f2_fma(f2_pack(s0, s1), sl2, nl2);
         }
@@ -795,7 +804,7 @@ __global__ void __launch_bounds__(384, 1)
           for (int e = 0; e < 2; ++e) {
             const int c = k + e;
             bool valid = (c <= hi_lim) && (c > lo_lim);
-            if (doc && valid) valid = (__ldg(p.doc_ids + (size_t)b * p.N + j0 + c) == doc_i);
+            if (doc_each && valid) valid = (__ldg(p.doc_ids + (size_t)b * p.N + j0 + c) == doc_i);
             if (!valid) pe[e] = 0.f;
           }
         }

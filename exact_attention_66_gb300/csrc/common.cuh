@@ -37,6 +37,12 @@ struct AttnParams {
   int window;
   float softcap;
   const int* doc_ids;   // [B, N] or nullptr
+  // Document runs: [start, end) of the run of equal ids around each position
+  // ([B, N], workspace), valid when *doc_unsorted == 0 (ids non-decreasing
+  // along N: every document is then one run, and the document mask of a row
+  // is an interval of columns).  Both nullptr without the document mod.
+  const int2* doc_bounds;
+  const int* doc_unsorted;
   const float* slopes;  // [Hq] or nullptr (default slopes)
   const uint8_t* map;   // [B, nT, nT] tile classes, or nullptr (analytic)
   int* status;          // device status word
@@ -68,6 +74,32 @@ __device__ __forceinline__ float tanh_exp(float y) {
   return copysignf(t, y);
 }
 
+// The same for a pair of lanes, its fp32 arithmetic two lanes per instruction
+// (scalar fp32 on the softmax warps slows the tensor pipe; the two-wide form
+// does not).
+__device__ __forceinline__ uint64_t tanh2_exp(uint64_t y2) {
+  float y0, y1;
+  f2_unpack(y2, y0, y1);
+  const uint32_t b0 = __float_as_uint(y0), b1 = __float_as_uint(y1);
+  float z0, z1;
+  f2_unpack(f2_mul(f2_pack(__uint_as_float(b0 & 0x7fffffffu), __uint_as_float(b1 & 0x7fffffffu)),
+                   f2_pack(2.0f * LOG2E, 2.0f * LOG2E)), z0, z1);
+  float u0, u1;
+  f2_unpack(f2_add(f2_pack(ex2(z0), ex2(z1)), f2_pack(1.0f, 1.0f)), u0, u1);
+  float t0, t1;
+  f2_unpack(f2_fma(f2_pack(rcp_approx(u0), rcp_approx(u1)), f2_pack(-2.0f, -2.0f), f2_pack(1.0f, 1.0f)), t0, t1);
+  return f2_pack(__uint_as_float(__float_as_uint(t0) | (b0 & 0x80000000u)),
+                 __uint_as_float(__float_as_uint(t1) | (b1 & 0x80000000u)));
+}
+
+// Document run [start, end) of position `pos` when the ids are runs, else
+// the whole sequence (the caller then tests ids element by element).
+__device__ __forceinline__ int2 doc_run(const AttnParams& p, int b, int pos, bool& runs) {
+  runs = p.doc_bounds != nullptr && *p.doc_unsorted == 0;
+  if (!runs || pos >= p.N) return make_int2(0, p.N);
+  return p.doc_bounds[(size_t)b * p.N + pos];
+}
+
 // Every lane of the warp waits; the warp proceeds only if all of them saw the
 // phase complete (keeps the warp converged for the .sync.aligned tcgen05 ops).
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const Abort& ab) {
@@ -81,6 +113,8 @@ struct RowMods {
   float sc_out;    // softcap: c * log2(e)
   float alibi_l2;  // slope * log2(e)
   int doc_i;       // doc id of the row
+  int2 doc_run;    // its document's columns [start, end) when doc_runs
+  bool doc_runs;
 };
 
 }  // namespace attn

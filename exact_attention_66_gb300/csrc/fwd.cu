@@ -401,6 +401,9 @@ __global__ void __launch_bounds__(384, 1)
       rm.sc_out = p.softcap * LOG2E;
       rm.alibi_l2 = (p.flags & MOD_ALIBI) ? alibi_slope(p, hq) * LOG2E : 0.f;
       rm.doc_i = ((p.flags & MOD_DOC) && i < p.N) ? p.doc_ids[(size_t)b * p.N + i] : 0;
+      rm.doc_runs = false;
+      rm.doc_run = make_int2(0, p.N);
+      if (p.flags & MOD_DOC) rm.doc_run = doc_run(p, b, i, rm.doc_runs);
     }
     float m = -INFINITY, l = 0.f;
     int ns = 0;
@@ -443,20 +446,37 @@ __global__ void __launch_bounds__(384, 1)
         const bool al = (p.flags & MOD_ALIBI) != 0;
         const bool win = (p.flags & MOD_WINDOW) != 0;
         const bool doc = (p.flags & MOD_DOC) != 0;
-        const float al_row = rm.alibi_l2 * (float)(j0 - i);
-        const int lo_lim = win ? (i - p.window - j0) : -0x7fffffff;  // valid iff c > lo_lim
+        int lo_lim = win ? (i - p.window - j0) : -0x7fffffff;  // valid iff c > lo_lim
+        int hi_m = hi_lim;                                      // valid iff c <= hi_m
+        if (doc && rm.doc_runs) {  // the row's document is one run of columns
+          lo_lim = max(lo_lim, rm.doc_run.x - 1 - j0);
+          hi_m = min(hi_m, rm.doc_run.y - 1 - j0);
+        }
+        const bool doc_each = doc && !rm.doc_runs;  // ids tested element by element
         const int* drow = doc ? p.doc_ids + (size_t)b * p.N + j0 : nullptr;
+        // fp32 arithmetic two lanes per instruction (see tanh2_exp).
+        const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
+        const uint64_t sc_in2 = f2_pack(rm.sc_in, rm.sc_in), sc_out2 = f2_pack(rm.sc_out, rm.sc_out);
+        const uint64_t al2 = f2_pack(rm.alibi_l2, rm.alibi_l2);
+        const float al_row = rm.alibi_l2 * (float)(j0 - i);
+        const uint64_t al_row2 = f2_pack(al_row, al_row);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          float x = __uint_as_float(s[c]);
-          x = sc ? tanh_exp(x * rm.sc_in) * rm.sc_out : x * scale_log2;
-          if (al) x = fmaf(rm.alibi_l2, (float)c, x + al_row);
+        for (int c = 0; c < 128; c += 2) {
+          uint64_t x2 = f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+          x2 = sc ? f2_mul(tanh2_exp(f2_mul(x2, sc_in2)), sc_out2) : f2_mul(x2, sl2);
+          if (al) x2 = f2_fma(f2_pack((float)c, (float)(c + 1)), al2, f2_add(x2, al_row2));
+          float x[2];
+          f2_unpack(x2, x[0], x[1]);
           if (partial) {
-            bool valid = (c <= hi_lim) && (c > lo_lim);
-            if (doc && valid) valid = (__ldg(drow + c) == rm.doc_i);
-            if (!valid) x = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              bool valid = (c + e <= hi_m) && (c + e > lo_lim);
+              if (doc_each && valid) valid = (__ldg(drow + c + e) == rm.doc_i);
+              if (!valid) x[e] = -INFINITY;
+            }
           }
-          s[c] = __float_as_uint(x);
+          s[c] = __float_as_uint(x[0]);
+          s[c + 1] = __float_as_uint(x[1]);
         }
         mt = row_max128(s);
       }

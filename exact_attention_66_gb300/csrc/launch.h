@@ -39,6 +39,7 @@ struct BwdLaunch {
 cudaError_t launch_bwd(const BwdLaunch& L, int d, bool mods, cudaStream_t st);
 
 cudaError_t launch_block_map(const AttnParams& p, uint8_t* map, cudaStream_t st);
+cudaError_t launch_doc_bounds(const AttnParams& p, int2* bounds, int* unsorted, cudaStream_t st);
 
 cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, void* q8, void* k8,
                                   void* v8, float* scales, const int8_t* signs, int B, int Hq,

@@ -391,6 +391,8 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+// Both lanes negated (sign bits flipped, no fp32 instruction).
+__device__ __forceinline__ uint64_t f2_neg(uint64_t a) { return a ^ 0x8000000080000000ull; }
 // Scalar fp32 add / mul / fma on the warps beside an MMA stream slow the
 // tensor pipe several-fold on this part, while the two-wide forms above do
 // not: the hot loops next to the MMAs do their fp32 arithmetic in pairs.

@@ -15,3 +15,18 @@ def pytest_sessionstart(session):
     if session.config.getoption("-m", default="") == "gpu":
         import __graft_entry__
         __graft_entry__.build()
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write the largest errors the GPU parity tests saw, if asked to."""
+    path = os.environ.get("ATTN_PARITY_REPORT")
+    if not path:
+        return
+    try:
+        from gpu_common import REPORT
+    except ImportError:
+        return
+    if REPORT:
+        import json
+        with open(path, "w") as f:
+            json.dump(REPORT, f, indent=1, sort_keys=True)

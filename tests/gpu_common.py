@@ -12,6 +12,16 @@ LSE_TOL = 1e-3    # max |LSE_gpu - LSE_oracle|
 GRAD_TOL = 2e-2   # ||G_gpu - G_oracle||_F / ||G_oracle||_F for dQ, dK, dV
 
 
+# Largest error seen per (workload, quantity), written out at the end of the
+# session when ATTN_PARITY_REPORT names a file (tests/conftest.py).
+REPORT = {}
+
+
+def record(workload, key, value):
+    cur = REPORT.setdefault(workload, {})
+    cur[key] = max(cur.get(key, 0.0), float(value))
+
+
 def lib():
     import exact_attention_66_gb300 as ea
     return ea

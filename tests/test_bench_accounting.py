@@ -1,0 +1,34 @@
+"""The benchmark's FLOP accounting (allowed query/key pairs, per row and in
+total) against the oracle's mask, on small seeded cases of every mask kind."""
+import numpy as np
+import pytest
+
+import attn_inputs as gen
+import bench
+from oracle import attn64
+
+CASES = [
+    dict(B=1, Hq=1, Hkv=1, N=300, d=64, causal=False, seed=1),
+    dict(B=2, Hq=1, Hkv=1, N=257, d=64, causal=True, seed=2),
+    dict(B=2, Hq=1, Hkv=1, N=700, d=64, causal=True, window=129, seed=3),
+    dict(B=3, Hq=1, Hkv=1, N=900, d=64, causal=True, window=200, doc=True, seed=4),
+    dict(B=2, Hq=1, Hkv=1, N=1000, d=64, causal=True, doc=True, seed=5),
+]
+
+
+@pytest.mark.parametrize("cfg", CASES, ids=lambda c: "-".join(k for k in ("causal", "window", "doc") if c.get(k)) or "none")
+def test_pair_counts_match_the_oracle_mask(cfg):
+    x = gen.make_inputs(**cfg)
+    docs = x.get("doc_ids")
+    m = attn64.Mods(causal=cfg.get("causal", False), window=cfg.get("window"), doc_ids=docs)
+    assert bench.allowed_pairs(cfg, docs) == attn64.flop_pairs(m, cfg["B"], cfg["N"])
+    rows = np.arange(0, cfg["N"], 7)
+    for b in range(cfg["B"]):
+        want = attn64.allowed(m, b, rows, np.arange(cfg["N"])).sum(axis=1)
+        assert np.array_equal(bench.row_pairs(cfg, docs, b, rows), want)
+
+
+def test_gqa_8k_flops():
+    fwd, bwd = bench.flops(gen.WORKLOADS["gqa_causal_8k"])
+    assert fwd == 4 * 64 * 128 * 8192 * 8193 // 2
+    assert bwd == 2.5 * fwd

@@ -24,6 +24,9 @@ CASES = [
     (1, 4, 4, 520, 128, dict(causal=True, alibi=True)),
     (2, 4, 2, 1000, 128, dict(causal=True, window=257, doc=True, softcap=30.0, alibi=True)),
     (1, 2, 2, 777, 64, dict(causal=True, window=129, doc=True, softcap=5.0, alibi=True)),
+    # document ids that are not one run per document (id = run index mod 3)
+    (2, 2, 2, 900, 128, dict(causal=True, doc="mod3")),
+    (1, 2, 2, 600, 64, dict(doc="mod3", softcap=20.0, alibi=True)),
 ]
 
 
@@ -38,8 +41,10 @@ def _run(case, seed):
     x = inputs(B, Hq, Hkv, N, d, seed=seed)
     if mk.get("doc"):
         x["doc_ids_np"] = gen.doc_ids(B, N, N, lo=60, hi=400)
+        if mk["doc"] == "mod3":
+            x["doc_ids_np"] = (x["doc_ids_np"] % 3).astype(np.int32)
     dev = to_dev(x)
-    m, om = mods_pair(x, **mk)
+    m, om = mods_pair(x, **dict(mk, doc=bool(mk.get("doc"))))
     s = default_scale(d)
     o, lse = ea.forward(dev["q"], dev["k"], dev["v"], s, m)
     dq, dk, dv = ea.backward(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], s, m)

@@ -12,7 +12,7 @@ import torch
 
 import attn_inputs as gen
 from oracle import attn64
-from gpu_common import LSE_TOL, lib, max_abs
+from gpu_common import LSE_TOL, lib, max_abs, record
 
 pytestmark = pytest.mark.gpu
 
@@ -110,4 +110,6 @@ def test_fp8_outlier_workload_hadamard_lowers_error():
             err[name].append((outs[name][b, h, rows] - O).ravel())
     rmse = {k: float(np.sqrt(np.mean(np.concatenate(v) ** 2))) for k, v in err.items()}
     print(f"fp8 outlier workload RMSE(O): {rmse} ratio {rmse['plain'] / rmse['hadamard']:.2f}")
+    record("fp8_outliers_16k", "RMSE_O_hadamard", rmse["hadamard"])
+    record("fp8_outliers_16k", "RMSE_O_plain", rmse["plain"])
     assert rmse["hadamard"] < rmse["plain"]

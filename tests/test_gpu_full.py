@@ -9,7 +9,7 @@ import torch
 
 import attn_inputs as gen
 from oracle import attn64
-from gpu_common import GRAD_TOL, LSE_TOL, O_TOL, lib, max_abs, rel_fro
+from gpu_common import GRAD_TOL, LSE_TOL, O_TOL, lib, max_abs, record, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -45,6 +45,7 @@ def _run_full(name):
 
 # (workload, [(b, hk) groups to check], sample everything in a group?)
 FULL = [
+    ("tiny_mha", [(0, 0), (0, 1)]),
     ("causal_mha_2k", [(0, 0), (7, 9), (15, 15)]),
     ("flex_mods_4k", [(0, 0), (3, 15)]),
     ("gqa_causal_8k", [(0, 0), (0, 7)]),
@@ -61,10 +62,16 @@ def test_full_size_sampled_parity(name, groups):
         heads = range(hk * G, (hk + 1) * G)
         for hq in list(heads)[:2] + [hk * G + G - 1]:
             O, L = attn64.head_forward(x["q"], x["k"], x["v"], s, om, b, hq, rows=rows)
-            assert max_abs(o[b, hq, rows], O) <= O_TOL
-            assert max_abs(lse[b, hq, rows], L) <= LSE_TOL
+            eo, el = max_abs(o[b, hq, rows], O), max_abs(lse[b, hq, rows], L)
+            record(name, "O_max_abs", eo)
+            record(name, "LSE_max_abs", el)
+            assert eo <= O_TOL
+            assert el <= LSE_TOL
         gq, gk, gv = attn64.sampled_backward(x["q"], x["k"], x["v"], x["do"], s, om, b, hk,
                                              q_rows=rows, kv_rows=rows)
-        assert rel_fro(dq[b, hk * G:(hk + 1) * G][:, rows], gq) <= GRAD_TOL
-        assert rel_fro(dk[b, hk, rows], gk) <= GRAD_TOL
-        assert rel_fro(dv[b, hk, rows], gv) <= GRAD_TOL
+        errs = {"dQ_rel_fro": rel_fro(dq[b, hk * G:(hk + 1) * G][:, rows], gq),
+                "dK_rel_fro": rel_fro(dk[b, hk, rows], gk),
+                "dV_rel_fro": rel_fro(dv[b, hk, rows], gv)}
+        for key, e in errs.items():
+            record(name, key, e)
+            assert e <= GRAD_TOL, (key, e)

@@ -29,6 +29,10 @@ CASES = [
     (1, 4, 4, 520, 128, dict(causal=True, alibi=True)),
     (2, 4, 2, 1000, 128, dict(causal=True, window=257, doc=True, softcap=30.0, alibi=True)),
     (1, 2, 2, 777, 64, dict(causal=True, window=129, doc=True, softcap=5.0, alibi=True)),
+    # document ids that are not one run per document (id = run index mod 3): the
+    # kernels test ids element by element instead of using run intervals
+    (2, 2, 2, 900, 128, dict(causal=True, doc="mod3")),
+    (1, 2, 2, 600, 64, dict(doc="mod3", softcap=20.0, alibi=True)),
 ]
 
 
@@ -48,8 +52,10 @@ def test_forward_parity(case):
     x = inputs(B, Hq, Hkv, N, d, seed=100 + N + d + Hq)
     if mk.get("doc"):
         x["doc_ids_np"] = _docs(B, N, N)
+        if mk["doc"] == "mod3":
+            x["doc_ids_np"] = (x["doc_ids_np"] % 3).astype(np.int32)
     dev = to_dev(x)
-    m, om = mods_pair(x, **mk)
+    m, om = mods_pair(x, **dict(mk, doc=bool(mk.get("doc"))))
     s = default_scale(d)
     o, lse = ea.forward(dev["q"], dev["k"], dev["v"], s, m)
     ea.attn_status()
