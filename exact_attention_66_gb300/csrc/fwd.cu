@@ -207,6 +207,46 @@ __device__ __forceinline__ void store_p_smem(uint8_t* tile, int r, const uint32_
   }
 }
 
+// Score mods of one row of a tile, in place, in log2 units: x = scale s, or
+// the soft-cap c tanh(scale s / c); minus the ALiBi bias; -inf where the mask
+// (column interval [lo_lim + 1, hi_lim], and the element-wise document test
+// when drow is set) forbids the pair on partial tiles.  fp32 arithmetic two
+// lanes per instruction.
+struct ModsArgs {
+  float scale_log2, sc_in, sc_out, alibi_l2, al_row;
+  int hi_lim, lo_lim;
+  const int* drow;  // document ids of the tile's columns, element-wise test
+  int doc_i;
+  bool partial;
+};
+template <bool SC, bool AL>
+__device__ __forceinline__ void score_mods(uint32_t (&s)[128], const ModsArgs& a) {
+  const uint64_t sl2 = f2_pack(a.scale_log2, a.scale_log2);
+  const uint64_t sc_in2 = f2_pack(a.sc_in, a.sc_in), sc_out2 = f2_pack(a.sc_out, a.sc_out);
+  const uint64_t al2 = f2_pack(a.alibi_l2, a.alibi_l2), al_row2 = f2_pack(a.al_row, a.al_row);
+#pragma unroll
+  for (int c = 0; c < 128; c += 2) {
+    uint64_t x2 = f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+    if (SC)
+      x2 = f2_mul(tanh2_exp(f2_mul(x2, sc_in2)), sc_out2);
+    else
+      x2 = f2_mul(x2, sl2);
+    if (AL) x2 = f2_fma(f2_pack((float)c, (float)(c + 1)), al2, f2_add(x2, al_row2));
+    float x0, x1;
+    f2_unpack(x2, x0, x1);
+    s[c] = __float_as_uint(x0);
+    s[c + 1] = __float_as_uint(x1);
+  }
+  if (a.partial) {
+#pragma unroll
+    for (int c = 0; c < 128; ++c) {
+      bool valid = (c <= a.hi_lim) && (c > a.lo_lim);
+      if (a.drow != nullptr && valid) valid = (__ldg(a.drow + c) == a.doc_i);
+      if (!valid) s[c] = __float_as_uint(-INFINITY);
+    }
+  }
+}
+
 template <int D, bool MODS, bool FP8>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -454,30 +494,15 @@ __global__ void __launch_bounds__(384, 1)
         }
         const bool doc_each = doc && !rm.doc_runs;  // ids tested element by element
         const int* drow = doc ? p.doc_ids + (size_t)b * p.N + j0 : nullptr;
-        // fp32 arithmetic two lanes per instruction (see tanh2_exp).
-        const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
-        const uint64_t sc_in2 = f2_pack(rm.sc_in, rm.sc_in), sc_out2 = f2_pack(rm.sc_out, rm.sc_out);
-        const uint64_t al2 = f2_pack(rm.alibi_l2, rm.alibi_l2);
+        // The score mods in log2 units, specialised on soft-cap / ALiBi so the
+        // unrolled loop carries no dead work.
         const float al_row = rm.alibi_l2 * (float)(j0 - i);
-        const uint64_t al_row2 = f2_pack(al_row, al_row);
-#pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          uint64_t x2 = f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-          x2 = sc ? f2_mul(tanh2_exp(f2_mul(x2, sc_in2)), sc_out2) : f2_mul(x2, sl2);
-          if (al) x2 = f2_fma(f2_pack((float)c, (float)(c + 1)), al2, f2_add(x2, al_row2));
-          float x[2];
-          f2_unpack(x2, x[0], x[1]);
-          if (partial) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              bool valid = (c + e <= hi_m) && (c + e > lo_lim);
-              if (doc_each && valid) valid = (__ldg(drow + c + e) == rm.doc_i);
-              if (!valid) x[e] = -INFINITY;
-            }
-          }
-          s[c] = __float_as_uint(x[0]);
-          s[c + 1] = __float_as_uint(x[1]);
-        }
+        const ModsArgs ma{scale_log2, rm.sc_in, rm.sc_out, rm.alibi_l2, al_row, hi_m, lo_lim,
+                          doc_each ? drow : nullptr, rm.doc_i, partial};
+        if (sc && al) score_mods<true, true>(s, ma);
+        else if (sc) score_mods<true, false>(s, ma);
+        else if (al) score_mods<false, true>(s, ma);
+        else score_mods<false, false>(s, ma);
         mt = row_max128(s);
       }
 
