@@ -39,6 +39,9 @@ WORKLOADS = {
                          doc=True, softcap=30.0, alibi=True, seed=4000),
     "fp8_outliers_16k": dict(B=2, Hq=16, Hkv=16, N=16384, d=128, causal=False,
                              outlier_frac=1e-3, outlier_scale=50.0, seed=5000),
+    # packed variable-length sequences (lengths drawn like the documents), causal
+    "varlen_packed_16k": dict(B=1, Hq=16, Hkv=4, N=16384, d=128, causal=True, doc=True,
+                              varlen=True, seed=6000),
 }
 
 DOC_LEN_MIN = 128

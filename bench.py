@@ -264,6 +264,8 @@ def run_ours(args, world, rank, local):
 
     if args.workload == "fp8_outliers_16k":
         return run_fp8(args, world, rank, local)
+    if gen.WORKLOADS[args.workload].get("varlen"):
+        return run_varlen(args, world, rank, local)
     name = args.workload
     cfg = dict(gen.WORKLOADS[name])
     if args.heads:  # smaller case of the same shape family (profiling); 8 query heads per KV head
@@ -431,6 +433,92 @@ def run_ours(args, world, rank, local):
         tf, el, desc = oracle_sample(dict(cfg, name=name), x, args.cpu_seconds, 512, fwd_only)
         line["cpu_baseline"] = {"value": round(tf, 5), "unit": UNIT, "cores": cpu_info(),
                                 "kind": "oracle", "sample": desc, "seconds": round(el, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_varlen(args, world, rank, local):
+    """Packed variable-length sequences through attn_fwd_varlen /
+    attn_bwd_varlen (causal inside each sequence), timed per call."""
+    import exact_attention_66_gb300 as ea
+
+    name = args.workload
+    cfg = dict(gen.WORKLOADS[name])
+    B, Hq, Hkv, N, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"]
+    scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = gen.make_inputs(**dict(cfg, seed=cfg["seed"] + 97 * rank))
+    ids = x["doc_ids"][0]
+    cu = np.concatenate([[0], np.cumsum(np.bincount(ids))]).astype(np.int32)
+    n_seqs = len(cu) - 1
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    dcu = torch.from_numpy(cu).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((1, Hq, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    mods = ea.make_mods(causal=True)
+    nf = ea.attn_workspace_size(ea.OP_FWD_VARLEN, 1, Hq, Hkv, N, d, mods)
+    nb = ea.attn_workspace_size(ea.OP_BWD_VARLEN, 1, Hq, Hkv, N, d, mods)
+    wf = torch.empty(nf, dtype=torch.uint8, device=dev)
+    wb = torch.empty(nb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ea.attn_fwd_varlen(q, k, v, o, lse, dcu, n_seqs, Hq, Hkv, N, d, scale, mods, wf, nf, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ea.attn_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, dcu, n_seqs, Hq, Hkv, N, d, scale, mods,
+                           wb, nb, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ea.attn_status(stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    t0.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier(world)
+    ea.attn_status(stream)
+    ms = allmax(world, t0.elapsed_time(t1)) / args.steps
+    k_fwd = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    k_bwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    peaks, src = load_peaks()
+    sustained = peaks["bf16_tflops_sustained"]
+    fwd_f, bwd_f = flops(cfg, x["doc_ids"])
+    fwd_t = fwd_f / (k_fwd * 1e-3) / 1e12
+    bwd_t = bwd_f / (k_bwd * 1e-3) / 1e12
+    line = {
+        "metric": f"attention TFLOPS fwd/bwd ({name})",
+        "value": round(world * (fwd_f + bwd_f) / (ms * 1e-3) / 1e12, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "B": 1, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "n_seqs": n_seqs,
+                   "mask": "causal within each packed sequence",
+                   "parallelism": "single" if world == 1 else f"replicas{world}", "l2": l2_note(cfg)},
+        "fwd_tflops": round(fwd_t, 1), "bwd_tflops": round(bwd_t, 1),
+        "fwd_frac_peak": round(fwd_t / sustained, 4), "bwd_frac_peak": round(bwd_t / sustained, 4),
+        "kernel_ms": {"fwd_varlen (ids, map, runs, forward)": round(k_fwd, 4),
+                      "bwd_varlen (ids, map, runs, row stats, dK/dV, dQ)": round(k_bwd, 4)},
+        "roofline": {"kernel": "bwd_varlen", "bound": "tensor", "achieved": round(bwd_t, 1),
+                     "peak": sustained, "unit": "TFLOP/s", "frac": round(bwd_t / sustained, 4), "traffic": None,
+                     "peak_source": f"{src} bf16_tflops_sustained"},
+        "e2e": None, "gpu_launches": 10 * args.steps, "clocks": clk,
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -13,15 +13,17 @@ import math
 
 from ._lib import (  # noqa: F401
     AttnError, Mods, EXPORTS, MOD_ALIBI, MOD_CAUSAL, MOD_DOC, MOD_SOFTCAP, MOD_WINDOW, OP_BWD,
-    OP_FWD, OP_FWD_FP8, OP_QUANT_FP8, TILE_FULL, TILE_PARTIAL, TILE_SKIP, attn_block_map, attn_bwd,
-    attn_bwd_profiled, attn_bwd_noalloc, NOALLOC_SCRATCH_BYTES,
-    attn_fwd, attn_fwd_fp8, attn_hadamard_quant_fp8, attn_status, attn_workspace_size, lib,
+    OP_BWD_VARLEN, OP_FWD, OP_FWD_FP8, OP_FWD_VARLEN, OP_QUANT_FP8, TILE_FULL, TILE_PARTIAL,
+    TILE_SKIP, attn_block_map, attn_bwd, attn_bwd_profiled, attn_bwd_noalloc, attn_bwd_varlen,
+    NOALLOC_SCRATCH_BYTES, attn_fwd, attn_fwd_fp8, attn_fwd_varlen, attn_hadamard_quant_fp8,
+    attn_status, attn_workspace_size, lib,
     make_mods, status_string,
 )
 
 __all__ = [
-    "forward", "backward", "hadamard_quant_fp8", "forward_fp8", "block_map", "make_mods",
-    "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc", "attn_hadamard_quant_fp8", "attn_fwd_fp8", "attn_block_map",
+    "forward", "backward", "forward_varlen", "backward_varlen", "hadamard_quant_fp8", "forward_fp8",
+    "block_map", "make_mods", "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc",
+    "attn_fwd_varlen", "attn_bwd_varlen", "attn_hadamard_quant_fp8", "attn_fwd_fp8", "attn_block_map",
     "attn_status", "attn_workspace_size", "AttnError",
 ]
 
@@ -64,6 +66,33 @@ def backward(q, k, v, o, lse, do, scale=None, mods=None, stream=None):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws, nws = _workspace(OP_BWD, B, Hq, Hkv, N, d, mods, q.device)
     attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods, ws, nws, stream)
+    return dq, dk, dv
+
+
+def forward_varlen(q, k, v, cu_seqlens, scale=None, mods=None, stream=None):
+    """(O, LSE) over packed sequences: q [1, Hq, total, d], k/v [1, Hkv, total, d],
+    cu_seqlens a device int32 tensor of the n_seqs + 1 sequence offsets."""
+    torch = _torch()
+    B, Hq, Hkv, total, d = _shape(q, k)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    n_seqs = cu_seqlens.numel() - 1
+    o = torch.empty_like(q)
+    l = torch.empty((1, Hq, total), dtype=torch.float32, device=q.device)
+    ws, nws = _workspace(OP_FWD_VARLEN, 1, Hq, Hkv, total, d, mods, q.device)
+    attn_fwd_varlen(q, k, v, o, l, cu_seqlens, n_seqs, Hq, Hkv, total, d, scale, mods, ws, nws, stream)
+    return o, l
+
+
+def backward_varlen(q, k, v, o, lse, do, cu_seqlens, scale=None, mods=None, stream=None):
+    """(dQ, dK, dV) for the forward_varlen that produced (o, lse)."""
+    torch = _torch()
+    B, Hq, Hkv, total, d = _shape(q, k)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    n_seqs = cu_seqlens.numel() - 1
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws, nws = _workspace(OP_BWD_VARLEN, 1, Hq, Hkv, total, d, mods, q.device)
+    attn_bwd_varlen(q, k, v, o, do, lse, dq, dk, dv, cu_seqlens, n_seqs, Hq, Hkv, total, d, scale, mods,
+                    ws, nws, stream)
     return dq, dk, dv
 
 

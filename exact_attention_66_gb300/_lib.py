@@ -21,12 +21,12 @@ STATUS_NAMES = {
 }
 
 MOD_CAUSAL, MOD_WINDOW, MOD_DOC, MOD_SOFTCAP, MOD_ALIBI = 1, 2, 4, 8, 16
-OP_FWD, OP_BWD, OP_FWD_FP8, OP_QUANT_FP8 = 0, 1, 2, 3
+OP_FWD, OP_BWD, OP_FWD_FP8, OP_QUANT_FP8, OP_FWD_VARLEN, OP_BWD_VARLEN = 0, 1, 2, 3, 4, 5
 TILE_SKIP, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 
 # Exported symbols, in the order include/attn.h declares them.
 EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc",
-           "attn_hadamard_quant_fp8",
+           "attn_fwd_varlen", "attn_bwd_varlen", "attn_hadamard_quant_fp8",
            "attn_fwd_fp8", "attn_block_map", "attn_status", "attn_status_string")
 
 
@@ -55,6 +55,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_bwd_profiled.argtypes = lib.attn_bwd.argtypes + [ctypes.POINTER(ctypes.c_void_p)]
     lib.attn_bwd_noalloc.argtypes = lib.attn_bwd.argtypes[:16] + [vp]  # no ws, ws_bytes
+    lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
+    lib.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_hadamard_quant_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp]
     lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_block_map.argtypes = [mp, i, i, vp, vp]
@@ -159,6 +161,21 @@ def attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale,
     _check(_lib.attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                                  _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, float(scale),
                                  _mods_ref(mods), _stream(stream)), "attn_bwd_noalloc")
+
+
+def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, n_seqs, Hq, Hkv, total, d, scale, mods=None,
+                    ws=None, ws_bytes=0, stream=None):
+    _check(_lib.attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
+                                n_seqs, Hq, Hkv, total, d, float(scale), _mods_ref(mods), _ptr(ws),
+                                int(ws_bytes), _stream(stream)), "attn_fwd_varlen")
+
+
+def attn_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, cu_seqlens, n_seqs, Hq, Hkv, total, d, scale,
+                    mods=None, ws=None, ws_bytes=0, stream=None):
+    _check(_lib.attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                                _ptr(dk), _ptr(dv), _ptr(cu_seqlens), n_seqs, Hq, Hkv, total, d,
+                                float(scale), _mods_ref(mods), _ptr(ws), int(ws_bytes),
+                                _stream(stream)), "attn_bwd_varlen")
 
 
 def attn_hadamard_quant_fp8(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N, d, ws=None,

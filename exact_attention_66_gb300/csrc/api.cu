@@ -37,9 +37,10 @@ size_t map_bytes(int B, int N) { return round_up((size_t)B * n_tiles(N) * n_tile
 // Workspace of the window / document mods: the block map, then (documents)
 // the run bounds of every position and the "ids not sorted" flag.
 size_t doc_bytes(int B, int N) { return round_up((size_t)B * N * sizeof(int2), 256) + 256; }
+size_t range_bytes(int B, int N) { return round_up((size_t)B * n_tiles(N) * sizeof(int2), 256); }
 size_t mods_bytes(int B, int N, uint32_t flags) {
   if (!needs_map(flags)) return 0;
-  return map_bytes(B, N) + ((flags & ATTN_MOD_DOC) ? doc_bytes(B, N) : 0);
+  return map_bytes(B, N) + 2 * range_bytes(B, N) + ((flags & ATTN_MOD_DOC) ? doc_bytes(B, N) : 0);
 }
 
 attn_status_t check_mods(const attn_mods_t* m) {
@@ -159,15 +160,18 @@ AttnParams make_params(int B, int Hq, int Hkv, int N, float scale, const attn_mo
   p.doc_ids = (mods && (mods->flags & ATTN_MOD_DOC)) ? mods->doc_ids : nullptr;
   p.slopes = (mods && (mods->flags & ATTN_MOD_ALIBI)) ? mods->alibi_slopes : nullptr;
   p.map = nullptr;
+  p.row_range = nullptr;
+  p.col_range = nullptr;
   p.doc_bounds = nullptr;
   p.doc_unsorted = nullptr;
   p.status = status;
   return p;
 }
 
-bool has_score_mods(uint32_t flags) {
-  return (flags & (ATTN_MOD_WINDOW | ATTN_MOD_DOC | ATTN_MOD_SOFTCAP | ATTN_MOD_ALIBI)) != 0;
-}
+// Soft-cap and ALiBi change the scores; the masks (causal, window,
+// documents) are column intervals or element tests on partial tiles only and
+// run in both kernel variants.
+bool has_score_mods(uint32_t flags) { return (flags & (ATTN_MOD_SOFTCAP | ATTN_MOD_ALIBI)) != 0; }
 
 // Backward row statistics: one {LSE * log2(e), D} pair per query row, rows
 // padded to whole 128-row tiles so that every tile's pairs are 16-byte aligned.
@@ -177,15 +181,50 @@ size_t bwd_rowstat_bytes(int B, int Hq, int N) {
 
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
+// Varlen workspace head: the sequence id of every packed row.
+size_t varlen_ids_bytes(int total) { return round_up((size_t)total * sizeof(int32_t), 256); }
+
+// Checks shared by the varlen entry points; on success writes the document
+// mods that describe the sequences (doc_ids = the ids in the workspace).
+attn_status_t varlen_setup(const int32_t* cu, int n_seqs, int Hq, int Hkv, int total, int d,
+                           const attn_mods_t* mods, void* ws, size_t ws_bytes, bool bwd,
+                           attn_mods_t* out, void* stream) {
+  attn_status_t st;
+  if (cu == nullptr || n_seqs < 1 || !aligned(cu, 4)) return ATTN_ERR_INVALID_ARG;
+  if ((st = check_shape(1, Hq, Hkv, total, d, false)) != ATTN_OK) return st;
+  if ((st = check_mods(mods)) != ATTN_OK) return st;
+  if (mods && (mods->flags & ATTN_MOD_DOC)) return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_workspace_size(bwd ? ATTN_OP_BWD_VARLEN : ATTN_OP_FWD_VARLEN, 1, Hq, Hkv,
+                                          total, d, mods);
+  if ((st = check_ws(ws, ws_bytes, need)) != ATTN_OK) return st;
+  int* status = nullptr;
+  if ((st = device_state(&status)) != ATTN_OK) return st;
+  int32_t* ids = static_cast<int32_t*>(ws);
+  if ((st = cuda_status(launch_seq_ids(cu, n_seqs, total, ids, static_cast<cudaStream_t>(stream)))) != ATTN_OK)
+    return st;
+  attn_mods_t m{};
+  if (mods) m = *mods;
+  m.flags |= ATTN_MOD_DOC;
+  m.doc_ids = ids;
+  *out = m;
+  return ATTN_OK;
+}
+
 // Fill the mods workspace (block map, document runs) and point p at it.
 attn_status_t prepare_mods(AttnParams& p, uint8_t* region, cudaStream_t s) {
   if (!needs_map(p.flags)) return ATTN_OK;
   attn_status_t st;
   if ((st = cuda_status(launch_block_map(p, region, s))) != ATTN_OK) return st;
   p.map = region;
+  int2* rows = reinterpret_cast<int2*>(region + map_bytes(p.B, p.N));
+  int2* cols = reinterpret_cast<int2*>(region + map_bytes(p.B, p.N) + range_bytes(p.B, p.N));
+  if ((st = cuda_status(launch_tile_ranges(p, region, rows, cols, s))) != ATTN_OK) return st;
+  p.row_range = rows;
+  p.col_range = cols;
   if (p.flags & ATTN_MOD_DOC) {
-    int2* bounds = reinterpret_cast<int2*>(region + map_bytes(p.B, p.N));
-    int* unsorted = reinterpret_cast<int*>(region + map_bytes(p.B, p.N) + doc_bytes(p.B, p.N) - 256);
+    uint8_t* dregion = region + map_bytes(p.B, p.N) + 2 * range_bytes(p.B, p.N);
+    int2* bounds = reinterpret_cast<int2*>(dregion);
+    int* unsorted = reinterpret_cast<int*>(dregion + doc_bytes(p.B, p.N) - 256);
     if ((st = cuda_status(launch_doc_bounds(p, bounds, unsorted, s))) != ATTN_OK) return st;
     p.doc_bounds = bounds;
     p.doc_unsorted = unsorted;
@@ -210,6 +249,13 @@ size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int N, int d, const a
       return bwd_rowstat_bytes(B, Hq, N) + mods_bytes(B, N, f);
     case ATTN_OP_QUANT_FP8:
       return round_up((size_t)(B * Hq + 2 * B * Hkv) * sizeof(unsigned), 256);
+    case ATTN_OP_FWD_VARLEN:
+    case ATTN_OP_BWD_VARLEN: {
+      if (B != 1 || (f & ATTN_MOD_DOC)) return 0;
+      const uint32_t fd = f | ATTN_MOD_DOC;  // the sequences are the documents
+      return varlen_ids_bytes(N) +
+             (op == ATTN_OP_FWD_VARLEN ? mods_bytes(1, N, fd) : bwd_rowstat_bytes(1, Hq, N) + mods_bytes(1, N, fd));
+    }
     default:
       return 0;
   }
@@ -240,7 +286,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   L.o = o;
   L.lse = lse;
   if ((st = prepare_mods(L.p, static_cast<uint8_t*>(ws), s)) != ATTN_OK) return st;
-  return cuda_status(launch_fwd_bf16(L, d, has_score_mods(L.p.flags), s));
+  return cuda_status(launch_fwd_bf16(L, d, has_score_mods(L.p.flags), needs_map(L.p.flags), s));
 }
 
 static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const void* o,
@@ -280,7 +326,7 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   if ((st = prepare_mods(L.p, wsb + bwd_rowstat_bytes(B, Hq, N), s)) != ATTN_OK) return st;
   if (events != nullptr)
     for (int e = 0; e < 4; ++e) L.events[e] = static_cast<cudaEvent_t>(events[e]);
-  return cuda_status(launch_bwd(L, d, has_score_mods(L.p.flags), s));
+  return cuda_status(launch_bwd(L, d, has_score_mods(L.p.flags), needs_map(L.p.flags), s));
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -347,7 +393,42 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const
   L.o = o;
   L.lse = lse;
   if ((st = prepare_mods(L.p, static_cast<uint8_t*>(ws), s)) != ATTN_OK) return st;
-  return cuda_status(launch_fwd_fp8(L, has_score_mods(L.p.flags), s));
+  return cuda_status(launch_fwd_fp8(L, has_score_mods(L.p.flags), needs_map(L.p.flags), s));
+}
+
+attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int32_t* cu_seqlens, int n_seqs, int Hq, int Hkv, int total, int d,
+                              float scale, const attn_mods_t* mods, void* ws, size_t ws_bytes,
+                              void* stream) {
+  attn_status_t st;
+  if ((st = check_tensors({q, k, v, o})) != ATTN_OK) return st;
+  if (lse == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  attn_mods_t m;
+  if ((st = varlen_setup(cu_seqlens, n_seqs, Hq, Hkv, total, d, mods, ws, ws_bytes, false, &m, stream)) !=
+      ATTN_OK)
+    return st;
+  const size_t head = varlen_ids_bytes(total);
+  return attn_fwd(q, k, v, o, lse, 1, Hq, Hkv, total, d, scale, &m, static_cast<uint8_t*>(ws) + head,
+                  ws_bytes - head, stream);
+}
+
+attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                              const int32_t* cu_seqlens, int n_seqs, int Hq, int Hkv, int total, int d,
+                              float scale, const attn_mods_t* mods, void* ws, size_t ws_bytes,
+                              void* stream) {
+  attn_status_t st;
+  if ((st = check_tensors({q, k, v, o, dout, dq, dk, dv})) != ATTN_OK) return st;
+  if (lse == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  attn_mods_t m;
+  if ((st = varlen_setup(cu_seqlens, n_seqs, Hq, Hkv, total, d, mods, ws, ws_bytes, true, &m, stream)) !=
+      ATTN_OK)
+    return st;
+  const size_t head = varlen_ids_bytes(total);
+  return attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, 1, Hq, Hkv, total, d, scale, &m,
+                  static_cast<uint8_t*>(ws) + head, ws_bytes - head, stream);
 }
 
 attn_status_t attn_block_map(const attn_mods_t* mods, int B, int N, uint8_t* map, void* stream) {

@@ -74,9 +74,54 @@ __global__ void __launch_bounds__(256) doc_bounds_kernel(const int* __restrict__
   bounds[t] = make_int2(start, lo);
 }
 
+// Sequence id of every packed row from the sequence offsets: the last s with
+// cu[s] <= row (binary search over cu[0..n_seqs]); -1 before cu[0].  Reads
+// only cu[0..n_seqs], whatever the values.
+__global__ void __launch_bounds__(256) seq_ids_kernel(const int* __restrict__ cu, int n_seqs, int total,
+                                                      int* __restrict__ ids) {
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= total) return;
+  int lo = 0, hi = n_seqs + 1;  // first index with cu[index] > row
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid] <= row) lo = mid + 1; else hi = mid;
+  }
+  ids[row] = min(lo - 1, n_seqs - 1);
+}
+
+cudaError_t launch_seq_ids(const int* cu, int n_seqs, int total, int* ids, cudaStream_t st) {
+  seq_ids_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(cu, n_seqs, total, ids);
+  return cudaGetLastError();
+}
+
+// Per Q tile (row of the map) and per KV tile (column): the range
+// [first, last + 1) of non-skipped tiles, (0, 0) when there is none.  Lets
+// the attention kernels start their tile loops at the first tile they need.
+__global__ void tile_range_kernel(const uint8_t* __restrict__ map, int nT, int2* __restrict__ rows,
+                                  int2* __restrict__ cols) {
+  const int b = blockIdx.y;
+  const int x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= nT) return;
+  const uint8_t* m = map + (size_t)b * nT * nT;
+  int r0 = nT, r1 = -1, c0 = nT, c1 = -1;
+  for (int y = 0; y < nT; ++y) {
+    if (m[(size_t)x * nT + y] != CLS_SKIP) { r0 = min(r0, y); r1 = y; }
+    if (m[(size_t)y * nT + x] != CLS_SKIP) { c0 = min(c0, y); c1 = y; }
+  }
+  rows[(size_t)b * nT + x] = r1 < 0 ? make_int2(0, 0) : make_int2(r0, r1 + 1);
+  cols[(size_t)b * nT + x] = c1 < 0 ? make_int2(0, 0) : make_int2(c0, c1 + 1);
+}
+
 cudaError_t launch_block_map(const AttnParams& p, uint8_t* map, cudaStream_t st) {
   const dim3 grid(p.nT, p.nT, p.B);
   block_map_kernel<<<grid, 256, 0, st>>>(p, map);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_ranges(const AttnParams& p, const uint8_t* map, int2* rows, int2* cols,
+                               cudaStream_t st) {
+  const dim3 grid((unsigned)((p.nT + 127) / 128), (unsigned)p.B);
+  tile_range_kernel<<<grid, 128, 0, st>>>(map, p.nT, rows, cols);
   return cudaGetLastError();
 }
 

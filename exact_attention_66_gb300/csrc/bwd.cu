@@ -239,10 +239,10 @@ struct KvBars {
 // Steps of a dK/dV CTA: query head g of the group (outer), non-skipped Q tile
 // I (inner, ascending).
 struct KvSteps {
-  int J, I_first, G;
+  int J, I_first, I_end, G;  // Q tiles of the KV tile: [I_first, I_end), skipped ones passed over
   __device__ __forceinline__ int next_I(const AttnParams& p, int b, int I) const {
-    while (I < p.nT && tile_class(p, b, I, J) == CLS_SKIP) ++I;
-    return I;
+    while (I < I_end && tile_class(p, b, I, J) == CLS_SKIP) ++I;
+    return I < I_end ? I : p.nT;
   }
   // Advance (g, I) to the next step; false when past the last one.
   __device__ __forceinline__ bool advance(const AttnParams& p, int b, int& g, int& I) const {
@@ -254,7 +254,8 @@ struct KvSteps {
   }
 };
 
-template <int D, bool MODS>
+// MODS: soft-cap / ALiBi compiled in; MASKS: window / document masks.
+template <int D, bool MODS, bool MASKS>
 __global__ void __launch_bounds__(384, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -273,8 +274,9 @@ __global__ void __launch_bounds__(384, 1)
   const int b = bh / p.Hkv, hk = bh - b * p.Hkv;
   const int G = p.Hq / p.Hkv;
   const bool causal = (p.flags & MOD_CAUSAL) != 0;
-  KvSteps steps{J, 0, G};
-  steps.I_first = steps.next_I(p, b, causal ? J : 0);
+  const int2 rg = MASKS ? kv_tile_range(p, b, J) : make_int2(0, p.nT);
+  KvSteps steps{J, 0, MASKS ? min(p.nT, rg.y) : p.nT, G};
+  steps.I_first = steps.next_I(p, b, max(causal ? J : 0, rg.x));
   const bool any = steps.I_first < p.nT;
 
   if (threadIdx.x == 0) {
@@ -421,8 +423,8 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const bool sc = MODS && (p.flags & MOD_SOFTCAP);
     const bool al = MODS && (p.flags & MOD_ALIBI);
-    const bool win = MODS && (p.flags & MOD_WINDOW);
-    const bool doc = MODS && (p.flags & MOD_DOC);
+    const bool win = MASKS && (p.flags & MOD_WINDOW) != 0;
+    const bool doc = MASKS && (p.flags & MOD_DOC) != 0;
     const float sc_in = p.scale / p.softcap, sc_out = p.softcap * LOG2E;
     const int doc_j = (doc && j < p.N) ? p.doc_ids[(size_t)b * p.N + j] : 0;
     bool doc_runs = false;
@@ -598,7 +600,7 @@ struct DqBars {
   int abort;
 };
 
-template <int D, bool MODS>
+template <int D, bool MODS, bool MASKS>
 __global__ void __launch_bounds__(384, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -617,12 +619,13 @@ __global__ void __launch_bounds__(384, 1)
   const int b = bh / p.Hq, hq = bh - b * p.Hq;
   const int hk = hq / (p.Hq / p.Hkv);
   const bool causal = (p.flags & MOD_CAUSAL) != 0;
-  const int J_end = causal ? min(p.nT, I + 1) : p.nT;
+  const int2 rg = MASKS ? q_tile_range(p, b, I) : make_int2(0, p.nT);
+  const int J_end = min(causal ? min(p.nT, I + 1) : p.nT, rg.y);
   auto next_J = [&](int J) {
     while (J < J_end && tile_class(p, b, I, J) == CLS_SKIP) ++J;
     return J;
   };
-  const int J_first = next_J(0);
+  const int J_first = next_J(rg.x);
 
   if (threadIdx.x == 0) {
     S.abort = 0;
@@ -734,8 +737,8 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const bool sc = MODS && (p.flags & MOD_SOFTCAP);
     const bool al = MODS && (p.flags & MOD_ALIBI);
-    const bool win = MODS && (p.flags & MOD_WINDOW);
-    const bool doc = MODS && (p.flags & MOD_DOC);
+    const bool win = MASKS && (p.flags & MOD_WINDOW) != 0;
+    const bool doc = MASKS && (p.flags & MOD_DOC) != 0;
     const float sc_in = p.scale / p.softcap, sc_out = p.softcap * LOG2E;
     const float al2 = al ? alibi_slope(p, hq) * LOG2E : 0.f;
     const size_t row = ((size_t)b * p.Hq + hq) * p.N + i;
@@ -849,7 +852,7 @@ static cudaError_t check_regs(K kern, int& cached) {
   return cached == BWD_LAUNCH_REGS ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
-template <int D, bool MODS>
+template <int D, bool MODS, bool MASKS>
 static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
   const AttnParams& p = L.p;
   const long long rows = (long long)p.B * p.Hq * p.nT * TILE;
@@ -861,7 +864,7 @@ static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
   if (e != cudaSuccess) return e;
 
   static int kv_regs = -1, dq_regs = -1;
-  auto kv = bwd_dkdv_kernel<D, MODS>;
+  auto kv = bwd_dkdv_kernel<D, MODS, MASKS>;
   if ((e = check_regs(kv, kv_regs)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::SMEM_BYTES)) !=
       cudaSuccess)
@@ -871,7 +874,7 @@ static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
       L.tq, L.tk, L.tv, L.tdo, L.rowstat, (__nv_bfloat16*)L.dk, (__nv_bfloat16*)L.dv, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  auto dqk = bwd_dq_kernel<D, MODS>;
+  auto dqk = bwd_dq_kernel<D, MODS, MASKS>;
   if ((e = check_regs(dqk, dq_regs)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(dqk, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM_BYTES)) !=
       cudaSuccess)
@@ -884,9 +887,12 @@ static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd(const BwdLaunch& L, int d, bool mods, cudaStream_t st) {
-  if (d == 128) return mods ? launch_bwd_t<128, true>(L, st) : launch_bwd_t<128, false>(L, st);
-  return mods ? launch_bwd_t<64, true>(L, st) : launch_bwd_t<64, false>(L, st);
+cudaError_t launch_bwd(const BwdLaunch& L, int d, bool mods, bool masks, cudaStream_t st) {
+  if (d == 128)
+    return mods ? launch_bwd_t<128, true, true>(L, st)
+                : masks ? launch_bwd_t<128, false, true>(L, st) : launch_bwd_t<128, false, false>(L, st);
+  return mods ? launch_bwd_t<64, true, true>(L, st)
+              : masks ? launch_bwd_t<64, false, true>(L, st) : launch_bwd_t<64, false, false>(L, st);
 }
 
 }  // namespace attn

@@ -45,8 +45,23 @@ struct AttnParams {
   const int* doc_unsorted;
   const float* slopes;  // [Hq] or nullptr (default slopes)
   const uint8_t* map;   // [B, nT, nT] tile classes, or nullptr (analytic)
+  // With a map: [first, last + 1) of the non-skipped tiles of each Q tile
+  // (row_range, over J) and of each KV tile (col_range, over I), [B, nT].
+  const int2* row_range;
+  const int2* col_range;
   int* status;          // device status word
 };
+
+// Non-skipped KV tiles of Q tile I (a superset without a map).
+__device__ __forceinline__ int2 q_tile_range(const AttnParams& p, int b, int I) {
+  if (p.row_range == nullptr || I >= p.nT) return make_int2(0, p.nT);
+  return p.row_range[(size_t)b * p.nT + I];
+}
+// Non-skipped Q tiles of KV tile J (a superset without a map).
+__device__ __forceinline__ int2 kv_tile_range(const AttnParams& p, int b, int J) {
+  if (p.col_range == nullptr || J >= p.nT) return make_int2(0, p.nT);
+  return p.col_range[(size_t)b * p.nT + J];
+}
 
 // Class of tile (I, J) for batch row b.  With no map the mask is causal or
 // none, and the class follows in closed form; the ragged last column tile

@@ -247,7 +247,9 @@ __device__ __forceinline__ void score_mods(uint32_t (&s)[128], const ModsArgs& a
   }
 }
 
-template <int D, bool MODS, bool FP8>
+// MODS: soft-cap / ALiBi score mods compiled in; MASKS: window / document
+// masks compiled in (causal and the sequence end always are).
+template <int D, bool MODS, bool FP8, bool MASKS>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
@@ -266,7 +268,11 @@ __global__ void __launch_bounds__(384, 1)
   const int b = bh / p.Hq, hq = bh - b * p.Hq;
   const int hk = hq / (p.Hq / p.Hkv);
   const int I0 = 2 * qblk;
-  const int J_end = (p.flags & MOD_CAUSAL) ? min(p.nT, I0 + 2) : p.nT;
+  // KV tiles [J_begin, J_end) cover every non-skipped tile of both Q tiles.
+  const int2 rg0 = MASKS ? q_tile_range(p, b, I0) : make_int2(0, p.nT);
+  const int2 rg1 = MASKS ? q_tile_range(p, b, I0 + 1) : make_int2(0, p.nT);
+  const int J_begin = min(rg0.y > rg0.x ? rg0.x : p.nT, rg1.y > rg1.x ? rg1.x : p.nT);
+  const int J_end = min((p.flags & MOD_CAUSAL) ? min(p.nT, I0 + 2) : p.nT, max(rg0.y, rg1.y));
 
   if (threadIdx.x == 0) {
     S.abort = 0;
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(384, 1)
         ++r;
         return true;
       };
-      int J = union_next(p, b, I0, 0, J_end);
+      int J = union_next(p, b, I0, J_begin, J_end);
       bool ok = J >= J_end || load(&tk, J);
       while (ok && J < J_end) {
         const int Jn = union_next(p, b, I0, J + 1, J_end);
@@ -364,7 +370,7 @@ __global__ void __launch_bounds__(384, 1)
         mma_commit(&S.s_full[t]);
         ++nk;
       };
-      int J = union_next(p, b, I0, 0, J_end);
+      int J = union_next(p, b, I0, J_begin, J_end);
       int c = CLS_SKIP;
       if (ok && J < J_end) {
         int ks;
@@ -440,15 +446,18 @@ __global__ void __launch_bounds__(384, 1)
       rm.sc_in = qk_scale / p.softcap;
       rm.sc_out = p.softcap * LOG2E;
       rm.alibi_l2 = (p.flags & MOD_ALIBI) ? alibi_slope(p, hq) * LOG2E : 0.f;
-      rm.doc_i = ((p.flags & MOD_DOC) && i < p.N) ? p.doc_ids[(size_t)b * p.N + i] : 0;
-      rm.doc_runs = false;
-      rm.doc_run = make_int2(0, p.N);
-      if (p.flags & MOD_DOC) rm.doc_run = doc_run(p, b, i, rm.doc_runs);
     }
+    const bool win = MASKS && (p.flags & MOD_WINDOW) != 0;
+    const bool doc = MASKS && (p.flags & MOD_DOC) != 0;
+    rm.doc_i = (doc && i < p.N) ? p.doc_ids[(size_t)b * p.N + i] : 0;
+    rm.doc_runs = false;
+    rm.doc_run = make_int2(0, p.N);
+    if (doc) rm.doc_run = doc_run(p, b, i, rm.doc_runs);
+    const bool doc_each = doc && !rm.doc_runs;  // ids tested element by element
     float m = -INFINITY, l = 0.f;
     int ns = 0;
     bool ok = true;
-    for (int J = 0; J < J_end; ++J) {
+    for (int J = J_begin; J < J_end; ++J) {
       const int cls = tile_class(p, b, I, J);
       if (cls == CLS_SKIP) continue;
       const bool partial = cls == CLS_PARTIAL;
@@ -470,13 +479,31 @@ __global__ void __launch_bounds__(384, 1)
       const int hi_lim = min(causal ? i : 0x7fffffff, p.N - 1) - j0;  // valid iff c <= hi_lim
       float mt;   // tile row max in log2 units
       float mul;  // factor still to apply to s inside the exponential
+      // Allowed columns of this row on a partial tile: (lo_lim, hi_m] (causal,
+      // the sequence end, the window, the row's document run), plus the
+      // element-wise document test when the ids are not runs.
+      int lo_lim = win ? (i - p.window - j0) : -0x7fffffff;  // valid iff c > lo_lim
+      int hi_m = hi_lim;                                      // valid iff c <= hi_m
+      if (doc && rm.doc_runs) {
+        lo_lim = max(lo_lim, rm.doc_run.x - 1 - j0);
+        hi_m = min(hi_m, rm.doc_run.y - 1 - j0);
+      }
+      const int* drow = doc ? p.doc_ids + (size_t)b * p.N + j0 : nullptr;
       if (!MODS) {
         // Raw scores: the scale is positive, so it commutes with the max and
         // is folded into the exponential's FMA.
         if (partial) {
+          if (!doc_each) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c > hi_lim) s[c] = __float_as_uint(-INFINITY);
+            for (int c = 0; c < 128; ++c)
+              if (c > hi_m || c <= lo_lim) s[c] = __float_as_uint(-INFINITY);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+              const bool valid = c <= hi_m && c > lo_lim && __ldg(drow + c) == rm.doc_i;
+              if (!valid) s[c] = __float_as_uint(-INFINITY);
+            }
+          }
         }
         mt = row_max128(s) * scale_log2;
         mul = scale_log2;
@@ -484,16 +511,6 @@ __global__ void __launch_bounds__(384, 1)
         mul = 1.0f;
         const bool sc = (p.flags & MOD_SOFTCAP) != 0;
         const bool al = (p.flags & MOD_ALIBI) != 0;
-        const bool win = (p.flags & MOD_WINDOW) != 0;
-        const bool doc = (p.flags & MOD_DOC) != 0;
-        int lo_lim = win ? (i - p.window - j0) : -0x7fffffff;  // valid iff c > lo_lim
-        int hi_m = hi_lim;                                      // valid iff c <= hi_m
-        if (doc && rm.doc_runs) {  // the row's document is one run of columns
-          lo_lim = max(lo_lim, rm.doc_run.x - 1 - j0);
-          hi_m = min(hi_m, rm.doc_run.y - 1 - j0);
-        }
-        const bool doc_each = doc && !rm.doc_runs;  // ids tested element by element
-        const int* drow = doc ? p.doc_ids + (size_t)b * p.N + j0 : nullptr;
         // The score mods in log2 units, specialised on soft-cap / ALiBi so the
         // unrolled loop carries no dead work.
         const float al_row = rm.alibi_l2 * (float)(j0 - i);
@@ -607,12 +624,12 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool MODS, bool FP8>
+template <int D, bool MODS, bool FP8, bool MASKS>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 void* o, float* lse, const float* scales, const AttnParams& p,
                                 cudaStream_t st) {
   using C = FwdCfg<D, FP8>;
-  auto kern = fwd_kernel<D, MODS, FP8>;
+  auto kern = fwd_kernel<D, MODS, FP8, MASKS>;
   // The register split inside the kernel assumes exactly LAUNCH_REGS per
   // thread at launch; refuse to launch any other build of it.
   static int regs = -1;
@@ -629,17 +646,17 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd_bf16(const FwdLaunch& L, int d, bool mods, cudaStream_t st) {
-  if (d == 128)
-    return mods ? launch_fwd_t<128, true, false>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st)
-                : launch_fwd_t<128, false, false>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st);
-  return mods ? launch_fwd_t<64, true, false>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st)
-              : launch_fwd_t<64, false, false>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st);
+cudaError_t launch_fwd_bf16(const FwdLaunch& L, int d, bool mods, bool masks, cudaStream_t st) {
+#define ATTN_FWD(DD, MO, MA) launch_fwd_t<DD, MO, false, MA>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st)
+  if (d == 128) return mods ? ATTN_FWD(128, true, true) : masks ? ATTN_FWD(128, false, true) : ATTN_FWD(128, false, false);
+  return mods ? ATTN_FWD(64, true, true) : masks ? ATTN_FWD(64, false, true) : ATTN_FWD(64, false, false);
+#undef ATTN_FWD
 }
 
-cudaError_t launch_fwd_fp8(const Fp8Launch& L, bool mods, cudaStream_t st) {
-  return mods ? launch_fwd_t<128, true, true>(L.tq, L.tk, L.tv, L.o, L.lse, L.scales, L.p, st)
-              : launch_fwd_t<128, false, true>(L.tq, L.tk, L.tv, L.o, L.lse, L.scales, L.p, st);
+cudaError_t launch_fwd_fp8(const Fp8Launch& L, bool mods, bool masks, cudaStream_t st) {
+#define ATTN_FWD8(MO, MA) launch_fwd_t<128, MO, true, MA>(L.tq, L.tk, L.tv, L.o, L.lse, L.scales, L.p, st)
+  return mods ? ATTN_FWD8(true, true) : masks ? ATTN_FWD8(false, true) : ATTN_FWD8(false, false);
+#undef ATTN_FWD8
 }
 
 }  // namespace attn

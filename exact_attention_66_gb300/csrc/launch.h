@@ -13,7 +13,8 @@ struct FwdLaunch {
   float* lse;
   AttnParams p;
 };
-cudaError_t launch_fwd_bf16(const FwdLaunch& L, int d, bool mods, cudaStream_t st);
+// mods: soft-cap / ALiBi present; masks: window / document masks present.
+cudaError_t launch_fwd_bf16(const FwdLaunch& L, int d, bool mods, bool masks, cudaStream_t st);
 
 struct Fp8Launch {
   CUtensorMap tq, tk, tv;  // e4m3 tensors
@@ -22,7 +23,7 @@ struct Fp8Launch {
   float* lse;
   AttnParams p;
 };
-cudaError_t launch_fwd_fp8(const Fp8Launch& L, bool mods, cudaStream_t st);
+cudaError_t launch_fwd_fp8(const Fp8Launch& L, bool mods, bool masks, cudaStream_t st);
 
 struct BwdLaunch {
   CUtensorMap tq, tk, tv, tdo;  // bf16 maps like the forward's
@@ -36,10 +37,13 @@ struct BwdLaunch {
   AttnParams p;
   cudaEvent_t events[4];  // optional: recorded before pre / dkdv / dq and after dq
 };
-cudaError_t launch_bwd(const BwdLaunch& L, int d, bool mods, cudaStream_t st);
+cudaError_t launch_bwd(const BwdLaunch& L, int d, bool mods, bool masks, cudaStream_t st);
 
 cudaError_t launch_block_map(const AttnParams& p, uint8_t* map, cudaStream_t st);
+cudaError_t launch_tile_ranges(const AttnParams& p, const uint8_t* map, int2* rows, int2* cols,
+                               cudaStream_t st);
 cudaError_t launch_doc_bounds(const AttnParams& p, int2* bounds, int* unsorted, cudaStream_t st);
+cudaError_t launch_seq_ids(const int* cu, int n_seqs, int total, int* ids, cudaStream_t st);
 
 cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, void* q8, void* k8,
                                   void* v8, float* scales, const int8_t* signs, int B, int Hq,

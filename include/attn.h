@@ -78,8 +78,16 @@ typedef struct {
   const float* alibi_slopes;  /* ATTN_MOD_ALIBI: device fp32 [Hq], or NULL for 2^(-8(h+1)/Hq) */
 } attn_mods_t;
 
-/* Operations for attn_workspace_size(). */
-enum { ATTN_OP_FWD = 0, ATTN_OP_BWD = 1, ATTN_OP_FWD_FP8 = 2, ATTN_OP_QUANT_FP8 = 3 };
+/* Operations for attn_workspace_size().  For the two varlen operations pass
+ * B = 1 and N = total (the packed row count). */
+enum {
+  ATTN_OP_FWD = 0,
+  ATTN_OP_BWD = 1,
+  ATTN_OP_FWD_FP8 = 2,
+  ATTN_OP_QUANT_FP8 = 3,
+  ATTN_OP_FWD_VARLEN = 4,
+  ATTN_OP_BWD_VARLEN = 5
+};
 
 /* Block-map tile classes (128 x 128 tiles). */
 enum { ATTN_TILE_SKIP = 0, ATTN_TILE_PARTIAL = 1, ATTN_TILE_FULL = 2 };
@@ -101,7 +109,8 @@ size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int N, int d, const a
  * (block sparsity, FlexAttention/FA4 page, "Limitations actuelles").
  * scale : multiplier of q.k (typically 1/sqrt(d)), finite and > 0.
  * ws    : workspace of attn_workspace_size(ATTN_OP_FWD, ...) bytes (may be
- *         NULL when that size is 0).
+ *         NULL when that size is 0; window / document mods need one for the
+ *         block map, its per-tile ranges and the document runs).
  */
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                        int B, int Hq, int Hkv, int N, int d, float scale,
@@ -116,8 +125,10 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  * over its partner tiles in ascending order (contrast the FlexAttention/FA4
  * page, "Limitations actuelles": nondeterministic backward with block
  * sparsity).  dK/dV of a KV head sum over its query heads (GQA).
- * ws : workspace of attn_workspace_size(ATTN_OP_BWD, ...) bytes (row sums
- *      D = rowsum(dO * O) and, with window/document mods, the block map).
+ * ws : workspace of attn_workspace_size(ATTN_OP_BWD, ...) bytes: the row
+ *      statistics {LSE log2(e), D = rowsum(dO * O)} of every query row, and,
+ *      with window/document mods, the block map, its per-tile ranges and
+ *      (documents) the document run of every position.
  */
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
@@ -158,9 +169,9 @@ attn_status_t attn_bwd_profiled(const void* q, const void* k, const void* v, con
  *
  * Arguments, layout and errors are those of attn_bwd, without ws/ws_bytes.
  * Limit: the workspace attn_bwd would need, attn_workspace_size(ATTN_OP_BWD,
- * ...) = 4*B*Hq*N bytes rounded up to 256, plus the block map with window or
- * document mods, must fit in ATTN_NOALLOC_SCRATCH_BYTES; otherwise the call
- * returns ATTN_ERR_WORKSPACE before touching the device.
+ * ...) (8 bytes per query row with rows padded to whole 128-row tiles, plus
+ * the window / document mask data), must fit in ATTN_NOALLOC_SCRATCH_BYTES;
+ * otherwise the call returns ATTN_ERR_WORKSPACE before touching the device.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
  * before any stream capture.
@@ -174,6 +185,37 @@ attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, cons
                                const void* dout, const float* lse, void* dq, void* dk, void* dv,
                                int B, int Hq, int Hkv, int N, int d, float scale,
                                const attn_mods_t* mods, void* stream);
+
+/*
+ * Packed variable-length sequences: n_seqs sequences stored back to back along
+ * the row axis, attending only within themselves -- the unpadded form of the
+ * document mask (FlexAttention/FA4 page, opening paragraphs: document
+ * masking among the mods it accelerates).  Sequence s occupies rows
+ * [cu_seqlens[s], cu_seqlens[s+1]) of every head.
+ * Layout: Q, O, dO, dQ [1, Hq, total, d]; K, V, dK, dV [1, Hkv, total, d];
+ *         LSE [1, Hq, total]; all bf16 except LSE (fp32).
+ * cu_seqlens : device int32 [n_seqs + 1]: 0 = cu_seqlens[0] <= cu_seqlens[1]
+ *              <= ... <= cu_seqlens[n_seqs] = total (not checked on the host;
+ *              a malformed array changes which rows attend to which, never
+ *              which memory is touched).
+ * mods       : causal / window / soft-cap / ALiBi as for attn_fwd, applied
+ *              inside each sequence (i, j are packed row indices, so i - j is
+ *              the in-sequence distance); ATTN_MOD_DOC must not be set
+ *              (ATTN_ERR_INVALID_ARG): the sequences are the documents.
+ * ws         : attn_workspace_size(ATTN_OP_FWD_VARLEN / ATTN_OP_BWD_VARLEN,
+ *              1, Hq, Hkv, total, d, mods) bytes: the per-row sequence ids,
+ *              then attn_fwd's / attn_bwd's workspace for the document mask.
+ * Otherwise as attn_fwd / attn_bwd (same kernels, B = 1, N = total).
+ */
+attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int32_t* cu_seqlens, int n_seqs, int Hq, int Hkv, int total,
+                              int d, float scale, const attn_mods_t* mods, void* ws,
+                              size_t ws_bytes, void* stream);
+attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                              const int32_t* cu_seqlens, int n_seqs, int Hq, int Hkv, int total,
+                              int d, float scale, const attn_mods_t* mods, void* ws,
+                              size_t ws_bytes, void* stream);
 
 /*
  * FP8 prologue (FlashAttention-3 digest, "Basse précision FP8 et incoherent

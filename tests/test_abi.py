@@ -93,10 +93,11 @@ def test_workspace_sizes(L):
     ws = L.attn_workspace_size
     assert ws(L.OP_FWD, 1, 2, 2, 1000, 128, L.make_mods(causal=True)) == 0
     m = L.make_mods(causal=True, window=64)
-    assert ws(L.OP_FWD, 4, 16, 16, 4096, 128, m) == 4 * 32 * 32
+    # block map (B*nT*nT bytes) + per-Q-tile and per-KV-tile ranges (2 x B*nT int2), each 256-aligned
+    assert ws(L.OP_FWD, 4, 16, 16, 4096, 128, m) == 4 * 32 * 32 + 2 * 1024
     # one {LSE, D} float pair per query row, rows padded to whole 128-row tiles
     assert ws(L.OP_BWD, 1, 64, 8, 8192, 128, L.make_mods(causal=True)) == 64 * 8192 * 8
-    assert ws(L.OP_BWD, 2, 2, 2, 1000, 64, m) == 2 * 2 * 1024 * 8 + 256
+    assert ws(L.OP_BWD, 2, 2, 2, 1000, 64, m) == 2 * 2 * 1024 * 8 + 256 + 2 * 256
     assert ws(L.OP_QUANT_FP8, 2, 16, 16, 16384, 128, None) == 512  # 96 fp32 amax words
     assert ws(L.OP_FWD, 1, 3, 2, 128, 128, None) == 0  # invalid shape -> 0
 
@@ -109,3 +110,25 @@ def test_status_strings(L):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
 def test_valid_call_without_gpu_reports_cuda_error(L):
     assert fwd(L) == 4  # ATTN_ERR_CUDA: no silent CPU path
+
+
+def test_varlen_entry_points_validate(L):
+    so = L.lib()
+    need = L.attn_workspace_size(L.OP_FWD_VARLEN, 1, 2, 2, 500, 128, None)
+    # sequence ids (500 int32, rounded to 256 B) + the document mask's workspace
+    assert need == 2048 + L.attn_workspace_size(L.OP_FWD, 1, 2, 2, 500, 128, L.make_mods(doc_ids=torch.zeros(1)))
+    assert L.attn_workspace_size(L.OP_FWD_VARLEN, 2, 2, 2, 500, 128, None) == 0  # B must be 1
+    assert L.attn_workspace_size(L.OP_BWD_VARLEN, 1, 2, 2, 500, 128, None) == \
+        2048 + L.attn_workspace_size(L.OP_BWD, 1, 2, 2, 500, 128, L.make_mods(doc_ids=torch.zeros(1)))
+
+    def fv(cu=A, n=3, mods=None, ws=A, nws=1 << 24, q=A):
+        return so.attn_fwd_varlen(q, A, A, A, A, cu, n, 2, 2, 500, 128, 0.1,
+                                  ctypes.byref(mods) if mods else None, ws, nws, None)
+    assert fv(cu=None) == 1          # no sequence offsets
+    assert fv(n=0) == 1              # no sequences
+    assert fv(cu=A + 2) == 1         # misaligned offsets
+    assert fv(q=None) == 1
+    assert fv(mods=L.make_mods(doc_ids=torch.zeros(1))) == 1  # the sequences are the documents
+    assert fv(ws=None, nws=0) == 3   # the workspace is always needed
+    assert so.attn_bwd_varlen(A, A, A, A, A, A, A, A, None, A, 3, 2, 2, 500, 128, 0.1, None, A,
+                              1 << 24, None) == 1  # null dv

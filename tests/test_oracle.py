@@ -370,3 +370,35 @@ def test_outlier_recipe():
     x = torch.ones(1000, 100)
     y = gen.with_outliers(x, 1e-3, 50.0, 1)
     assert int((y == 50.0).sum()) == 100 and int((y == 1.0).sum()) == 100000 - 100
+
+
+def _seq_ids(cu, total):
+    ids = np.zeros(total, dtype=np.int32)
+    for s_ in range(len(cu) - 1):
+        ids[cu[s_]:cu[s_ + 1]] = s_
+    return ids
+
+
+@pytest.mark.parametrize("mk", [dict(causal=True), dict(causal=True, window=5),
+                                dict(softcap=3.0, alibi=True), dict()])
+def test_packed_sequences_equal_separate_runs(mk):
+    """Packed variable-length sequences (document mask from the sequence
+    offsets) give, row for row, the attention of each sequence run alone --
+    forward and backward."""
+    lens = [7, 1, 13, 4]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    total, d, Hq, Hkv = int(cu[-1]), 16, 4, 2
+    x = gen.make_inputs(1, Hq, Hkv, total, d, 41)
+    s = 0.3
+    packed = A.Mods(doc_ids=_seq_ids(cu, total)[None, :], **mk)
+    O, L = A.forward(x["q"], x["k"], x["v"], s, packed)
+    gq, gk, gv = A.backward(x["q"], x["k"], x["v"], x["do"], s, packed)
+    for a, b in zip(cu[:-1], cu[1:]):
+        sl = {n: x[n][:, :, a:b] for n in ("q", "k", "v", "do")}
+        m1 = A.Mods(**mk)
+        O1, L1 = A.forward(sl["q"], sl["k"], sl["v"], s, m1)
+        g1 = A.backward(sl["q"], sl["k"], sl["v"], sl["do"], s, m1)
+        np.testing.assert_allclose(O[:, :, a:b], O1, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(L[:, :, a:b], L1, rtol=0, atol=1e-12)
+        for full, part in zip((gq, gk, gv), g1):
+            np.testing.assert_allclose(full[:, :, a:b], part, rtol=0, atol=1e-12)
