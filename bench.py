@@ -579,6 +579,18 @@ def run_fp8(args, world, rank, local):
     ms = allmax(world, t0.elapsed_time(t1)) / args.steps
     k_pro = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     k_fwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    # the same prologue with RoPE fused in front of the rotation
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for rep in range(2):
+        if rep:
+            r0.record(stream)
+        for _ in range(args.steps):
+            ea.attn_rope_hadamard_quant_fp8(q, k, v, q8, k8, v8, sc, signs, B, Hq, Hkv, N, d, 10000.0,
+                                            wq, nq, stream)
+    r1.record(stream)
+    torch.cuda.synchronize(dev)
+    ea.attn_status(stream)
+    k_rope = r0.elapsed_time(r1) / args.steps
     peaks, src = load_peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]  # dense e4m3 = 2x bf16 (nominal ratio)
     fwd_f = 4.0 * Hq * d * allowed_pairs(cfg)
@@ -599,7 +611,9 @@ def run_fp8(args, world, rank, local):
                      "unit": "TFLOP/s", "frac": round(fwd_t / fp8_peak, 4), "traffic": None,
                      "peak_source": f"{src} bf16_tflops_sustained x 2 (nominal e4m3/bf16 ratio)"},
         "prologue": {"achieved": round(pro_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(pro_gbs / peaks["hbm_gbs"], 4), "bytes": pro_bytes},
+                     "frac": round(pro_gbs / peaks["hbm_gbs"], 4), "bytes": pro_bytes,
+                     "with_rope_ms": round(k_rope, 4),
+                     "with_rope_gbs": round(pro_bytes / (k_rope * 1e-3) / 1e9, 1)},
         "e2e": None, "gpu_launches": 4 * args.steps, "clocks": clk,
     }
     if rank == 0:

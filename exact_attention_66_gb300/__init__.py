@@ -16,6 +16,7 @@ from ._lib import (  # noqa: F401
     OP_BWD_VARLEN, OP_FWD, OP_FWD_FP8, OP_FWD_VARLEN, OP_QUANT_FP8, TILE_FULL, TILE_PARTIAL,
     TILE_SKIP, attn_block_map, attn_bwd, attn_bwd_profiled, attn_bwd_noalloc, attn_bwd_varlen,
     NOALLOC_SCRATCH_BYTES, attn_fwd, attn_fwd_fp8, attn_fwd_varlen, attn_hadamard_quant_fp8,
+    attn_rope_hadamard_quant_fp8,
     attn_status, attn_workspace_size, lib,
     make_mods, status_string,
 )
@@ -23,7 +24,8 @@ from ._lib import (  # noqa: F401
 __all__ = [
     "forward", "backward", "forward_varlen", "backward_varlen", "hadamard_quant_fp8", "forward_fp8",
     "block_map", "make_mods", "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc",
-    "attn_fwd_varlen", "attn_bwd_varlen", "attn_hadamard_quant_fp8", "attn_fwd_fp8", "attn_block_map",
+    "attn_fwd_varlen", "attn_bwd_varlen", "attn_hadamard_quant_fp8", "attn_rope_hadamard_quant_fp8",
+    "attn_fwd_fp8", "attn_block_map",
     "attn_status", "attn_workspace_size", "AttnError",
 ]
 
@@ -96,8 +98,9 @@ def backward_varlen(q, k, v, o, lse, do, cu_seqlens, scale=None, mods=None, stre
     return dq, dk, dv
 
 
-def hadamard_quant_fp8(q, k, v, signs=None, stream=None):
-    """(q8, k8, v8, scales): e4m3 tensors (as uint8) and fp32 dequantisation scales."""
+def hadamard_quant_fp8(q, k, v, signs=None, stream=None, rope_base=None):
+    """(q8, k8, v8, scales): e4m3 tensors (as uint8) and fp32 dequantisation scales
+    (with rope_base, RoPE is applied to Q and K first, in the same pass)."""
     torch = _torch()
     B, Hq, Hkv, N, d = _shape(q, k)
     q8 = torch.empty(q.shape, dtype=torch.uint8, device=q.device)
@@ -105,7 +108,11 @@ def hadamard_quant_fp8(q, k, v, signs=None, stream=None):
     v8 = torch.empty(v.shape, dtype=torch.uint8, device=q.device)
     scales = torch.empty(B * Hq + 2 * B * Hkv, dtype=torch.float32, device=q.device)
     ws, nws = _workspace(OP_QUANT_FP8, B, Hq, Hkv, N, d, None, q.device)
-    attn_hadamard_quant_fp8(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N, d, ws, nws, stream)
+    if rope_base is None:
+        attn_hadamard_quant_fp8(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N, d, ws, nws, stream)
+    else:
+        attn_rope_hadamard_quant_fp8(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N, d, rope_base,
+                                     ws, nws, stream)
     return q8, k8, v8, scales
 
 

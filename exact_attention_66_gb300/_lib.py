@@ -26,7 +26,7 @@ TILE_SKIP, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 
 # Exported symbols, in the order include/attn.h declares them.
 EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc",
-           "attn_fwd_varlen", "attn_bwd_varlen", "attn_hadamard_quant_fp8",
+           "attn_fwd_varlen", "attn_bwd_varlen", "attn_hadamard_quant_fp8", "attn_rope_hadamard_quant_fp8",
            "attn_fwd_fp8", "attn_block_map", "attn_status", "attn_status_string")
 
 
@@ -58,6 +58,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_hadamard_quant_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp]
+    lib.attn_rope_hadamard_quant_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_block_map.argtypes = [mp, i, i, vp, vp]
     lib.attn_status.argtypes = [vp]
@@ -183,6 +184,14 @@ def attn_hadamard_quant_fp8(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N, d
     _check(_lib.attn_hadamard_quant_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(q8), _ptr(k8), _ptr(v8),
                                         _ptr(scales), _ptr(signs), B, Hq, Hkv, N, d, _ptr(ws),
                                         int(ws_bytes), _stream(stream)), "attn_hadamard_quant_fp8")
+
+
+def attn_rope_hadamard_quant_fp8(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N, d, rope_base,
+                                 ws=None, ws_bytes=0, stream=None):
+    _check(_lib.attn_rope_hadamard_quant_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(q8), _ptr(k8), _ptr(v8),
+                                             _ptr(scales), _ptr(signs), B, Hq, Hkv, N, d, float(rope_base),
+                                             _ptr(ws), int(ws_bytes), _stream(stream)),
+           "attn_rope_hadamard_quant_fp8")
 
 
 def attn_fwd_fp8(q8, k8, v8, scales, o, lse, B, Hq, Hkv, N, d, scale, mods=None, ws=None,

@@ -349,10 +349,9 @@ attn_status_t attn_bwd_profiled(const void* q, const void* k, const void* v, con
                   stream, events);
 }
 
-attn_status_t attn_hadamard_quant_fp8(const void* q, const void* k, const void* v, void* q8,
-                                      void* k8, void* v8, float* scales, const int8_t* signs,
-                                      int B, int Hq, int Hkv, int N, int d, void* ws,
-                                      size_t ws_bytes, void* stream) {
+static attn_status_t quant_impl(const void* q, const void* k, const void* v, void* q8, void* k8,
+                                void* v8, float* scales, const int8_t* signs, int B, int Hq, int Hkv,
+                                int N, int d, float rope_base, void* ws, size_t ws_bytes, void* stream) {
   attn_status_t st;
   if ((st = check_shape(B, Hq, Hkv, N, d, true)) != ATTN_OK) return st;
   if ((st = check_tensors({q, k, v, q8, k8, v8})) != ATTN_OK) return st;
@@ -362,9 +361,24 @@ attn_status_t attn_hadamard_quant_fp8(const void* q, const void* k, const void* 
   if ((st = check_ws(ws, ws_bytes, need)) != ATTN_OK) return st;
   int* status = nullptr;
   if ((st = device_state(&status)) != ATTN_OK) return st;
-  return cuda_status(launch_hadamard_quant(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N,
+  return cuda_status(launch_hadamard_quant(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N, rope_base,
                                            static_cast<unsigned*>(ws),
                                            static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_hadamard_quant_fp8(const void* q, const void* k, const void* v, void* q8,
+                                      void* k8, void* v8, float* scales, const int8_t* signs,
+                                      int B, int Hq, int Hkv, int N, int d, void* ws,
+                                      size_t ws_bytes, void* stream) {
+  return quant_impl(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N, d, 0.f, ws, ws_bytes, stream);
+}
+
+attn_status_t attn_rope_hadamard_quant_fp8(const void* q, const void* k, const void* v, void* q8,
+                                           void* k8, void* v8, float* scales, const int8_t* signs,
+                                           int B, int Hq, int Hkv, int N, int d, float rope_base,
+                                           void* ws, size_t ws_bytes, void* stream) {
+  if (!(std::isfinite(rope_base) && rope_base > 1.f)) return ATTN_ERR_INVALID_ARG;
+  return quant_impl(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N, d, rope_base, ws, ws_bytes, stream);
 }
 
 attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* scales,

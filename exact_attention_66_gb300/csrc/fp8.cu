@@ -15,6 +15,12 @@
 // (batch, head) of the rotated tensors (integer atomic max of the non-negative
 // float bits, so the result does not depend on the order), pass 2 recomputes
 // the rotation and writes e4m3 codes scaled by 448 / amax.
+//
+// Optionally RoPE is fused in front of the rotation (the digest's "fused with
+// RoPE at no extra cost"): the row at position n of its head has its element
+// pairs (c, c + 64) turned by n * base^(-2c/128) before the signs and the
+// Hadamard butterflies, in the same registers -- lane l pairs with lane
+// l ^ 16 -- so RoPE costs no extra pass over memory.
 #include "common.cuh"
 #include "launch.h"
 
@@ -28,6 +34,7 @@ struct QuantTensors {
   unsigned* amax[3];          // [B * H] float bits (workspace)
   float* scale[3];            // [B * H] dequantisation scales (output)
   const int8_t* signs;        // [Hkv, 128] or nullptr
+  float rope_k;               // RoPE: inv_freq(c) = exp2(-c * rope_k), rope_k = 2 log2(base) / 128; 0 = off
   int N, Hkv, G;              // G = Hq / Hkv
 };
 
@@ -46,7 +53,21 @@ __device__ __forceinline__ void load_row(const QuantTensors& t, int ti, long lon
   v[1] = bf16hi_f32(raw.x);
   v[2] = bf16lo_f32(raw.y);
   v[3] = bf16hi_f32(raw.y);
-  if (ti == 2 || t.signs == nullptr) return;
+  if (ti == 2) return;
+  if (t.rope_k != 0.f) {  // RoPE on Q and K rows, rotate-half pairs (c, c + 64)
+    const int lane = lane_id();
+    const float pos = (float)(row % t.N);
+    const bool first = lane < 16;  // elements 4 lane .. 4 lane + 3 < 64
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float partner = __shfl_xor_sync(0xffffffffu, v[r], 16);
+      const int c = (4 * lane + r) & 63;
+      float sn, cs;
+      sincosf(pos * exp2f(-(float)c * t.rope_k), &sn, &cs);
+      v[r] = first ? fmaf(v[r], cs, -partner * sn) : fmaf(v[r], cs, partner * sn);
+    }
+  }
+  if (t.signs == nullptr) return;
   const int head = (int)((row / t.N) % t.heads[ti]);
   const int hk = ti == 0 ? head / t.G : head;
   const char4 sg = __ldg(reinterpret_cast<const char4*>(t.signs + hk * 128) + lane_id());
@@ -135,8 +156,9 @@ __global__ void __launch_bounds__(256) quant_write_kernel(const QuantTensors t) 
 
 cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, void* q8, void* k8,
                                   void* v8, float* scales, const int8_t* signs, int B, int Hq,
-                                  int Hkv, int N, unsigned* amax_ws, cudaStream_t st) {
+                                  int Hkv, int N, float rope_base, unsigned* amax_ws, cudaStream_t st) {
   QuantTensors t{};
+  t.rope_k = rope_base > 0.f ? 2.0f * log2f(rope_base) / 128.0f : 0.f;
   t.x[0] = (const __nv_bfloat16*)q;
   t.x[1] = (const __nv_bfloat16*)k;
   t.x[2] = (const __nv_bfloat16*)v;

@@ -239,6 +239,22 @@ attn_status_t attn_hadamard_quant_fp8(const void* q, const void* k, const void* 
                                       size_t ws_bytes, void* stream);
 
 /*
+ * attn_hadamard_quant_fp8 with rotary position embedding fused in front of the
+ * rotation (FlashAttention-3 digest, "Basse précision FP8 et incoherent
+ * processing": the Hadamard transform can be fused with RoPE at no extra
+ * cost): each Q and K row is first turned by RoPE -- row n of a head has its
+ * element pairs (c, c + d/2), c < d/2, rotated by the angle
+ * n * rope_base^(-2c/d) -- in the same pass, then signed, rotated and
+ * quantised as above.  rope_base: finite and > 1 (e.g. 10000), else
+ * ATTN_ERR_INVALID_ARG.  Other arguments, workspace and errors as
+ * attn_hadamard_quant_fp8 (signs may be NULL: RoPE then quantisation only).
+ */
+attn_status_t attn_rope_hadamard_quant_fp8(const void* q, const void* k, const void* v, void* q8,
+                                           void* k8, void* v8, float* scales, const int8_t* signs,
+                                           int B, int Hq, int Hkv, int N, int d, float rope_base,
+                                           void* ws, size_t ws_bytes, void* stream);
+
+/*
  * FP8 forward: O (bf16) and LSE (fp32, of the dequantised scores) from the
  * e4m3 tensors and scales written by attn_hadamard_quant_fp8.  Q K^T runs in
  * e4m3 with fp32 accumulation, P is rounded to e4m3 for P V, and the

@@ -386,11 +386,31 @@ def quantize_e4m3(x: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return e4m3_round(x / scales[:, :, None, None])
 
 
-def fp8_prologue(q, k, v, signs: Optional[np.ndarray], Hkv: int):
-    """Rotated-and-quantised Q, K (rotation skipped when signs is None) and V.
+def rope(x, base: float) -> np.ndarray:
+    """Rotary position embedding of every row, fp64, rotate-half pairing:
+    element c < d/2 of the row at position n (its index along N) pairs with
+    element c + d/2 and the pair turns by the angle n * base^(-2c/d):
+    (a, b) -> (a cos - b sin, b cos + a sin).  The FA3 digest ("Basse
+    précision FP8 et incoherent processing") names RoPE only as the step the
+    Hadamard rotation can be fused with; this is its usual definition."""
+    X = _f64(x)
+    d = X.shape[-1]
+    h = d // 2
+    inv = base ** (-2.0 * np.arange(h) / d)
+    ang = np.arange(X.shape[2], dtype=np.float64)[:, None] * inv[None, :]
+    c, sn = np.cos(ang), np.sin(ang)
+    a, b = X[..., :h], X[..., h:]
+    return np.concatenate([a * c - b * sn, b * c + a * sn], axis=-1)
+
+
+def fp8_prologue(q, k, v, signs: Optional[np.ndarray], Hkv: int, rope_base: Optional[float] = None):
+    """Rotated-and-quantised Q, K (rotation skipped when signs is None; RoPE
+    first when rope_base is given) and V.
 
     Returns (q8, k8, v8) as fp64 e4m3 values and scales [3, B, H].
     """
+    if rope_base is not None:
+        q, k = rope(q, rope_base), rope(k, rope_base)
     Q = rotate_heads(q, signs, Hkv) if signs is not None else _f64(q)
     K = rotate_heads(k, signs, Hkv) if signs is not None else _f64(k)
     V = _f64(v)

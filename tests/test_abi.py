@@ -132,3 +132,13 @@ def test_varlen_entry_points_validate(L):
     assert fv(ws=None, nws=0) == 3   # the workspace is always needed
     assert so.attn_bwd_varlen(A, A, A, A, A, A, A, A, None, A, 3, 2, 2, 500, 128, 0.1, None, A,
                               1 << 24, None) == 1  # null dv
+
+
+
+def test_rope_prologue_validates(L):
+    so = L.lib()
+    for base in (0.0, 1.0, -5.0, float("nan"), float("inf")):
+        assert so.attn_rope_hadamard_quant_fp8(A, A, A, A, A, A, A, None, 1, 2, 2, 64, 128, base, A, 4096,
+                                               None) == 1
+    assert so.attn_rope_hadamard_quant_fp8(A, A, A, A, A, A, A, None, 1, 2, 2, 64, 64, 1e4, A, 4096,
+                                           None) == 2  # d must be 128

@@ -65,6 +65,44 @@ def test_prologue_matches_oracle(rotate, shape):
         assert same > 0.999, same
 
 
+# RoPE angles are formed in fp32 on the GPU (position x an fp32 inverse
+# frequency): at position n they are off by up to about 3 n 2^-24 radians
+# (~4e-4 at n = 2100), which moves each rotated element by at most that
+# fraction of its row's largest element.
+ROPE_REL = 1e-3
+
+
+@pytest.mark.parametrize("rotate", [True, False], ids=["hadamard", "plain"])
+@pytest.mark.parametrize("shape", [(1, 4, 2, 300), (2, 2, 1, 2100)], ids=str)
+def test_rope_prologue_matches_oracle(rotate, shape):
+    """RoPE fused in front of the Hadamard rotation and the quantiser."""
+    ea = lib()
+    B, Hq, Hkv, N = shape
+    base = 10000.0
+    x = gen.make_inputs(B, Hq, Hkv, N, 128, 17 + N, need_do=False, outlier_frac=1e-3, outlier_scale=50.0)
+    signs = gen.hadamard_signs(Hkv, 128, 37 + N)
+    dev = {k: v.cuda() for k, v in x.items()}
+    dsig = torch.from_numpy(signs).cuda() if rotate else None
+    q8, k8, v8, sc = ea.hadamard_quant_fp8(dev["q"], dev["k"], dev["v"], dsig, rope_base=base)
+    ea.attn_status()
+    sc = sc.cpu().numpy().astype(np.float64)
+    parts = [(q8, x["q"], Hq, 0, True), (k8, x["k"], Hkv, B * Hq, True),
+             (v8, x["v"], Hkv, B * Hq + B * Hkv, False)]
+    for codes, src, H, off, rot in parts:
+        ref = attn64.rope(src, base) if rot else attn64._f64(src)
+        if rotate and rot:
+            ref = attn64.rotate_heads(ref, signs, Hkv)
+        s_ref = attn64.head_amax_scales(ref)
+        s_gpu = sc[off:off + B * H].reshape(B, H)
+        np.testing.assert_allclose(s_gpu, s_ref, rtol=ROPE_REL if rot else 2e-6)
+        exact = ref / s_ref[:, :, None, None]
+        dec = _dec(codes)
+        slack = ROPE_REL * np.abs(exact).max(axis=-1, keepdims=True) + 1e-12 if rot else 1e-12
+        assert (np.abs(dec - exact) <= _quantum(exact) + slack).all()
+        same = (dec == attn64.e4m3_round(exact)).mean()
+        assert same > 0.995, same
+
+
 def test_fp8_forward_matches_attention_on_dequantised_inputs():
     ea = lib()
     B, Hq, Hkv, N = 1, 4, 2, 700

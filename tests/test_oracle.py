@@ -402,3 +402,33 @@ def test_packed_sequences_equal_separate_runs(mk):
         np.testing.assert_allclose(L[:, :, a:b], L1, rtol=0, atol=1e-12)
         for full, part in zip((gq, gk, gv), g1):
             np.testing.assert_allclose(full[:, :, a:b], part, rtol=0, atol=1e-12)
+
+
+def test_rope_closed_forms():
+    """RoPE: identity at position 0; a d = 2 row turns by exactly n radians at
+    position n (its only frequency is base^0 = 1); row norms are kept."""
+    x = np.zeros((1, 1, 5, 2))
+    x[..., 0] = 1.0
+    r = A.rope(x, 10000.0)
+    n = np.arange(5)
+    np.testing.assert_allclose(r[0, 0, :, 0], np.cos(n), atol=1e-15)
+    np.testing.assert_allclose(r[0, 0, :, 1], np.sin(n), atol=1e-15)
+    y = np.random.default_rng(3).standard_normal((2, 3, 17, 8))
+    ry = A.rope(y, 500.0)
+    np.testing.assert_allclose(ry[:, :, 0], y[:, :, 0], atol=0)
+    np.testing.assert_allclose(np.linalg.norm(ry, axis=-1), np.linalg.norm(y, axis=-1), rtol=1e-13)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    """<rope(q)[n], rope(k)[m]> is a function of n - m: the same q and k
+    vectors placed at every position give a Toeplitz score matrix."""
+    rng = np.random.default_rng(5)
+    qv, kv = rng.standard_normal(16), rng.standard_normal(16)
+    N = 12
+    q = np.broadcast_to(qv, (1, 1, N, 16)).copy()
+    k = np.broadcast_to(kv, (1, 1, N, 16)).copy()
+    S = A.rope(q, 100.0)[0, 0] @ A.rope(k, 100.0)[0, 0].T
+    for t in range(-N + 1, N):
+        diag = np.diagonal(S, offset=t)
+        np.testing.assert_allclose(diag, diag[0], rtol=1e-12, atol=1e-12)
+    assert not np.allclose(S[0, 0], S[0, 1])  # and does depend on it
