@@ -42,6 +42,8 @@ WORKLOADS = {
     # packed variable-length sequences (lengths drawn like the documents), causal
     "varlen_packed_16k": dict(B=1, Hq=16, Hkv=4, N=16384, d=128, causal=True, doc=True,
                               varlen=True, seed=6000),
+    # causal prefill with K/V in a shuffled paged cache of 16-row blocks
+    "paged_prefill_8k": dict(B=2, Hq=32, Hkv=8, N=8192, d=128, causal=True, paged=True, seed=7000),
 }
 
 DOC_LEN_MIN = 128

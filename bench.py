@@ -266,6 +266,8 @@ def run_ours(args, world, rank, local):
         return run_fp8(args, world, rank, local)
     if gen.WORKLOADS[args.workload].get("varlen"):
         return run_varlen(args, world, rank, local)
+    if gen.WORKLOADS[args.workload].get("paged"):
+        return run_paged(args, world, rank, local)
     name = args.workload
     cfg = dict(gen.WORKLOADS[name])
     if args.heads:  # smaller case of the same shape family (profiling); 8 query heads per KV head
@@ -518,6 +520,77 @@ def run_varlen(args, world, rank, local):
                      "peak": sustained, "unit": "TFLOP/s", "frac": round(bwd_t / sustained, 4), "traffic": None,
                      "peak_source": f"{src} bf16_tflops_sustained"},
         "e2e": None, "gpu_launches": 10 * args.steps, "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_paged(args, world, rank, local):
+    """Causal prefill forward with K/V read through a block table from a
+    shuffled cache of 16-row blocks (attn_fwd_paged), beside the same forward
+    on contiguous K/V."""
+    import exact_attention_66_gb300 as ea
+
+    name = args.workload
+    cfg = dict(gen.WORKLOADS[name])
+    B, Hq, Hkv, N, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"]
+    scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = gen.make_inputs(**dict(cfg, seed=cfg["seed"] + 97 * rank, need_do=False))
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    nb = N // 16
+    num_blocks = B * nb
+    perm = torch.from_numpy(np.random.default_rng(cfg["seed"]).permutation(num_blocks).astype(np.int32))
+    table = perm.reshape(B, nb).to(dev)
+    kc = torch.empty(num_blocks, Hkv, 16, d, dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    kc[table.reshape(-1).long()] = k.reshape(B, Hkv, nb, 16, d).permute(0, 2, 1, 3, 4).reshape(-1, Hkv, 16, d)
+    vc[table.reshape(-1).long()] = v.reshape(B, Hkv, nb, 16, d).permute(0, 2, 1, 3, 4).reshape(-1, Hkv, 16, d)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    mods = ea.make_mods(causal=True)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ea.attn_status(stream)
+        return e0.elapsed_time(e1) / args.steps
+
+    barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ms = timed(lambda: ea.attn_fwd_paged(q, kc, vc, table, num_blocks, o, lse, B, Hq, Hkv, N, d, scale, mods,
+                                         None, 0, stream))
+    clk = clocks.stop()
+    ms_contig = timed(lambda: ea.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, N, d, scale, mods, None, 0, stream))
+    ms = allmax(world, ms)
+    peaks, src = load_peaks()
+    sustained = peaks["bf16_tflops_sustained"]
+    fwd_f, _ = flops(cfg)
+    t = fwd_f / (ms * 1e-3) / 1e12
+    line = {
+        "metric": f"attention TFLOPS fwd ({name}, paged K/V)", "value": round(world * t, 2), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "mask": "causal",
+                   "block_size": 16, "num_blocks": num_blocks,
+                   "parallelism": "single" if world == 1 else f"replicas{world}", "l2": l2_note(cfg)},
+        "fwd_tflops": round(t, 1), "fwd_frac_peak": round(t / sustained, 4),
+        "kernel_ms": {"fwd_paged": round(ms, 4), "fwd_contiguous_same_inputs": round(ms_contig, 4)},
+        "roofline": {"kernel": "fwd_paged", "bound": "tensor", "achieved": round(t, 1), "peak": sustained,
+                     "unit": "TFLOP/s", "frac": round(t / sustained, 4), "traffic": None,
+                     "peak_source": f"{src} bf16_tflops_sustained"},
+        "e2e": None, "gpu_launches": args.steps, "clocks": clk,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

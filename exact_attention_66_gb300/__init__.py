@@ -16,13 +16,14 @@ from ._lib import (  # noqa: F401
     OP_BWD_VARLEN, OP_FWD, OP_FWD_FP8, OP_FWD_VARLEN, OP_QUANT_FP8, TILE_FULL, TILE_PARTIAL,
     TILE_SKIP, attn_block_map, attn_bwd, attn_bwd_profiled, attn_bwd_noalloc, attn_bwd_varlen,
     NOALLOC_SCRATCH_BYTES, attn_fwd, attn_fwd_fp8, attn_fwd_varlen, attn_hadamard_quant_fp8,
-    attn_rope_hadamard_quant_fp8,
+    attn_rope_hadamard_quant_fp8, attn_fwd_paged,
     attn_status, attn_workspace_size, lib,
     make_mods, status_string,
 )
 
 __all__ = [
-    "forward", "backward", "forward_varlen", "backward_varlen", "hadamard_quant_fp8", "forward_fp8",
+    "forward", "backward", "forward_paged", "forward_varlen", "backward_varlen", "hadamard_quant_fp8",
+    "forward_fp8", "attn_fwd_paged",
     "block_map", "make_mods", "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc",
     "attn_fwd_varlen", "attn_bwd_varlen", "attn_hadamard_quant_fp8", "attn_rope_hadamard_quant_fp8",
     "attn_fwd_fp8", "attn_block_map",
@@ -69,6 +70,21 @@ def backward(q, k, v, o, lse, do, scale=None, mods=None, stream=None):
     ws, nws = _workspace(OP_BWD, B, Hq, Hkv, N, d, mods, q.device)
     attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods, ws, nws, stream)
     return dq, dk, dv
+
+
+def forward_paged(q, k_cache, v_cache, block_table, scale=None, mods=None, stream=None):
+    """(O, LSE) with K/V read from a paged cache: q [B, Hq, N, d], caches
+    [num_blocks, Hkv, 16, d], block_table a device int32 [B, N / 16]."""
+    torch = _torch()
+    B, Hq, N, d = q.shape
+    num_blocks, Hkv = k_cache.shape[0], k_cache.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q)
+    l = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    ws, nws = _workspace(OP_FWD, B, Hq, Hkv, N, d, mods, q.device)
+    attn_fwd_paged(q, k_cache, v_cache, block_table, num_blocks, o, l, B, Hq, Hkv, N, d, scale, mods, ws,
+                   nws, stream)
+    return o, l
 
 
 def forward_varlen(q, k, v, cu_seqlens, scale=None, mods=None, stream=None):

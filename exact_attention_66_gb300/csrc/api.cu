@@ -143,6 +143,20 @@ bool make_map(CUtensorMap* m, const void* ptr, bool e4m3, int d, int N, long lon
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// K/V cache of 16-row blocks, [kv_blocks, Hkv, 16, d] bf16: 3-D map over
+// (d, 16 rows, block x head) with 64-column x 16-row boxes, 128-byte swizzle.
+bool make_paged_map(CUtensorMap* m, const void* ptr, int d, long long planes) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, 16, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)16 * d * 2};
+  cuuint32_t box[3] = {64, 16, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 AttnParams make_params(int B, int Hq, int Hkv, int N, float scale, const attn_mods_t* mods,
                        int* status) {
   AttnParams p{};
@@ -164,6 +178,9 @@ AttnParams make_params(int B, int Hq, int Hkv, int N, float scale, const attn_mo
   p.col_range = nullptr;
   p.doc_bounds = nullptr;
   p.doc_unsorted = nullptr;
+  p.block_table = nullptr;
+  p.kv_blocks = 0;
+  p.bt_stride = 0;
   p.status = status;
   return p;
 }
@@ -408,6 +425,41 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const
   L.lse = lse;
   if ((st = prepare_mods(L.p, static_cast<uint8_t*>(ws), s)) != ATTN_OK) return st;
   return cuda_status(launch_fwd_fp8(L, has_score_mods(L.p.flags), needs_map(L.p.flags), s));
+}
+
+attn_status_t attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_table, int num_blocks, void* o, float* lse, int B,
+                             int Hq, int Hkv, int N, int d, float scale, const attn_mods_t* mods,
+                             void* ws, size_t ws_bytes, void* stream) {
+  attn_status_t st;
+  if ((st = check_shape(B, Hq, Hkv, N, d, false)) != ATTN_OK) return st;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((st = check_tensors({q, k_cache, v_cache, o})) != ATTN_OK) return st;
+  if (lse == nullptr || block_table == nullptr || num_blocks < 1) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(lse, 4) || !aligned(block_table, 4)) return ATTN_ERR_UNSUPPORTED;
+  if (N % 16 != 0) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)num_blocks * Hkv >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if ((st = check_mods(mods)) != ATTN_OK) return st;
+  const size_t need = attn_workspace_size(ATTN_OP_FWD, B, Hq, Hkv, N, d, mods);
+  if ((st = check_ws(ws, ws_bytes, need)) != ATTN_OK) return st;
+  int* status = nullptr;
+  if ((st = device_state(&status)) != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  FwdLaunch L{};
+  L.p = make_params(B, Hq, Hkv, N, scale, mods, status);
+  if (!make_map(&L.tq, q, false, d, N, (long long)B * Hq) ||
+      !make_paged_map(&L.tk, k_cache, d, (long long)num_blocks * Hkv) ||
+      !make_paged_map(&L.tv, v_cache, d, (long long)num_blocks * Hkv))
+    return ATTN_ERR_CUDA;
+  L.o = o;
+  L.lse = lse;
+  L.p.block_table = block_table;
+  L.p.kv_blocks = num_blocks;
+  L.p.bt_stride = N / 16;
+  if ((st = prepare_mods(L.p, static_cast<uint8_t*>(ws), s)) != ATTN_OK) return st;
+  return cuda_status(launch_fwd_bf16(L, d, has_score_mods(L.p.flags), needs_map(L.p.flags), s));
 }
 
 attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -44,6 +44,11 @@ struct AttnParams {
   const int2* doc_bounds;
   const int* doc_unsorted;
   const float* slopes;  // [Hq] or nullptr (default slopes)
+  // Paged K/V (forward only): K and V live in blocks of 16 rows,
+  // cache [kv_blocks, Hkv, 16, d]; row n of batch b is row n % 16 of block
+  // block_table[b * bt_stride + n / 16].  nullptr: contiguous [B, Hkv, N, d].
+  const int* block_table;
+  int kv_blocks, bt_stride;
   const uint8_t* map;   // [B, nT, nT] tile classes, or nullptr (analytic)
   // With a map: [first, last + 1) of the non-skipped tiles of each Q tile
   // (row_range, over J) and of each KV tile (col_range, over I), [B, nT].

@@ -321,9 +321,27 @@ __global__ void __launch_bounds__(384, 1)
         const int st = r % C::RST;
         if (!mbar_wait(&S.empty[st], ((r / C::RST) & 1) ^ 1, ab)) return false;
         mbar_arrive_tx(&S.full[st], C::TILE_BYTES);
-        for (int ch = 0; ch < C::CH; ++ch)
-          tma_load_3d(smem + C::R_OFF + st * C::TILE_BYTES + ch * 16384, map, &S.full[st], ch * C::BOX,
-                      J * TILE, b * p.Hkv + hk);
+        uint8_t* dst = smem + C::R_OFF + st * C::TILE_BYTES;
+        if (p.block_table == nullptr) {
+          for (int ch = 0; ch < C::CH; ++ch)
+            tma_load_3d(dst + ch * 16384, map, &S.full[st], ch * C::BOX, J * TILE, b * p.Hkv + hk);
+        } else {
+          // Paged: the tile's 8 blocks of 16 rows, each a 16-row box at its
+          // 2 KB offset (the 128-byte swizzle repeats every 8 rows, so the
+          // layout matches a whole-tile load).  Blocks past the sequence end
+          // use an out-of-range block index: TMA fills them with zeros.
+          int z[TILE / 16];  // all 8 table entries in flight before the first copy
+#pragma unroll
+          for (int sb = 0; sb < TILE / 16; ++sb) {
+            const int lb = J * (TILE / 16) + sb;
+            z[sb] = lb < p.bt_stride ? __ldg(p.block_table + (size_t)b * p.bt_stride + lb) * p.Hkv + hk
+                                     : p.kv_blocks * p.Hkv;
+          }
+#pragma unroll
+          for (int sb = 0; sb < TILE / 16; ++sb)
+            for (int ch = 0; ch < C::CH; ++ch)
+              tma_load_3d(dst + ch * 16384 + sb * 2048, map, &S.full[st], ch * C::BOX, 0, z[sb]);
+        }
         ++r;
         return true;
       };

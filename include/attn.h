@@ -187,6 +187,24 @@ attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, cons
                                const attn_mods_t* mods, void* stream);
 
 /*
+ * Forward over a paged K/V cache (the inference layout of the kernel fusion
+ * page's serving discussion: keys and values in fixed blocks of 16 rows
+ * addressed through a block table).  Same computation and mods as attn_fwd,
+ * with K and V read through the table instead of from [B, Hkv, N, d].
+ * k_cache, v_cache : bf16 [num_blocks, Hkv, 16, d]; block j of head h holds
+ *                    16 consecutive key (value) rows of that head.
+ * block_table      : device int32 [B, N / 16]: key rows [16 t, 16 t + 16) of
+ *                    batch row b are block block_table[b][t]; an index outside
+ *                    [0, num_blocks) reads zeros.
+ * N must be a multiple of 16 and d = 128 (ATTN_ERR_UNSUPPORTED otherwise);
+ * workspace as attn_fwd (ATTN_OP_FWD).
+ */
+attn_status_t attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_table, int num_blocks, void* o, float* lse, int B,
+                             int Hq, int Hkv, int N, int d, float scale, const attn_mods_t* mods,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Packed variable-length sequences: n_seqs sequences stored back to back along
  * the row axis, attending only within themselves -- the unpadded form of the
  * document mask (FlexAttention/FA4 page, opening paragraphs: document

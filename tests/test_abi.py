@@ -142,3 +142,16 @@ def test_rope_prologue_validates(L):
                                                None) == 1
     assert so.attn_rope_hadamard_quant_fp8(A, A, A, A, A, A, A, None, 1, 2, 2, 64, 64, 1e4, A, 4096,
                                            None) == 2  # d must be 128
+
+
+def test_paged_forward_validates(L):
+    so = L.lib()
+
+    def fp(table=A, nb=8, N=128, d=128, q=A):
+        return so.attn_fwd_paged(q, A, A, table, nb, A, A, 1, 2, 2, N, d, 0.1, None, None, 0, None)
+    assert fp(table=None) == 1
+    assert fp(nb=0) == 1
+    assert fp(q=None) == 1
+    assert fp(N=120) == 2      # N must be a multiple of 16
+    assert fp(d=64) == 2       # d = 128 only
+    assert fp(table=A + 2) == 2
