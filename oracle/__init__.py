@@ -9,8 +9,9 @@ the CUDA path (``exact_attention_66_gb300``); the only common module is
 Modules
 -------
 attn64    plain definition of masked/modded softmax attention in fp64 numpy,
-          forward and backward, the 128x128 block-sparsity map by brute force,
-          the signed Hadamard rotation and e4m3 quantisation.
+          forward and backward, the decode step over a paged K/V cache, the
+          128x128 block-sparsity map by brute force, the signed Hadamard
+          rotation, RoPE and e4m3 quantisation.
 brute     scalar triple loops for tiny shapes, written independently of
           attn64, used only to pin it.
 

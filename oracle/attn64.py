@@ -157,6 +157,58 @@ def forward(q, k, v, scale: float, mods: Mods = None):
     return O, L
 
 
+def decode_paged(q, k_cache, v_cache, block_table, seqlens, scale: float, mods: Mods = None):
+    """Decode step over a paged K/V cache: O [B, Hq, d] and LSE [B, Hq] (fp64).
+
+    "Les kernels d'attention rapide et la fusion d'opérateurs accélèrent les
+    modèles d'IA", section "Attention de type FlashAttention et attention
+    paginée": the K/V cache grows by one token per step and is stored in
+    fixed-size blocks (16 tokens in the page's example) that a block table maps
+    from logical to physical positions; the attention kernel translates every
+    position through that table.
+
+    Reading taken here: ``q`` [B, Hq, d] holds the newest token of each
+    sequence, at position i = L_b - 1 with L_b = ``seqlens[b]``; it attends to
+    the L_b cached keys j = 0 .. L_b - 1, where row j of sequence b, KV head hk
+    is row j % 16 of physical block ``block_table[b, j // 16]`` of the cache
+    [num_blocks, Hkv, 16, d].  The scores and mods are those of ``logits`` /
+    ``allowed`` with that i (the causal test j <= i then always holds; the
+    window keeps i - j < W; ALiBi subtracts slope * (i - j)).  A sequence with
+    L_b = 0 gets O = 0, LSE = -inf.  Document masks do not apply.
+    """
+    mods = mods or Mods()
+    if mods.doc_ids is not None:
+        raise ValueError("document masks do not apply to a decode step")
+    Q = _f64(q)
+    KC = _f64(k_cache)
+    VC = _f64(v_cache)
+    table = np.asarray(block_table)
+    lens = np.asarray(seqlens)
+    B, Hq, d = Q.shape
+    Hkv, blk = KC.shape[1], KC.shape[2]
+    G = Hq // Hkv
+    O = np.zeros((B, Hq, d))
+    LSE = np.full((B, Hq), -np.inf)
+    for b in range(B):
+        L = int(lens[b])
+        if L == 0:
+            continue
+        blocks = table[b, :-(-L // blk)]
+        rows = np.array([L - 1])
+        cols = np.arange(L)
+        m = allowed(mods, b, rows, cols)
+        for hk in range(Hkv):
+            K = KC[blocks, hk].reshape(-1, d)[:L]
+            V = VC[blocks, hk].reshape(-1, d)[:L]
+            for hq in range(hk * G, (hk + 1) * G):
+                qh = np.broadcast_to(Q[b, hq], (L, d))  # row L - 1 is the query
+                _, x = logits(qh, K, scale, mods, hq, Hq, rows, cols)
+                P, lse = _softmax_rows(x, m)
+                O[b, hq] = (P @ V)[0]
+                LSE[b, hq] = lse[0]
+    return O, LSE
+
+
 def group_backward(q, k, v, do, scale: float, mods: Mods, b: int, hk: int):
     """dQ for the query heads of KV head ``hk`` and dK, dV of that KV head.
 

@@ -432,3 +432,89 @@ def test_rope_scores_depend_on_relative_position_only():
         diag = np.diagonal(S, offset=t)
         np.testing.assert_allclose(diag, diag[0], rtol=1e-12, atol=1e-12)
     assert not np.allclose(S[0, 0], S[0, 1])  # and does depend on it
+
+
+# ---------------------------------------------------------------------------
+# Decode over a paged K/V cache ("Les kernels d'attention rapide ...", section
+# "Attention de type FlashAttention et attention paginée": block table from
+# logical to physical blocks of 16 tokens).
+
+def _paged_case(B, Hq, Hkv, lens, d, seed, spare=3, blk=16):
+    rng = np.random.default_rng(seed)
+    nbs = [-(-L // blk) for L in lens]
+    width = max(max(nbs), 1)
+    num_blocks = sum(nbs) + spare
+    perm = rng.permutation(num_blocks)
+    table = np.full((B, width), -1, dtype=np.int32)  # unused entries: never read
+    used = 0
+    for b, nb in enumerate(nbs):
+        table[b, :nb] = perm[used:used + nb]
+        used += nb
+    q = rng.standard_normal((B, Hq, d))
+    kc = rng.standard_normal((num_blocks, Hkv, blk, d))
+    vc = rng.standard_normal((num_blocks, Hkv, blk, d))
+    return q, kc, vc, table, np.asarray(lens)
+
+
+DECODE_MODS = {
+    "none": dict(),
+    "window": dict(window=5),
+    "softcap_alibi": dict(softcap=2.0, alibi=True),
+    "all": dict(window=9, softcap=3.0, alibi=True),
+}
+
+
+@pytest.mark.parametrize("mk", list(DECODE_MODS), ids=list(DECODE_MODS))
+def test_decode_matches_brute_force_last_row(mk):
+    """The decode step equals the last row of the causal brute-force forward run
+    on the sequence's rows, gathered here by an explicit loop over positions."""
+    B, Hq, Hkv, d = 2, 4, 2, 8
+    lens = [37, 17]
+    q, kc, vc, table, sl = _paged_case(B, Hq, Hkv, lens, d, seed=11)
+    cfg = DECODE_MODS[mk]
+    slopes = list(A.alibi_slopes(Hq)) if cfg.get("alibi") else None
+    O, L = A.decode_paged(q, kc, vc, table, sl, 0.4, A.Mods(causal=True, **cfg))
+    for b, n in enumerate(lens):
+        K = [[[float(x) for x in kc[table[b, j // 16], hk, j % 16]] for j in range(n)] for hk in range(Hkv)]
+        V = [[[float(x) for x in vc[table[b, j // 16], hk, j % 16]] for j in range(n)] for hk in range(Hkv)]
+        Qrows = [[[0.0] * d for _ in range(n - 1)] + [list(q[b, h])] for h in range(Hq)]
+        Ob, Lb = brute.forward([Qrows], [K], [V], 0.4, causal=True, window=cfg.get("window"),
+                               softcap=cfg.get("softcap"), slopes=slopes)
+        for h in range(Hq):
+            np.testing.assert_allclose(O[b, h], Ob[0][h][n - 1], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(L[b, h], Lb[0][h][n - 1], rtol=1e-12, atol=1e-12)
+
+
+def test_decode_closed_forms():
+    B, Hq, Hkv, d = 3, 2, 1, 8
+    q, kc, vc, table, sl = _paged_case(B, Hq, Hkv, [1, 0, 21], d, seed=5)
+    O, L = A.decode_paged(q, kc, vc, table, sl, 0.5, A.Mods(causal=True))
+    # one cached token: O is its value row, LSE its score
+    v0, k0 = vc[table[0, 0], 0, 0], kc[table[0, 0], 0, 0]
+    for h in range(Hq):
+        np.testing.assert_allclose(O[0, h], v0, rtol=1e-14)
+        np.testing.assert_allclose(L[0, h], 0.5 * q[0, h] @ k0, rtol=1e-14)
+    # empty sequence: O = 0, LSE = -inf
+    assert np.all(O[1] == 0.0) and np.all(np.isneginf(L[1]))
+    # window 1: only the newest token itself
+    Ow, _ = A.decode_paged(q, kc, vc, table, sl, 0.5, A.Mods(causal=True, window=1))
+    np.testing.assert_allclose(Ow[2, 0], vc[table[2, 20 // 16], 0, 20 % 16], rtol=1e-14)
+    # constant values: O is that constant
+    vconst = np.full_like(vc, 0.75)
+    Oc, _ = A.decode_paged(q, kc, vconst, table, sl, 0.5)
+    np.testing.assert_allclose(Oc[[0, 2]], 0.75, rtol=1e-14)
+
+
+def test_decode_block_placement_is_invisible():
+    """Moving the physical blocks (and the table with them) changes nothing."""
+    B, Hq, Hkv, d = 2, 4, 2, 8
+    q, kc, vc, table, sl = _paged_case(B, Hq, Hkv, [40, 33], d, seed=9)
+    O, L = A.decode_paged(q, kc, vc, table, sl, 0.3, A.Mods(alibi=True))
+    perm = np.random.default_rng(1).permutation(kc.shape[0])  # new slot of each block
+    kc2 = np.empty_like(kc)
+    vc2 = np.empty_like(vc)
+    kc2[perm] = kc
+    vc2[perm] = vc
+    table2 = np.where(table >= 0, perm[np.maximum(table, 0)], -1)
+    O2, L2 = A.decode_paged(q, kc2, vc2, table2, sl, 0.3, A.Mods(alibi=True))
+    assert np.array_equal(O, O2) and np.array_equal(L, L2)
