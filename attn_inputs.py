@@ -18,6 +18,12 @@ Workloads (all synthetic; the pages name no dataset):
                       N(0,1) with 0.1 % of entries scaled by 50 (the outlier
                       experiment of the FlashAttention-3 digest, "Basse
                       précision FP8 et incoherent processing").
+* ``varlen_packed_16k`` packed sequences (lengths drawn like the documents).
+* ``paged_prefill_8k`` causal prefill with K/V in a shuffled 16-row block cache.
+* ``paged_decode_8k`` B=32 Hq=64 Hkv=8 d=128: one decode token per sequence
+                      over a shuffled paged cache, context lengths uniform in
+                      [4096, 8192] (the kernel fusion page's paged KV cache,
+                      block_size 16).
 
 Recipe: Q/K/V/dO are ``torch.randn`` fp32 draws from a CPU generator seeded
 per tensor, rounded to bf16.  Document lengths are integers uniform in
@@ -44,6 +50,9 @@ WORKLOADS = {
                               varlen=True, seed=6000),
     # causal prefill with K/V in a shuffled paged cache of 16-row blocks
     "paged_prefill_8k": dict(B=2, Hq=32, Hkv=8, N=8192, d=128, causal=True, paged=True, seed=7000),
+    # one decode step per sequence over a shuffled paged cache; N is the longest
+    # context, lengths uniform in [min_len, N]
+    "paged_decode_8k": dict(B=32, Hq=64, Hkv=8, N=8192, d=128, min_len=4096, decode=True, seed=8000),
 }
 
 DOC_LEN_MIN = 128
@@ -119,6 +128,35 @@ def make_inputs(B, Hq, Hkv, N, d, seed, *, need_do=True, outlier_frac=0.0,
     if doc:
         out["doc_ids"] = doc_ids(B, N, seed + 10)
     return out
+
+
+def paged_decode_inputs(B, Hq, Hkv, N, d, seed, *, min_len=1, lens=None, spare=8, block=16, **_):
+    """One decode step over a paged K/V cache.
+
+    Returns q [B, Hq, d] and the caches [num_blocks, Hkv, block, d] (CPU bf16),
+    the block table int32 [B, ceil(N / block)] and the lengths int32 [B].
+    Lengths are uniform integers in [min_len, N] (seed + 10) unless given;
+    sequence b owns ceil(L_b / block) blocks at shuffled physical slots
+    (seed + 11), a few spare slots stay unused, and table entries past a
+    sequence's last block are -1.  Seeds: q = seed, K cache = seed + 1,
+    V cache = seed + 2.
+    """
+    if lens is None:
+        lens = np.random.default_rng(int(seed) + 10).integers(min_len, N + 1, size=B)
+    lens = np.asarray(lens, dtype=np.int32)
+    width = -(-N // block)
+    nbs = [-(-int(L) // block) for L in lens]
+    num_blocks = sum(nbs) + spare
+    perm = np.random.default_rng(int(seed) + 11).permutation(num_blocks).astype(np.int32)
+    table = np.full((B, width), -1, dtype=np.int32)
+    used = 0
+    for b, nb in enumerate(nbs):
+        table[b, :nb] = perm[used:used + nb]
+        used += nb
+    return dict(q=randn_bf16((B, Hq, d), seed),
+                k_cache=randn_bf16((num_blocks, Hkv, block, d), seed + 1),
+                v_cache=randn_bf16((num_blocks, Hkv, block, d), seed + 2),
+                block_table=table, seqlens=lens)
 
 
 def workload_inputs(name: str, **overrides):

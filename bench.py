@@ -8,7 +8,7 @@ shape).  Throughput counts algorithmic FLOPs: 4*B*Hq*d*(allowed pairs) for
 the forward and 2.5x that for the backward.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
-  python bench.py --workload causal_mha_2k|flex_mods_4k|tiny_mha|fp8_outliers_16k
+  python bench.py --workload causal_mha_2k|flex_mods_4k|tiny_mha|fp8_outliers_16k|...
 
 Prints ONE JSON line (rank 0); the default workload is the one the metric is
 quoted on, the others are the smaller parity workloads timed the same way
@@ -268,6 +268,8 @@ def run_ours(args, world, rank, local):
         return run_varlen(args, world, rank, local)
     if gen.WORKLOADS[args.workload].get("paged"):
         return run_paged(args, world, rank, local)
+    if gen.WORKLOADS[args.workload].get("decode"):
+        return run_decode(args, world, rank, local)
     name = args.workload
     cfg = dict(gen.WORKLOADS[name])
     if args.heads:  # smaller case of the same shape family (profiling); 8 query heads per KV head
@@ -591,6 +593,103 @@ def run_paged(args, world, rank, local):
                      "unit": "TFLOP/s", "frac": round(t / sustained, 4), "traffic": None,
                      "peak_source": f"{src} bf16_tflops_sustained"},
         "e2e": None, "gpu_launches": args.steps, "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def decode_bytes(B, Hq, Hkv, d, lens):
+    """Algorithmic HBM bytes of one decode step: every cached K and V row of
+    every sequence once, the block-table entries used, Q read, O and LSE
+    written."""
+    lens = np.asarray(lens, np.int64)
+    kv = 2 * int(lens.sum()) * Hkv * d * 2
+    table = 4 * int(((lens + 15) // 16).sum()) + 4 * B
+    return kv + table + 2 * B * Hq * d * 2 + 4 * B * Hq
+
+
+def run_decode(args, world, rank, local):
+    """One decode step per sequence over a shuffled paged K/V cache
+    (attn_decode_paged): HBM-bound, reported in GB/s of algorithmic bytes
+    against the measured copy bandwidth."""
+    import exact_attention_66_gb300 as ea
+
+    name = args.workload
+    cfg = dict(gen.WORKLOADS[name])
+    B, Hq, Hkv, N, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"]
+    scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = gen.paged_decode_inputs(**dict(cfg, seed=cfg["seed"] + 97 * rank))
+    q_host = x["q"].pin_memory()
+    q = q_host.to(dev)
+    kc, vc = x["k_cache"].to(dev), x["v_cache"].to(dev)
+    table = torch.from_numpy(x["block_table"]).to(dev)
+    lens = torch.from_numpy(x["seqlens"]).to(dev)
+    num_blocks, max_blocks = kc.shape[0], table.shape[1]
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    nws = ea.attn_workspace_size(ea.OP_DECODE_PAGED, B, Hq, Hkv, 16 * max_blocks, d, None)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ea.attn_decode_paged(q, kc, vc, table, max_blocks, lens, num_blocks, o, lse, B, Hq, Hkv, d, scale,
+                             None, ws, nws, stream)
+
+    def step_e2e():  # the new tokens' queries in, outputs back (the cache stays resident)
+        q.copy_(q_host, non_blocking=True)
+        step()
+        o_host.copy_(o, non_blocking=True)
+        lse_host.copy_(lse, non_blocking=True)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        ea.attn_status(stream)
+        return e0.elapsed_time(e1) / args.steps
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ms = timed(step)
+    clk = clocks.stop()
+    ms_e2e = timed(step_e2e)
+    ms, ms_e2e = allmax(world, ms), allmax(world, ms_e2e)
+    peaks, src = load_peaks()
+    nbytes = decode_bytes(B, Hq, Hkv, d, x["seqlens"])
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    hbm = peaks["hbm_gbs"]
+    bytes_io = q.numel() * 2 + o.numel() * 2 + lse.numel() * 4
+    line = {
+        "metric": f"paged decode HBM throughput ({name})", "value": round(world * gbs, 1), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d, "max_context": N,
+                   "context_lengths": f"uniform in [{cfg['min_len']}, {N}], total {int(x['seqlens'].sum())}",
+                   "block_size": 16, "num_blocks": num_blocks,
+                   "parallelism": "single" if world == 1 else f"replicas{world}",
+                   "l2": f"cache larger than L2 ({2 * kc.numel() * 2 / 2**20:.0f} MiB of K and V)"},
+        "tokens_per_s": round(world * B / (ms * 1e-3), 1),
+        "algorithmic_bytes_per_step": nbytes,
+        "roofline": {"kernel": "decode_paged (setup, main and merge launches together)", "bound": "hbm",
+                     "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                     "traffic": None, "peak_source": f"{src} hbm_gbs"},
+        "e2e": {"value": round(world * nbytes / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": q.numel() * 2, "d2h_bytes_per_step": bytes_io - q.numel() * 2,
+                "ms_per_step": round(ms_e2e, 4)},
+        "gpu_launches": 3 * args.steps, "clocks": clk,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

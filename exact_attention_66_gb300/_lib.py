@@ -21,12 +21,12 @@ STATUS_NAMES = {
 }
 
 MOD_CAUSAL, MOD_WINDOW, MOD_DOC, MOD_SOFTCAP, MOD_ALIBI = 1, 2, 4, 8, 16
-OP_FWD, OP_BWD, OP_FWD_FP8, OP_QUANT_FP8, OP_FWD_VARLEN, OP_BWD_VARLEN = 0, 1, 2, 3, 4, 5
+OP_FWD, OP_BWD, OP_FWD_FP8, OP_QUANT_FP8, OP_FWD_VARLEN, OP_BWD_VARLEN, OP_DECODE_PAGED = 0, 1, 2, 3, 4, 5, 6
 TILE_SKIP, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 
 # Exported symbols, in the order include/attn.h declares them.
 EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc",
-           "attn_fwd_paged", "attn_fwd_varlen", "attn_bwd_varlen", "attn_hadamard_quant_fp8", "attn_rope_hadamard_quant_fp8",
+           "attn_fwd_paged", "attn_decode_paged", "attn_fwd_varlen", "attn_bwd_varlen", "attn_hadamard_quant_fp8", "attn_rope_hadamard_quant_fp8",
            "attn_fwd_fp8", "attn_block_map", "attn_status", "attn_status_string")
 
 
@@ -56,6 +56,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_bwd_profiled.argtypes = lib.attn_bwd.argtypes + [ctypes.POINTER(ctypes.c_void_p)]
     lib.attn_bwd_noalloc.argtypes = lib.attn_bwd.argtypes[:16] + [vp]  # no ws, ws_bytes
     lib.attn_fwd_paged.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
+    lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, i, vp, i, vp, vp, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_hadamard_quant_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp]
@@ -170,6 +171,13 @@ def attn_fwd_paged(q, k_cache, v_cache, block_table, num_blocks, o, lse, B, Hq, 
     _check(_lib.attn_fwd_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), num_blocks,
                                _ptr(o), _ptr(lse), B, Hq, Hkv, N, d, float(scale), _mods_ref(mods),
                                _ptr(ws), int(ws_bytes), _stream(stream)), "attn_fwd_paged")
+
+
+def attn_decode_paged(q, k_cache, v_cache, block_table, max_blocks, seqlens, num_blocks, o, lse, B, Hq,
+                      Hkv, d, scale, mods=None, ws=None, ws_bytes=0, stream=None):
+    _check(_lib.attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), max_blocks,
+                                  _ptr(seqlens), num_blocks, _ptr(o), _ptr(lse), B, Hq, Hkv, d, float(scale),
+                                  _mods_ref(mods), _ptr(ws), int(ws_bytes), _stream(stream)), "attn_decode_paged")
 
 
 def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, n_seqs, Hq, Hkv, total, d, scale, mods=None,

@@ -249,11 +249,60 @@ attn_status_t prepare_mods(AttnParams& p, uint8_t* region, cudaStream_t s) {
   return ATTN_OK;
 }
 
+// ---- paged decode ----------------------------------------------------------
+// Work items of `ct` key tiles, about this many in all (16 for each SM of a
+// 152-SM part), so that every persistent CTA walks many items and the last
+// ones finish together.  A pure function of the shape, so that the workspace
+// size is too.
+constexpr long long kDecodeTargetItems = 16 * 152;
+
+struct DecodeSplit {
+  int ct, max_chunks;
+};
+DecodeSplit decode_split(int B, int Hkv, int N) {
+  const int tiles = n_tiles(N);
+  const long long units = (long long)B * Hkv * tiles;
+  long long ct = (units + kDecodeTargetItems - 1) / kDecodeTargetItems;
+  if (ct < 1) ct = 1;
+  if (ct > tiles) ct = tiles;
+  return {(int)ct, (int)((tiles + ct - 1) / ct)};
+}
+size_t decode_info_bytes(int B) { return round_up((size_t)B * sizeof(int4), 256) + 256; }
+size_t decode_ws_bytes(int B, int Hq, int Hkv, int N) {
+  const size_t rows = (size_t)B * Hq * decode_split(B, Hkv, N).max_chunks;
+  return decode_info_bytes(B) + round_up(rows * 128 * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+}
+attn_status_t check_decode(int B, int Hq, int Hkv, int N, int num_blocks, int d, const attn_mods_t* mods) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 16 || num_blocks < 1) return ATTN_ERR_INVALID_ARG;
+  if (N % 16 != 0 || Hq % Hkv != 0 || Hq / Hkv > 128 || d != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)num_blocks * Hkv >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  attn_status_t st;
+  if ((st = check_mods(mods)) != ATTN_OK) return st;
+  if (mods && (mods->flags & ATTN_MOD_DOC)) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * Hq * decode_split(B, Hkv, N).max_chunks * 128 >= (1ll << 40)) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * Hkv * decode_split(B, Hkv, N).max_chunks >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+int sm_count() {
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 }  // namespace
 
 extern "C" {
 
 size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int N, int d, const attn_mods_t* mods) {
+  if (op == ATTN_OP_DECODE_PAGED)
+    return check_decode(B, Hq, Hkv, N, 1, d, mods) == ATTN_OK ? decode_ws_bytes(B, Hq, Hkv, N) : 0;
   if (check_shape(B, Hq, Hkv, N, d, op == ATTN_OP_FWD_FP8 || op == ATTN_OP_QUANT_FP8) != ATTN_OK ||
       check_mods(mods) != ATTN_OK)
     return 0;
@@ -460,6 +509,76 @@ attn_status_t attn_fwd_paged(const void* q, const void* k_cache, const void* v_c
   L.p.bt_stride = N / 16;
   if ((st = prepare_mods(L.p, static_cast<uint8_t*>(ws), s)) != ATTN_OK) return st;
   return cuda_status(launch_fwd_bf16(L, d, has_score_mods(L.p.flags), needs_map(L.p.flags), s));
+}
+
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, int max_blocks, const int32_t* seqlens,
+                                int num_blocks, void* o, float* lse, int B, int Hq, int Hkv, int d,
+                                float scale, const attn_mods_t* mods, void* ws, size_t ws_bytes,
+                                void* stream) {
+  attn_status_t st;
+  if (max_blocks < 1 || max_blocks > (1 << 26)) return max_blocks < 1 ? ATTN_ERR_INVALID_ARG : ATTN_ERR_UNSUPPORTED;
+  const int N = 16 * max_blocks;
+  if ((st = check_decode(B, Hq, Hkv, N, num_blocks, d, mods)) != ATTN_OK) return st;
+  if ((st = check_tensors({q, k_cache, v_cache, o})) != ATTN_OK) return st;
+  if (lse == nullptr || block_table == nullptr || seqlens == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(lse, 4) || !aligned(block_table, 4) || !aligned(seqlens, 4)) return ATTN_ERR_UNSUPPORTED;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, decode_ws_bytes(B, Hq, Hkv, N))) != ATTN_OK) return st;
+  int* status = nullptr;
+  if ((st = device_state(&status)) != ATTN_OK) return st;
+  const int sms = sm_count();
+  if (sms < 1) return ATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  const int G = Hq / Hkv;
+  const DecodeSplit sp = decode_split(B, Hkv, N);
+  DecodeLaunch L{};
+  {  // Q as [B*Hkv, G, d]: one box holds the G query heads of a KV head
+    auto enc = encode_fn();
+    if (!enc) return ATTN_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)G, (cuuint64_t)B * Hkv};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)G * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&L.tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return ATTN_ERR_CUDA;
+  }
+  if (!make_paged_map(&L.tk, k_cache, d, (long long)num_blocks * Hkv) ||
+      !make_paged_map(&L.tv, v_cache, d, (long long)num_blocks * Hkv))
+    return ATTN_ERR_CUDA;
+  L.o = o;
+  L.lse = lse;
+  DecodeParams& p = L.p;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = G;
+  p.bt_stride = max_blocks;
+  p.kv_blocks = num_blocks;
+  p.ct = sp.ct;
+  p.max_chunks = sp.max_chunks;
+  p.scale_log2 = scale * LOG2E;
+  p.flags = mod_flags(mods) & (ATTN_MOD_WINDOW | ATTN_MOD_SOFTCAP | ATTN_MOD_ALIBI);
+  p.window = (p.flags & ATTN_MOD_WINDOW) ? mods->window : 0;
+  const float cap = (p.flags & ATTN_MOD_SOFTCAP) ? mods->softcap : 1.0f;
+  p.sc_in = scale / cap;
+  p.sc_out = cap * LOG2E;
+  p.slopes = (p.flags & ATTN_MOD_ALIBI) ? mods->alibi_slopes : nullptr;
+  p.block_table = block_table;
+  p.seqlens = seqlens;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.seq_info = reinterpret_cast<int4*>(w);
+  p.n_items = reinterpret_cast<int*>(w + decode_info_bytes(B) - 256);
+  const size_t rows = (size_t)B * Hq * sp.max_chunks;
+  p.o_part = reinterpret_cast<float*>(w + decode_info_bytes(B));
+  p.lse_part = reinterpret_cast<float*>(w + decode_info_bytes(B) + round_up(rows * 128 * sizeof(float), 256));
+  p.status = status;
+  const long long items = (long long)B * Hkv * sp.max_chunks;
+  L.grid = (int)(items < sms ? items : sms);
+  return cuda_status(launch_decode(L, has_score_mods(p.flags), s));
 }
 
 attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,

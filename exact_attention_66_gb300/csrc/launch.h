@@ -39,6 +39,37 @@ struct BwdLaunch {
 };
 cudaError_t launch_bwd(const BwdLaunch& L, int d, bool mods, bool masks, cudaStream_t st);
 
+// Decode step over a paged K/V cache (d = 128): one query token per sequence.
+struct DecodeParams {
+  int B, Hq, Hkv, G;       // G = Hq / Hkv query heads per KV head (<= 128)
+  int bt_stride;           // block-table row length (blocks per sequence at most)
+  int kv_blocks;           // cache blocks
+  int ct;                  // key tiles of 128 per work item (chunk)
+  int max_chunks;          // chunks per (sequence, head) in the partial buffers
+  float scale_log2;        // scale * log2(e)
+  float sc_in, sc_out;     // soft-cap: scale / c and c * log2(e)
+  uint32_t flags;          // MOD_WINDOW | MOD_SOFTCAP | MOD_ALIBI (causal is implied)
+  int window;
+  const float* slopes;     // [Hq] or nullptr (default ALiBi slopes)
+  const int* block_table;  // [B, bt_stride]
+  const int* seqlens;      // [B] cached tokens, the query being the last
+  int4* seq_info;          // [B] workspace: {L, first key tile, chunks, first item}
+  int* n_items;            // workspace: number of items
+  float* o_part;           // [B, Hq, max_chunks, 128] workspace: O / l of each chunk
+  float* lse_part;         // [B, Hq, max_chunks] workspace: log2-sum-exp of each chunk
+  int* status;             // device status word
+};
+struct DecodeLaunch {
+  CUtensorMap tq;      // Q as [B*Hkv, G, 128]: box of G rows x 64 columns
+  CUtensorMap tk, tv;  // cache [kv_blocks*Hkv, 16, 128]: 16-row boxes
+  void* o;             // bf16 [B, Hq, 128]
+  float* lse;          // [B, Hq]
+  int grid;            // persistent CTAs
+  DecodeParams p;
+};
+// mods: soft-cap / ALiBi present.
+cudaError_t launch_decode(const DecodeLaunch& L, bool mods, cudaStream_t st);
+
 cudaError_t launch_block_map(const AttnParams& p, uint8_t* map, cudaStream_t st);
 cudaError_t launch_tile_ranges(const AttnParams& p, const uint8_t* map, int2* rows, int2* cols,
                                cudaStream_t st);

@@ -79,14 +79,16 @@ typedef struct {
 } attn_mods_t;
 
 /* Operations for attn_workspace_size().  For the two varlen operations pass
- * B = 1 and N = total (the packed row count). */
+ * B = 1 and N = total (the packed row count); for the paged decode step pass
+ * N = 16 * max_blocks (the longest sequence the block table can hold). */
 enum {
   ATTN_OP_FWD = 0,
   ATTN_OP_BWD = 1,
   ATTN_OP_FWD_FP8 = 2,
   ATTN_OP_QUANT_FP8 = 3,
   ATTN_OP_FWD_VARLEN = 4,
-  ATTN_OP_BWD_VARLEN = 5
+  ATTN_OP_BWD_VARLEN = 5,
+  ATTN_OP_DECODE_PAGED = 6
 };
 
 /* Block-map tile classes (128 x 128 tiles). */
@@ -203,6 +205,39 @@ attn_status_t attn_fwd_paged(const void* q, const void* k_cache, const void* v_c
                              const int32_t* block_table, int num_blocks, void* o, float* lse, int B,
                              int Hq, int Hkv, int N, int d, float scale, const attn_mods_t* mods,
                              void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Decode step over a paged K/V cache ("Les kernels d'attention rapide et la
+ * fusion d'opérateurs accélèrent les modèles d'IA", section "Attention de
+ * type FlashAttention et attention paginée": the cache grows one token per
+ * step, in fixed blocks of 16 tokens mapped through a block table).  The
+ * newest token of each sequence attends to every cached key of its sequence.
+ * q           : bf16 [B, Hq, d], the token at position L_b - 1 of sequence b.
+ * k_cache,
+ * v_cache     : bf16 [num_blocks, Hkv, 16, d], as for attn_fwd_paged.
+ * block_table : device int32 [B, max_blocks]: cached rows [16 t, 16 t + 16) of
+ *               sequence b are block block_table[b][t]; only the first
+ *               ceil(L_b / 16) entries of a row are read.
+ * seqlens     : device int32 [B]: L_b, the cached tokens of sequence b (the
+ *               query included), 0 <= L_b <= 16 * max_blocks; L_b = 0 gives
+ *               O = 0, LSE = -inf.
+ * o, lse      : bf16 [B, Hq, d] and fp32 [B, Hq] (natural log), written.
+ * mods        : CAUSAL is implied (accepted, no effect); WINDOW keeps keys with
+ *               (L_b - 1) - j < window; SOFTCAP and ALIBI as in attn_fwd with
+ *               query position i = L_b - 1; DOC is ATTN_ERR_UNSUPPORTED.
+ * ws          : attn_workspace_size(ATTN_OP_DECODE_PAGED, B, Hq, Hkv,
+ *               16 * max_blocks, d, mods) bytes: per-chunk partial outputs.
+ * Requirements: d = 128, Hq % Hkv == 0 and Hq / Hkv <= 128 (else
+ * ATTN_ERR_UNSUPPORTED).  Device-side: a length outside [0, 16 * max_blocks]
+ * or a table entry outside [0, num_blocks) is reported as ATTN_ERR_BOUNDS by
+ * attn_status (the call then leaves O and LSE unspecified).
+ * Asynchronous on `stream`; the caller owns every buffer.
+ */
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, int max_blocks, const int32_t* seqlens,
+                                int num_blocks, void* o, float* lse, int B, int Hq, int Hkv, int d,
+                                float scale, const attn_mods_t* mods, void* ws, size_t ws_bytes,
+                                void* stream);
 
 /*
  * Packed variable-length sequences: n_seqs sequences stored back to back along
