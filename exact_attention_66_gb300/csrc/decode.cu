@@ -21,9 +21,12 @@
 //  * the G query heads of a KV head are the rows of one 128-row tcgen05 tile
 //    (rows >= G stay zero): S = Q K^T and O += P V are each one MMA chain
 //    per key tile, and every K and V row is read once for all G heads;
-//  * a key tile arrives as eight 16-row TMA boxes (one per cache block) in a
-//    4-slot ring, in the order K(t0), K(t1), V(t0), K(t2), V(t1), ... so that
-//    S of the next tile is computed while the softmax of this one runs;
+//  * a key tile arrives as sixteen 2 KB TMA boxes (one per cache block and
+//    64-column half), issued by 16 lanes of a producer warp at once: one warp
+//    streams K tiles and another V tiles, each through its own 2-slot ring,
+//    so that the one-box-per-instruction issue rate of a single thread does
+//    not limit the stream; S of the next tile is computed while the softmax
+//    of this one runs;
 //  * each item leaves O / l (fp32) and its log2-sum-exp in a workspace, and
 //    a second kernel merges the chunks of every (sequence, head) by their
 //    LSE.
@@ -37,18 +40,35 @@ namespace {
 
 constexpr int DEC_D = 128;
 constexpr int DEC_THREADS = 256;
-constexpr int DEC_TB = TILE * DEC_D * 2;  // one bf16 tile of 128 rows (32 KB)
-constexpr int DEC_RST = 4;                // K/V ring slots
-constexpr int DEC_Q_OFF = 0;              // two Q tiles (item parity)
-constexpr int DEC_P_OFF = 2 * DEC_TB;
-constexpr int DEC_R_OFF = 3 * DEC_TB;
-constexpr int DEC_BAR_OFF = DEC_R_OFF + DEC_RST * DEC_TB;
-constexpr int DEC_SMEM = smem_one_cta(DEC_BAR_OFF + 256 + 1024);
-static_assert(DEC_SMEM <= 232448, "decode shared memory exceeds 227 KB");
+constexpr int DEC_TB = TILE * DEC_D * 2;  // one bf16 K or V tile of 128 rows (32 KB)
+
+// Shared-memory layout.  The MMAs read Q and P as 128-row tiles, of which only
+// the G rows of the query heads matter.  With G <= 8 (SMALL) a Q or P tile is
+// a single 8-row swizzle group per 64-column half (1 KB) and the MMA
+// descriptor's stride between 8-row groups is 0, so its other fifteen groups
+// re-read the same eight rows (the S and O rows they produce are never read);
+// the room saved goes to deeper K and V rings, i.e. more bytes in flight.
+template <bool SMALL>
+struct DecCfg {
+  static constexpr int QCH = SMALL ? 1024 : 16384;      // one 64-column half of a Q / P tile
+  static constexpr int QTB = 2 * QCH;                   // one Q / P tile
+  static constexpr uint32_t QSBO = SMALL ? 0u : 1024u;  // MMA stride between 8-row groups
+  static constexpr int KS = SMALL ? 3 : 2, VS = SMALL ? 3 : 2;  // K ring and V ring slots
+  static constexpr int Q_OFF = 0;                       // two Q tiles (item parity)
+  static constexpr int P_OFF = 2 * QTB;
+  static constexpr int K_OFF = 3 * QTB;
+  static constexpr int V_OFF = K_OFF + KS * DEC_TB;
+  static constexpr int BAR_OFF = V_OFF + VS * DEC_TB;
+  static constexpr int SMEM = smem_one_cta(BAR_OFF + 256 + 1024);
+};
+static_assert(DecCfg<true>::SMEM <= 232448 && DecCfg<false>::SMEM <= 232448, "decode shared memory exceeds 227 KB");
+static_assert(DecCfg<true>::K_OFF % 1024 == 0 && DecCfg<false>::K_OFF % 1024 == 0, "swizzled tiles need 1 KB alignment");
+constexpr int DEC_MAX_SLOTS = 3;
 
 struct DecBars {
   uint64_t q_full[2], q_empty[2];        // Q tile of an item (TMA) / its last S done (commit)
-  uint64_t full[DEC_RST], empty[DEC_RST];  // K/V ring
+  uint64_t kfull[DEC_MAX_SLOTS], kempty[DEC_MAX_SLOTS];  // K ring
+  uint64_t vfull[DEC_MAX_SLOTS], vempty[DEC_MAX_SLOTS];  // V ring
   uint64_t s_full[2], s_free[2];         // S buffers
   uint64_t p_full, o_full, o_free;       // P written, P V done, O read by the epilogue
   uint64_t drain;
@@ -71,34 +91,61 @@ __device__ __forceinline__ void seq_chunks(const DecodeParams& p, int b, int& L,
 }
 
 // One CTA: per-sequence chunk counts and the exclusive prefix of the items
-// (chunks x KV heads) over the sequences.
+// (chunks x KV heads) over the sequences.  Thread t owns sequences
+// [t * per, (t + 1) * per); the scan runs on warp shuffles.
+constexpr int DEC_SETUP_PER = 8;  // sequences a thread keeps in registers
 __global__ void __launch_bounds__(1024) decode_setup_kernel(const DecodeParams p) {
-  __shared__ int part[1024];
-  const int t = threadIdx.x;
+  __shared__ int warp_sum[32];
+  pdl_launch_dependents();  // the main kernel's prologue needs nothing from here
+  const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
   const int per = (p.B + 1023) / 1024;
   const int b0 = min(p.B, t * per), b1 = min(p.B, b0 + per);
+  int L[DEC_SETUP_PER], J0[DEC_SETUP_PER], n[DEC_SETUP_PER];
   int sum = 0;
-  for (int b = b0; b < b1; ++b) {
-    int L, J0, n;
-    seq_chunks(p, b, L, J0, n);
-    sum += n * p.Hkv;
+  for (int base = b0; base < b1; base += DEC_SETUP_PER) {  // one pass when per <= DEC_SETUP_PER
+    const int m = min(DEC_SETUP_PER, b1 - base);
+#pragma unroll
+    for (int k = 0; k < DEC_SETUP_PER; ++k)
+      if (k < m) seq_chunks(p, base + k, L[k], J0[k], n[k]);
+#pragma unroll
+    for (int k = 0; k < DEC_SETUP_PER; ++k)
+      if (k < m) sum += n[k] * p.Hkv;
   }
-  part[t] = sum;
+  int incl = sum;  // inclusive scan over the block
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) warp_sum[wid] = incl;
   __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {  // inclusive scan
-    const int v = t >= off ? part[t - off] : 0;
-    __syncthreads();
-    part[t] += v;
-    __syncthreads();
+  if (wid == 0) {
+    int w = warp_sum[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += v;
+    }
+    warp_sum[lane] = w;
   }
-  int run = t > 0 ? part[t - 1] : 0;
-  for (int b = b0; b < b1; ++b) {
-    int L, J0, n;
-    seq_chunks(p, b, L, J0, n);
-    p.seq_info[b] = make_int4(L, J0, n, run);
-    run += n * p.Hkv;
+  __syncthreads();
+  int run = incl - sum + (wid > 0 ? warp_sum[wid - 1] : 0);
+  for (int base = b0; base < b1; base += DEC_SETUP_PER) {
+    const int m = min(DEC_SETUP_PER, b1 - base);
+    if (per > DEC_SETUP_PER) {  // more than fit in registers: recompute this group
+#pragma unroll
+      for (int k = 0; k < DEC_SETUP_PER; ++k)
+        if (k < m) seq_chunks(p, base + k, L[k], J0[k], n[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < DEC_SETUP_PER; ++k) {
+      if (k < m) {
+        p.seq_info[base + k] = make_int4(L[k], J0[k], n[k], run);
+        run += n[k] * p.Hkv;
+      }
+    }
   }
-  if (t == 1023) *p.n_items = part[1023];
+  if (t == 1023) *p.n_items = warp_sum[31];
 }
 
 // A key tile of this CTA's work, in the order every role walks it.
@@ -151,47 +198,51 @@ struct DecWalker {
   }
 };
 
-// S(tmem, 128 x 128 fp32) = Q K^T, both K-major 128-byte swizzled bf16 tiles
-// of 256-byte rows (two 16 KB column chunks).
+// S(tmem, 128 x 128 fp32) = Q K^T: Q and K K-major 128-byte swizzled bf16
+// tiles of 256-byte rows, K as two 16 KB column halves, Q in the layout of C.
+template <typename C>
 __device__ __forceinline__ void dec_issue_s(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
   constexpr uint32_t id = idesc_bf16(128, 128, false, false);
-  const uint64_t ad = opaque(sdesc_sw128(q_smem, 16, 1024)), bd = opaque(sdesc_sw128(k_smem, 16, 1024));
+  const uint64_t ad = opaque(sdesc_sw128(q_smem, 16, C::QSBO)), bd = opaque(sdesc_sw128(k_smem, 16, 1024));
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-    mma_f16_ss(d_tmem, sdesc_add(ad, off), sdesc_add(bd, off), id, kk > 0 ? 1u : 0u);
+    const uint32_t step = (kk % 4) * 32;
+    mma_f16_ss(d_tmem, sdesc_add(ad, (kk / 4) * C::QCH + step), sdesc_add(bd, (kk / 4) * 16384 + step), id,
+               kk > 0 ? 1u : 0u);
   }
 }
 
-// O(tmem) (+)= P V: P K-major (128 keys), V MN-major (128 keys x 128).
+// O(tmem) (+)= P V: P K-major (128 keys, layout of C), V MN-major (128 keys x 128).
+template <typename C>
 __device__ __forceinline__ void dec_issue_pv(uint32_t o_tmem, uint32_t p_smem, uint32_t v_smem, bool first) {
   constexpr uint32_t id = idesc_bf16(128, 128, false, true);
-  const uint64_t pd = opaque(sdesc_sw128(p_smem, 16, 1024)), vd = opaque(sdesc_sw128(v_smem, 16384, 1024));
+  const uint64_t pd = opaque(sdesc_sw128(p_smem, 16, C::QSBO)), vd = opaque(sdesc_sw128(v_smem, 16384, 1024));
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t poff = (kk / 4) * 16384 + (kk % 4) * 32;
+    const uint32_t poff = (kk / 4) * C::QCH + (kk % 4) * 32;
     mma_f16_ss(o_tmem, sdesc_add(pd, poff), sdesc_add(vd, kk * 16 * 128), id, (first && kk == 0) ? 0u : 1u);
   }
 }
 
 // MODS: soft-cap / ALiBi compiled in (the window is a column interval and
-// runs in both variants).
-template <bool MODS>
+// runs in both variants); SMALL: at most 8 query heads per KV head.
+template <bool MODS, bool SMALL>
 __global__ void __launch_bounds__(DEC_THREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const DecodeParams p) {
+  using C = DecCfg<SMALL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  DecBars& S = *reinterpret_cast<DecBars*>(smem + DEC_BAR_OFF);
+  DecBars& S = *reinterpret_cast<DecBars*>(smem + C::BAR_OFF);
   const Abort ab{&S.abort, p.status};
   const int warp = warp_id(), lane = lane_id();
   const int G = p.G;
   const int nsw = (G + 31) / 32;  // softmax warps (4 .. 3 + nsw): one thread per query head
 
   // Rows >= G of the Q tiles never receive data: zero them (and P) once.
-  for (int g = threadIdx.x; g < 3 * DEC_TB / 16; g += DEC_THREADS) {
-    const int row = ((g * 16) % 16384) / 128;
-    if (g * 16 >= 2 * DEC_TB || row >= G)
+  for (int g = threadIdx.x; g < 3 * C::QTB / 16; g += DEC_THREADS) {
+    const int row = ((g * 16) % C::QCH) / 128;
+    if (g * 16 >= 2 * C::QTB || row >= G)
       *reinterpret_cast<uint4*>(smem + g * 16) = make_uint4(0u, 0u, 0u, 0u);
   }
   fence_async_smem();
@@ -203,9 +254,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       mbar_init(&S.s_full[i], 1);
       mbar_init(&S.s_free[i], 32 * nsw);
     }
-    for (int s = 0; s < DEC_RST; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 1);
+    for (int s = 0; s < C::KS; ++s) {
+      mbar_init(&S.kfull[s], 1);
+      mbar_init(&S.kempty[s], 1);
+    }
+    for (int s = 0; s < C::VS; ++s) {
+      mbar_init(&S.vfull[s], 1);
+      mbar_init(&S.vempty[s], 1);
     }
     mbar_init(&S.p_full, 32 * nsw);
     mbar_init(&S.o_full, 1);
@@ -217,89 +272,112 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     tmem_alloc(&S.tmem_base, 512);
     tmem_relinquish();
   }
+  // The item table comes from the set-up kernel, which may still be running.
+  pdl_wait();
+  pdl_launch_dependents();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;  // S0 @0, S1 @128, O @256
-  const uint32_t sQ = smem_u32(smem + DEC_Q_OFF), sP = smem_u32(smem + DEC_P_OFF);
-  const uint32_t sR = smem_u32(smem + DEC_R_OFF);
+  const uint32_t sQ = smem_u32(smem + C::Q_OFF), sP = smem_u32(smem + C::P_OFF);
+  const uint32_t sK = smem_u32(smem + C::K_OFF), sV = smem_u32(smem + C::V_OFF);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 3) {
+    // ----------------------------------------------------------- TMA producers
+    // Warp 0 streams Q (once per item) and the K tiles, warp 3 the V tiles.
+    const bool is_k = warp == 0;
     if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      DecWalker w;
-      w.init(p);
-      int r = 0, nq = 0;  // ring loads, Q loads
-      auto load_q = [&](const DecTile& t) -> bool {
+      tma_prefetch_desc(is_k ? &tk : &tv);
+      if (is_k) tma_prefetch_desc(&tq);
+    }
+    uint64_t* full = is_k ? S.kfull : S.vfull;
+    uint64_t* empty = is_k ? S.kempty : S.vempty;
+    const int slots = is_k ? C::KS : C::VS;
+    uint8_t* ring = smem + (is_k ? C::K_OFF : C::V_OFF);
+    const CUtensorMap* map = is_k ? &tk : &tv;
+    DecWalker w;
+    w.init(p);
+    int r = 0, nq = 0;  // tiles loaded, Q loads
+    bool ok = true;
+    // Lane l < 16 copies box (cache block l / 2, column half l % 2) of a tile.
+    // Blocks wholly past the sequence end take an out-of-range index (TMA
+    // fills zeros); table entries outside [0, kv_blocks) are an error.  The
+    // entries of the next tile are fetched while this one waits for its slot.
+    auto lookup = [&](const DecTile& t, int& z, bool& bad) {
+      z = p.kv_blocks * p.Hkv;
+      bad = false;
+      if (lane < 16) {
+        const int lb = t.J * (TILE / 16) + (lane >> 1);
+        if (lb * 16 < t.L) {
+          const int e = __ldg(p.block_table + (size_t)t.b * p.bt_stride + lb);
+          bad = e < 0 || e >= p.kv_blocks;
+          z = e * p.Hkv + t.hk;
+        }
+      }
+    };
+    DecTile t, tn;
+    int z = 0;
+    bool bad = false;
+    bool have = w.next(p, t);
+    if (have) lookup(t, z, bad);
+    while (ok && have) {
+      if (is_k && t.first) {
         const int qb = t.item & 1;
-        if (t.item >= 2 && !mbar_wait(&S.q_empty[qb], ((t.item >> 1) - 1) & 1, ab)) return false;
-        mbar_arrive_tx(&S.q_full[qb], 2 * G * 128);
-        for (int ch = 0; ch < 2; ++ch)
-          tma_load_3d(smem + DEC_Q_OFF + qb * DEC_TB + ch * 16384, &tq, &S.q_full[qb], ch * 64, 0,
-                      t.b * p.Hkv + t.hk);
-        ++nq;
-        return true;
-      };
-      auto load_kv = [&](const CUtensorMap* map, const DecTile& t) -> bool {
-        // The tile's 8 cache blocks; blocks wholly past the sequence end take an
-        // out-of-range index (TMA fills zeros), table entries outside
-        // [0, kv_blocks) are an error.
-        int z[TILE / 16];
-#pragma unroll
-        for (int sb = 0; sb < TILE / 16; ++sb) {
-          const int lb = t.J * (TILE / 16) + sb;
-          z[sb] = p.kv_blocks * p.Hkv;
-          if (lb * 16 < t.L) {
-            const int e = __ldg(p.block_table + (size_t)t.b * p.bt_stride + lb);
-            if (e < 0 || e >= p.kv_blocks) {
-              raise_error(ab, DEV_ERR_BOUNDS);
-              return false;
-            }
-            z[sb] = e * p.Hkv + t.hk;
+        if (lane == 0) {
+          ok = t.item < 2 || mbar_wait(&S.q_empty[qb], ((t.item >> 1) - 1) & 1, ab);
+          if (ok) {
+            mbar_arrive_tx(&S.q_full[qb], 2 * G * 128);
+            for (int ch = 0; ch < 2; ++ch)
+              tma_load_3d(smem + C::Q_OFF + qb * C::QTB + ch * C::QCH, &tq, &S.q_full[qb], ch * 64, 0,
+                          t.b * p.Hkv + t.hk);
           }
         }
-        const int st = r % DEC_RST;
-        if (!mbar_wait(&S.empty[st], ((r / DEC_RST) & 1) ^ 1, ab)) return false;
-        mbar_arrive_tx(&S.full[st], DEC_TB);
-        uint8_t* dst = smem + DEC_R_OFF + st * DEC_TB;
-#pragma unroll
-        for (int sb = 0; sb < TILE / 16; ++sb)
-#pragma unroll
-          for (int ch = 0; ch < 2; ++ch)
-            tma_load_3d(dst + ch * 16384 + sb * 2048, map, &S.full[st], ch * 64, 0, z[sb]);
-        ++r;
-        return true;
-      };
-      DecTile cur, nxt;
-      bool have = w.next(p, cur);
-      bool ok = !have || (load_q(cur) && load_kv(&tk, cur));
-      while (ok && have) {
-        const bool hn = w.next(p, nxt);
-        if (hn && nxt.first && !(ok = load_q(nxt))) break;
-        if (hn && !(ok = load_kv(&tk, nxt))) break;
-        if (!(ok = load_kv(&tv, cur))) break;
-        cur = nxt;
-        have = hn;
+        if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+        ++nq;
       }
-      // Every copy issued lands before the CTA can exit.
+      const int st = r % slots;
+      if (lane == 0) ok = mbar_wait(&empty[st], ((r / slots) & 1) ^ 1, ab);
+      if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
+      if (__any_sync(0xffffffffu, bad)) {  // the table entries are needed only now
+        if (lane == 0) raise_error(ab, DEV_ERR_BOUNDS);
+        ok = false;
+        break;
+      }
+      if (lane == 0) mbar_arrive_tx(&full[st], DEC_TB);
+      __syncwarp();
+      if (lane < 16)
+        tma_load_3d(ring + st * DEC_TB + (lane & 1) * 16384 + (lane >> 1) * 2048, map, &full[st], (lane & 1) * 64, 0, z);
+      ++r;
+      have = w.next(p, tn);
+      if (have) {
+        t = tn;
+        lookup(t, z, bad);
+      }
+    }
+    // Every copy issued lands before the CTA can exit.
+    if (lane == 0) {
       for (int qb = 0; qb < 2; ++qb)
         if (nq > qb) mbar_wait_drain(&S.q_full[qb], ((nq - 1 - qb) >> 1) & 1);
-      for (int s = 0; s < DEC_RST; ++s)
-        if (r > s) mbar_wait_drain(&S.full[s], ((r - 1 - s) / DEC_RST) & 1);
+      for (int s = 0; s < slots; ++s)
+        if (r > s) mbar_wait_drain(&full[s], ((r - 1 - s) / slots) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       DecWalker w;
       w.init(p);
-      int r = 0, ns = 0;  // ring slots consumed, S tiles issued
+      int nk = 0, nv = 0, ns = 0;  // K and V tiles consumed, S tiles issued
       bool ok = true;
-      auto slot = [&](int& st) -> bool {
-        st = r % DEC_RST;
-        const bool good = mbar_wait(&S.full[st], (r / DEC_RST) & 1, ab);
-        ++r;
+      auto kslot = [&](int& st) -> bool {
+        st = nk % C::KS;
+        const bool good = mbar_wait(&S.kfull[st], (nk / C::KS) & 1, ab);
+        ++nk;
+        tc_fence_after();
+        return good;
+      };
+      auto vslot = [&](int& st) -> bool {
+        st = nv % C::VS;
+        const bool good = mbar_wait(&S.vfull[st], (nv / C::VS) & 1, ab);
+        ++nv;
         tc_fence_after();
         return good;
       };
@@ -308,9 +386,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         if (t.first && !mbar_wait(&S.q_full[qb], (t.item >> 1) & 1, ab)) return false;
         if (ns >= 2 && !mbar_wait(&S.s_free[ns & 1], ((ns >> 1) - 1) & 1, ab)) return false;
         tc_fence_after();
-        dec_issue_s(tmem + (uint32_t)(ns & 1) * 128, sQ + qb * DEC_TB, sR + ks * DEC_TB);
+        dec_issue_s<C>(tmem + (uint32_t)(ns & 1) * 128, sQ + qb * C::QTB, sK + ks * DEC_TB);
         mma_commit(&S.s_full[ns & 1]);
-        mma_commit(&S.empty[ks]);
+        mma_commit(&S.kempty[ks]);
         if (t.last) mma_commit(&S.q_empty[qb]);
         ++ns;
         return true;
@@ -318,19 +396,19 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       DecTile cur, nxt;
       bool have = w.next(p, cur);
       int ks = 0, vs = 0, npv = 0;
-      if (have) ok = slot(ks) && issue_s(cur, ks);
+      if (have) ok = kslot(ks) && issue_s(cur, ks);
       while (ok && have) {
         const bool hn = w.next(p, nxt);
-        if (hn && !(ok = slot(ks) && issue_s(nxt, ks))) break;
-        if (!(ok = slot(vs))) break;
+        if (hn && !(ok = kslot(ks) && issue_s(nxt, ks))) break;
+        if (!(ok = vslot(vs))) break;
         if (!(ok = mbar_wait(&S.p_full, npv & 1, ab))) break;
         // The first P V of an item overwrites O: the epilogue of the previous
         // item must have read it.
         if (cur.first && cur.item >= 1 && !(ok = mbar_wait(&S.o_free, (cur.item - 1) & 1, ab))) break;
         tc_fence_after();
-        dec_issue_pv(tmem + 256, sP, sR + vs * DEC_TB, cur.first);
+        dec_issue_pv<C>(tmem + 256, sP, sV + vs * DEC_TB, cur.first);
         mma_commit(&S.o_full);
-        mma_commit(&S.empty[vs]);
+        mma_commit(&S.vempty[vs]);
         ++npv;
         cur = nxt;
         have = hn;
@@ -346,7 +424,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const bool active = r < G;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tO = tmem + lane_off + 256;
-    uint8_t* p_tile = smem + DEC_P_OFF;
+    uint8_t* p_tile = smem + C::P_OFF;
     const bool win = (p.flags & MOD_WINDOW) != 0;
     const bool sc = MODS && (p.flags & MOD_SOFTCAP);
     const bool al = MODS && (p.flags & MOD_ALIBI);
@@ -454,7 +532,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       if (active) {  // P row r into the 128-byte swizzled K-major tile
 #pragma unroll
         for (int g = 0; g < 16; ++g) {
-          const uint32_t addr = (uint32_t)((g >> 3) * 16384 + r * 128 + (((g & 7) ^ (r & 7)) << 4));
+          const uint32_t addr = (uint32_t)((g >> 3) * C::QCH + r * 128 + (((g & 7) ^ (r & 7)) << 4));
           *reinterpret_cast<uint4*>(p_tile + addr) = make_uint4(s[4 * g], s[4 * g + 1], s[4 * g + 2], s[4 * g + 3]);
         }
       }
@@ -498,8 +576,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
 }
 
 // One warp per (sequence, query head): merge the chunks' O / l by their LSE.
+// Lane c holds the log2-sum-exp and weight of chunk c; every lane
+// accumulates four output columns over the chunks, DEC_MERGE chunks' loads in
+// flight at a time (one round for the usual chunk counts).
+constexpr int DEC_MERGE = 16;
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p, __nv_bfloat16* __restrict__ o,
                                                              float* __restrict__ lse) {
+  pdl_wait();  // the partial results come from the main kernel
   const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= p.B * p.Hq) return;
@@ -514,15 +597,24 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   float W = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
-    for (int c = 0; c < n; ++c) {
-      const float wc = exp2f(lp[c] - M);
-      const float4 v = op[(size_t)c * (DEC_D / 4) + lane];
-      W += wc;
-      acc.x += wc * v.x;
-      acc.y += wc * v.y;
-      acc.z += wc * v.z;
-      acc.w += wc * v.w;
+    for (int c0 = 0; c0 < n; c0 += DEC_MERGE) {
+      const float wl = (lane < DEC_MERGE && c0 + lane < n) ? exp2f(lp[c0 + lane] - M) : 0.f;
+      W += wl;
+      float4 v[DEC_MERGE];
+#pragma unroll
+      for (int u = 0; u < DEC_MERGE; ++u)
+        v[u] = c0 + u < n ? op[(size_t)(c0 + u) * (DEC_D / 4) + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < DEC_MERGE; ++u) {
+        const float wc = __shfl_sync(0xffffffffu, wl, u);
+        acc.x += wc * v[u].x;
+        acc.y += wc * v[u].y;
+        acc.z += wc * v[u].z;
+        acc.w += wc * v[u].w;
+      }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
   }
   const float inv = W > 0.f ? 1.0f / W : 0.f;
   uint2 pk;
@@ -534,18 +626,39 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
 
 }  // namespace
 
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous one in the stream finishes (it calls pdl_wait() before reading
+// that kernel's results).
+template <typename... Args>
+static cudaError_t launch_pdl(void (*kern)(Args...), unsigned grid, unsigned threads, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_decode(const DecodeLaunch& L, bool mods, cudaStream_t st) {
   decode_setup_kernel<<<1, 1024, 0, st>>>(L.p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kern = mods ? decode_kernel<true> : decode_kernel<false>;
-  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM)) != cudaSuccess)
+  const bool small = L.p.G <= 8;
+  auto kern = mods ? (small ? decode_kernel<true, true> : decode_kernel<true, false>)
+                   : (small ? decode_kernel<false, true> : decode_kernel<false, false>);
+  const int smem = small ? DecCfg<true>::SMEM : DecCfg<false>::SMEM;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
+  if ((e = launch_pdl(kern, (unsigned)L.grid, DEC_THREADS, (size_t)smem, st, L.tq, L.tk, L.tv, L.p)) != cudaSuccess)
     return e;
-  kern<<<(unsigned)L.grid, DEC_THREADS, DEC_SMEM, st>>>(L.tq, L.tk, L.tv, L.p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long warps = (long long)L.p.B * L.p.Hq;
-  decode_combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(L.p, (__nv_bfloat16*)L.o, L.lse);
-  return cudaGetLastError();
+  return launch_pdl(decode_combine_kernel, (unsigned)((warps + 7) / 8), 256u, 0, st, L.p, (__nv_bfloat16*)L.o,
+                    L.lse);
 }
 
 }  // namespace attn
