@@ -616,6 +616,8 @@ def run_decode(args, world, rank, local):
 
     name = args.workload
     cfg = dict(gen.WORKLOADS[name])
+    if args.batch:  # smaller case of the same workload (profiling)
+        cfg["B"] = args.batch
     B, Hq, Hkv, N, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"]
     scale = 1.0 / math.sqrt(d)
     dev = torch.device("cuda", local)
@@ -840,6 +842,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host copies) leg")
     ap.add_argument("--workload", choices=sorted(gen.WORKLOADS), default=WORKLOAD,
                     help="workload to time; the default is the one the metric is quoted on")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="paged_decode_8k only: this many sequences instead of the workload's (profiling)")
     ap.add_argument("--heads", type=int, default=0,
                     help="query heads (8 per KV head) for a smaller profiling case; default: the workload's 64")
     args = ap.parse_args()

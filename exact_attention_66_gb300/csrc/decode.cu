@@ -70,7 +70,8 @@ struct DecBars {
   uint64_t kfull[DEC_MAX_SLOTS], kempty[DEC_MAX_SLOTS];  // K ring
   uint64_t vfull[DEC_MAX_SLOTS], vempty[DEC_MAX_SLOTS];  // V ring
   uint64_t s_full[2], s_free[2];         // S buffers
-  uint64_t p_full, o_full, o_free;       // P written, P V done, O read by the epilogue
+  uint64_t p_full, o_full;               // P written, P V done
+  uint64_t o_free[2];                    // O buffer read by its item's epilogue
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -264,7 +265,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     }
     mbar_init(&S.p_full, 32 * nsw);
     mbar_init(&S.o_full, 1);
-    mbar_init(&S.o_free, 32 * nsw);
+    mbar_init(&S.o_free[0], 32 * nsw);
+    mbar_init(&S.o_free[1], 32 * nsw);
     mbar_init(&S.drain, 1);
     fence_mbar_init();
   }
@@ -277,7 +279,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   pdl_launch_dependents();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = S.tmem_base;  // S0 @0, S1 @128, O @256
+  const uint32_t tmem = S.tmem_base;  // S0 @0, S1 @128, O0 @256, O1 @384 (by item parity)
   const uint32_t sQ = smem_u32(smem + C::Q_OFF), sP = smem_u32(smem + C::P_OFF);
   const uint32_t sK = smem_u32(smem + C::K_OFF), sV = smem_u32(smem + C::V_OFF);
 
@@ -402,11 +404,14 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         if (hn && !(ok = kslot(ks) && issue_s(nxt, ks))) break;
         if (!(ok = vslot(vs))) break;
         if (!(ok = mbar_wait(&S.p_full, npv & 1, ab))) break;
-        // The first P V of an item overwrites O: the epilogue of the previous
-        // item must have read it.
-        if (cur.first && cur.item >= 1 && !(ok = mbar_wait(&S.o_free, (cur.item - 1) & 1, ab))) break;
+        // The first P V of an item overwrites its O buffer: the epilogue of
+        // the item two before, which used the same buffer, must have read it
+        // (one barrier per buffer, so a later epilogue cannot alias its phase).
+        if (cur.first && cur.item >= 2 &&
+            !(ok = mbar_wait(&S.o_free[cur.item & 1], ((cur.item >> 1) - 1) & 1, ab)))
+          break;
         tc_fence_after();
-        dec_issue_pv<C>(tmem + 256, sP, sV + vs * DEC_TB, cur.first);
+        dec_issue_pv<C>(tmem + 256 + (uint32_t)(cur.item & 1) * 128, sP, sV + vs * DEC_TB, cur.first);
         mma_commit(&S.o_full);
         mma_commit(&S.vempty[vs]);
         ++npv;
@@ -423,13 +428,42 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const int r = wq * 32 + lane;  // query head r of the group (TMEM lane r)
     const bool active = r < G;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const uint32_t tO = tmem + lane_off + 256;
+    const uint32_t tO0 = tmem + lane_off + 256;  // + 128 for odd items
     uint8_t* p_tile = smem + C::P_OFF;
     const bool win = (p.flags & MOD_WINDOW) != 0;
     const bool sc = MODS && (p.flags & MOD_SOFTCAP);
     const bool al = MODS && (p.flags & MOD_ALIBI);
     const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
     const uint64_t sc_in2 = f2_pack(p.sc_in, p.sc_in), sc_out2 = f2_pack(p.sc_out, p.sc_out);
+    // An item's output is written once the next tile's P is out (or at the
+    // end), so the softmax never waits for the item's last P V by itself.
+    struct Pending {
+      bool on;
+      int buf;      // O buffer (item parity)
+      size_t prow;  // row of the partial buffers: (b * Hq + hq) * max_chunks + chunk
+      float m, l;   // running max (log2 units) and sum
+    };
+    Pending pend{false, 0, 0u, 0.f, 0.f};
+    auto epilogue = [&](const Pending& e) {
+      const float inv = e.l > 0.f ? 1.0f / e.l : 0.f;
+      float4* dst = reinterpret_cast<float4*>(p.o_part + e.prow * DEC_D);
+      const uint32_t tO = tO0 + (uint32_t)e.buf * 128;
+#pragma unroll
+      for (int q4 = 0; q4 < DEC_D / 32; ++q4) {
+        uint32_t ov[32];
+        tmem_ld32(tO + q4 * 32, ov);
+        tmem_wait_ld(ov);
+        if (active) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            dst[q4 * 8 + c] = make_float4(__uint_as_float(ov[4 * c]) * inv, __uint_as_float(ov[4 * c + 1]) * inv,
+                                          __uint_as_float(ov[4 * c + 2]) * inv, __uint_as_float(ov[4 * c + 3]) * inv);
+        }
+      }
+      if (active) p.lse_part[e.prow] = e.l > 0.f ? e.m + log2f(e.l) : -INFINITY;
+      tc_fence_before();
+      mbar_arrive(&S.o_free[e.buf]);
+    };
     DecWalker w;
     w.init(p);
     DecTile t;
@@ -517,6 +551,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         if (!(ok = wait_warp(&S.o_full, (n - 1) & 1, ab))) break;
         tc_fence_after();
         if (!t.first && __any_sync(0xffffffffu, need)) {
+          const uint32_t tO = tO0 + (uint32_t)(t.item & 1) * 128;
 #pragma unroll
           for (int q4 = 0; q4 < DEC_D / 32; ++q4) {
             uint32_t ov[32];
@@ -540,30 +575,18 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       tc_fence_before();
       mbar_arrive(&S.p_full);
 
-      if (t.last) {
-        // ------------------------------------------------------ item epilogue
-        if (!(ok = wait_warp(&S.o_full, n & 1, ab))) break;
-        tc_fence_after();
-        const float inv = l > 0.f ? 1.0f / l : 0.f;
-        const size_t prow = ((size_t)t.b * p.Hq + hq) * p.max_chunks + t.c;
-        float4* dst = reinterpret_cast<float4*>(p.o_part + prow * DEC_D);
-#pragma unroll
-        for (int q4 = 0; q4 < DEC_D / 32; ++q4) {
-          uint32_t ov[32];
-          tmem_ld32(tO + q4 * 32, ov);
-          tmem_wait_ld(ov);
-          if (active) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              dst[q4 * 8 + c] = make_float4(__uint_as_float(ov[4 * c]) * inv, __uint_as_float(ov[4 * c + 1]) * inv,
-                                            __uint_as_float(ov[4 * c + 2]) * inv, __uint_as_float(ov[4 * c + 3]) * inv);
-          }
-        }
-        if (active) p.lse_part[prow] = l > 0.f ? m + log2f(l) : -INFINITY;
-        tc_fence_before();
-        mbar_arrive(&S.o_free);
+      // The finished item before this one: its last P V completed before P
+      // was overwritten above, and its O buffer is not the one in use.
+      if (pend.on) {
+        epilogue(pend);
+        pend.on = false;
       }
+      if (t.last) pend = Pending{true, t.item & 1, ((size_t)t.b * p.Hq + hq) * p.max_chunks + t.c, m, l};
       ++n;
+    }
+    if (ok && pend.on && (ok = wait_warp(&S.o_full, (n - 1) & 1, ab))) {
+      tc_fence_after();
+      epilogue(pend);
     }
   }
 
