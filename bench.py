@@ -687,7 +687,8 @@ def run_decode(args, world, rank, local):
         "algorithmic_bytes_per_step": nbytes,
         "roofline": {"kernel": "decode_paged (setup, main and merge launches together)", "bound": "hbm",
                      "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
-                     "traffic": None, "peak_source": f"{src} hbm_gbs"},
+                     "traffic": traffic_record("decode_paged") if not args.batch else None,
+                     "peak_source": f"{src} hbm_gbs"},
         "e2e": {"value": round(world * nbytes / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": q.numel() * 2, "d2h_bytes_per_step": bytes_io - q.numel() * 2,
                 "ms_per_step": round(ms_e2e, 4)},
