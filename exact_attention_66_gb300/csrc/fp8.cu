@@ -9,18 +9,23 @@
 // Sylvester Hadamard matrix and s the +-1 vector of the row's KV head, so
 // (q M)(k M)^T = q k^T exactly in real arithmetic; V is not rotated.
 //
-// Two bandwidth-bound passes over Q, K, V (one warp per 128-element row, each
-// lane holding four consecutive elements; butterflies of distance 1 and 2 in
-// registers, 4..64 through warp shuffles): pass 1 finds the amax of every
+// Two bandwidth-bound passes over Q, K, V: pass 1 finds the amax of every
 // (batch, head) of the rotated tensors (integer atomic max of the non-negative
 // float bits, so the result does not depend on the order), pass 2 recomputes
-// the rotation and writes e4m3 codes scaled by 448 / amax.
+// the rotation and writes e4m3 codes scaled by 448 / amax.  Layout: eight
+// lanes per 128-element row, lane l8 holding elements 16 l8 .. 16 l8 + 15, so
+// a warp works on four rows at once; it walks groups of 16 consecutive rows
+// and loads the next group before transforming the current one.  The
+// butterflies of distance 1..8 stay in registers (two lanes of fp32 per
+// instruction from distance 2 on), 16..64 go through three warp shuffles; the
+// signs are applied to the bf16 bits while converting, and 1 / sqrt(128)
+// is folded into the amax and the quantisation multiplier.
 //
 // Optionally RoPE is fused in front of the rotation (the digest's "fused with
 // RoPE at no extra cost"): the row at position n of its head has its element
 // pairs (c, c + 64) turned by n * base^(-2c/128) before the signs and the
-// Hadamard butterflies, in the same registers -- lane l pairs with lane
-// l ^ 16 -- so RoPE costs no extra pass over memory.
+// Hadamard butterflies, in the same registers -- lane l8 pairs with lane
+// l8 ^ 4 -- so RoPE costs no extra pass over memory.
 #include "common.cuh"
 #include "launch.h"
 
@@ -33,12 +38,14 @@ struct QuantTensors {
   int heads[3];               // H of each tensor
   unsigned* amax[3];          // [B * H] float bits (workspace)
   float* scale[3];            // [B * H] dequantisation scales (output)
-  const int8_t* signs;        // [Hkv, 128] or nullptr
+  const int8_t* signs;        // [Hkv, 128] or nullptr (no rotation)
   float rope_k;               // RoPE: inv_freq(c) = exp2(-c * rope_k), rope_k = 2 log2(base) / 128; 0 = off
   int N, Hkv, G;              // G = Hq / Hkv
 };
 
 constexpr int ROWS_PER_WARP = 16;
+constexpr int SLABS = ROWS_PER_WARP / 4;       // four rows per warp instruction
+constexpr float HAD_NORM = 0.08838834764831845f;  // 1 / sqrt(128)
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -46,87 +53,212 @@ __device__ __forceinline__ float warp_max(float x) {
   return x;
 }
 
-// Rotated (or plain) row values of this lane: elements 4 * lane .. 4 * lane + 3.
-__device__ __forceinline__ void load_row(const QuantTensors& t, int ti, long long row, float (&v)[4]) {
-  const uint2 raw = __ldg(reinterpret_cast<const uint2*>(t.x[ti] + row * 128) + lane_id());
-  v[0] = bf16lo_f32(raw.x);
-  v[1] = bf16hi_f32(raw.x);
-  v[2] = bf16lo_f32(raw.y);
-  v[3] = bf16hi_f32(raw.y);
-  if (ti == 2) return;
-  if (t.rope_k != 0.f) {  // RoPE on Q and K rows, rotate-half pairs (c, c + 64)
-    const int lane = lane_id();
-    const float pos = (float)(row % t.N);
-    const bool first = lane < 16;  // elements 4 lane .. 4 lane + 3 < 64
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float partner = __shfl_xor_sync(0xffffffffu, v[r], 16);
-      const int c = (4 * lane + r) & 63;
-      float sn, cs;
-      sincosf(pos * exp2f(-(float)c * t.rope_k), &sn, &cs);
-      v[r] = first ? fmaf(v[r], cs, -partner * sn) : fmaf(v[r], cs, partner * sn);
-    }
-  }
-  if (t.signs == nullptr) return;
-  const int head = (int)((row / t.N) % t.heads[ti]);
-  const int hk = ti == 0 ? head / t.G : head;
-  const char4 sg = __ldg(reinterpret_cast<const char4*>(t.signs + hk * 128) + lane_id());
-  v[0] *= (float)sg.x;
-  v[1] *= (float)sg.y;
-  v[2] *= (float)sg.z;
-  v[3] *= (float)sg.w;
-  // Walsh-Hadamard butterflies: (a, b) -> (a + b, a - b) for index pairs j, j ^ h.
-  float a = v[0], b = v[1];
-  v[0] = a + b;
-  v[1] = a - b;
-  a = v[2];
-  b = v[3];
-  v[2] = a + b;
-  v[3] = a - b;
-  a = v[0];
-  b = v[2];
-  v[0] = a + b;
-  v[2] = a - b;
-  a = v[1];
-  b = v[3];
-  v[1] = a + b;
-  v[3] = a - b;
-  const int lane = lane_id();
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float other = __shfl_xor_sync(0xffffffffu, v[r], m);
-      v[r] = (lane & m) ? (other - v[r]) : (v[r] + other);
-    }
-  }
-  const float norm = 0.08838834764831845f;  // 1 / sqrt(128)
-#pragma unroll
-  for (int r = 0; r < 4; ++r) v[r] *= norm;
+// This lane's 16 bf16 elements of a row.
+struct Raw16 {
+  uint4 a, b;
+};
+__device__ __forceinline__ Raw16 load16(const QuantTensors& t, int ti, long long row, int l8) {
+  const uint4* p = reinterpret_cast<const uint4*>(t.x[ti] + row * 128 + 16 * l8);
+  return Raw16{__ldg(p), __ldg(p + 1)};
 }
 
-__global__ void __launch_bounds__(256) quant_amax_kernel(const QuantTensors t) {
-  const int ti = blockIdx.y;
-  const long long warp_g = (long long)blockIdx.x * 8 + warp_id();
-  const long long r0 = warp_g * ROWS_PER_WARP;
-  if (r0 >= t.rows[ti]) return;
-  const long long r1 = min(r0 + ROWS_PER_WARP, t.rows[ti]);
-  long long cur_bh = r0 / t.N;
-  float mx = 0.f;
-  for (long long row = r0; row < r1; ++row) {
-    const long long bh = row / t.N;
-    if (bh != cur_bh) {  // the warp's rows crossed into the next head: flush
-      const float red = warp_max(mx);
-      if (lane_id() == 0) atomicMax(t.amax[ti] + cur_bh, __float_as_uint(red));
-      cur_bh = bh;
-      mx = 0.f;
+// This lane's 16 values of the row: RoPE (when on), then the signed
+// Walsh-Hadamard transform without its 1 / sqrt(128) (Q and K with signs), or
+// the plain values.  Every lane of the warp must call it (warp shuffles).
+__device__ __forceinline__ void transform16(const QuantTensors& t, int ti, long long row, int l8, const Raw16& raw,
+                                            const float (&inv_freq)[16], float (&v)[16]) {
+  const uint32_t w[8] = {raw.a.x, raw.a.y, raw.a.z, raw.a.w, raw.b.x, raw.b.y, raw.b.z, raw.b.w};
+  if (ti == 2 || (t.rope_k == 0.f && t.signs == nullptr)) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[2 * k] = bf16lo_f32(w[k]);
+      v[2 * k + 1] = bf16hi_f32(w[k]);
     }
-    float v[4];
-    load_row(t, ti, row, v);
-    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+    return;
   }
-  mx = warp_max(mx);
-  if (lane_id() == 0) atomicMax(t.amax[ti] + cur_bh, __float_as_uint(mx));
+  uint32_t sgn[4] = {0u, 0u, 0u, 0u};  // sign bytes of elements 4 j .. 4 j + 3
+  if (t.signs != nullptr) {
+    const int head = (int)((row / t.N) % t.heads[ti]);
+    const int hk = ti == 0 ? head / t.G : head;
+    const uint4 sg = __ldg(reinterpret_cast<const uint4*>(t.signs + hk * 128 + 16 * l8));
+    sgn[0] = sg.x;
+    sgn[1] = sg.y;
+    sgn[2] = sg.z;
+    sgn[3] = sg.w;
+  }
+  if (t.rope_k != 0.f) {  // RoPE first (before the signs), rotate-half pairs (c, c + 64)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[2 * k] = bf16lo_f32(w[k]);
+      v[2 * k + 1] = bf16hi_f32(w[k]);
+    }
+    const float pos = (float)(row % t.N);
+    const bool first = l8 < 4;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float partner = __shfl_xor_sync(0xffffffffu, v[e], 4);
+      // Angle reduced to [-pi, pi] by Cody and Waite's two-constant method:
+      // 2 pi = C1 - C2 with C1 = fl(2 pi) and C2 = 1.7484556e-7 its excess;
+      // both steps are fused multiply-adds, so k C1 enters exactly.  Then the
+      // fast sine / cosine, accurate to a few 1e-7 on that interval.
+      const float ang = pos * inv_freq[e];
+      const float kf = rintf(ang * 0.15915494309189535f);  // 1 / (2 pi)
+      const float red = fmaf(kf, 1.7484556e-07f, fmaf(-kf, 6.28318548f, ang));
+      float sn, cs;
+      __sincosf(red, &sn, &cs);
+      v[e] = first ? fmaf(v[e], cs, -partner * sn) : fmaf(v[e], cs, partner * sn);
+    }
+    if (t.signs == nullptr) return;
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      v[e] = __uint_as_float(__float_as_uint(v[e]) ^ (((sgn[e >> 2] >> (8 * (e & 3) + 7)) & 1u) << 31));
+  } else {  // signs applied to the bf16 bits while converting
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t sb = sgn[k >> 1] >> (16 * (k & 1));  // sign bytes of elements 2 k, 2 k + 1
+      v[2 * k] = __uint_as_float((w[k] << 16) ^ ((sb & 0x80u) << 24));
+      v[2 * k + 1] = __uint_as_float((w[k] & 0xFFFF0000u) ^ ((sb & 0x8000u) << 16));
+    }
+  }
+  // Butterflies (a, b) -> (a + b, a - b) on index pairs (j, j ^ h).  h = 1: scalar.
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float a0 = v[2 * k], b0 = v[2 * k + 1];
+    v[2 * k] = a0 + b0;
+    v[2 * k + 1] = a0 - b0;
+  }
+  uint64_t P[8];  // pairs (v[2 k], v[2 k + 1])
+#pragma unroll
+  for (int k = 0; k < 8; ++k) P[k] = f2_pack(v[2 * k], v[2 * k + 1]);
+  const uint64_t m1 = f2_pack(-1.f, -1.f);
+#pragma unroll
+  for (int hb = 1; hb < 8; hb <<= 1) {  // h = 2, 4, 8: pair index bit hb
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k & hb) continue;
+      const uint64_t a2 = P[k], b2 = P[k | hb];
+      P[k] = f2_add(a2, b2);
+      P[k | hb] = f2_fma(b2, m1, a2);
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) {  // h = 16, 32, 64: lane bit m of l8
+    const float sgn_self = (l8 & m) ? -1.f : 1.f;
+    const uint64_t s2 = f2_pack(sgn_self, sgn_self);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float x0, x1;
+      f2_unpack(P[k], x0, x1);
+      const float o0 = __shfl_xor_sync(0xffffffffu, x0, m), o1 = __shfl_xor_sync(0xffffffffu, x1, m);
+      P[k] = f2_fma(P[k], s2, f2_pack(o0, o1));  // lower index: a + b; upper: a' - b'
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) f2_unpack(P[k], v[2 * k], v[2 * k + 1]);
+}
+
+// RoPE inverse frequencies of this lane's 16 elements (c mod 64 = 16 (l8 & 3) + e).
+__device__ __forceinline__ void rope_freqs(const QuantTensors& t, int l8, float (&f)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) f[e] = t.rope_k != 0.f ? exp2f(-(float)(16 * (l8 & 3) + e) * t.rope_k) : 0.f;
+}
+
+// Scale of the values transform16 returns for tensor ti (1 / sqrt(128) when rotated).
+__device__ __forceinline__ float out_norm(const QuantTensors& t, int ti) {
+  return (ti != 2 && t.signs != nullptr) ? HAD_NORM : 1.0f;
+}
+
+// Work: groups of 16 consecutive rows of Q, then K, then V; a warp walks the
+// groups gi, gi + stride, ... and loads the next group before transforming
+// the current one, so its loads stay in flight for the whole pass.
+struct Group {
+  int ti;
+  long long r0, r1;
+};
+__device__ __forceinline__ bool group_of(const QuantTensors& t, long long gi, Group& g) {
+#pragma unroll
+  for (int ti = 0; ti < 3; ++ti) {
+    const long long n = (t.rows[ti] + ROWS_PER_WARP - 1) / ROWS_PER_WARP;
+    if (gi < n) {
+      g.ti = ti;
+      g.r0 = gi * ROWS_PER_WARP;
+      g.r1 = min(g.r0 + ROWS_PER_WARP, t.rows[ti]);
+      return true;
+    }
+    gi -= n;
+  }
+  return false;
+}
+__device__ __forceinline__ void load_group(const QuantTensors& t, const Group& g, int l8, int q, Raw16 (&raw)[SLABS]) {
+#pragma unroll
+  for (int s = 0; s < SLABS; ++s) {
+    const long long row = g.r0 + 4 * s + q;
+    raw[s] = row < g.r1 ? load16(t, g.ti, row, l8) : Raw16{make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+  }
+}
+
+// Pass 1 (WRITE false): amax of every (batch, head).  Pass 2 (WRITE true):
+// e4m3 codes scaled by 448 / amax.
+template <bool WRITE>
+__global__ void __launch_bounds__(256) quant_pass_kernel(const QuantTensors t) {
+  const int lane = lane_id(), l8 = lane & 7, q = lane >> 3;
+  float inv_freq[16];
+  rope_freqs(t, l8, inv_freq);
+  const long long stride = (long long)gridDim.x * 8;
+  long long gi = (long long)blockIdx.x * 8 + warp_id();
+  Group cur;
+  bool have = group_of(t, gi, cur);
+  Raw16 raw[SLABS];
+  if (have) load_group(t, cur, l8, q, raw);
+  while (have) {
+    Group nxt;
+    const bool hn = group_of(t, gi + stride, nxt);
+    Raw16 rawn[SLABS];
+    if (hn) load_group(t, nxt, l8, q, rawn);
+    const int ti = cur.ti;
+    const float norm = out_norm(t, ti);
+    const bool one_head = cur.r0 / t.N == (cur.r1 - 1) / t.N;
+    float mx = 0.f;
+#pragma unroll
+    for (int s = 0; s < SLABS; ++s) {
+      const long long row_raw = cur.r0 + 4 * s + q;
+      const long long row = min(row_raw, cur.r1 - 1);
+      float v[16];
+      transform16(t, ti, row, l8, raw[s], inv_freq, v);
+      if (WRITE) {
+        if (row_raw >= cur.r1) continue;
+        const float a = __uint_as_float(t.amax[ti][row / t.N]);
+        const float mul = a > 0.f ? (448.0f / a) * norm : 1.0f;
+        uint4 codes;
+        codes.x = pack_e4m3x4(v[0] * mul, v[1] * mul, v[2] * mul, v[3] * mul);
+        codes.y = pack_e4m3x4(v[4] * mul, v[5] * mul, v[6] * mul, v[7] * mul);
+        codes.z = pack_e4m3x4(v[8] * mul, v[9] * mul, v[10] * mul, v[11] * mul);
+        codes.w = pack_e4m3x4(v[12] * mul, v[13] * mul, v[14] * mul, v[15] * mul);
+        reinterpret_cast<uint4*>(t.out[ti] + row * 128)[l8] = codes;
+      } else {
+        float rm = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) rm = fmaxf(rm, fabsf(v[e]));
+        if (row_raw >= cur.r1) rm = 0.f;
+        if (one_head) {
+          mx = fmaxf(mx, rm);
+        } else {  // rows of two heads in this group (short sequences): one atomic per row
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1) rm = fmaxf(rm, __shfl_xor_sync(0xffffffffu, rm, o));
+          if (l8 == 0 && row_raw < cur.r1) atomicMax(t.amax[ti] + row / t.N, __float_as_uint(rm * norm));
+        }
+      }
+    }
+    if (!WRITE && one_head) {
+      mx = warp_max(mx);
+      if (lane == 0) atomicMax(t.amax[ti] + cur.r0 / t.N, __float_as_uint(mx * norm));
+    }
+    cur = nxt;
+#pragma unroll
+    for (int s = 0; s < SLABS; ++s) raw[s] = rawn[s];
+    gi += stride;
+    have = hn;
+  }
 }
 
 __global__ void quant_scale_kernel(const QuantTensors t, int B) {
@@ -135,22 +267,6 @@ __global__ void quant_scale_kernel(const QuantTensors t, int B) {
   for (int i = threadIdx.x + blockIdx.x * blockDim.x; i < n; i += blockDim.x * gridDim.x) {
     const float a = __uint_as_float(t.amax[ti][i]);
     t.scale[ti][i] = a > 0.f ? a / 448.0f : 1.0f;
-  }
-}
-
-__global__ void __launch_bounds__(256) quant_write_kernel(const QuantTensors t) {
-  const int ti = blockIdx.y;
-  const long long warp_g = (long long)blockIdx.x * 8 + warp_id();
-  const long long r0 = warp_g * ROWS_PER_WARP;
-  if (r0 >= t.rows[ti]) return;
-  const long long r1 = min(r0 + ROWS_PER_WARP, t.rows[ti]);
-  for (long long row = r0; row < r1; ++row) {
-    const float a = __uint_as_float(t.amax[ti][row / t.N]);
-    const float inv = a > 0.f ? 448.0f / a : 1.0f;
-    float v[4];
-    load_row(t, ti, row, v);
-    reinterpret_cast<uint32_t*>(t.out[ti] + row * 128)[lane_id()] =
-        pack_e4m3x4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
   }
 }
 
@@ -180,13 +296,18 @@ cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, v
   t.G = Hq / Hkv;
   cudaError_t e = cudaMemsetAsync(amax_ws, 0, sizeof(unsigned) * (size_t)(B * Hq + 2 * B * Hkv), st);
   if (e != cudaSuccess) return e;
-  const long long warps = (t.rows[0] + ROWS_PER_WARP - 1) / ROWS_PER_WARP;
-  const dim3 grid((unsigned)((warps + 7) / 8), 3);
-  quant_amax_kernel<<<grid, 256, 0, st>>>(t);
+  long long groups = 0;
+  for (int i = 0; i < 3; ++i) groups += (t.rows[i] + ROWS_PER_WARP - 1) / ROWS_PER_WARP;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  // Two 8-warp blocks per SM stay resident (register-limited); each warp walks many groups.
+  const long long blocks = min((groups + 7) / 8, (long long)sms * 2);
+  quant_pass_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(t);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   quant_scale_kernel<<<dim3(1, 3), 256, 0, st>>>(t, B);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  quant_write_kernel<<<grid, 256, 0, st>>>(t);
+  quant_pass_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(t);
   return cudaGetLastError();
 }
 
