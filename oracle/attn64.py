@@ -158,7 +158,7 @@ def forward(q, k, v, scale: float, mods: Mods = None):
 
 
 def decode_paged(q, k_cache, v_cache, block_table, seqlens, scale: float, mods: Mods = None):
-    """Decode step over a paged K/V cache: O [B, Hq, d] and LSE [B, Hq] (fp64).
+    """Decode step over a paged K/V cache, in fp64.
 
     "Les kernels d'attention rapide et la fusion d'opérateurs accélèrent les
     modèles d'IA", section "Attention de type FlashAttention et attention
@@ -167,45 +167,58 @@ def decode_paged(q, k_cache, v_cache, block_table, seqlens, scale: float, mods: 
     from logical to physical positions; the attention kernel translates every
     position through that table.
 
-    Reading taken here: ``q`` [B, Hq, d] holds the newest token of each
-    sequence, at position i = L_b - 1 with L_b = ``seqlens[b]``; it attends to
-    the L_b cached keys j = 0 .. L_b - 1, where row j of sequence b, KV head hk
-    is row j % 16 of physical block ``block_table[b, j // 16]`` of the cache
-    [num_blocks, Hkv, 16, d].  The scores and mods are those of ``logits`` /
-    ``allowed`` with that i (the causal test j <= i then always holds; the
-    window keeps i - j < W; ALiBi subtracts slope * (i - j)).  A sequence with
-    L_b = 0 gets O = 0, LSE = -inf.  Document masks do not apply.
+    Reading taken here: ``q`` is [B, Hq, d] (one new token per sequence) or
+    [B, Hq, T, d] (T new tokens, e.g. drafts to verify); token t of sequence b
+    sits at position i_t = L_b - T + t, L_b = ``seqlens[b]`` counting the new
+    tokens, and attends to the cached keys j = 0 .. L_b - 1 that the mods allow
+    for i_t (causal j <= i_t always applies; the window keeps i_t - j < W;
+    ALiBi subtracts slope * (i_t - j)).  Row j of sequence b, KV head hk is row
+    j % 16 of physical block ``block_table[b, j // 16]`` of the cache
+    [num_blocks, Hkv, 16, d].  A token with no allowed key (L_b = 0, or
+    i_t < 0) gets O = 0, LSE = -inf.  Document masks do not apply.  Returns
+    O with q's shape and LSE [B, Hq] or [B, Hq, T].
     """
     mods = mods or Mods()
     if mods.doc_ids is not None:
         raise ValueError("document masks do not apply to a decode step")
     Q = _f64(q)
+    one = Q.ndim == 3
+    if one:
+        Q = Q[:, :, None, :]
     KC = _f64(k_cache)
     VC = _f64(v_cache)
     table = np.asarray(block_table)
     lens = np.asarray(seqlens)
-    B, Hq, d = Q.shape
+    B, Hq, T, d = Q.shape
     Hkv, blk = KC.shape[1], KC.shape[2]
     G = Hq // Hkv
-    O = np.zeros((B, Hq, d))
-    LSE = np.full((B, Hq), -np.inf)
+    causal = Mods(causal=True, window=mods.window, softcap=mods.softcap, alibi=mods.alibi,
+                  alibi_slopes=mods.alibi_slopes)
+    O = np.zeros((B, Hq, T, d))
+    LSE = np.full((B, Hq, T), -np.inf)
     for b in range(B):
         L = int(lens[b])
         if L == 0:
             continue
         blocks = table[b, :-(-L // blk)]
-        rows = np.array([L - 1])
+        ts = [t for t in range(T) if L - T + t >= 0]  # tokens with a position
+        if not ts:
+            continue
+        rows = np.array([L - T + t for t in ts])
         cols = np.arange(L)
-        m = allowed(mods, b, rows, cols)
+        m = allowed(causal, b, rows, cols)
         for hk in range(Hkv):
             K = KC[blocks, hk].reshape(-1, d)[:L]
             V = VC[blocks, hk].reshape(-1, d)[:L]
             for hq in range(hk * G, (hk + 1) * G):
-                qh = np.broadcast_to(Q[b, hq], (L, d))  # row L - 1 is the query
-                _, x = logits(qh, K, scale, mods, hq, Hq, rows, cols)
+                qh = np.zeros((L, d))
+                qh[rows] = Q[b, hq, ts]
+                _, x = logits(qh, K, scale, causal, hq, Hq, rows, cols)
                 P, lse = _softmax_rows(x, m)
-                O[b, hq] = (P @ V)[0]
-                LSE[b, hq] = lse[0]
+                O[b, hq, ts] = P @ V
+                LSE[b, hq, ts] = lse
+    if one:
+        return O[:, :, 0], LSE[:, :, 0]
     return O, LSE
 
 

@@ -464,25 +464,46 @@ DECODE_MODS = {
 }
 
 
+@pytest.mark.parametrize("T", [1, 3], ids=["one_token", "three_tokens"])
 @pytest.mark.parametrize("mk", list(DECODE_MODS), ids=list(DECODE_MODS))
-def test_decode_matches_brute_force_last_row(mk):
-    """The decode step equals the last row of the causal brute-force forward run
-    on the sequence's rows, gathered here by an explicit loop over positions."""
+def test_decode_matches_brute_force_last_rows(mk, T):
+    """The decode step equals the last T rows of the causal brute-force forward
+    run on the sequence's rows, gathered here by an explicit loop over
+    positions, with the new tokens' queries in those rows."""
     B, Hq, Hkv, d = 2, 4, 2, 8
     lens = [37, 17]
     q, kc, vc, table, sl = _paged_case(B, Hq, Hkv, lens, d, seed=11)
+    if T > 1:
+        q = np.random.default_rng(12).standard_normal((B, Hq, T, d))
     cfg = DECODE_MODS[mk]
     slopes = list(A.alibi_slopes(Hq)) if cfg.get("alibi") else None
     O, L = A.decode_paged(q, kc, vc, table, sl, 0.4, A.Mods(causal=True, **cfg))
+    if T == 1:
+        O, L = O[:, :, None], L[:, :, None]
+        q = q[:, :, None]
     for b, n in enumerate(lens):
         K = [[[float(x) for x in kc[table[b, j // 16], hk, j % 16]] for j in range(n)] for hk in range(Hkv)]
         V = [[[float(x) for x in vc[table[b, j // 16], hk, j % 16]] for j in range(n)] for hk in range(Hkv)]
-        Qrows = [[[0.0] * d for _ in range(n - 1)] + [list(q[b, h])] for h in range(Hq)]
+        Qrows = [[[0.0] * d for _ in range(n - T)] + [list(q[b, h, t]) for t in range(T)] for h in range(Hq)]
         Ob, Lb = brute.forward([Qrows], [K], [V], 0.4, causal=True, window=cfg.get("window"),
                                softcap=cfg.get("softcap"), slopes=slopes)
         for h in range(Hq):
-            np.testing.assert_allclose(O[b, h], Ob[0][h][n - 1], rtol=1e-12, atol=1e-12)
-            np.testing.assert_allclose(L[b, h], Lb[0][h][n - 1], rtol=1e-12, atol=1e-12)
+            for t in range(T):
+                np.testing.assert_allclose(O[b, h, t], Ob[0][h][n - T + t], rtol=1e-12, atol=1e-12)
+                np.testing.assert_allclose(L[b, h, t], Lb[0][h][n - T + t], rtol=1e-12, atol=1e-12)
+
+
+def test_decode_tokens_before_the_cache_start_are_empty():
+    """With more new tokens than cached positions, the tokens at negative
+    positions have no key: O = 0, LSE = -inf; the others are unaffected."""
+    B, Hq, Hkv, d, T = 1, 2, 1, 8, 4
+    q, kc, vc, table, sl = _paged_case(B, Hq, Hkv, [2], d, seed=3)
+    q4 = np.random.default_rng(4).standard_normal((B, Hq, T, d))
+    O, L = A.decode_paged(q4, kc, vc, table, sl, 0.5)
+    assert np.all(O[:, :, :2] == 0.0) and np.all(np.isneginf(L[:, :, :2]))
+    O2, L2 = A.decode_paged(q4[:, :, 2:], kc, vc, table, sl, 0.5)
+    np.testing.assert_array_equal(O[:, :, 2:], O2)
+    np.testing.assert_array_equal(L[:, :, 2:], L2)
 
 
 def test_decode_closed_forms():
