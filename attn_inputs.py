@@ -130,10 +130,11 @@ def make_inputs(B, Hq, Hkv, N, d, seed, *, need_do=True, outlier_frac=0.0,
     return out
 
 
-def paged_decode_inputs(B, Hq, Hkv, N, d, seed, *, min_len=1, lens=None, spare=8, block=16, **_):
+def paged_decode_inputs(B, Hq, Hkv, N, d, seed, *, min_len=1, lens=None, spare=8, block=16, q_len=1, **_):
     """One decode step over a paged K/V cache.
 
-    Returns q [B, Hq, d] and the caches [num_blocks, Hkv, block, d] (CPU bf16),
+    Returns q [B, Hq, d] ([B, Hq, q_len, d] when q_len > 1: the newest q_len
+    tokens) and the caches [num_blocks, Hkv, block, d] (CPU bf16),
     the block table int32 [B, ceil(N / block)] and the lengths int32 [B].
     Lengths are uniform integers in [min_len, N] (seed + 10) unless given;
     sequence b owns ceil(L_b / block) blocks at shuffled physical slots
@@ -153,7 +154,7 @@ def paged_decode_inputs(B, Hq, Hkv, N, d, seed, *, min_len=1, lens=None, spare=8
     for b, nb in enumerate(nbs):
         table[b, :nb] = perm[used:used + nb]
         used += nb
-    return dict(q=randn_bf16((B, Hq, d), seed),
+    return dict(q=randn_bf16((B, Hq, d) if q_len == 1 else (B, Hq, q_len, d), seed),
                 k_cache=randn_bf16((num_blocks, Hkv, block, d), seed + 1),
                 v_cache=randn_bf16((num_blocks, Hkv, block, d), seed + 2),
                 block_table=table, seqlens=lens)

@@ -638,7 +638,7 @@ def run_decode(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        ea.attn_decode_paged(q, kc, vc, table, max_blocks, lens, num_blocks, o, lse, B, Hq, Hkv, d, scale,
+        ea.attn_decode_paged(q, kc, vc, table, max_blocks, lens, num_blocks, o, lse, B, Hq, Hkv, 1, d, scale,
                              None, ws, nws, stream)
 
     def step_e2e():  # the new tokens' queries in, outputs back (the cache stays resident)

@@ -16,14 +16,14 @@ from ._lib import (  # noqa: F401
     OP_BWD_VARLEN, OP_DECODE_PAGED, OP_FWD, OP_FWD_FP8, OP_FWD_VARLEN, OP_QUANT_FP8, TILE_FULL, TILE_PARTIAL,
     TILE_SKIP, attn_block_map, attn_bwd, attn_bwd_profiled, attn_bwd_noalloc, attn_bwd_varlen,
     NOALLOC_SCRATCH_BYTES, attn_fwd, attn_fwd_fp8, attn_fwd_varlen, attn_hadamard_quant_fp8,
-    attn_rope_hadamard_quant_fp8, attn_fwd_paged, attn_decode_paged,
+    attn_rope_hadamard_quant_fp8, attn_fwd_paged, attn_decode_paged, attn_decode_workspace_size,
     attn_status, attn_workspace_size, lib,
     make_mods, status_string,
 )
 
 __all__ = [
     "forward", "backward", "forward_paged", "decode_paged", "forward_varlen", "backward_varlen", "hadamard_quant_fp8",
-    "forward_fp8", "attn_fwd_paged", "attn_decode_paged",
+    "forward_fp8", "attn_fwd_paged", "attn_decode_paged", "attn_decode_workspace_size",
     "block_map", "make_mods", "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc",
     "attn_fwd_varlen", "attn_bwd_varlen", "attn_hadamard_quant_fp8", "attn_rope_hadamard_quant_fp8",
     "attn_fwd_fp8", "attn_block_map",
@@ -89,20 +89,24 @@ def forward_paged(q, k_cache, v_cache, block_table, scale=None, mods=None, strea
 
 def decode_paged(q, k_cache, v_cache, block_table, seqlens, scale=None, mods=None, stream=None):
     """(O, LSE) of one decode step: q [B, Hq, d] (the newest token of each
-    sequence), caches [num_blocks, Hkv, 16, d], block_table a device int32
-    [B, max_blocks], seqlens a device int32 [B] of cached tokens per sequence
-    (the query's own included)."""
+    sequence) or [B, Hq, T, d] (its T newest tokens), caches
+    [num_blocks, Hkv, 16, d], block_table a device int32 [B, max_blocks],
+    seqlens a device int32 [B] of cached tokens per sequence (the new ones
+    included).  O has q's shape; LSE is [B, Hq] or [B, Hq, T]."""
     torch = _torch()
-    B, Hq, d = q.shape
+    one = q.dim() == 3
+    q4 = q.unsqueeze(2) if one else q
+    B, Hq, T, d = q4.shape
     num_blocks, Hkv = k_cache.shape[0], k_cache.shape[1]
     max_blocks = block_table.shape[1]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    o = torch.empty_like(q)
-    l = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-    ws, nws = _workspace(OP_DECODE_PAGED, B, Hq, Hkv, 16 * max_blocks, d, mods, q.device)
-    attn_decode_paged(q, k_cache, v_cache, block_table, max_blocks, seqlens, num_blocks, o, l, B, Hq, Hkv, d,
+    o = torch.empty_like(q4)
+    l = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    nws = attn_decode_workspace_size(B, Hq, Hkv, T, max_blocks, d, mods)
+    ws = torch.empty(nws, dtype=torch.uint8, device=q.device) if nws else None
+    attn_decode_paged(q4, k_cache, v_cache, block_table, max_blocks, seqlens, num_blocks, o, l, B, Hq, Hkv, T, d,
                       scale, mods, ws, nws, stream)
-    return o, l
+    return (o.squeeze(2), l.squeeze(2)) if one else (o, l)
 
 
 def forward_varlen(q, k, v, cu_seqlens, scale=None, mods=None, stream=None):

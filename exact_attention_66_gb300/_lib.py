@@ -26,7 +26,7 @@ TILE_SKIP, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 
 # Exported symbols, in the order include/attn.h declares them.
 EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc",
-           "attn_fwd_paged", "attn_decode_paged", "attn_fwd_varlen", "attn_bwd_varlen", "attn_hadamard_quant_fp8", "attn_rope_hadamard_quant_fp8",
+           "attn_fwd_paged", "attn_decode_paged", "attn_decode_workspace_size", "attn_fwd_varlen", "attn_bwd_varlen", "attn_hadamard_quant_fp8", "attn_rope_hadamard_quant_fp8",
            "attn_fwd_fp8", "attn_block_map", "attn_status", "attn_status_string")
 
 
@@ -56,7 +56,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_bwd_profiled.argtypes = lib.attn_bwd.argtypes + [ctypes.POINTER(ctypes.c_void_p)]
     lib.attn_bwd_noalloc.argtypes = lib.attn_bwd.argtypes[:16] + [vp]  # no ws, ws_bytes
     lib.attn_fwd_paged.argtypes = [vp, vp, vp, vp, i, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
-    lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, i, vp, i, vp, vp, i, i, i, i, f, mp, vp, sz, vp]
+    lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, i, vp, i, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
+    lib.attn_decode_workspace_size.argtypes = [i, i, i, i, i, i, mp]
+    lib.attn_decode_workspace_size.restype = sz
     lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_hadamard_quant_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp]
@@ -174,10 +176,15 @@ def attn_fwd_paged(q, k_cache, v_cache, block_table, num_blocks, o, lse, B, Hq, 
 
 
 def attn_decode_paged(q, k_cache, v_cache, block_table, max_blocks, seqlens, num_blocks, o, lse, B, Hq,
-                      Hkv, d, scale, mods=None, ws=None, ws_bytes=0, stream=None):
+                      Hkv, q_len, d, scale, mods=None, ws=None, ws_bytes=0, stream=None):
     _check(_lib.attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), max_blocks,
-                                  _ptr(seqlens), num_blocks, _ptr(o), _ptr(lse), B, Hq, Hkv, d, float(scale),
-                                  _mods_ref(mods), _ptr(ws), int(ws_bytes), _stream(stream)), "attn_decode_paged")
+                                  _ptr(seqlens), num_blocks, _ptr(o), _ptr(lse), B, Hq, Hkv, q_len, d,
+                                  float(scale), _mods_ref(mods), _ptr(ws), int(ws_bytes), _stream(stream)),
+           "attn_decode_paged")
+
+
+def attn_decode_workspace_size(B, Hq, Hkv, q_len, max_blocks, d, mods=None) -> int:
+    return int(_lib.attn_decode_workspace_size(B, Hq, Hkv, q_len, max_blocks, d, _mods_ref(mods)))
 
 
 def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens, n_seqs, Hq, Hkv, total, d, scale, mods=None,

@@ -268,18 +268,19 @@ DecodeSplit decode_split(int B, int Hkv, int N) {
   return {(int)ct, (int)((tiles + ct - 1) / ct)};
 }
 size_t decode_info_bytes(int B) { return round_up((size_t)B * sizeof(int4), 256) + 256; }
-size_t decode_ws_bytes(int B, int Hq, int Hkv, int N) {
-  const size_t rows = (size_t)B * Hq * decode_split(B, Hkv, N).max_chunks;
+size_t decode_ws_bytes(int B, int Hq, int Hkv, int T, int N) {
+  const size_t rows = (size_t)B * Hq * T * decode_split(B, Hkv, N).max_chunks;
   return decode_info_bytes(B) + round_up(rows * 128 * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
 }
-attn_status_t check_decode(int B, int Hq, int Hkv, int N, int num_blocks, int d, const attn_mods_t* mods) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || N < 16 || num_blocks < 1) return ATTN_ERR_INVALID_ARG;
-  if (N % 16 != 0 || Hq % Hkv != 0 || Hq / Hkv > 128 || d != 128) return ATTN_ERR_UNSUPPORTED;
+attn_status_t check_decode(int B, int Hq, int Hkv, int T, int N, int num_blocks, int d, const attn_mods_t* mods) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || N < 16 || num_blocks < 1) return ATTN_ERR_INVALID_ARG;
+  if (N % 16 != 0 || Hq % Hkv != 0 || (long long)(Hq / Hkv) * T > 128 || d != 128) return ATTN_ERR_UNSUPPORTED;
   if ((long long)num_blocks * Hkv >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   attn_status_t st;
   if ((st = check_mods(mods)) != ATTN_OK) return st;
   if (mods && (mods->flags & ATTN_MOD_DOC)) return ATTN_ERR_UNSUPPORTED;
-  if ((long long)B * Hq * decode_split(B, Hkv, N).max_chunks * 128 >= (1ll << 40)) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * Hq * T * decode_split(B, Hkv, N).max_chunks * 128 >= (1ll << 40)) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * Hq * T >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   if ((long long)B * Hkv * decode_split(B, Hkv, N).max_chunks >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
@@ -302,7 +303,7 @@ extern "C" {
 
 size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int N, int d, const attn_mods_t* mods) {
   if (op == ATTN_OP_DECODE_PAGED)
-    return check_decode(B, Hq, Hkv, N, 1, d, mods) == ATTN_OK ? decode_ws_bytes(B, Hq, Hkv, N) : 0;
+    return N % 16 == 0 ? attn_decode_workspace_size(B, Hq, Hkv, 1, N / 16, d, mods) : 0;
   if (check_shape(B, Hq, Hkv, N, d, op == ATTN_OP_FWD_FP8 || op == ATTN_OP_QUANT_FP8) != ATTN_OK ||
       check_mods(mods) != ATTN_OK)
     return 0;
@@ -511,20 +512,27 @@ attn_status_t attn_fwd_paged(const void* q, const void* k_cache, const void* v_c
   return cuda_status(launch_fwd_bf16(L, d, has_score_mods(L.p.flags), needs_map(L.p.flags), s));
 }
 
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int q_len, int max_blocks, int d,
+                                  const attn_mods_t* mods) {
+  if (max_blocks < 1 || max_blocks > (1 << 26)) return 0;
+  const int N = 16 * max_blocks;
+  return check_decode(B, Hq, Hkv, q_len, N, 1, d, mods) == ATTN_OK ? decode_ws_bytes(B, Hq, Hkv, q_len, N) : 0;
+}
+
 attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, int max_blocks, const int32_t* seqlens,
-                                int num_blocks, void* o, float* lse, int B, int Hq, int Hkv, int d,
-                                float scale, const attn_mods_t* mods, void* ws, size_t ws_bytes,
+                                int num_blocks, void* o, float* lse, int B, int Hq, int Hkv, int q_len,
+                                int d, float scale, const attn_mods_t* mods, void* ws, size_t ws_bytes,
                                 void* stream) {
   attn_status_t st;
   if (max_blocks < 1 || max_blocks > (1 << 26)) return max_blocks < 1 ? ATTN_ERR_INVALID_ARG : ATTN_ERR_UNSUPPORTED;
   const int N = 16 * max_blocks;
-  if ((st = check_decode(B, Hq, Hkv, N, num_blocks, d, mods)) != ATTN_OK) return st;
+  if ((st = check_decode(B, Hq, Hkv, q_len, N, num_blocks, d, mods)) != ATTN_OK) return st;
   if ((st = check_tensors({q, k_cache, v_cache, o})) != ATTN_OK) return st;
   if (lse == nullptr || block_table == nullptr || seqlens == nullptr) return ATTN_ERR_INVALID_ARG;
   if (!aligned(lse, 4) || !aligned(block_table, 4) || !aligned(seqlens, 4)) return ATTN_ERR_UNSUPPORTED;
   if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-  if ((st = check_ws(ws, ws_bytes, decode_ws_bytes(B, Hq, Hkv, N))) != ATTN_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, decode_ws_bytes(B, Hq, Hkv, q_len, N))) != ATTN_OK) return st;
   int* status = nullptr;
   if ((st = device_state(&status)) != ATTN_OK) return st;
   const int sms = sm_count();
@@ -534,12 +542,13 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   const int G = Hq / Hkv;
   const DecodeSplit sp = decode_split(B, Hkv, N);
   DecodeLaunch L{};
-  {  // Q as [B*Hkv, G, d]: one box holds the G query heads of a KV head
+  {  // Q as [B*Hkv, G*q_len, d]: one box holds the G query heads x q_len tokens of a KV head
     auto enc = encode_fn();
     if (!enc) return ATTN_ERR_CUDA;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)G, (cuuint64_t)B * Hkv};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)G * d * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)G, 1};
+    const int R = G * q_len;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)R, (cuuint64_t)B * Hkv};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)R * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)R, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     if (enc(&L.tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -556,6 +565,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.G = G;
+  p.q_len = q_len;
   p.bt_stride = max_blocks;
   p.kv_blocks = num_blocks;
   p.ct = sp.ct;
@@ -572,7 +582,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.seq_info = reinterpret_cast<int4*>(w);
   p.n_items = reinterpret_cast<int*>(w + decode_info_bytes(B) - 256);
-  const size_t rows = (size_t)B * Hq * sp.max_chunks;
+  const size_t rows = (size_t)B * Hq * q_len * sp.max_chunks;
   p.o_part = reinterpret_cast<float*>(w + decode_info_bytes(B));
   p.lse_part = reinterpret_cast<float*>(w + decode_info_bytes(B) + round_up(rows * 128 * sizeof(float), 256));
   p.status = status;

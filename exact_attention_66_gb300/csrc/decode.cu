@@ -1,6 +1,7 @@
-// Decode step over a paged K/V cache for sm_103a: the newest token of every
-// sequence attends to all of that sequence's cached keys, which are read
-// through a block table of 16-row blocks.
+// Decode step over a paged K/V cache for sm_103a: the newest token (or the T
+// newest tokens, causal among themselves) of every sequence attends to that
+// sequence's cached keys, which are read through a block table of 16-row
+// blocks.
 //
 // Method ("Les kernels d'attention rapide et la fusion d'opérateurs
 // accélèrent les modèles d'IA", section "Attention de type FlashAttention et
@@ -18,9 +19,10 @@
 //    128) and a persistent grid of one CTA per SM walks its items
 //    round-robin.  The TMA producer runs ahead across item boundaries, so an
 //    SM keeps its loads in flight from its first tile to its last;
-//  * the G query heads of a KV head are the rows of one 128-row tcgen05 tile
-//    (rows >= G stay zero): S = Q K^T and O += P V are each one MMA chain
-//    per key tile, and every K and V row is read once for all G heads;
+//  * the G query heads x T tokens of a KV head are the rows of one 128-row
+//    tcgen05 tile (rows >= G T stay zero): S = Q K^T and O += P V are each one
+//    MMA chain per key tile, and every K and V row is read once for all of
+//    them;
 //  * a key tile arrives as sixteen 2 KB TMA boxes (one per cache block and
 //    64-column half), issued by 16 lanes of a producer warp at once: one warp
 //    streams K tiles and another V tiles, each through its own 2-slot ring,
@@ -43,7 +45,7 @@ constexpr int DEC_THREADS = 256;
 constexpr int DEC_TB = TILE * DEC_D * 2;  // one bf16 K or V tile of 128 rows (32 KB)
 
 // Shared-memory layout.  The MMAs read Q and P as 128-row tiles, of which only
-// the G rows of the query heads matter.  With G <= 8 (SMALL) a Q or P tile is
+// the R = G T rows of the query heads and tokens matter.  With R <= 8 (SMALL) a Q or P tile is
 // a single 8-row swizzle group per 64-column half (1 KB) and the MMA
 // descriptor's stride between 8-row groups is 0, so its other fifteen groups
 // re-read the same eight rows (the S and O rows they produce are never read);
@@ -87,7 +89,8 @@ __device__ __forceinline__ void seq_chunks(const DecodeParams& p, int b, int& L,
     L = 0;
   }
   const int J_hi = (L + TILE - 1) / TILE;
-  J0 = (p.flags & MOD_WINDOW) ? max(0, L - p.window) / TILE : 0;
+  // keys of the earliest new token, at L - T, reach back to L - T - W + 1
+  J0 = (p.flags & MOD_WINDOW) ? max(0, L - p.q_len - p.window + 1) / TILE : 0;
   n = L > 0 ? (J_hi - J0 + p.ct - 1) / p.ct : 0;
 }
 
@@ -238,12 +241,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   const Abort ab{&S.abort, p.status};
   const int warp = warp_id(), lane = lane_id();
   const int G = p.G;
-  const int nsw = (G + 31) / 32;  // softmax warps (4 .. 3 + nsw): one thread per query head
+  const int R = G * p.q_len;      // tile rows in use: (query head, token) pairs
+  const int nsw = (R + 31) / 32;  // softmax warps (4 .. 3 + nsw): one thread per row
 
-  // Rows >= G of the Q tiles never receive data: zero them (and P) once.
+  // Rows >= R of the Q tiles never receive data: zero them (and P) once.
   for (int g = threadIdx.x; g < 3 * C::QTB / 16; g += DEC_THREADS) {
     const int row = ((g * 16) % C::QCH) / 128;
-    if (g * 16 >= 2 * C::QTB || row >= G)
+    if (g * 16 >= 2 * C::QTB || row >= R)
       *reinterpret_cast<uint4*>(smem + g * 16) = make_uint4(0u, 0u, 0u, 0u);
   }
   fence_async_smem();
@@ -327,7 +331,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         if (lane == 0) {
           ok = t.item < 2 || mbar_wait(&S.q_empty[qb], ((t.item >> 1) - 1) & 1, ab);
           if (ok) {
-            mbar_arrive_tx(&S.q_full[qb], 2 * G * 128);
+            mbar_arrive_tx(&S.q_full[qb], 2 * R * 128);
             for (int ch = 0; ch < 2; ++ch)
               tma_load_3d(smem + C::Q_OFF + qb * C::QTB + ch * C::QCH, &tq, &S.q_full[qb], ch * 64, 0,
                           t.b * p.Hkv + t.hk);
@@ -425,8 +429,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   } else if (warp >= 4 && warp < 4 + nsw) {
     // -------------------------------------------------------------- softmax
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // query head r of the group (TMEM lane r)
-    const bool active = r < G;
+    const int r = wq * 32 + lane;  // tile row (TMEM lane) r: query head r / T, token r % T
+    const bool active = r < R;
+    const int rr = min(r, R - 1);
+    const int g = rr / p.q_len, tok = rr - g * p.q_len;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tO0 = tmem + lane_off + 256;  // + 128 for odd items
     uint8_t* p_tile = smem + C::P_OFF;
@@ -440,7 +446,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     struct Pending {
       bool on;
       int buf;      // O buffer (item parity)
-      size_t prow;  // row of the partial buffers: (b * Hq + hq) * max_chunks + chunk
+      size_t prow;  // row of the partial buffers: ((b * Hq + hq) * T + token) * max_chunks + chunk
       float m, l;   // running max (log2 units) and sum
     };
     Pending pend{false, 0, 0u, 0.f, 0.f};
@@ -471,7 +477,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     int n = 0;  // tiles processed
     bool ok = true;
     while (ok && w.next(p, t)) {
-      const int hq = t.hk * G + min(r, G - 1);
+      const int hq = t.hk * G + g;
+      const int i = t.L - p.q_len + tok;  // this row's token position
       if (t.first) {
         m = -INFINITY;
         l = 0.f;
@@ -491,11 +498,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       tc_fence_before();
       mbar_arrive(&S.s_free[n & 1]);
 
-      // Keys j0 + c are allowed iff lo_lim < c <= hi_lim: j <= i = L - 1, and
-      // with the window i - j < W.
+      // Keys j0 + c are allowed iff lo_lim < c <= hi_lim: j <= i, and with
+      // the window i - j < W (rows differ only by their token's position).
       const int j0 = t.J * TILE;
-      const int hi_lim = t.L - 1 - j0;
-      const int lo_lim = win ? t.L - p.window - 1 - j0 : -1;
+      const int hi_lim = i - j0;
+      const int lo_lim = win ? i - p.window - j0 : -1;
       const bool partial = hi_lim < TILE - 1 || lo_lim >= 0;
       float mt, mul;
       if (!(sc || al)) {
@@ -509,7 +516,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       } else {
         // log2-unit logits: soft-cap c tanh(scale s / c), then ALiBi
         // slope (j - i).
-        const float al_base = al2 * (float)(j0 - (t.L - 1));
+        const float al_base = al2 * (float)(j0 - i);
         const uint64_t al2x = f2_pack(al2, al2), alb = f2_pack(al_base, al_base);
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
@@ -566,9 +573,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       }
       if (active) {  // P row r into the 128-byte swizzled K-major tile
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {
-          const uint32_t addr = (uint32_t)((g >> 3) * C::QCH + r * 128 + (((g & 7) ^ (r & 7)) << 4));
-          *reinterpret_cast<uint4*>(p_tile + addr) = make_uint4(s[4 * g], s[4 * g + 1], s[4 * g + 2], s[4 * g + 3]);
+        for (int q16 = 0; q16 < 16; ++q16) {
+          const uint32_t addr = (uint32_t)((q16 >> 3) * C::QCH + r * 128 + (((q16 & 7) ^ (r & 7)) << 4));
+          *reinterpret_cast<uint4*>(p_tile + addr) =
+              make_uint4(s[4 * q16], s[4 * q16 + 1], s[4 * q16 + 2], s[4 * q16 + 3]);
         }
       }
       fence_async_smem();
@@ -581,7 +589,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         epilogue(pend);
         pend.on = false;
       }
-      if (t.last) pend = Pending{true, t.item & 1, ((size_t)t.b * p.Hq + hq) * p.max_chunks + t.c, m, l};
+      if (t.last)
+        pend = Pending{true, t.item & 1, (((size_t)t.b * p.Hq + hq) * p.q_len + tok) * p.max_chunks + t.c, m, l};
       ++n;
     }
     if (ok && pend.on && (ok = wait_warp(&S.o_full, (n - 1) & 1, ab))) {
@@ -598,7 +607,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   }
 }
 
-// One warp per (sequence, query head): merge the chunks' O / l by their LSE.
+// One warp per (sequence, query head, token): merge the chunks' O / l by their LSE.
 // Lane c holds the log2-sum-exp and weight of chunk c; every lane
 // accumulates four output columns over the chunks, DEC_MERGE chunks' loads in
 // flight at a time (one round for the usual chunk counts).
@@ -608,8 +617,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   pdl_wait();  // the partial results come from the main kernel
   const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
-  if (gw >= p.B * p.Hq) return;
-  const int b = gw / p.Hq;
+  if (gw >= p.B * p.Hq * p.q_len) return;
+  const int b = gw / (p.Hq * p.q_len);
   const int n = p.seq_info[b].z;
   const float* lp = p.lse_part + (size_t)gw * p.max_chunks;
   const float4* op = reinterpret_cast<const float4*>(p.o_part + (size_t)gw * p.max_chunks * DEC_D);
@@ -672,14 +681,14 @@ cudaError_t launch_decode(const DecodeLaunch& L, bool mods, cudaStream_t st) {
   decode_setup_kernel<<<1, 1024, 0, st>>>(L.p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const bool small = L.p.G <= 8;
+  const bool small = L.p.G * L.p.q_len <= 8;
   auto kern = mods ? (small ? decode_kernel<true, true> : decode_kernel<true, false>)
                    : (small ? decode_kernel<false, true> : decode_kernel<false, false>);
   const int smem = small ? DecCfg<true>::SMEM : DecCfg<false>::SMEM;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
   if ((e = launch_pdl(kern, (unsigned)L.grid, DEC_THREADS, (size_t)smem, st, L.tq, L.tk, L.tv, L.p)) != cudaSuccess)
     return e;
-  const long long warps = (long long)L.p.B * L.p.Hq;
+  const long long warps = (long long)L.p.B * L.p.Hq * L.p.q_len;
   return launch_pdl(decode_combine_kernel, (unsigned)((warps + 7) / 8), 256u, 0, st, L.p, (__nv_bfloat16*)L.o,
                     L.lse);
 }

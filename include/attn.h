@@ -211,23 +211,27 @@ attn_status_t attn_fwd_paged(const void* q, const void* k_cache, const void* v_c
  * fusion d'opérateurs accélèrent les modèles d'IA", section "Attention de
  * type FlashAttention et attention paginée": the cache grows one token per
  * step, in fixed blocks of 16 tokens mapped through a block table).  The
- * newest token of each sequence attends to every cached key of its sequence.
- * q           : bf16 [B, Hq, d], the token at position L_b - 1 of sequence b.
+ * q_len newest tokens of each sequence (1 for plain decoding; several, e.g.
+ * draft tokens to verify) attend to the cached keys of their sequence, causal
+ * among themselves.
+ * q           : bf16 [B, Hq, q_len, d]; token t of sequence b is at position
+ *               L_b - q_len + t.
  * k_cache,
  * v_cache     : bf16 [num_blocks, Hkv, 16, d], as for attn_fwd_paged.
  * block_table : device int32 [B, max_blocks]: cached rows [16 t, 16 t + 16) of
  *               sequence b are block block_table[b][t]; only the first
  *               ceil(L_b / 16) entries of a row are read.
- * seqlens     : device int32 [B]: L_b, the cached tokens of sequence b (the
- *               query included), 0 <= L_b <= 16 * max_blocks; L_b = 0 gives
- *               O = 0, LSE = -inf.
- * o, lse      : bf16 [B, Hq, d] and fp32 [B, Hq] (natural log), written.
+ * seqlens     : device int32 [B]: L_b, the cached tokens of sequence b (the new
+ *               ones included), 0 <= L_b <= 16 * max_blocks.  A token with no
+ *               key (L_b = 0, or a position below 0) gets O = 0, LSE = -inf.
+ * o, lse      : bf16 [B, Hq, q_len, d] and fp32 [B, Hq, q_len] (natural log),
+ *               written.
  * mods        : CAUSAL is implied (accepted, no effect); WINDOW keeps keys with
- *               (L_b - 1) - j < window; SOFTCAP and ALIBI as in attn_fwd with
- *               query position i = L_b - 1; DOC is ATTN_ERR_UNSUPPORTED.
- * ws          : attn_workspace_size(ATTN_OP_DECODE_PAGED, B, Hq, Hkv,
- *               16 * max_blocks, d, mods) bytes: per-chunk partial outputs.
- * Requirements: d = 128, Hq % Hkv == 0 and Hq / Hkv <= 128 (else
+ *               i - j < window for the token at position i; SOFTCAP and ALIBI as
+ *               in attn_fwd; DOC is ATTN_ERR_UNSUPPORTED.
+ * ws          : attn_decode_workspace_size(B, Hq, Hkv, q_len, max_blocks, d,
+ *               mods) bytes: per-chunk partial outputs.
+ * Requirements: d = 128, Hq % Hkv == 0, (Hq / Hkv) * q_len <= 128 (else
  * ATTN_ERR_UNSUPPORTED).  Device-side: a length outside [0, 16 * max_blocks]
  * or a table entry outside [0, num_blocks) is reported as ATTN_ERR_BOUNDS by
  * attn_status (the call then leaves O and LSE unspecified).
@@ -235,9 +239,15 @@ attn_status_t attn_fwd_paged(const void* q, const void* k_cache, const void* v_c
  */
 attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, int max_blocks, const int32_t* seqlens,
-                                int num_blocks, void* o, float* lse, int B, int Hq, int Hkv, int d,
-                                float scale, const attn_mods_t* mods, void* ws, size_t ws_bytes,
+                                int num_blocks, void* o, float* lse, int B, int Hq, int Hkv, int q_len,
+                                int d, float scale, const attn_mods_t* mods, void* ws, size_t ws_bytes,
                                 void* stream);
+
+/* Workspace bytes of attn_decode_paged (0 for invalid arguments).
+ * attn_workspace_size(ATTN_OP_DECODE_PAGED, B, Hq, Hkv, 16 * max_blocks, d,
+ * mods) is the same for q_len = 1. */
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int q_len, int max_blocks, int d,
+                                  const attn_mods_t* mods);
 
 /*
  * Packed variable-length sequences: n_seqs sequences stored back to back along

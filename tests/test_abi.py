@@ -160,15 +160,15 @@ def test_paged_forward_validates(L):
 def test_decode_validates(L):
     so = L.lib()
 
-    def dc(q=A, table=A, mb=8, sl=A, nb=8, lse=A, B=2, Hq=8, Hkv=2, d=128, scale=0.1, mods=None,
+    def dc(q=A, table=A, mb=8, sl=A, nb=8, lse=A, B=2, Hq=8, Hkv=2, T=1, d=128, scale=0.1, mods=None,
            ws=A, nws=1 << 30):
-        return so.attn_decode_paged(q, A, A, table, mb, sl, nb, A, lse, B, Hq, Hkv, d, scale,
+        return so.attn_decode_paged(q, A, A, table, mb, sl, nb, A, lse, B, Hq, Hkv, T, d, scale,
                                     ctypes.byref(mods) if mods else None, ws, nws, None)
     for kw in (dict(table=None), dict(sl=None), dict(lse=None), dict(q=None), dict(mb=0), dict(nb=0),
-               dict(B=0), dict(Hq=0), dict(scale=float("nan")), dict(scale=0.0)):
+               dict(B=0), dict(Hq=0), dict(T=0), dict(scale=float("nan")), dict(scale=0.0)):
         assert dc(**kw) == 1, kw
-    for kw in (dict(d=64), dict(Hq=3, Hkv=2), dict(Hq=129 * 2, Hkv=2), dict(sl=A + 2), dict(table=A + 2),
-               dict(q=A + 8), dict(lse=A + 2)):
+    for kw in (dict(d=64), dict(Hq=3, Hkv=2), dict(Hq=129 * 2, Hkv=2), dict(Hq=32, Hkv=1, T=5),
+               dict(sl=A + 2), dict(table=A + 2), dict(q=A + 8), dict(lse=A + 2)):
         assert dc(**kw) == 2, kw
     assert dc(mods=L.Mods(L.MOD_DOC, 0, 0.0, A, None)) == 2    # documents do not apply
     assert dc(mods=L.Mods(L.MOD_WINDOW, 0, 0.0, None, None)) == 1  # window must be >= 1
@@ -189,6 +189,15 @@ def test_decode_workspace_size(L):
     for B, Hq, Hkv, N in ((32, 64, 8, 8192), (1, 8, 8, 16), (3, 12, 4, 4000), (128, 32, 8, 32768)):
         assert so.attn_workspace_size(6, B, Hq, Hkv, N, 128, None) == expect(B, Hq, Hkv, N)
     assert so.attn_workspace_size(6, 2, 8, 2, 100, 128, None) == 0     # N not a multiple of 16
+    so.attn_decode_workspace_size.restype = ctypes.c_size_t
+    for B, Hq, Hkv, T, mb in ((32, 64, 8, 1, 512), (4, 32, 8, 4, 40), (3, 8, 1, 16, 7)):
+        tiles = -(-16 * mb // 128)
+        ct = min(max(1, -(-(B * Hkv * tiles) // 2432)), tiles)
+        rows = B * Hq * T * (-(-tiles // ct))
+        r256 = lambda x: -(-x // 256) * 256
+        assert so.attn_decode_workspace_size(B, Hq, Hkv, T, mb, 128, None) == \
+            r256(16 * B) + 256 + r256(rows * 512) + r256(rows * 4)
+    assert so.attn_decode_workspace_size(2, 64, 1, 3, 8, 128, None) == 0  # 64 heads x 3 tokens > 128 rows
     assert so.attn_workspace_size(6, 2, 8, 2, 128, 64, None) == 0      # d = 128 only
     docm = L.Mods(L.MOD_DOC, 0, 0.0, A, None)
     assert so.attn_workspace_size(6, 2, 8, 2, 128, 128, ctypes.byref(docm)) == 0

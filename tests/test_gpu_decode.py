@@ -1,8 +1,8 @@
 """Decode step over a paged K/V cache (attn_decode_paged) against the fp64
-oracle's decode: one query token per sequence, context lengths from 0 to
-several key tiles, GQA groups from 1 to 64 heads, window / soft-cap / ALiBi;
-plus determinism, independence of the block placement and the device-side
-bounds report."""
+oracle's decode: one or several new tokens per sequence, context lengths from
+0 to several key tiles, GQA groups from 1 to 64 heads, window / soft-cap /
+ALiBi; plus determinism, independence of the block placement and the
+device-side bounds report."""
 import numpy as np
 import pytest
 import torch
@@ -13,20 +13,23 @@ from gpu_common import LSE_TOL, O_TOL, default_scale, lib, max_abs, record
 
 pytestmark = pytest.mark.gpu
 
-# (B, Hq, Hkv, max_len, lens or None (uniform in [1, max_len]), mods)
+# (B, Hq, Hkv, max_len, lens or None (uniform in [1, max_len]), mods, new tokens per sequence)
 CASES = [
-    (4, 32, 8, 700, None, {}),                                  # many chunks per sequence
-    (3, 32, 2, 1024, [1000, 1, 333], dict(window=300, softcap=20.0, alibi=True)),
-    (2, 4, 4, 256, [129, 256], {}),                             # G = 1, exact tile multiple
-    (1, 64, 1, 520, [517], dict(alibi=True)),                  # G = 64: two softmax warps
-    (3, 16, 2, 96, [0, 50, 96], dict(window=7)),               # an empty sequence
-    (5, 24, 8, 2048, None, dict(softcap=30.0)),                 # G = 3
+    (4, 32, 8, 700, None, {}, 1),                                  # many chunks per sequence
+    (3, 32, 2, 1024, [1000, 1, 333], dict(window=300, softcap=20.0, alibi=True), 1),
+    (2, 4, 4, 256, [129, 256], {}, 1),                             # G = 1, exact tile multiple
+    (1, 64, 1, 520, [517], dict(alibi=True), 1),                  # G = 64: two softmax warps
+    (3, 16, 2, 96, [0, 50, 96], dict(window=7), 1),               # an empty sequence
+    (5, 24, 8, 2048, None, dict(softcap=30.0), 1),                 # G = 3
+    (4, 32, 8, 900, None, {}, 4),                                  # 4 tokens: 16 rows per item
+    (3, 16, 8, 600, [600, 2, 130], dict(window=50, alibi=True), 3),  # 6 rows; a token before the cache start
+    (2, 32, 2, 300, [300, 257], dict(softcap=20.0), 8),           # 128 rows: all four softmax warps
 ]
 
 
 def _ids(c):
-    B, Hq, Hkv, n, lens, m = c
-    return f"B{B}_H{Hq}x{Hkv}_L{n}_" + ("-".join(m) or "none")
+    B, Hq, Hkv, n, lens, m, T = c
+    return f"B{B}_H{Hq}x{Hkv}_L{n}_T{T}_" + ("-".join(m) or "none")
 
 
 def _run(ea, x, mods, scale):
@@ -40,14 +43,14 @@ def _run(ea, x, mods, scale):
 @pytest.mark.parametrize("case", CASES, ids=_ids)
 def test_decode_matches_oracle(case):
     ea = lib()
-    B, Hq, Hkv, n, lens, mk = case
-    x = gen.paged_decode_inputs(B, Hq, Hkv, n, 128, seed=900 + n, lens=lens)
+    B, Hq, Hkv, n, lens, mk, T = case
+    x = gen.paged_decode_inputs(B, Hq, Hkv, n, 128, seed=900 + n, lens=lens, q_len=T)
     s = default_scale(128)
     o, lse = _run(ea, x, ea.make_mods(causal=True, **mk), s)
     O, L = attn64.decode_paged(x["q"], x["k_cache"], x["v_cache"], x["block_table"], x["seqlens"], s,
                                attn64.Mods(causal=True, **mk))
     og, lg = o.float().cpu().numpy(), lse.cpu().numpy()
-    empty = x["seqlens"] == 0
+    empty = np.isneginf(L)  # tokens without any key
     assert np.all(og[empty] == 0.0) and np.all(np.isneginf(lg[empty]))
     eo, el = max_abs(og[~empty], O[~empty]), max_abs(lg[~empty], L[~empty])
     record("decode_cases", "O_max_abs", eo)
