@@ -53,6 +53,9 @@ WORKLOADS = {
     # one decode step per sequence over a shuffled paged cache; N is the longest
     # context, lengths uniform in [min_len, N]
     "paged_decode_8k": dict(B=32, Hq=64, Hkv=8, N=8192, d=128, min_len=4096, decode=True, seed=8000),
+    # the same with 4 new tokens per sequence (drafts to verify)
+    "paged_decode_4tok_8k": dict(B=32, Hq=64, Hkv=8, N=8192, d=128, min_len=4096, decode=True, q_len=4,
+                                 seed=8100),
 }
 
 DOC_LEN_MIN = 128

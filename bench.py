@@ -598,14 +598,14 @@ def run_paged(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def decode_bytes(B, Hq, Hkv, d, lens):
+def decode_bytes(B, Hq, Hkv, d, lens, T=1):
     """Algorithmic HBM bytes of one decode step: every cached K and V row of
     every sequence once, the block-table entries used, Q read, O and LSE
-    written."""
+    written (T new tokens per sequence)."""
     lens = np.asarray(lens, np.int64)
     kv = 2 * int(lens.sum()) * Hkv * d * 2
     table = 4 * int(((lens + 15) // 16).sum()) + 4 * B
-    return kv + table + 2 * B * Hq * d * 2 + 4 * B * Hq
+    return kv + table + 2 * B * Hq * T * d * 2 + 4 * B * Hq * T
 
 
 def run_decode(args, world, rank, local):
@@ -619,6 +619,7 @@ def run_decode(args, world, rank, local):
     if args.batch:  # smaller case of the same workload (profiling)
         cfg["B"] = args.batch
     B, Hq, Hkv, N, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"]
+    T = cfg.get("q_len", 1)
     scale = 1.0 / math.sqrt(d)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -630,15 +631,15 @@ def run_decode(args, world, rank, local):
     lens = torch.from_numpy(x["seqlens"]).to(dev)
     num_blocks, max_blocks = kc.shape[0], table.shape[1]
     o = torch.empty_like(q)
-    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
-    nws = ea.attn_workspace_size(ea.OP_DECODE_PAGED, B, Hq, Hkv, 16 * max_blocks, d, None)
+    lse = torch.empty((B, Hq, T) if T > 1 else (B, Hq), dtype=torch.float32, device=dev)
+    nws = ea.attn_decode_workspace_size(B, Hq, Hkv, T, max_blocks, d, None)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev)
     o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        ea.attn_decode_paged(q, kc, vc, table, max_blocks, lens, num_blocks, o, lse, B, Hq, Hkv, 1, d, scale,
+        ea.attn_decode_paged(q, kc, vc, table, max_blocks, lens, num_blocks, o, lse, B, Hq, Hkv, T, d, scale,
                              None, ws, nws, stream)
 
     def step_e2e():  # the new tokens' queries in, outputs back (the cache stays resident)
@@ -670,7 +671,7 @@ def run_decode(args, world, rank, local):
     ms_e2e = timed(step_e2e)
     ms, ms_e2e = allmax(world, ms), allmax(world, ms_e2e)
     peaks, src = load_peaks()
-    nbytes = decode_bytes(B, Hq, Hkv, d, x["seqlens"])
+    nbytes = decode_bytes(B, Hq, Hkv, d, x["seqlens"], T)
     gbs = nbytes / (ms * 1e-3) / 1e9
     hbm = peaks["hbm_gbs"]
     bytes_io = q.numel() * 2 + o.numel() * 2 + lse.numel() * 4
@@ -678,16 +679,16 @@ def run_decode(args, world, rank, local):
         "metric": f"paged decode HBM throughput ({name})", "value": round(world * gbs, 1), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d, "max_context": N,
+        "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "d": d, "new_tokens": T, "max_context": N,
                    "context_lengths": f"uniform in [{cfg['min_len']}, {N}], total {int(x['seqlens'].sum())}",
                    "block_size": 16, "num_blocks": num_blocks,
                    "parallelism": "single" if world == 1 else f"replicas{world}",
                    "l2": f"cache larger than L2 ({2 * kc.numel() * 2 / 2**20:.0f} MiB of K and V)"},
-        "tokens_per_s": round(world * B / (ms * 1e-3), 1),
+        "tokens_per_s": round(world * B * T / (ms * 1e-3), 1),
         "algorithmic_bytes_per_step": nbytes,
         "roofline": {"kernel": "decode_paged (setup, main and merge launches together)", "bound": "hbm",
                      "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
-                     "traffic": traffic_record("decode_paged") if not args.batch else None,
+                     "traffic": traffic_record("decode_paged") if not args.batch and T == 1 else None,
                      "peak_source": f"{src} hbm_gbs"},
         "e2e": {"value": round(world * nbytes / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": q.numel() * 2, "d2h_bytes_per_step": bytes_io - q.numel() * 2,
@@ -844,7 +845,7 @@ def main():
     ap.add_argument("--workload", choices=sorted(gen.WORKLOADS), default=WORKLOAD,
                     help="workload to time; the default is the one the metric is quoted on")
     ap.add_argument("--batch", type=int, default=0,
-                    help="paged_decode_8k only: this many sequences instead of the workload's (profiling)")
+                    help="paged decode workloads only: this many sequences instead of the workload's (profiling)")
     ap.add_argument("--heads", type=int, default=0,
                     help="query heads (8 per KV head) for a smaller profiling case; default: the workload's 64")
     args = ap.parse_args()
