@@ -259,6 +259,56 @@ def l2_note(cfg):
     return f"inputs fit in L2 (Q {q_bytes / 2**10:.0f} KiB): warm-cache timing"
 
 
+def pipelined_e2e(dev, compute_stream, ins, outs, compute, steps, world):
+    """Time ``steps`` end-to-end steps through the public API, pipelined.
+
+    Every step copies its inputs from pinned host memory into one of two
+    device buffer sets (``ins``: [(host, (dev0, dev1))]), runs ``compute(b)``
+    on ``compute_stream`` with buffer set b, and copies its results back into
+    pinned host memory (``outs``: [((dev0, dev1), (host0, host1))]).  The
+    copies run on their own streams, so step i's inputs arrive while step
+    i - 1 computes and its results leave while step i + 1 computes; events
+    keep a buffer set from being overwritten before its step has read it and
+    its results have left.  Returns ms per step (CUDA events, from before the
+    first copy in to after the last copy out)."""
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def one(i):
+        b = i & 1
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_comp[b])  # step i - 2 has read buffer set b
+            for host, bufs in ins:
+                bufs[b].copy_(host, non_blocking=True)
+            ev_in[b].record(s_in)
+        compute_stream.wait_event(ev_in[b])
+        if i >= 2:
+            compute_stream.wait_event(ev_out[b])  # step i - 2's results have left
+        compute(b)
+        ev_comp[b].record(compute_stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[b])
+            for bufs, hosts in outs:
+                hosts[b].copy_(bufs[b], non_blocking=True)
+            ev_out[b].record(s_out)
+
+    for i in range(2):  # warm-up
+        one(i)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(steps):
+        one(i)
+    s_out.wait_stream(compute_stream)
+    e1.record(s_out)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / steps
+
+
 def run_ours(args, world, rank, local):
     import exact_attention_66_gb300 as ea
 
@@ -347,37 +397,30 @@ def run_ours(args, world, rank, local):
         k_kv = [e[3].elapsed_time(e[4]) for e in evs]
         k_dq = [e[4].elapsed_time(e[5]) for e in evs]
 
-    # end to end through the public API: pinned host inputs in, results out
-    outs = (("o", o), ("lse", lse)) if fwd_only else (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))
-    ins = ("q", "k", "v") if fwd_only else ("q", "k", "v", "do")
-    out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs}
-    h2d = sum(host[n].numel() * host[n].element_size() for n in ins)
-    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    # end to end through the public API: every step's inputs in from pinned host
+    # memory and its results out, pipelined over two buffer sets
+    in_names = ("q", "k", "v") if fwd_only else ("q", "k", "v", "do")
+    out_names = ("o", "lse") if fwd_only else ("o", "lse", "dq", "dk", "dv")
     e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
-
-    def e2e_step():
-        for n, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
-            if n in ins:
-                dst.copy_(host[n], non_blocking=True)
-        fo, fl = ea.forward(q, k, v, scale, mods, out=o, lse=lse, stream=stream)
-        if not fwd_only:
-            ea.attn_bwd(q, k, v, fo, do, fl, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods, ws, nws, stream)
-        for n, src in outs:
-            out_host[n].copy_(src, non_blocking=True)
-
+    h2d = sum(host[n].numel() * host[n].element_size() for n in in_names)
+    d2h = sum(t.numel() * t.element_size() for t in (o, lse, dq, dk, dv)[:len(out_names)])
     e2e_ms = float("nan")
     if e2e_steps:
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = allmax(world, e0.elapsed_time(e1)) / e2e_steps
+        dev_in = {n: (t, torch.empty_like(t)) for n, t in zip(("q", "k", "v", "do"), (q, k, v, do))}
+        dev_out = {n: (t, torch.empty_like(t)) for n, t in zip(("o", "lse", "dq", "dk", "dv"), (o, lse, dq, dk, dv))}
+        host_out = {n: tuple(torch.empty(dev_out[n][0].shape, dtype=dev_out[n][0].dtype, pin_memory=True)
+                             for _ in range(2)) for n in out_names}
+
+        def compute(b):
+            qb, kb, vb, dob = (dev_in[n][b] for n in ("q", "k", "v", "do"))
+            ob, lb, dqb, dkb, dvb = (dev_out[n][b] for n in ("o", "lse", "dq", "dk", "dv"))
+            fo, fl = ea.forward(qb, kb, vb, scale, mods, out=ob, lse=lb, stream=stream)
+            if not fwd_only:
+                ea.attn_bwd(qb, kb, vb, fo, dob, fl, dqb, dkb, dvb, B, Hq, Hkv, N, d, scale, mods, ws, nws, stream)
+
+        e2e_ms = pipelined_e2e(dev, stream, [(host[n], dev_in[n]) for n in in_names],
+                               [(dev_out[n], host_out[n]) for n in out_names], compute, e2e_steps, world)
+        e2e_ms = allmax(world, e2e_ms)
     ea.attn_status(stream)
 
     fwd_f, bwd_f = flops(cfg, docs)
@@ -429,7 +472,8 @@ def run_ours(args, world, rank, local):
         "roofline": roofline,
         "e2e": None if not e2e_steps else {
             "value": round(world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+            "pipelined": "copies in and out on their own streams, two device buffer sets"},
         "gpu_launches": launches * args.steps,
         "clocks": clk,
     }
@@ -634,19 +678,12 @@ def run_decode(args, world, rank, local):
     lse = torch.empty((B, Hq, T) if T > 1 else (B, Hq), dtype=torch.float32, device=dev)
     nws = ea.attn_decode_workspace_size(B, Hq, Hkv, T, max_blocks, d, None)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev)
-    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        ea.attn_decode_paged(q, kc, vc, table, max_blocks, lens, num_blocks, o, lse, B, Hq, Hkv, T, d, scale,
+    def step(bufs=None):
+        qq, oo, ll = bufs if bufs is not None else (q, o, lse)
+        ea.attn_decode_paged(qq, kc, vc, table, max_blocks, lens, num_blocks, oo, ll, B, Hq, Hkv, T, d, scale,
                              None, ws, nws, stream)
-
-    def step_e2e():  # the new tokens' queries in, outputs back (the cache stays resident)
-        q.copy_(q_host, non_blocking=True)
-        step()
-        o_host.copy_(o, non_blocking=True)
-        lse_host.copy_(lse, non_blocking=True)
 
     def timed(fn):
         for _ in range(args.warmup):
@@ -668,7 +705,13 @@ def run_decode(args, world, rank, local):
     time.sleep(0.3)
     ms = timed(step)
     clk = clocks.stop()
-    ms_e2e = timed(step_e2e)
+    # end to end: the new tokens' queries in, outputs back (the cache stays
+    # resident), pipelined over two buffer sets
+    q2, o2, l2 = (q, torch.empty_like(q)), (o, torch.empty_like(o)), (lse, torch.empty_like(lse))
+    pin2 = lambda t: tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for _ in range(2))  # noqa: E731
+    ms_e2e = pipelined_e2e(dev, stream, [(q_host, q2)], [(o2, pin2(o)), (l2, pin2(lse))],
+                           lambda b: step((q2[b], o2[b], l2[b])), max(3, args.steps), world)
+    ea.attn_status(stream)
     ms, ms_e2e = allmax(world, ms), allmax(world, ms_e2e)
     peaks, src = load_peaks()
     nbytes = decode_bytes(B, Hq, Hkv, d, x["seqlens"], T)
@@ -692,7 +735,8 @@ def run_decode(args, world, rank, local):
                      "peak_source": f"{src} hbm_gbs"},
         "e2e": {"value": round(world * nbytes / (ms_e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": q.numel() * 2, "d2h_bytes_per_step": bytes_io - q.numel() * 2,
-                "ms_per_step": round(ms_e2e, 4)},
+                "ms_per_step": round(ms_e2e, 4),
+                "pipelined": "copies in and out on their own streams, two device buffer sets"},
         "gpu_launches": 3 * args.steps, "clocks": clk,
     }
     if rank == 0:
