@@ -816,7 +816,8 @@ def run_fp8(args, world, rank, local):
     fwd_f = 4.0 * Hq * d * allowed_pairs(cfg)
     fwd_t = fwd_f / (k_fwd * 1e-3) / 1e12
     rows = B * Hq * N + 2 * B * Hkv * N
-    pro_bytes = rows * (2 * 2 * d + d)  # bf16 row read by each of the two passes, e4m3 row written
+    pro_bytes = rows * (2 * d + d)  # algorithmic: every bf16 row read once, its e4m3 row written
+    moved = rows * (2 * 2 * d + d)  # what the two passes move (the amax pass reads every row too)
     pro_gbs = pro_bytes / (k_pro * 1e-3) / 1e9
     line = {
         "metric": f"attention TFLOPS fwd ({name}, e4m3)", "value": round(world * fwd_f / (ms * 1e-3) / 1e12, 2),
@@ -832,6 +833,7 @@ def run_fp8(args, world, rank, local):
                      "peak_source": f"{src} bf16_tflops_sustained x 2 (nominal e4m3/bf16 ratio)"},
         "prologue": {"achieved": round(pro_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(pro_gbs / peaks["hbm_gbs"], 4), "bytes": pro_bytes,
+                     "bytes_moved_two_passes": moved, "moved_gbs": round(moved / (k_pro * 1e-3) / 1e9, 1),
                      "with_rope_ms": round(k_rope, 4),
                      "with_rope_gbs": round(pro_bytes / (k_rope * 1e-3) / 1e9, 1)},
         "e2e": None, "gpu_launches": 4 * args.steps, "clocks": clk,
