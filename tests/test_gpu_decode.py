@@ -116,3 +116,44 @@ def test_decode_bad_table_entry_reports_bounds():
     o, lse = _run(ea, x, None, 0.1)  # clean call afterwards
     O, L = attn64.decode_paged(x["q"], x["k_cache"], x["v_cache"], x["block_table"], x["seqlens"], 0.1)
     assert max_abs(o.float().cpu().numpy(), O) <= O_TOL
+
+
+def _random_case(i):
+    rng = np.random.default_rng(5000 + i)
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 3, 4, 8, 16]))
+    T = int(rng.choice([1, 1, 2, 3, 4]))
+    while G * T > 128:
+        T -= 1
+    B = int(rng.integers(1, 6))
+    n = int(rng.choice([16, 100, 128, 129, 640, 1500]))
+    lens = rng.integers(0, n + 1, size=B)
+    lens[0] = n  # one sequence fills its table row exactly
+    mk = {}
+    if rng.random() < 0.5:
+        mk["window"] = int(rng.choice([1, 37, 128, 4000]))
+    if rng.random() < 0.4:
+        mk["softcap"] = float(rng.choice([5.0, 30.0]))
+    if rng.random() < 0.4:
+        mk["alibi"] = True
+    return B, G * Hkv, Hkv, n, [int(x) for x in lens], mk, T
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_decode_random_shapes(i):
+    """Seeded random shapes: GQA groups x tokens on both sides of the compact
+    layout (8 rows), lengths 0 .. a full table row, every mod combination."""
+    ea = lib()
+    B, Hq, Hkv, n, lens, mk, T = _random_case(i)
+    x = gen.paged_decode_inputs(B, Hq, Hkv, n, 128, seed=7000 + i, lens=lens, q_len=T)
+    s = default_scale(128)
+    o, lse = _run(ea, x, ea.make_mods(**mk), s)
+    O, L = attn64.decode_paged(x["q"], x["k_cache"], x["v_cache"], x["block_table"], x["seqlens"], s,
+                               attn64.Mods(**mk))
+    og, lg = o.float().cpu().numpy(), lse.cpu().numpy()
+    empty = np.isneginf(L)
+    assert np.all(og[empty] == 0.0) and np.all(np.isneginf(lg[empty]))
+    eo, el = max_abs(og[~empty], O[~empty]), max_abs(lg[~empty], L[~empty])
+    record("decode_cases", "O_max_abs", eo)
+    record("decode_cases", "LSE_max_abs", el)
+    assert eo <= O_TOL and el <= LSE_TOL, (B, Hq, Hkv, n, lens, mk, T, eo, el)
