@@ -579,6 +579,8 @@ def run_paged(args, world, rank, local):
 
     name = args.workload
     cfg = dict(gen.WORKLOADS[name])
+    if args.heads:  # smaller case of the same workload (profiling)
+        cfg["Hq"] = cfg["Hkv"] = args.heads
     B, Hq, Hkv, N, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"]
     scale = 1.0 / math.sqrt(d)
     dev = torch.device("cuda", local)
@@ -750,6 +752,8 @@ def run_fp8(args, world, rank, local):
 
     name = args.workload
     cfg = dict(gen.WORKLOADS[name])
+    if args.heads:  # smaller case of the same workload (profiling)
+        cfg["Hq"] = cfg["Hkv"] = args.heads
     B, Hq, Hkv, N, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"]
     scale = 1.0 / math.sqrt(d)
     dev = torch.device("cuda", local)
@@ -829,10 +833,12 @@ def run_fp8(args, world, rank, local):
         "fwd_tflops": round(fwd_t, 1), "fwd_frac_fp8_peak": round(fwd_t / fp8_peak, 4),
         "kernel_ms": {"hadamard_quant": round(k_pro, 4), "fwd_fp8": round(k_fwd, 4)},
         "roofline": {"kernel": "fwd_fp8", "bound": "tensor", "achieved": round(fwd_t, 1), "peak": fp8_peak,
-                     "unit": "TFLOP/s", "frac": round(fwd_t / fp8_peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(fwd_t / fp8_peak, 4),
+                     "traffic": traffic_record("fwd_fp8") if not args.heads else None,
                      "peak_source": f"{src} bf16_tflops_sustained x 2 (nominal e4m3/bf16 ratio)"},
         "prologue": {"achieved": round(pro_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(pro_gbs / peaks["hbm_gbs"], 4), "bytes": pro_bytes,
+                     "traffic": traffic_record("hadamard_quant") if not args.heads else None,
                      "bytes_moved_two_passes": moved, "moved_gbs": round(moved / (k_pro * 1e-3) / 1e9, 1),
                      "with_rope_ms": round(k_rope, 4),
                      "with_rope_gbs": round(pro_bytes / (k_rope * 1e-3) / 1e9, 1)},
@@ -893,7 +899,8 @@ def main():
     ap.add_argument("--batch", type=int, default=0,
                     help="paged decode workloads only: this many sequences instead of the workload's (profiling)")
     ap.add_argument("--heads", type=int, default=0,
-                    help="query heads (8 per KV head) for a smaller profiling case; default: the workload's 64")
+                    help="query heads for a smaller profiling case (8 per KV head; fp8_outliers_16k: as many KV "
+                         "heads); default: the workload's")
     args = ap.parse_args()
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
