@@ -204,8 +204,9 @@ __device__ __forceinline__ void score_mods(uint32_t (&s)[128], const ModsArgs& a
 }
 
 // MODS: soft-cap / ALiBi score mods compiled in; MASKS: window / document
-// masks compiled in (causal and the sequence end always are).
-template <int D, bool MODS, bool FP8, bool MASKS>
+// masks compiled in (causal and the sequence end always are); PAGED: K and V
+// read through a block table.
+template <int D, bool MODS, bool FP8, bool MASKS, bool PAGED>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
@@ -272,32 +273,63 @@ __global__ void __launch_bounds__(384, 1)
         for (int ch = 0; ch < C::CH; ++ch)
           tma_load_3d(smem + C::Q_OFF + t * C::TILE_BYTES + ch * 16384, &tq, &S.q_full, ch * C::BOX,
                       (I0 + t) * TILE, b * p.Hq + hq);
-      int r = 0;
-      auto load = [&](const CUtensorMap* map, int J) -> bool {
-        const int st = r % C::RST;
-        if (!mbar_wait(&S.empty[st], ((r / C::RST) & 1) ^ 1, ab)) return false;
-        mbar_arrive_tx(&S.full[st], C::TILE_BYTES);
-        uint8_t* dst = smem + C::R_OFF + st * C::TILE_BYTES;
-        if (p.block_table == nullptr) {
+    }
+    // Both walks issue K(J0), then per union tile J: K(next J), V(J).  The
+    // last load into each stage completes phase ((loads into it - 1) & 1):
+    // lane 0 waits for all of them before the CTA can exit.
+    int r = 0;
+    auto drain = [&]() {
+      mbar_wait_drain(&S.q_full, 0);
+      for (int s = 0; s < C::RST; ++s)
+        if (r > s) mbar_wait_drain(&S.full[s], ((r - 1 - s) / C::RST) & 1);
+    };
+    if (!PAGED) {
+      // Contiguous K/V: lane 0 issues one box per 64-column chunk of a tile.
+      if (lane == 0) {
+        auto load = [&](const CUtensorMap* map, int J) -> bool {
+          const int st = r % C::RST;
+          if (!mbar_wait(&S.empty[st], ((r / C::RST) & 1) ^ 1, ab)) return false;
+          mbar_arrive_tx(&S.full[st], C::TILE_BYTES);
+          uint8_t* dst = smem + C::R_OFF + st * C::TILE_BYTES;
           for (int ch = 0; ch < C::CH; ++ch)
             tma_load_3d(dst + ch * 16384, map, &S.full[st], ch * C::BOX, J * TILE, b * p.Hkv + hk);
-        } else {
-          // Paged: the tile's 8 blocks of 16 rows, each a 16-row box at its
-          // 2 KB offset (the 128-byte swizzle repeats every 8 rows, so the
-          // layout matches a whole-tile load).  Blocks past the sequence end
-          // use an out-of-range block index: TMA fills them with zeros.
-          int z[TILE / 16];  // all 8 table entries in flight before the first copy
-#pragma unroll
-          for (int sb = 0; sb < TILE / 16; ++sb) {
-            const int lb = J * (TILE / 16) + sb;
-            z[sb] = lb < p.bt_stride ? __ldg(p.block_table + (size_t)b * p.bt_stride + lb) * p.Hkv + hk
-                                     : p.kv_blocks * p.Hkv;
-          }
-#pragma unroll
-          for (int sb = 0; sb < TILE / 16; ++sb)
-            for (int ch = 0; ch < C::CH; ++ch)
-              tma_load_3d(dst + ch * 16384 + sb * 2048, map, &S.full[st], ch * C::BOX, 0, z[sb]);
+          ++r;
+          return true;
+        };
+        int J = union_next(p, b, I0, J_begin, J_end);
+        bool ok = J >= J_end || load(&tk, J);
+        while (ok && J < J_end) {
+          const int Jn = union_next(p, b, I0, J + 1, J_end);
+          if (Jn < J_end && !(ok = load(&tk, Jn))) break;
+          if (!(ok = load(&tv, J))) break;
+          J = Jn;
         }
+        drain();
+      }
+    } else {
+      // Paged K/V: the tile's 8 blocks of 16 rows, each a 16-row box at its 2 KB
+      // offset (the 128-byte swizzle repeats every 8 rows, so the layout
+      // matches a whole-tile load), one box per lane of the warp -- small
+      // boxes cost per box, so one thread issuing all of them would limit the
+      // stream.  Each lane fetches its table entry while lane 0 waits for the
+      // slot.  Blocks past the sequence end use an out-of-range block index:
+      // TMA fills them with zeros.
+      auto load = [&](const CUtensorMap* map, int J) -> bool {
+        const int st = r % C::RST;
+        int z = p.kv_blocks * p.Hkv;
+        if (lane < 8 * C::CH) {
+          const int lb = J * (TILE / 16) + lane / C::CH;
+          if (lb < p.bt_stride) z = __ldg(p.block_table + (size_t)b * p.bt_stride + lb) * p.Hkv + hk;
+        }
+        bool good = true;
+        if (lane == 0) {
+          good = mbar_wait(&S.empty[st], ((r / C::RST) & 1) ^ 1, ab);
+          if (good) mbar_arrive_tx(&S.full[st], C::TILE_BYTES);
+        }
+        if (!__shfl_sync(0xffffffffu, good, 0)) return false;
+        if (lane < 8 * C::CH)
+          tma_load_3d(smem + C::R_OFF + st * C::TILE_BYTES + (lane % C::CH) * 16384 + (lane / C::CH) * 2048, map,
+                      &S.full[st], (lane % C::CH) * C::BOX, 0, z);
         ++r;
         return true;
       };
@@ -309,11 +341,7 @@ __global__ void __launch_bounds__(384, 1)
         if (!(ok = load(&tv, J))) break;
         J = Jn;
       }
-      // Let every copy this thread issued land before the CTA can exit: the
-      // last load into each stage completes phase ((loads into it - 1) & 1).
-      mbar_wait_drain(&S.q_full, 0);
-      for (int s = 0; s < C::RST; ++s)
-        if (r > s) mbar_wait_drain(&S.full[s], ((r - 1 - s) / C::RST) & 1);
+      if (lane == 0) drain();
     }
   } else if (warp == 1 || warp == 2) {
     // ---------------------------------------------------------- MMA issuers
@@ -598,12 +626,12 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool MODS, bool FP8, bool MASKS>
+template <int D, bool MODS, bool FP8, bool MASKS, bool PAGED = false>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 void* o, float* lse, const float* scales, const AttnParams& p,
                                 cudaStream_t st) {
   using C = FwdCfg<D, FP8>;
-  auto kern = fwd_kernel<D, MODS, FP8, MASKS>;
+  auto kern = fwd_kernel<D, MODS, FP8, MASKS, PAGED>;
   // The register split inside the kernel assumes exactly LAUNCH_REGS per
   // thread at launch; refuse to launch any other build of it.
   static int regs = -1;
@@ -622,8 +650,14 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 
 cudaError_t launch_fwd_bf16(const FwdLaunch& L, int d, bool mods, bool masks, cudaStream_t st) {
 #define ATTN_FWD(DD, MO, MA) launch_fwd_t<DD, MO, false, MA>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st)
+#define ATTN_FWDP(MO, MA) launch_fwd_t<128, MO, false, MA, true>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st)
+  if (L.p.block_table != nullptr) {  // paged K/V: d = 128 only
+    if (d != 128) return cudaErrorInvalidValue;
+    return mods ? ATTN_FWDP(true, true) : masks ? ATTN_FWDP(false, true) : ATTN_FWDP(false, false);
+  }
   if (d == 128) return mods ? ATTN_FWD(128, true, true) : masks ? ATTN_FWD(128, false, true) : ATTN_FWD(128, false, false);
   return mods ? ATTN_FWD(64, true, true) : masks ? ATTN_FWD(64, false, true) : ATTN_FWD(64, false, false);
+#undef ATTN_FWDP
 #undef ATTN_FWD
 }
 
