@@ -65,10 +65,11 @@ __device__ __forceinline__ Raw16 load16(const QuantTensors& t, int ti, long long
 // This lane's 16 values of the row: RoPE (when on), then the signed
 // Walsh-Hadamard transform without its 1 / sqrt(128) (Q and K with signs), or
 // the plain values.  Every lane of the warp must call it (warp shuffles).
+template <bool ROPE>
 __device__ __forceinline__ void transform16(const QuantTensors& t, int ti, long long row, int l8, const Raw16& raw,
                                             const float (&inv_freq)[16], float (&v)[16]) {
   const uint32_t w[8] = {raw.a.x, raw.a.y, raw.a.z, raw.a.w, raw.b.x, raw.b.y, raw.b.z, raw.b.w};
-  if (ti == 2 || (t.rope_k == 0.f && t.signs == nullptr)) {
+  if (ti == 2 || (!ROPE && t.signs == nullptr)) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       v[2 * k] = bf16lo_f32(w[k]);
@@ -86,7 +87,7 @@ __device__ __forceinline__ void transform16(const QuantTensors& t, int ti, long 
     sgn[2] = sg.z;
     sgn[3] = sg.w;
   }
-  if (t.rope_k != 0.f) {  // RoPE first (before the signs), rotate-half pairs (c, c + 64)
+  if (ROPE) {  // RoPE first (before the signs), rotate-half pairs (c, c + 64)
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       v[2 * k] = bf16lo_f32(w[k]);
@@ -198,12 +199,13 @@ __device__ __forceinline__ void load_group(const QuantTensors& t, const Group& g
 }
 
 // Pass 1 (WRITE false): amax of every (batch, head).  Pass 2 (WRITE true):
-// e4m3 codes scaled by 448 / amax.
-template <bool WRITE>
+// e4m3 codes scaled by 448 / amax.  ROPE: rotary embedding in front (its 16
+// inverse frequencies per lane are only kept in registers when it is on).
+template <bool WRITE, bool ROPE>
 __global__ void __launch_bounds__(256) quant_pass_kernel(const QuantTensors t) {
   const int lane = lane_id(), l8 = lane & 7, q = lane >> 3;
   float inv_freq[16];
-  rope_freqs(t, l8, inv_freq);
+  if (ROPE) rope_freqs(t, l8, inv_freq);
   const long long stride = (long long)gridDim.x * 8;
   long long gi = (long long)blockIdx.x * 8 + warp_id();
   Group cur;
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(256) quant_pass_kernel(const QuantTensors t) {
       const long long row_raw = cur.r0 + 4 * s + q;
       const long long row = min(row_raw, cur.r1 - 1);
       float v[16];
-      transform16(t, ti, row, l8, raw[s], inv_freq, v);
+      transform16<ROPE>(t, ti, row, l8, raw[s], inv_freq, v);
       if (WRITE) {
         if (row_raw >= cur.r1) continue;
         const float a = __uint_as_float(t.amax[ti][row / t.N]);
@@ -303,11 +305,12 @@ cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, v
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   // Two 8-warp blocks per SM stay resident (register-limited); each warp walks many groups.
   const long long blocks = min((groups + 7) / 8, (long long)sms * 2);
-  quant_pass_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(t);
+  const bool rope = t.rope_k != 0.f;
+  (rope ? quant_pass_kernel<false, true> : quant_pass_kernel<false, false>)<<<(unsigned)blocks, 256, 0, st>>>(t);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   quant_scale_kernel<<<dim3(1, 3), 256, 0, st>>>(t, B);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  quant_pass_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(t);
+  (rope ? quant_pass_kernel<true, true> : quant_pass_kernel<true, false>)<<<(unsigned)blocks, 256, 0, st>>>(t);
   return cudaGetLastError();
 }
 
