@@ -157,12 +157,25 @@ def barrier(world):
 
 
 def allmax(world, x: float) -> float:
+    """Largest of the ranks' values (the slowest replica's time sets the step)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_seed(cfg, rank: int) -> int:
+    """Each replica draws its own inputs (replicas do not repeat one another's work)."""
+    return cfg["seed"] + 97 * rank
+
+
+def job_throughput(world: int, work_per_rank: float, max_ms: float) -> float:
+    """Whole-job throughput of weak-scaled replicas: every rank does the same work per
+    step, and the step lasts as long as the slowest rank (per second)."""
+    return world * work_per_rank / (max_ms * 1e-3)
 
 
 # ------------------------------------------------------- oracle baseline ----
@@ -329,7 +342,7 @@ def run_ours(args, world, rank, local):
     scale = 1.0 / math.sqrt(d)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    x = gen.make_inputs(**dict(cfg, seed=cfg["seed"] + 97 * rank))
+    x = gen.make_inputs(**dict(cfg, seed=replica_seed(cfg, rank)))
     host = {k: x[k].pin_memory() for k in ("q", "k", "v", "do")}
     q, k, v, do = (host[n].to(dev) for n in ("q", "k", "v", "do"))
     o = torch.empty_like(q)
@@ -427,7 +440,7 @@ def run_ours(args, world, rank, local):
     if fwd_only:
         bwd_f = 0.0
     ms = total_ms / args.steps
-    value = world * (fwd_f + bwd_f) / (ms * 1e-3) / 1e12
+    value = job_throughput(world, fwd_f + bwd_f, ms) / 1e12
     peaks, src = load_peaks()
     sustained = peaks["bf16_tflops_sustained"]
     burst = peaks["bf16_tflops"]
@@ -471,7 +484,7 @@ def run_ours(args, world, rank, local):
         "kernel_ms": {n: round(t, 4) for n, (t, _) in kernels.items()},
         "roofline": roofline,
         "e2e": None if not e2e_steps else {
-            "value": round(world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "value": round(job_throughput(world, fwd_f + bwd_f, e2e_ms) / 1e12, 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
             "pipelined": "copies in and out on their own streams, two device buffer sets"},
         "gpu_launches": launches * args.steps,
@@ -496,7 +509,7 @@ def run_varlen(args, world, rank, local):
     scale = 1.0 / math.sqrt(d)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    x = gen.make_inputs(**dict(cfg, seed=cfg["seed"] + 97 * rank))
+    x = gen.make_inputs(**dict(cfg, seed=replica_seed(cfg, rank)))
     ids = x["doc_ids"][0]
     cu = np.concatenate([[0], np.cumsum(np.bincount(ids))]).astype(np.int32)
     n_seqs = len(cu) - 1
@@ -585,7 +598,7 @@ def run_paged(args, world, rank, local):
     scale = 1.0 / math.sqrt(d)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    x = gen.make_inputs(**dict(cfg, seed=cfg["seed"] + 97 * rank, need_do=False))
+    x = gen.make_inputs(**dict(cfg, seed=replica_seed(cfg, rank), need_do=False))
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     nb = N // 16
     num_blocks = B * nb
@@ -669,7 +682,7 @@ def run_decode(args, world, rank, local):
     scale = 1.0 / math.sqrt(d)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    x = gen.paged_decode_inputs(**dict(cfg, seed=cfg["seed"] + 97 * rank))
+    x = gen.paged_decode_inputs(**dict(cfg, seed=replica_seed(cfg, rank)))
     q_host = x["q"].pin_memory()
     q = q_host.to(dev)
     kc, vc = x["k_cache"].to(dev), x["v_cache"].to(dev)
@@ -758,7 +771,7 @@ def run_fp8(args, world, rank, local):
     scale = 1.0 / math.sqrt(d)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    x = gen.make_inputs(**dict(cfg, seed=cfg["seed"] + 97 * rank, need_do=False))
+    x = gen.make_inputs(**dict(cfg, seed=replica_seed(cfg, rank), need_do=False))
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     signs = torch.from_numpy(gen.hadamard_signs(Hkv, d, cfg["seed"] + 20)).to(dev)
     q8 = torch.empty(q.shape, dtype=torch.uint8, device=dev)
