@@ -14,7 +14,7 @@ Prints ONE JSON line (rank 0); the default workload is the one the metric is
 quoted on, the others are the smaller parity workloads timed the same way
 (tiny_mha: forward only; fp8_outliers_16k: Hadamard + e4m3 prologue and the
 e4m3 forward).  ``--impl reference`` times the fp64 CPU
-oracle (the reference arm of this build) on bounded row slices of the same
+oracle (the reference arm) on bounded row slices of the same
 workload.  Under torchrun each rank runs an independent replica (weak
 scaling, no data-path collective; the process group only carries the
 timing barrier and max).
