@@ -268,18 +268,19 @@ DecodeSplit decode_split(int B, int Hkv, int N) {
   return {(int)ct, (int)((tiles + ct - 1) / ct)};
 }
 size_t decode_info_bytes(int B) { return round_up((size_t)B * sizeof(int4), 256) + 256; }
-size_t decode_ws_bytes(int B, int Hq, int Hkv, int T, int N) {
+size_t decode_ws_bytes(int B, int Hq, int Hkv, int T, int N, int d) {
   const size_t rows = (size_t)B * Hq * T * decode_split(B, Hkv, N).max_chunks;
-  return decode_info_bytes(B) + round_up(rows * 128 * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
+  return decode_info_bytes(B) + round_up(rows * d * sizeof(float), 256) + round_up(rows * sizeof(float), 256);
 }
 attn_status_t check_decode(int B, int Hq, int Hkv, int T, int N, int num_blocks, int d, const attn_mods_t* mods) {
   if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || N < 16 || num_blocks < 1) return ATTN_ERR_INVALID_ARG;
-  if (N % 16 != 0 || Hq % Hkv != 0 || (long long)(Hq / Hkv) * T > 128 || d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (N % 16 != 0 || Hq % Hkv != 0 || (long long)(Hq / Hkv) * T > 128 || (d != 64 && d != 128))
+    return ATTN_ERR_UNSUPPORTED;
   if ((long long)num_blocks * Hkv >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   attn_status_t st;
   if ((st = check_mods(mods)) != ATTN_OK) return st;
   if (mods && (mods->flags & ATTN_MOD_DOC)) return ATTN_ERR_UNSUPPORTED;
-  if ((long long)B * Hq * T * decode_split(B, Hkv, N).max_chunks * 128 >= (1ll << 40)) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * Hq * T * decode_split(B, Hkv, N).max_chunks * d >= (1ll << 40)) return ATTN_ERR_UNSUPPORTED;
   if ((long long)B * Hq * T >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   if ((long long)B * Hkv * decode_split(B, Hkv, N).max_chunks >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
@@ -483,7 +484,6 @@ attn_status_t attn_fwd_paged(const void* q, const void* k_cache, const void* v_c
                              void* ws, size_t ws_bytes, void* stream) {
   attn_status_t st;
   if ((st = check_shape(B, Hq, Hkv, N, d, false)) != ATTN_OK) return st;
-  if (d != 128) return ATTN_ERR_UNSUPPORTED;
   if ((st = check_tensors({q, k_cache, v_cache, o})) != ATTN_OK) return st;
   if (lse == nullptr || block_table == nullptr || num_blocks < 1) return ATTN_ERR_INVALID_ARG;
   if (!aligned(lse, 4) || !aligned(block_table, 4)) return ATTN_ERR_UNSUPPORTED;
@@ -516,7 +516,7 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int q_len, int max_blo
                                   const attn_mods_t* mods) {
   if (max_blocks < 1 || max_blocks > (1 << 26)) return 0;
   const int N = 16 * max_blocks;
-  return check_decode(B, Hq, Hkv, q_len, N, 1, d, mods) == ATTN_OK ? decode_ws_bytes(B, Hq, Hkv, q_len, N) : 0;
+  return check_decode(B, Hq, Hkv, q_len, N, 1, d, mods) == ATTN_OK ? decode_ws_bytes(B, Hq, Hkv, q_len, N, d) : 0;
 }
 
 attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
@@ -532,7 +532,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   if (lse == nullptr || block_table == nullptr || seqlens == nullptr) return ATTN_ERR_INVALID_ARG;
   if (!aligned(lse, 4) || !aligned(block_table, 4) || !aligned(seqlens, 4)) return ATTN_ERR_UNSUPPORTED;
   if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-  if ((st = check_ws(ws, ws_bytes, decode_ws_bytes(B, Hq, Hkv, q_len, N))) != ATTN_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, decode_ws_bytes(B, Hq, Hkv, q_len, N, d))) != ATTN_OK) return st;
   int* status = nullptr;
   if ((st = device_state(&status)) != ATTN_OK) return st;
   const int sms = sm_count();
@@ -566,6 +566,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   p.Hkv = Hkv;
   p.G = G;
   p.q_len = q_len;
+  p.d = d;
   p.bt_stride = max_blocks;
   p.kv_blocks = num_blocks;
   p.ct = sp.ct;
@@ -584,7 +585,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   p.n_items = reinterpret_cast<int*>(w + decode_info_bytes(B) - 256);
   const size_t rows = (size_t)B * Hq * q_len * sp.max_chunks;
   p.o_part = reinterpret_cast<float*>(w + decode_info_bytes(B));
-  p.lse_part = reinterpret_cast<float*>(w + decode_info_bytes(B) + round_up(rows * 128 * sizeof(float), 256));
+  p.lse_part = reinterpret_cast<float*>(w + decode_info_bytes(B) + round_up(rows * d * sizeof(float), 256));
   p.status = status;
   const long long items = (long long)B * Hkv * sp.max_chunks;
   L.grid = (int)(items < sms ? items : sms);

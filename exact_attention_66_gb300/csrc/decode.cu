@@ -40,9 +40,7 @@ namespace attn {
 
 namespace {
 
-constexpr int DEC_D = 128;
 constexpr int DEC_THREADS = 256;
-constexpr int DEC_TB = TILE * DEC_D * 2;  // one bf16 K or V tile of 128 rows (32 KB)
 
 // Shared-memory layout.  The MMAs read Q and P as 128-row tiles, of which only
 // the R = G T rows of the query heads and tokens matter.  With R <= 8 (SMALL) a Q or P tile is
@@ -50,22 +48,27 @@ constexpr int DEC_TB = TILE * DEC_D * 2;  // one bf16 K or V tile of 128 rows (3
 // descriptor's stride between 8-row groups is 0, so its other fifteen groups
 // re-read the same eight rows (the S and O rows they produce are never read);
 // the room saved goes to deeper K and V rings, i.e. more bytes in flight.
-template <bool SMALL>
+template <int D, bool SMALL>
 struct DecCfg {
-  static constexpr int QCH = SMALL ? 1024 : 16384;      // one 64-column half of a Q / P tile
-  static constexpr int QTB = 2 * QCH;                   // one Q / P tile
+  static constexpr int CH = D / 64;                     // 64-column chunks of a Q / K / V row
+  static constexpr int TB = TILE * D * 2;               // one bf16 K or V tile of 128 rows
+  static constexpr int QCH = SMALL ? 1024 : 16384;      // one 64-column chunk of a Q / P tile
+  static constexpr int QTB = CH * QCH;                  // one Q tile
+  static constexpr int PTB = 2 * QCH;                   // the P tile (128 keys)
   static constexpr uint32_t QSBO = SMALL ? 0u : 1024u;  // MMA stride between 8-row groups
-  static constexpr int KS = SMALL ? 3 : 2, VS = SMALL ? 3 : 2;  // K ring and V ring slots
+  // K ring and V ring slots (shared memory left after Q and P; twice as many
+  // of the half-size tiles of d = 64)
+  static constexpr int KS = (SMALL ? 3 : 2) * (D == 64 ? 2 : 1), VS = KS;
   static constexpr int Q_OFF = 0;                       // two Q tiles (item parity)
   static constexpr int P_OFF = 2 * QTB;
-  static constexpr int K_OFF = 3 * QTB;
-  static constexpr int V_OFF = K_OFF + KS * DEC_TB;
-  static constexpr int BAR_OFF = V_OFF + VS * DEC_TB;
-  static constexpr int SMEM = smem_one_cta(BAR_OFF + 256 + 1024);
+  static constexpr int K_OFF = P_OFF + PTB;
+  static constexpr int V_OFF = K_OFF + KS * TB;
+  static constexpr int BAR_OFF = V_OFF + VS * TB;
+  static constexpr int SMEM = smem_one_cta(BAR_OFF + 512 + 1024);
+  static_assert(SMEM <= 232448, "decode shared memory exceeds 227 KB");
+  static_assert(K_OFF % 1024 == 0, "swizzled tiles need 1 KB alignment");
 };
-static_assert(DecCfg<true>::SMEM <= 232448 && DecCfg<false>::SMEM <= 232448, "decode shared memory exceeds 227 KB");
-static_assert(DecCfg<true>::K_OFF % 1024 == 0 && DecCfg<false>::K_OFF % 1024 == 0, "swizzled tiles need 1 KB alignment");
-constexpr int DEC_MAX_SLOTS = 3;
+constexpr int DEC_MAX_SLOTS = 6;
 
 struct DecBars {
   uint64_t q_full[2], q_empty[2];        // Q tile of an item (TMA) / its last S done (commit)
@@ -78,7 +81,7 @@ struct DecBars {
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(DecBars) <= 256, "decode barrier block");
+static_assert(sizeof(DecBars) <= 512, "decode barrier block");
 
 // Sequence b's length, first key tile and number of chunks.  A length outside
 // [0, 16 * bt_stride] is reported and the sequence treated as empty.
@@ -203,23 +206,23 @@ struct DecWalker {
 };
 
 // S(tmem, 128 x 128 fp32) = Q K^T: Q and K K-major 128-byte swizzled bf16
-// tiles of 256-byte rows, K as two 16 KB column halves, Q in the layout of C.
+// tiles of D columns, K as 16 KB 64-column chunks, Q in the layout of C.
 template <typename C>
 __device__ __forceinline__ void dec_issue_s(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
   constexpr uint32_t id = idesc_bf16(128, 128, false, false);
   const uint64_t ad = opaque(sdesc_sw128(q_smem, 16, C::QSBO)), bd = opaque(sdesc_sw128(k_smem, 16, 1024));
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
+  for (int kk = 0; kk < C::CH * 4; ++kk) {
     const uint32_t step = (kk % 4) * 32;
     mma_f16_ss(d_tmem, sdesc_add(ad, (kk / 4) * C::QCH + step), sdesc_add(bd, (kk / 4) * 16384 + step), id,
                kk > 0 ? 1u : 0u);
   }
 }
 
-// O(tmem) (+)= P V: P K-major (128 keys, layout of C), V MN-major (128 keys x 128).
+// O(tmem) (+)= P V: P K-major (128 keys, layout of C), V MN-major (128 keys x D).
 template <typename C>
 __device__ __forceinline__ void dec_issue_pv(uint32_t o_tmem, uint32_t p_smem, uint32_t v_smem, bool first) {
-  constexpr uint32_t id = idesc_bf16(128, 128, false, true);
+  constexpr uint32_t id = idesc_bf16(128, C::CH * 64, false, true);
   const uint64_t pd = opaque(sdesc_sw128(p_smem, 16, C::QSBO)), vd = opaque(sdesc_sw128(v_smem, 16384, 1024));
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
@@ -230,11 +233,11 @@ __device__ __forceinline__ void dec_issue_pv(uint32_t o_tmem, uint32_t p_smem, u
 
 // MODS: soft-cap / ALiBi compiled in (the window is a column interval and
 // runs in both variants); SMALL: at most 8 query heads per KV head.
-template <bool MODS, bool SMALL>
+template <int D, bool MODS, bool SMALL>
 __global__ void __launch_bounds__(DEC_THREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const DecodeParams p) {
-  using C = DecCfg<SMALL>;
+  using C = DecCfg<D, SMALL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   DecBars& S = *reinterpret_cast<DecBars*>(smem + C::BAR_OFF);
@@ -245,7 +248,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   const int nsw = (R + 31) / 32;  // softmax warps (4 .. 3 + nsw): one thread per row
 
   // Rows >= R of the Q tiles never receive data: zero them (and P) once.
-  for (int g = threadIdx.x; g < 3 * C::QTB / 16; g += DEC_THREADS) {
+  for (int g = threadIdx.x; g < (2 * C::QTB + C::PTB) / 16; g += DEC_THREADS) {
     const int row = ((g * 16) % C::QCH) / 128;
     if (g * 16 >= 2 * C::QTB || row >= R)
       *reinterpret_cast<uint4*>(smem + g * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -311,8 +314,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     auto lookup = [&](const DecTile& t, int& z, bool& bad) {
       z = p.kv_blocks * p.Hkv;
       bad = false;
-      if (lane < 16) {
-        const int lb = t.J * (TILE / 16) + (lane >> 1);
+      if (lane < 8 * C::CH) {
+        const int lb = t.J * (TILE / 16) + lane / C::CH;
         if (lb * 16 < t.L) {
           const int e = __ldg(p.block_table + (size_t)t.b * p.bt_stride + lb);
           bad = e < 0 || e >= p.kv_blocks;
@@ -331,8 +334,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         if (lane == 0) {
           ok = t.item < 2 || mbar_wait(&S.q_empty[qb], ((t.item >> 1) - 1) & 1, ab);
           if (ok) {
-            mbar_arrive_tx(&S.q_full[qb], 2 * R * 128);
-            for (int ch = 0; ch < 2; ++ch)
+            mbar_arrive_tx(&S.q_full[qb], C::CH * R * 128);
+            for (int ch = 0; ch < C::CH; ++ch)
               tma_load_3d(smem + C::Q_OFF + qb * C::QTB + ch * C::QCH, &tq, &S.q_full[qb], ch * 64, 0,
                           t.b * p.Hkv + t.hk);
           }
@@ -348,10 +351,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         ok = false;
         break;
       }
-      if (lane == 0) mbar_arrive_tx(&full[st], DEC_TB);
+      if (lane == 0) mbar_arrive_tx(&full[st], C::TB);
       __syncwarp();
-      if (lane < 16)
-        tma_load_3d(ring + st * DEC_TB + (lane & 1) * 16384 + (lane >> 1) * 2048, map, &full[st], (lane & 1) * 64, 0, z);
+      if (lane < 8 * C::CH)
+        tma_load_3d(ring + st * C::TB + (lane % C::CH) * 16384 + (lane / C::CH) * 2048, map, &full[st],
+                    (lane % C::CH) * 64, 0, z);
       ++r;
       have = w.next(p, tn);
       if (have) {
@@ -392,7 +396,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         if (t.first && !mbar_wait(&S.q_full[qb], (t.item >> 1) & 1, ab)) return false;
         if (ns >= 2 && !mbar_wait(&S.s_free[ns & 1], ((ns >> 1) - 1) & 1, ab)) return false;
         tc_fence_after();
-        dec_issue_s<C>(tmem + (uint32_t)(ns & 1) * 128, sQ + qb * C::QTB, sK + ks * DEC_TB);
+        dec_issue_s<C>(tmem + (uint32_t)(ns & 1) * 128, sQ + qb * C::QTB, sK + ks * C::TB);
         mma_commit(&S.s_full[ns & 1]);
         mma_commit(&S.kempty[ks]);
         if (t.last) mma_commit(&S.q_empty[qb]);
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             !(ok = mbar_wait(&S.o_free[cur.item & 1], ((cur.item >> 1) - 1) & 1, ab)))
           break;
         tc_fence_after();
-        dec_issue_pv<C>(tmem + 256 + (uint32_t)(cur.item & 1) * 128, sP, sV + vs * DEC_TB, cur.first);
+        dec_issue_pv<C>(tmem + 256 + (uint32_t)(cur.item & 1) * 128, sP, sV + vs * C::TB, cur.first);
         mma_commit(&S.o_full);
         mma_commit(&S.vempty[vs]);
         ++npv;
@@ -452,10 +456,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     Pending pend{false, 0, 0u, 0.f, 0.f};
     auto epilogue = [&](const Pending& e) {
       const float inv = e.l > 0.f ? 1.0f / e.l : 0.f;
-      float4* dst = reinterpret_cast<float4*>(p.o_part + e.prow * DEC_D);
+      float4* dst = reinterpret_cast<float4*>(p.o_part + e.prow * D);
       const uint32_t tO = tO0 + (uint32_t)e.buf * 128;
 #pragma unroll
-      for (int q4 = 0; q4 < DEC_D / 32; ++q4) {
+      for (int q4 = 0; q4 < D / 32; ++q4) {
         uint32_t ov[32];
         tmem_ld32(tO + q4 * 32, ov);
         tmem_wait_ld(ov);
@@ -560,7 +564,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         if (!t.first && __any_sync(0xffffffffu, need)) {
           const uint32_t tO = tO0 + (uint32_t)(t.item & 1) * 128;
 #pragma unroll
-          for (int q4 = 0; q4 < DEC_D / 32; ++q4) {
+          for (int q4 = 0; q4 < D / 32; ++q4) {
             uint32_t ov[32];
             tmem_ld32(tO + q4 * 32, ov);
             tmem_wait_ld(ov);
@@ -612,8 +616,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
 // accumulates four output columns over the chunks, DEC_MERGE chunks' loads in
 // flight at a time (one round for the usual chunk counts).
 constexpr int DEC_MERGE = 16;
+template <int D>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p, __nv_bfloat16* __restrict__ o,
                                                              float* __restrict__ lse) {
+  constexpr int NV = D / 64;  // float2 pairs of output columns per lane (D / 32 columns)
   pdl_wait();  // the partial results come from the main kernel
   const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
@@ -621,38 +627,42 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   const int b = gw / (p.Hq * p.q_len);
   const int n = p.seq_info[b].z;
   const float* lp = p.lse_part + (size_t)gw * p.max_chunks;
-  const float4* op = reinterpret_cast<const float4*>(p.o_part + (size_t)gw * p.max_chunks * DEC_D);
+  const float2* op = reinterpret_cast<const float2*>(p.o_part + (size_t)gw * p.max_chunks * D) + lane * NV;
   float M = -INFINITY;
   for (int c = lane; c < n; c += 32) M = fmaxf(M, lp[c]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float W = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float2 acc[NV];
+#pragma unroll
+  for (int j = 0; j < NV; ++j) acc[j] = make_float2(0.f, 0.f);
   if (M != -INFINITY) {
     for (int c0 = 0; c0 < n; c0 += DEC_MERGE) {
       const float wl = (lane < DEC_MERGE && c0 + lane < n) ? exp2f(lp[c0 + lane] - M) : 0.f;
       W += wl;
-      float4 v[DEC_MERGE];
+      float2 v[DEC_MERGE][NV];
 #pragma unroll
       for (int u = 0; u < DEC_MERGE; ++u)
-        v[u] = c0 + u < n ? op[(size_t)(c0 + u) * (DEC_D / 4) + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+          v[u][j] = c0 + u < n ? op[(size_t)(c0 + u) * (D / 2) + j] : make_float2(0.f, 0.f);
 #pragma unroll
       for (int u = 0; u < DEC_MERGE; ++u) {
         const float wc = __shfl_sync(0xffffffffu, wl, u);
-        acc.x += wc * v[u].x;
-        acc.y += wc * v[u].y;
-        acc.z += wc * v[u].z;
-        acc.w += wc * v[u].w;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          acc[j].x += wc * v[u][j].x;
+          acc[j].y += wc * v[u][j].y;
+        }
       }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
   }
   const float inv = W > 0.f ? 1.0f / W : 0.f;
-  uint2 pk;
-  pk.x = pack_bf16(acc.x * inv, acc.y * inv);
-  pk.y = pack_bf16(acc.z * inv, acc.w * inv);
-  reinterpret_cast<uint2*>(o + (size_t)gw * DEC_D)[lane] = pk;
+  uint32_t* orow = reinterpret_cast<uint32_t*>(o + (size_t)gw * D) + lane * NV;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) orow[j] = pack_bf16(acc[j].x * inv, acc[j].y * inv);
   if (lane == 0) lse[gw] = W > 0.f ? (M + log2f(W)) * LN2 : -INFINITY;
 }
 
@@ -677,20 +687,26 @@ static cudaError_t launch_pdl(void (*kern)(Args...), unsigned grid, unsigned thr
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-cudaError_t launch_decode(const DecodeLaunch& L, bool mods, cudaStream_t st) {
-  decode_setup_kernel<<<1, 1024, 0, st>>>(L.p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+template <int D>
+static cudaError_t launch_decode_d(const DecodeLaunch& L, bool mods, cudaStream_t st) {
   const bool small = L.p.G * L.p.q_len <= 8;
-  auto kern = mods ? (small ? decode_kernel<true, true> : decode_kernel<true, false>)
-                   : (small ? decode_kernel<false, true> : decode_kernel<false, false>);
-  const int smem = small ? DecCfg<true>::SMEM : DecCfg<false>::SMEM;
+  auto kern = mods ? (small ? decode_kernel<D, true, true> : decode_kernel<D, true, false>)
+                   : (small ? decode_kernel<D, false, true> : decode_kernel<D, false, false>);
+  const int smem = small ? DecCfg<D, true>::SMEM : DecCfg<D, false>::SMEM;
+  cudaError_t e;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
   if ((e = launch_pdl(kern, (unsigned)L.grid, DEC_THREADS, (size_t)smem, st, L.tq, L.tk, L.tv, L.p)) != cudaSuccess)
     return e;
   const long long warps = (long long)L.p.B * L.p.Hq * L.p.q_len;
-  return launch_pdl(decode_combine_kernel, (unsigned)((warps + 7) / 8), 256u, 0, st, L.p, (__nv_bfloat16*)L.o,
+  return launch_pdl(decode_combine_kernel<D>, (unsigned)((warps + 7) / 8), 256u, 0, st, L.p, (__nv_bfloat16*)L.o,
                     L.lse);
+}
+
+cudaError_t launch_decode(const DecodeLaunch& L, bool mods, cudaStream_t st) {
+  decode_setup_kernel<<<1, 1024, 0, st>>>(L.p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return L.p.d == 64 ? launch_decode_d<64>(L, mods, st) : launch_decode_d<128>(L, mods, st);
 }
 
 }  // namespace attn

@@ -650,10 +650,11 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
 
 cudaError_t launch_fwd_bf16(const FwdLaunch& L, int d, bool mods, bool masks, cudaStream_t st) {
 #define ATTN_FWD(DD, MO, MA) launch_fwd_t<DD, MO, false, MA>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st)
-#define ATTN_FWDP(MO, MA) launch_fwd_t<128, MO, false, MA, true>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st)
-  if (L.p.block_table != nullptr) {  // paged K/V: d = 128 only
-    if (d != 128) return cudaErrorInvalidValue;
-    return mods ? ATTN_FWDP(true, true) : masks ? ATTN_FWDP(false, true) : ATTN_FWDP(false, false);
+#define ATTN_FWDP(DD, MO, MA) launch_fwd_t<DD, MO, false, MA, true>(L.tq, L.tk, L.tv, L.o, L.lse, nullptr, L.p, st)
+  if (L.p.block_table != nullptr) {  // paged K/V
+    if (d == 128)
+      return mods ? ATTN_FWDP(128, true, true) : masks ? ATTN_FWDP(128, false, true) : ATTN_FWDP(128, false, false);
+    return mods ? ATTN_FWDP(64, true, true) : masks ? ATTN_FWDP(64, false, true) : ATTN_FWDP(64, false, false);
   }
   if (d == 128) return mods ? ATTN_FWD(128, true, true) : masks ? ATTN_FWD(128, false, true) : ATTN_FWD(128, false, false);
   return mods ? ATTN_FWD(64, true, true) : masks ? ATTN_FWD(64, false, true) : ATTN_FWD(64, false, false);

@@ -39,10 +39,11 @@ struct BwdLaunch {
 };
 cudaError_t launch_bwd(const BwdLaunch& L, int d, bool mods, bool masks, cudaStream_t st);
 
-// Decode step over a paged K/V cache (d = 128): q_len new tokens per sequence.
+// Decode step over a paged K/V cache (d = 64 or 128): q_len new tokens per sequence.
 struct DecodeParams {
   int B, Hq, Hkv, G;       // G = Hq / Hkv query heads per KV head
   int q_len;               // new tokens per sequence (G * q_len <= 128)
+  int d;                   // head dimension: 64 or 128
   int bt_stride;           // block-table row length (blocks per sequence at most)
   int kv_blocks;           // cache blocks
   int ct;                  // key tiles of 128 per work item (chunk)
@@ -56,14 +57,14 @@ struct DecodeParams {
   const int* seqlens;      // [B] cached tokens, the new ones the last q_len
   int4* seq_info;          // [B] workspace: {L, first key tile, chunks, first item}
   int* n_items;            // workspace: number of items
-  float* o_part;           // [B, Hq, q_len, max_chunks, 128] workspace: O / l of each chunk
+  float* o_part;           // [B, Hq, q_len, max_chunks, d] workspace: O / l of each chunk
   float* lse_part;         // [B, Hq, q_len, max_chunks] workspace: log2-sum-exp of each chunk
   int* status;             // device status word
 };
 struct DecodeLaunch {
-  CUtensorMap tq;      // Q as [B*Hkv, G*q_len, 128]: box of G*q_len rows x 64 columns
-  CUtensorMap tk, tv;  // cache [kv_blocks*Hkv, 16, 128]: 16-row boxes
-  void* o;             // bf16 [B, Hq, q_len, 128]
+  CUtensorMap tq;      // Q as [B*Hkv, G*q_len, d]: box of G*q_len rows x 64 columns
+  CUtensorMap tk, tv;  // cache [kv_blocks*Hkv, 16, d]: 16-row boxes
+  void* o;             // bf16 [B, Hq, q_len, d]
   float* lse;          // [B, Hq, q_len]
   int grid;            // persistent CTAs
   DecodeParams p;

@@ -198,7 +198,7 @@ attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, cons
  * block_table      : device int32 [B, N / 16]: key rows [16 t, 16 t + 16) of
  *                    batch row b are block block_table[b][t]; an index outside
  *                    [0, num_blocks) reads zeros.
- * N must be a multiple of 16 and d = 128 (ATTN_ERR_UNSUPPORTED otherwise);
+ * N must be a multiple of 16 (ATTN_ERR_UNSUPPORTED otherwise); d = 64 or 128;
  * workspace as attn_fwd (ATTN_OP_FWD).
  */
 attn_status_t attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache,
@@ -231,7 +231,7 @@ attn_status_t attn_fwd_paged(const void* q, const void* k_cache, const void* v_c
  *               in attn_fwd; DOC is ATTN_ERR_UNSUPPORTED.
  * ws          : attn_decode_workspace_size(B, Hq, Hkv, q_len, max_blocks, d,
  *               mods) bytes: per-chunk partial outputs.
- * Requirements: d = 128, Hq % Hkv == 0, (Hq / Hkv) * q_len <= 128 (else
+ * Requirements: d = 64 or 128, Hq % Hkv == 0, (Hq / Hkv) * q_len <= 128 (else
  * ATTN_ERR_UNSUPPORTED).  Device-side: a length outside [0, 16 * max_blocks]
  * or a table entry outside [0, num_blocks) is reported as ATTN_ERR_BOUNDS by
  * attn_status (the call then leaves O and LSE unspecified).

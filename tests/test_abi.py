@@ -153,7 +153,8 @@ def test_paged_forward_validates(L):
     assert fp(nb=0) == 1
     assert fp(q=None) == 1
     assert fp(N=120) == 2      # N must be a multiple of 16
-    assert fp(d=64) == 2       # d = 128 only
+    assert fp(d=96) == 2       # d = 64 or 128
+    assert fp(d=64) in (4, 5)  # valid: stops at the device check (no GPU here)
     assert fp(table=A + 2) == 2
 
 
@@ -167,7 +168,7 @@ def test_decode_validates(L):
     for kw in (dict(table=None), dict(sl=None), dict(lse=None), dict(q=None), dict(mb=0), dict(nb=0),
                dict(B=0), dict(Hq=0), dict(T=0), dict(scale=float("nan")), dict(scale=0.0)):
         assert dc(**kw) == 1, kw
-    for kw in (dict(d=64), dict(Hq=3, Hkv=2), dict(Hq=129 * 2, Hkv=2), dict(Hq=32, Hkv=1, T=5),
+    for kw in (dict(d=96), dict(Hq=3, Hkv=2), dict(Hq=129 * 2, Hkv=2), dict(Hq=32, Hkv=1, T=5),
                dict(sl=A + 2), dict(table=A + 2), dict(q=A + 8), dict(lse=A + 2)):
         assert dc(**kw) == 2, kw
     assert dc(mods=L.Mods(L.MOD_DOC, 0, 0.0, A, None)) == 2    # documents do not apply
@@ -190,14 +191,14 @@ def test_decode_workspace_size(L):
         assert so.attn_workspace_size(6, B, Hq, Hkv, N, 128, None) == expect(B, Hq, Hkv, N)
     assert so.attn_workspace_size(6, 2, 8, 2, 100, 128, None) == 0     # N not a multiple of 16
     so.attn_decode_workspace_size.restype = ctypes.c_size_t
-    for B, Hq, Hkv, T, mb in ((32, 64, 8, 1, 512), (4, 32, 8, 4, 40), (3, 8, 1, 16, 7)):
+    for B, Hq, Hkv, T, mb, d in ((32, 64, 8, 1, 512, 128), (4, 32, 8, 4, 40, 128), (3, 8, 1, 16, 7, 64)):
         tiles = -(-16 * mb // 128)
         ct = min(max(1, -(-(B * Hkv * tiles) // 2432)), tiles)
         rows = B * Hq * T * (-(-tiles // ct))
         r256 = lambda x: -(-x // 256) * 256
-        assert so.attn_decode_workspace_size(B, Hq, Hkv, T, mb, 128, None) == \
-            r256(16 * B) + 256 + r256(rows * 512) + r256(rows * 4)
+        assert so.attn_decode_workspace_size(B, Hq, Hkv, T, mb, d, None) == \
+            r256(16 * B) + 256 + r256(rows * 4 * d) + r256(rows * 4)
     assert so.attn_decode_workspace_size(2, 64, 1, 3, 8, 128, None) == 0  # 64 heads x 3 tokens > 128 rows
-    assert so.attn_workspace_size(6, 2, 8, 2, 128, 64, None) == 0      # d = 128 only
+    assert so.attn_workspace_size(6, 2, 8, 2, 128, 96, None) == 0      # d = 64 or 128
     docm = L.Mods(L.MOD_DOC, 0, 0.0, A, None)
     assert so.attn_workspace_size(6, 2, 8, 2, 128, 128, ctypes.byref(docm)) == 0

@@ -13,8 +13,10 @@ from gpu_common import LSE_TOL, O_TOL, default_scale, lib, max_abs, record
 
 pytestmark = pytest.mark.gpu
 
-# (B, Hq, Hkv, max_len, lens or None (uniform in [1, max_len]), mods, new tokens per sequence)
+# (B, Hq, Hkv, max_len, lens or None (uniform in [1, max_len]), mods, new tokens per sequence[, d])
 CASES = [
+    (3, 16, 2, 1500, None, dict(alibi=True), 1, 64),              # d = 64, general layout
+    (4, 16, 8, 700, [700, 1, 300, 129], dict(window=200), 3, 64),  # d = 64, compact layout, 3 tokens
     (4, 32, 8, 700, None, {}, 1),                                  # many chunks per sequence
     (3, 32, 2, 1024, [1000, 1, 333], dict(window=300, softcap=20.0, alibi=True), 1),
     (2, 4, 4, 256, [129, 256], {}, 1),                             # G = 1, exact tile multiple
@@ -28,8 +30,9 @@ CASES = [
 
 
 def _ids(c):
-    B, Hq, Hkv, n, lens, m, T = c
-    return f"B{B}_H{Hq}x{Hkv}_L{n}_T{T}_" + ("-".join(m) or "none")
+    B, Hq, Hkv, n, lens, m, T = c[:7]
+    d = c[7] if len(c) > 7 else 128
+    return f"B{B}_H{Hq}x{Hkv}_L{n}_T{T}_d{d}_" + ("-".join(m) or "none")
 
 
 def _run(ea, x, mods, scale):
@@ -43,9 +46,10 @@ def _run(ea, x, mods, scale):
 @pytest.mark.parametrize("case", CASES, ids=_ids)
 def test_decode_matches_oracle(case):
     ea = lib()
-    B, Hq, Hkv, n, lens, mk, T = case
-    x = gen.paged_decode_inputs(B, Hq, Hkv, n, 128, seed=900 + n, lens=lens, q_len=T)
-    s = default_scale(128)
+    B, Hq, Hkv, n, lens, mk, T = case[:7]
+    d = case[7] if len(case) > 7 else 128
+    x = gen.paged_decode_inputs(B, Hq, Hkv, n, d, seed=900 + n, lens=lens, q_len=T)
+    s = default_scale(d)
     o, lse = _run(ea, x, ea.make_mods(causal=True, **mk), s)
     O, L = attn64.decode_paged(x["q"], x["k_cache"], x["v_cache"], x["block_table"], x["seqlens"], s,
                                attn64.Mods(causal=True, **mk))

@@ -11,17 +11,19 @@ from gpu_common import LSE_TOL, O_TOL, default_scale, inputs, lib, max_abs, mods
 
 pytestmark = pytest.mark.gpu
 
-# (B, Hq, Hkv, N, mods)
+# (B, Hq, Hkv, N, mods, d)
 CASES = [
-    (2, 8, 2, 1024, dict(causal=True)),
-    (1, 4, 4, 400, {}),                                       # ragged last tile: blocks past N are zeros
-    (2, 4, 1, 640, dict(causal=True, window=200, softcap=20.0, alibi=True)),
+    (2, 8, 2, 1024, dict(causal=True), 128),
+    (1, 4, 4, 400, {}, 128),                                       # ragged last tile: blocks past N are zeros
+    (2, 4, 1, 640, dict(causal=True, window=200, softcap=20.0, alibi=True), 128),
+    (2, 8, 2, 1024, dict(causal=True), 64),
+    (1, 4, 1, 400, dict(window=100, alibi=True), 64),
 ]
 
 
 def _ids(c):
-    B, Hq, Hkv, N, m = c
-    return f"B{B}_H{Hq}x{Hkv}_N{N}_" + ("-".join(m) or "none")
+    B, Hq, Hkv, N, m, d = c
+    return f"B{B}_H{Hq}x{Hkv}_N{N}_d{d}_" + ("-".join(m) or "none")
 
 
 def _page(x, B, Hkv, N, rng, spare=7):
@@ -39,9 +41,8 @@ def _page(x, B, Hkv, N, rng, spare=7):
 @pytest.mark.parametrize("case", CASES, ids=_ids)
 def test_paged_forward(case):
     ea = lib()
-    B, Hq, Hkv, N, mk = case
-    d = 128
-    x = inputs(B, Hq, Hkv, N, d, seed=700 + N)
+    B, Hq, Hkv, N, mk, d = case
+    x = inputs(B, Hq, Hkv, N, d, seed=700 + N + d)
     rng = np.random.default_rng(N)
     kc, table, num_blocks = _page(x["k"], B, Hkv, N, rng)
     vc, _, _ = _page(x["v"], B, Hkv, N, np.random.default_rng(N))  # same permutation
