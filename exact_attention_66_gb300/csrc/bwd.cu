@@ -244,13 +244,16 @@ struct KvSteps {
     while (I < I_end && tile_class(p, b, I, J) == CLS_SKIP) ++I;
     return I < I_end ? I : p.nT;
   }
-  // Advance (g, I) to the next step; false when past the last one.
+  // Advance (g, I) to the next step; false when past the last one.  The query
+  // heads of the group are the inner loop.  Measured on the causal GQA 8K
+  // workload against Q tiles inner: 1.8 % less time, although the Q / dO
+  // tiles in use at once then span every head and DRAM reads rise from 0.85
+  // to 1.43 GB per launch (a quarter of the HBM rate, far from the bound).
   __device__ __forceinline__ bool advance(const AttnParams& p, int b, int& g, int& I) const {
+    if (++g < G) return true;
+    g = 0;
     I = next_I(p, b, I + 1);
-    if (I < p.nT) return true;
-    ++g;
-    I = I_first;
-    return g < G;
+    return I < p.nT;
   }
 };
 
