@@ -227,17 +227,12 @@ attn_status_t varlen_setup(const int32_t* cu, int n_seqs, int Hq, int Hkv, int t
   return ATTN_OK;
 }
 
-// Fill the mods workspace (block map, document runs) and point p at it.
+// Fill the mods workspace (document runs, block map, tile ranges) and point
+// p at it.  The runs come first: the block map classifies tiles from them
+// when the ids are non-decreasing.
 attn_status_t prepare_mods(AttnParams& p, uint8_t* region, cudaStream_t s) {
   if (!needs_map(p.flags)) return ATTN_OK;
   attn_status_t st;
-  if ((st = cuda_status(launch_block_map(p, region, s))) != ATTN_OK) return st;
-  p.map = region;
-  int2* rows = reinterpret_cast<int2*>(region + map_bytes(p.B, p.N));
-  int2* cols = reinterpret_cast<int2*>(region + map_bytes(p.B, p.N) + range_bytes(p.B, p.N));
-  if ((st = cuda_status(launch_tile_ranges(p, region, rows, cols, s))) != ATTN_OK) return st;
-  p.row_range = rows;
-  p.col_range = cols;
   if (p.flags & ATTN_MOD_DOC) {
     uint8_t* dregion = region + map_bytes(p.B, p.N) + 2 * range_bytes(p.B, p.N);
     int2* bounds = reinterpret_cast<int2*>(dregion);
@@ -246,6 +241,13 @@ attn_status_t prepare_mods(AttnParams& p, uint8_t* region, cudaStream_t s) {
     p.doc_bounds = bounds;
     p.doc_unsorted = unsorted;
   }
+  if ((st = cuda_status(launch_block_map(p, region, s))) != ATTN_OK) return st;
+  p.map = region;
+  int2* rows = reinterpret_cast<int2*>(region + map_bytes(p.B, p.N));
+  int2* cols = reinterpret_cast<int2*>(region + map_bytes(p.B, p.N) + range_bytes(p.B, p.N));
+  if ((st = cuda_status(launch_tile_ranges(p, region, rows, cols, s))) != ATTN_OK) return st;
+  p.row_range = rows;
+  p.col_range = cols;
   return ATTN_OK;
 }
 

@@ -1,9 +1,15 @@
 // Block-sparsity map: every 128 x 128 tile (b, I, J) is classified as skip /
-// partial / full by testing each of its (i, j) pairs against the mask
-// (FlexAttention/FA4 page, "Limitations actuelles": block sparsity; tile
-// size 128 as named there).  Tiles that the causal or window bound rules out
-// as a whole are classified without the element test (every pair of such a
-// tile fails the same condition, so the result is the same).
+// partial / full from the allowed (i, j) pairs it holds (FlexAttention/FA4
+// page, "Limitations actuelles": block sparsity; tile size 128 as named
+// there).  Tiles that the causal or window bound rules out as a whole are
+// classified at once.  Otherwise one thread per row finds the row's allowed
+// columns in the tile: with causal, window and the sequence end they form
+// the interval [max(j_lo, i - window + 1), min(j_hi, i, N - 1)], and a
+// document whose ids form one run ([start, end) from the document-run
+// kernel, when every batch row's ids are non-decreasing) narrows it to
+// [start, end - 1].  The tile is full when every row's interval is the whole
+// tile, skip when every interval is empty.  Without the runs, or with ids
+// that decrease somewhere, the document test goes pair by pair.
 #include "common.cuh"
 #include "launch.h"
 
@@ -22,19 +28,33 @@ __global__ void __launch_bounds__(256) block_map_kernel(const AttnParams p, uint
     if (threadIdx.x == 0) *out = CLS_SKIP;
     return;
   }
+  const bool doc_pairs = doc && (p.doc_bounds == nullptr || *p.doc_unsorted != 0);
   const int r = threadIdx.x & (TILE - 1);
   const int half = threadIdx.x >> 7;
   const int i = i_lo + r;
   bool any_ok = false, all_ok = true;
-  if (i < p.N) {
-    const int di = doc ? p.doc_ids[(size_t)b * p.N + i] : 0;
+  if (i < p.N && !doc_pairs) {
+    if (half == 0) {
+      int lo = j_lo, hi = min(j_lo + TILE, p.N) - 1;
+      if (causal) hi = min(hi, i);
+      if (win) lo = max(lo, i - p.window + 1);
+      if (doc) {
+        const int2 run = p.doc_bounds[(size_t)b * p.N + i];
+        lo = max(lo, run.x);
+        hi = min(hi, run.y - 1);
+      }
+      any_ok = lo <= hi;
+      all_ok = lo == j_lo && hi == j_lo + TILE - 1;
+    }
+  } else if (i < p.N) {
+    const int di = p.doc_ids[(size_t)b * p.N + i];
 #pragma unroll 4
     for (int c = 0; c < TILE / 2; ++c) {
       const int j = j_lo + half * (TILE / 2) + c;
       bool ok = j < p.N;
       if (ok && causal) ok = j <= i;
       if (ok && win) ok = (i - j) < p.window;
-      if (ok && doc) ok = p.doc_ids[(size_t)b * p.N + j] == di;
+      if (ok) ok = p.doc_ids[(size_t)b * p.N + j] == di;
       any_ok |= ok;
       all_ok &= ok;
     }
