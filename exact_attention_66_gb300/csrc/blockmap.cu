@@ -117,19 +117,31 @@ cudaError_t launch_seq_ids(const int* cu, int n_seqs, int total, int* ids, cudaS
 // Per Q tile (row of the map) and per KV tile (column): the range
 // [first, last + 1) of non-skipped tiles, (0, 0) when there is none.  Lets
 // the attention kernels start their tile loops at the first tile they need.
-__global__ void tile_range_kernel(const uint8_t* __restrict__ map, int nT, int2* __restrict__ rows,
-                                  int2* __restrict__ cols) {
-  const int b = blockIdx.y;
-  const int x = blockIdx.x * blockDim.x + threadIdx.x;
-  if (x >= nT) return;
+// One warp per (b, x): its lanes stride over map row x and map column x,
+// then min / max reductions across the warp.
+__global__ void __launch_bounds__(256) tile_range_kernel(const uint8_t* __restrict__ map, int nT, int B,
+                                                         int2* __restrict__ rows, int2* __restrict__ cols) {
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= (long long)B * nT) return;
+  const int b = (int)(gw / nT), x = (int)(gw - (long long)b * nT);
   const uint8_t* m = map + (size_t)b * nT * nT;
   int r0 = nT, r1 = -1, c0 = nT, c1 = -1;
-  for (int y = 0; y < nT; ++y) {
+  for (int y = lane; y < nT; y += 32) {
     if (m[(size_t)x * nT + y] != CLS_SKIP) { r0 = min(r0, y); r1 = y; }
     if (m[(size_t)y * nT + x] != CLS_SKIP) { c0 = min(c0, y); c1 = y; }
   }
-  rows[(size_t)b * nT + x] = r1 < 0 ? make_int2(0, 0) : make_int2(r0, r1 + 1);
-  cols[(size_t)b * nT + x] = c1 < 0 ? make_int2(0, 0) : make_int2(c0, c1 + 1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    r0 = min(r0, __shfl_xor_sync(0xffffffffu, r0, o));
+    r1 = max(r1, __shfl_xor_sync(0xffffffffu, r1, o));
+    c0 = min(c0, __shfl_xor_sync(0xffffffffu, c0, o));
+    c1 = max(c1, __shfl_xor_sync(0xffffffffu, c1, o));
+  }
+  if (lane == 0) {
+    rows[(size_t)b * nT + x] = r1 < 0 ? make_int2(0, 0) : make_int2(r0, r1 + 1);
+    cols[(size_t)b * nT + x] = c1 < 0 ? make_int2(0, 0) : make_int2(c0, c1 + 1);
+  }
 }
 
 cudaError_t launch_block_map(const AttnParams& p, uint8_t* map, cudaStream_t st) {
@@ -140,8 +152,8 @@ cudaError_t launch_block_map(const AttnParams& p, uint8_t* map, cudaStream_t st)
 
 cudaError_t launch_tile_ranges(const AttnParams& p, const uint8_t* map, int2* rows, int2* cols,
                                cudaStream_t st) {
-  const dim3 grid((unsigned)((p.nT + 127) / 128), (unsigned)p.B);
-  tile_range_kernel<<<grid, 128, 0, st>>>(map, p.nT, rows, cols);
+  const long long threads = (long long)p.B * p.nT * 32;
+  tile_range_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(map, p.nT, p.B, rows, cols);
   return cudaGetLastError();
 }
 
