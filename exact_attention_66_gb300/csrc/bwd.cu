@@ -217,8 +217,6 @@ struct KvCfg {
 };
 static_assert(KvCfg<128>::SMEM_BYTES <= 232448, "dK/dV shared memory exceeds 227 KB");
 
-constexpr bool KV_X_FIRST = false;
-
 struct KvBars {
   uint64_t in_full;              // K_J, V_J
   uint64_t qfull[3], qempty[3];  // Q ring
@@ -236,8 +234,8 @@ struct KvBars {
   int abort;
 };
 
-// Steps of a dK/dV CTA: query head g of the group (outer), non-skipped Q tile
-// I (inner, ascending).
+// Steps of a dK/dV CTA: non-skipped Q tile I (outer, ascending), query head
+// g of the group (inner).
 struct KvSteps {
   int J, I_first, I_end, G;  // Q tiles of the KV tile: [I_first, I_end), skipped ones passed over
   __device__ __forceinline__ int next_I(const AttnParams& p, int b, int I) const {
@@ -358,9 +356,9 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ MMA issuer
     // One thread issues every GEMM, in the order in which the softmax releases
     // X and fills P^T / dS^T, so it never waits on an event that comes after
-    // one it could already act on.  KV_X_FIRST: per step n, S(n+1), dV(n),
-    // dP(n+1), dK(n) (the X chain ahead of the accumulations); otherwise
-    // dP(n), dV(n), S(n+1), dK(n).
+    // one it could already act on: per step n, dP(n), dV(n), S(n+1), dK(n).
+    // (Putting the X chain ahead of the accumulations -- S(n+1), dV(n),
+    // dP(n+1), dK(n) -- measured slower.)
     if (lane == 0) {
       bool ok = mbar_wait(&S.in_full, 0, ab);
       tc_fence_after();
@@ -387,20 +385,17 @@ __global__ void __launch_bounds__(384, 1)
           return true;
         };
         ok = issue_s(0);
-        if (KV_X_FIRST && ok) ok = issue_dp(0);
         while (ok) {
           int g2 = g, I2 = I;
           const bool has_next = steps.advance(p, b, g2, I2);
-          if (!KV_X_FIRST && !(ok = issue_dp(n))) break;
-          if (KV_X_FIRST && has_next && !(ok = issue_s(n + 1))) break;
+          if (!(ok = issue_dp(n))) break;
           // dV += P^T(n) dO(n); dO(n) is free after it.
           if (!(ok = mbar_wait(&S.p_full, n & 1, ab))) break;
           tc_fence_after();
           issue_acc<D, true>(tdV, 0, tPT, do_at(n), n == 0);
           mma_commit(&S.pt_free);
           mma_commit(&S.dempty[n % C::DOS]);
-          if (KV_X_FIRST && has_next && !(ok = issue_dp(n + 1))) break;
-          if (!KV_X_FIRST && has_next && !(ok = issue_s(n + 1))) break;
+          if (has_next && !(ok = issue_s(n + 1))) break;
           // dK += dS^T(n) Q(n); Q(n) is free after it.
           if (!(ok = mbar_wait(&S.ds_full, n & 1, ab))) break;
           tc_fence_after();
