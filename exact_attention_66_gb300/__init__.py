@@ -17,7 +17,7 @@ from ._lib import (  # noqa: F401
     TILE_SKIP, attn_block_map, attn_bwd, attn_bwd_profiled, attn_bwd_noalloc, attn_bwd_varlen,
     NOALLOC_SCRATCH_BYTES, attn_fwd, attn_fwd_fp8, attn_fwd_varlen, attn_hadamard_quant_fp8,
     attn_rope_hadamard_quant_fp8, attn_fwd_paged, attn_decode_paged, attn_decode_workspace_size,
-    attn_status, attn_workspace_size, lib,
+    attn_status, attn_test_hooks, attn_workspace_size, lib, STALL_BWD, STALL_FWD,
     make_mods, status_string,
 )
 

@@ -27,7 +27,7 @@ TILE_SKIP, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 # Exported symbols, in the order include/attn.h declares them.
 EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc",
            "attn_fwd_paged", "attn_decode_paged", "attn_decode_workspace_size", "attn_fwd_varlen", "attn_bwd_varlen", "attn_hadamard_quant_fp8", "attn_rope_hadamard_quant_fp8",
-           "attn_fwd_fp8", "attn_block_map", "attn_status", "attn_status_string")
+           "attn_fwd_fp8", "attn_block_map", "attn_test_hooks", "attn_status", "attn_status_string")
 
 
 class AttnError(RuntimeError):
@@ -65,11 +65,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_rope_hadamard_quant_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
     lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, mp, vp, sz, vp]
     lib.attn_block_map.argtypes = [mp, i, i, vp, vp]
+    lib.attn_test_hooks.argtypes = [ctypes.c_ulonglong, i]
     lib.attn_status.argtypes = [vp]
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
     for name in ("attn_fwd", "attn_bwd", "attn_bwd_profiled", "attn_bwd_noalloc", "attn_hadamard_quant_fp8", "attn_fwd_fp8",
-                 "attn_block_map", "attn_status"):
+                 "attn_block_map", "attn_test_hooks", "attn_status"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -226,6 +227,15 @@ def attn_fwd_fp8(q8, k8, v8, scales, o, lse, B, Hq, Hkv, N, d, scale, mods=None,
 
 def attn_block_map(mods, B, N, out, stream=None):
     _check(_lib.attn_block_map(_mods_ref(mods), B, N, _ptr(out), _stream(stream)), "attn_block_map")
+
+
+STALL_FWD, STALL_BWD = 1, 2  # ATTN_STALL_FWD, ATTN_STALL_BWD
+
+
+def attn_test_hooks(wait_limit_ns=0, stall=0):
+    """Pipeline-wait limit (ns; 0 = the default 1 s) and stall bits for the
+    kernels launched after this call (see include/attn.h)."""
+    _check(_lib.attn_test_hooks(int(wait_limit_ns), int(stall)), "attn_test_hooks")
 
 
 def attn_status(stream=None):

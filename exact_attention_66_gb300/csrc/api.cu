@@ -2,6 +2,7 @@
 // validation, workspace carve-up, TMA descriptor encoding and kernel launch.
 // Every argument check runs before the first CUDA call, so a bad call returns
 // its status without touching the device.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -21,6 +22,11 @@ using namespace attn;
 namespace {
 
 constexpr int kMaxDevices = 64;
+
+// Test hooks (attn_test_hooks): the pipeline-wait limit and the stall bits
+// copied into the parameters of every later launch.
+std::atomic<unsigned long long> g_wait_ns{ATTN_WAIT_TIMEOUT_NS};
+std::atomic<int> g_stall{0};
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -182,6 +188,8 @@ AttnParams make_params(int B, int Hq, int Hkv, int N, float scale, const attn_mo
   p.kv_blocks = 0;
   p.bt_stride = 0;
   p.status = status;
+  p.wait_ns = g_wait_ns.load();
+  p.stall = g_stall.load();
   return p;
 }
 
@@ -583,6 +591,7 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   p.block_table = block_table;
   p.seqlens = seqlens;
   uint8_t* w = static_cast<uint8_t*>(ws);
+  p.wait_ns = g_wait_ns.load();
   p.seq_info = reinterpret_cast<int4*>(w);
   p.n_items = reinterpret_cast<int*>(w + decode_info_bytes(B) - 256);
   const size_t rows = (size_t)B * Hq * q_len * sp.max_chunks;
@@ -638,6 +647,13 @@ attn_status_t attn_block_map(const attn_mods_t* mods, int B, int N, uint8_t* map
   if ((st = device_state(&status)) != ATTN_OK) return st;
   AttnParams p = make_params(B, 1, 1, N, 1.0f, mods, status);
   return cuda_status(launch_block_map(p, map, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_test_hooks(unsigned long long wait_limit_ns, int stall) {
+  if (stall & ~(ATTN_STALL_FWD | ATTN_STALL_BWD)) return ATTN_ERR_INVALID_ARG;
+  g_wait_ns.store(wait_limit_ns == 0 ? ATTN_WAIT_TIMEOUT_NS : wait_limit_ns);
+  g_stall.store(stall);
+  return ATTN_OK;
 }
 
 attn_status_t attn_status(void* stream) {

@@ -10,12 +10,12 @@
 // Three kernels:
 //  * bwd_pre:  D = rowsum(dO * O) per query row (bandwidth bound).
 //  * bwd_dkdv: one CTA per (batch, KV head, 128-row KV tile).  K_J and V_J stay
-//    in shared memory; Q/dO tiles of every query head of the GQA group and
-//    every needed Q tile stream through a 2-stage TMA ring.  S^T = K Q^T and
-//    dP^T = V dO^T land in TMEM; two softmax warpgroups (a thread per KV row,
-//    64 query columns each) turn them into P^T (bf16, to shared memory) and
-//    dS^T (bf16, written back over dP^T in TMEM); dV += P^T dO reads P^T from
-//    shared memory, dK += dS^T Q reads dS^T from TMEM.
+//    in shared memory; Q tiles (3-slot TMA ring) and dO tiles (2-slot ring) of
+//    every query head of the GQA group and every needed Q tile stream past
+//    them.  S^T = K Q^T and dP^T = V dO^T land in one shared TMEM region; two
+//    softmax warpgroups (a thread per KV row, 64 query columns each) turn them
+//    into P^T and dS^T, packed bf16 in TMEM; dV += P^T dO and dK += dS^T Q
+//    read their A operand from TMEM.
 //  * bwd_dq:   one CTA per (batch, query head, 128-row Q tile), streaming K/V
 //    tiles: S = Q K^T and dP = dO V^T in TMEM, dS to shared memory,
 //    dQ += dS K.
@@ -27,172 +27,13 @@
 // partner tiles in a fixed order: no atomics, so the result is bitwise
 // reproducible (contrast the nondeterministic block-sparse backward on the
 // FlexAttention/FA4 page, "Limitations actuelles").
-#include "common.cuh"
+#include "bwd_common.cuh"
 #include "launch.h"
 
 namespace attn {
 
-// ------------------------------------------------------------------ bwd_pre
-// Row statistics of the backward, one pair per query row, rows padded to whole
-// 128-row tiles: {LSE * log2(e), D = rowsum(dO * O)}.  Padding rows and rows
-// with no allowed key get +inf (so that P = exp2(x - inf) = 0) and D = 0.
-template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
-                                                      const __nv_bfloat16* __restrict__ dout,
-                                                      const float* __restrict__ lse,
-                                                      float2* __restrict__ rowstat, int N,
-                                                      long long rows_padded) {
-  constexpr int TPR = D / 8;  // threads per row, 8 bf16 each
-  const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long row = gt / TPR;
-  const int part = (int)(gt % TPR);
-  const long long np = (long long)((N + TILE - 1) / TILE) * TILE;
-  const long long bh = row / np;
-  const int i = (int)(row - bh * np);
-  const bool real = row < rows_padded && i < N;
-  float acc = 0.f;
-  if (real) {
-    const long long src = bh * N + i;
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + src * D) + part);
-    const uint4 g = __ldg(reinterpret_cast<const uint4*>(dout + src * D) + part);
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      acc = fmaf(bf16lo_f32(aw[w]), bf16lo_f32(gw[w]), acc);
-      acc = fmaf(bf16hi_f32(aw[w]), bf16hi_f32(gw[w]), acc);
-    }
-  }
-#pragma unroll
-  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows_padded && part == 0) {
-    float l2 = INFINITY;
-    if (real) {
-      const float v = lse[bh * N + i];
-      l2 = v == -INFINITY ? INFINITY : v * LOG2E;
-    }
-    rowstat[row] = make_float2(l2, acc);
-  }
-}
-
-// D(tmem, 128 x 128) = A B^T, A and B K-major 128-byte swizzled tiles of
-// ROW_BYTES per row (16 KB column chunks), one MMA per 32 bytes of a row.
-// Issue loops are unrolled: the tensor pipe queues few MMAs, and a rolled
-// loop's per-iteration overhead in the issuing thread leaves it idle.
-template <int ROW_BYTES>
-__device__ __forceinline__ void issue_nt(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
-  constexpr uint32_t id = idesc_bf16(128, 128, false, false);
-  const uint64_t ad = opaque(sdesc_sw128(a_smem, 16, 1024)), bd = opaque(sdesc_sw128(b_smem, 16, 1024));
-#pragma unroll
-  for (int kk = 0; kk < ROW_BYTES / 32; ++kk) {
-    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-    mma_f16_ss(d_tmem, sdesc_add(ad, off), sdesc_add(bd, off), id, kk > 0 ? 1u : 0u);
-  }
-}
-
-// D(tmem, 128 x 128) = A B^T with A packed bf16 in TMEM (128 lanes x D
-// elements, D / 2 columns) and B a K-major shared-memory tile.
-template <int D>
-__device__ __forceinline__ void issue_nt_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem) {
-  constexpr uint32_t id = idesc_bf16(128, 128, false, false);
-  const uint64_t bd = opaque(sdesc_sw128(b_smem, 16, 1024));
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk)
-    mma_f16_ts(d_tmem, a_tmem + kk * 8, sdesc_add(bd, (kk / 4) * 16384 + (kk % 4) * 32), id,
-               kk > 0 ? 1u : 0u);
-}
-
-// Copy row r of a K-major 128-byte swizzled bf16 tile (D elements per row)
-// into this warp's TMEM lanes as packed bf16 (A-operand layout).
-template <int D>
-__device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int r, uint32_t t_addr) {
-#pragma unroll
-  for (int q4 = 0; q4 < D / 64; ++q4) {  // 32 words = 64 elements = one 128-byte chunk row
-    uint32_t v[32];
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const uint4 x = *reinterpret_cast<const uint4*>(tile + q4 * 16384 + r * 128 + ((g ^ (r & 7)) << 4));
-      v[4 * g] = x.x;
-      v[4 * g + 1] = x.y;
-      v[4 * g + 2] = x.z;
-      v[4 * g + 3] = x.w;
-    }
-    tmem_st32(t_addr + q4 * 32, v);
-  }
-}
-
-// D(tmem, 128 x D) += A(128 x 128 keys) B(128 keys x D, MN-major in shared
-// memory).  A is a K-major shared-memory tile (A_TMEM false; a_tmem ignored)
-// or packed bf16 in TMEM (A_TMEM true; a_smem ignored).
-template <int D, bool A_TMEM>
-__device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_smem, uint32_t a_tmem,
-                                          uint32_t b_smem, bool first) {
-  constexpr uint32_t id = idesc_bf16(128, D, false, true);
-  const uint64_t ad = opaque(sdesc_sw128(a_smem, 16, 1024)), bd = opaque(sdesc_sw128(b_smem, 16384, 1024));
-#pragma unroll
-  for (int kk = 0; kk < TILE / 16; ++kk) {
-    const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-    const uint64_t b = sdesc_add(bd, kk * 16 * 128);
-    if (A_TMEM)
-      mma_f16_ts(d_tmem, a_tmem + kk * 8, b, id, acc);
-    else
-      mma_f16_ss(d_tmem, sdesc_add(ad, (kk / 4) * 16384 + (kk % 4) * 32), b, id, acc);
-  }
-}
-
-// Store 32 packed bf16 words (64 consecutive columns starting at 64 * w) of
-// row r into a 128 x 128 bf16 K-major swizzled tile.
-__device__ __forceinline__ void store_half_row(uint8_t* tile, int r, int w, const uint32_t (&v)[32]) {
-#pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    const uint32_t addr = (uint32_t)(w * 16384 + r * 128 + ((g ^ (r & 7)) << 4));
-    *reinterpret_cast<uint4*>(tile + addr) = make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-  }
-}
-
-// Columns [col0, col0 + NC) of an fp32 TMEM row (NC a multiple of 32) as
-// bf16 * mul into dst (global), if in range; zeros when the accumulator was
-// never written.
-template <int NC>
-__device__ __forceinline__ void store_cols(uint32_t t_col, bool have, float mul, __nv_bfloat16* dst,
-                                           bool in_range) {
-#pragma unroll
-  for (int q4 = 0; q4 < NC / 32; ++q4) {
-    uint32_t v[32];
-    if (have) {
-      tmem_ld32(t_col + q4 * 32, v);
-      tmem_wait_ld(v);
-    } else {
-#pragma unroll
-      for (int c = 0; c < 32; ++c) v[c] = 0u;
-    }
-    uint32_t pk[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k)
-      pk[k] = pack_bf16(__uint_as_float(v[2 * k]) * mul, __uint_as_float(v[2 * k + 1]) * mul);
-    if (in_range) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + q4 * 32);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-    }
-  }
-}
-
-// Load 64 consecutive fp32 TMEM columns of this warp's lanes.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&v)[64]) {
-  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-  tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-}
-__device__ __forceinline__ void tmem_wait64(uint32_t (&v)[64]) {
-  tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-  tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-}
-
-constexpr int BWD_LAUNCH_REGS = 168, BWD_REGS_LOW = 80, BWD_REGS_HIGH = 208;
-static_assert(128 * BWD_REGS_LOW + 256 * BWD_REGS_HIGH <= 384 * BWD_LAUNCH_REGS, "register split");
-
 // ================================================================== dK, dV
-// Shared memory: K_J, V_J and two stages of (Q_I, dO_I).  TMEM (512 columns):
+// Shared memory: K_J, V_J, a 3-slot Q ring and a 2-slot dO ring.  TMEM (512 columns):
 //   X   [0, 128)        S^T(n), then dP^T(n) once the softmax has copied S^T out
 //   P^T [128, 192)      packed bf16, A operand of dV += P^T dO
 //   dS^T [192, 256)     packed bf16, A operand of dK += dS^T Q
@@ -230,6 +71,7 @@ struct KvBars {
   uint64_t ds_full;            // dS^T(n) stored in TMEM     (256)
   uint64_t ds_free;            // dK(n) done reading dS^T    (MMA commit)
   uint64_t fin;                // every MMA done
+  uint64_t never;              // test hook: a phase that nothing completes
   uint32_t tmem_base;
   int abort;
 };
@@ -246,7 +88,7 @@ struct KvSteps {
   // heads of the group are the inner loop.  Measured on the causal GQA 8K
   // workload against Q tiles inner: 1.8 % less time, although the Q / dO
   // tiles in use at once then span every head and DRAM reads rise from 0.85
-  // to 1.43 GB per launch (a quarter of the HBM rate, far from the bound).
+  // to 1.43 GB per launch (0.79 TB/s, about an eighth of the HBM rate).
   __device__ __forceinline__ bool advance(const AttnParams& p, int b, int& g, int& I) const {
     if (++g < G) return true;
     g = 0;
@@ -266,7 +108,7 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   KvBars& S = *reinterpret_cast<KvBars*>(smem + C::BAR_OFF);
-  const Abort ab{&S.abort, p.status};
+  const Abort ab{&S.abort, p.status, p.wait_ns};
   const int warp = warp_id(), lane = lane_id();
 
   const int BHk = p.B * p.Hkv;
@@ -300,6 +142,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&S.ds_full, 256);
     mbar_init(&S.ds_free, 1);
     mbar_init(&S.fin, 1);
+    mbar_init(&S.never, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -431,7 +274,9 @@ __global__ void __launch_bounds__(384, 1)
     const uint64_t sc_in2 = f2_pack(sc_in, sc_in), sc_out2 = f2_pack(sc_out, sc_out);
     const uint64_t one2 = f2_pack(1.f, 1.f);
     bool ok = true;
-    if (any) {
+    // Test hook: warpgroup 0 waits on a phase nothing completes (attn_test_hooks).
+    if ((p.stall & STALL_BWD) && w == 0) ok = wait_warp(&S.never, 0, ab);
+    if (ok && any) {
       int g = 0, I = steps.I_first, n = 0;
       do {
         const int hq = hk * G + g;
@@ -608,7 +453,7 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   DqBars& S = *reinterpret_cast<DqBars*>(smem + C::BAR_OFF);
-  const Abort ab{&S.abort, p.status};
+  const Abort ab{&S.abort, p.status, p.wait_ns};
   const int warp = warp_id(), lane = lane_id();
 
   const int BH = p.B * p.Hq;
@@ -839,17 +684,6 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ------------------------------------------------------------------ launch
-template <typename K>
-static cudaError_t check_regs(K kern, int& cached) {
-  if (cached < 0) {
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return cudaErrorInvalidDeviceFunction;
-    cached = fa.numRegs;
-  }
-  // The register split inside the kernel assumes this allocation at launch.
-  return cached == BWD_LAUNCH_REGS ? cudaSuccess : cudaErrorInvalidConfiguration;
-}
-
 template <int D, bool MODS, bool MASKS>
 static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
   const AttnParams& p = L.p;
@@ -857,7 +691,7 @@ static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
   const long long threads = rows * (D / 8);
   if (L.events[0]) cudaEventRecord(L.events[0], st);
   bwd_pre_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
-      (const __nv_bfloat16*)L.o, (const __nv_bfloat16*)L.dout, L.lse, L.rowstat, p.N, rows);
+      (const __nv_bfloat16*)L.o, (const __nv_bfloat16*)L.dout, L.lse, L.rowstat, p.N, rows, PreExtra{});
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

@@ -18,6 +18,10 @@ constexpr int BWD_MAX_N = 1024 * 128;
 
 enum : uint32_t { MOD_CAUSAL = 1u, MOD_WINDOW = 2u, MOD_DOC = 4u, MOD_SOFTCAP = 8u, MOD_ALIBI = 16u };
 enum : int { CLS_SKIP = 0, CLS_PARTIAL = 1, CLS_FULL = 2 };
+// Test hooks (attn_test_hooks in include/attn.h): kernels of the selected kind
+// make one consumer warpgroup wait first on an mbarrier that nothing
+// completes, so that the wait runs into its time limit.
+enum : int { STALL_FWD = 1, STALL_BWD = 2 };
 
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -55,6 +59,8 @@ struct AttnParams {
   const int2* row_range;
   const int2* col_range;
   int* status;          // device status word
+  unsigned long long wait_ns;  // time limit of a pipeline wait (ns)
+  int stall;                   // STALL_* test hook bits, 0 normally
 };
 
 // Non-skipped KV tiles of Q tile I (a superset without a map).

@@ -79,6 +79,7 @@ struct FwdBars {
   uint64_t p_full[2];          // P_t written (128 arrivals)
   uint64_t o_full[2];          // P_t V done (MMA commit)
   uint64_t mma_drain[2];
+  uint64_t never;              // test hook: a phase that nothing completes
   uint32_t tmem_base;
   int abort;
 };
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   FwdBars& S = *reinterpret_cast<FwdBars*>(smem + C::BAR_OFF);
-  const Abort ab{&S.abort, p.status};
+  const Abort ab{&S.abort, p.status, p.wait_ns};
   const int warp = warp_id(), lane = lane_id();
 
   // Work item, heaviest Q blocks first (longest-processing-time order).
@@ -248,6 +249,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(&S.mma_drain[0], 1);
     mbar_init(&S.mma_drain[1], 1);
+    mbar_init(&S.never, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -461,7 +463,10 @@ __global__ void __launch_bounds__(384, 1)
     float m = -INFINITY, l = 0.f;
     int ns = 0;
     bool ok = true;
-    for (int J = J_begin; J < J_end; ++J) {
+    // Test hook: the first tile's warpgroup waits on a phase nothing completes,
+    // runs into the wait limit, and the whole grid drains (attn_test_hooks).
+    if ((p.stall & STALL_FWD) && t == 0) ok = wait_warp(&S.never, 0, ab);
+    for (int J = J_begin; ok && J < J_end; ++J) {
       const int cls = tile_class(p, b, I, J);
       if (cls == CLS_SKIP) continue;
       const bool partial = cls == CLS_PARTIAL;

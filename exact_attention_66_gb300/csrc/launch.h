@@ -60,6 +60,7 @@ struct DecodeParams {
   float* o_part;           // [B, Hq, q_len, max_chunks, d] workspace: O / l of each chunk
   float* lse_part;         // [B, Hq, q_len, max_chunks] workspace: log2-sum-exp of each chunk
   int* status;             // device status word
+  unsigned long long wait_ns;  // time limit of a pipeline wait (ns)
 };
 struct DecodeLaunch {
   CUtensorMap tq;      // Q as [B*Hkv, G*q_len, d]: box of G*q_len rows x 64 columns

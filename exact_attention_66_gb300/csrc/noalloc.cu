@@ -17,14 +17,25 @@ void* g_scratch_addr[kMaxDevices];  // device address of g_noalloc_scratch, per 
 std::mutex g_scratch_mu;
 
 // Device address of the scratch on the current device, looked up on first use.
+// The device is checked first, so that a GPU this library was not built for
+// gets ATTN_ERR_DEVICE (as from attn_bwd) rather than a failed lookup.  The
+// first lookup on a device loads this file's module there (module loading is
+// lazy), which is when the array is reserved.
 attn_status_t scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
   if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return ATTN_ERR_CUDA;
+    if (major != 10 || minor != 3) return ATTN_ERR_DEVICE;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();  // leave no pending error behind for a later launch check
+      return ATTN_ERR_CUDA;
+    }
     g_scratch_addr[dev] = p;
   }
   *out = g_scratch_addr[dev];

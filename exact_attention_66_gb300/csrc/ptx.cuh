@@ -18,7 +18,10 @@ namespace attn {
 // Device status codes (kept equal to the host enum in include/attn.h).
 enum : int { DEV_OK = 0, DEV_ERR_TIMEOUT = 6, DEV_ERR_BOUNDS = 7 };
 
-// A wait gives up after this many nanoseconds of %globaltimer.
+// Default limit of a pipeline wait, in nanoseconds of %globaltimer (the
+// launch parameters carry the limit in force; see Abort).  Drain waits on the
+// error path, which wait only for copies and MMAs already in flight, always
+// use this one.
 #ifndef ATTN_WAIT_TIMEOUT_NS
 #define ATTN_WAIT_TIMEOUT_NS 1000000000ull
 #endif
@@ -75,6 +78,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 struct Abort {
   volatile int* cta;     // shared memory
   int* global;           // device status word
+  unsigned long long limit;  // ns a wait may take before it records DEV_ERR_TIMEOUT
 };
 
 __device__ __forceinline__ void raise_error(const Abort& ab, int code) {
@@ -94,7 +98,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
       if (mbar_try(a, parity)) return true;
     if (*ab.cta != 0) return false;
     if (*(volatile int*)ab.global != 0) { *ab.cta = *(volatile int*)ab.global; return false; }
-    if (globaltimer() - t0 > ATTN_WAIT_TIMEOUT_NS) {
+    if (globaltimer() - t0 > ab.limit) {
       raise_error(ab, DEV_ERR_TIMEOUT);
       return false;
     }

@@ -175,8 +175,12 @@ attn_status_t attn_bwd_profiled(const void* q, const void* k, const void* v, con
  * the window / document mask data), must fit in ATTN_NOALLOC_SCRATCH_BYTES;
  * otherwise the call returns ATTN_ERR_WORKSPACE before touching the device.
  * Set-up: the first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.
+ * (cudaGetSymbolAddress, with that device current).  Because CUDA loads
+ * modules lazily, that lookup is also when the library's module is loaded on
+ * the device and the array is reserved there, which can synchronise the
+ * device.  Make that first call once per device at set-up time, before any
+ * stream capture and outside any section that must not synchronise; later
+ * calls only read the cached address.
  * Sharing: every call uses the same array, which keeps the last call's
  * contents.  Each call overwrites all of the scratch it reads (nothing there
  * has to start at zero), so consecutive calls are fine; calls that overlap on
@@ -339,6 +343,30 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const
  * ATTN_TILE_PARTIAL.  Only the mask flags of mods matter.
  */
 attn_status_t attn_block_map(const attn_mods_t* mods, int B, int N, uint8_t* map, void* stream);
+
+/* Stall selectors of attn_test_hooks. */
+enum { ATTN_STALL_FWD = 1, ATTN_STALL_BWD = 2 };
+
+/*
+ * Test hooks for the device-side failure path.  Every pipeline wait in the
+ * kernels is bounded: a wait that runs out of time records ATTN_ERR_TIMEOUT
+ * in the status word, every other wait of the grid gives up, copies and MMAs
+ * in flight drain, tensor memory is released and the kernel returns, so the
+ * context stays usable (the FlashAttention-3 digest's asynchronous
+ * producer/consumer pipeline, "Fonctionnalités des GPU Hopper", is what these
+ * waits belong to; the bound itself is this library's own).
+ * wait_limit_ns : time limit of each pipeline wait in kernels launched after
+ *                 this call; 0 restores the default (1 s).
+ * stall         : 0, or an OR of ATTN_STALL_FWD (forward kernels: the first
+ *                 query tile's compute warpgroup of every CTA first waits on a
+ *                 barrier that nothing completes) and ATTN_STALL_BWD (the
+ *                 backward's main kernel: one compute warpgroup does the same).
+ *                 A stalled kernel ends with ATTN_ERR_TIMEOUT and leaves its
+ *                 outputs unspecified.  Other bits: ATTN_ERR_INVALID_ARG.
+ * Process-wide settings, read when a call launches its kernels; not meant to
+ * change while other threads launch.  No device work, no synchronisation.
+ */
+attn_status_t attn_test_hooks(unsigned long long wait_limit_ns, int stall);
 
 /*
  * Synchronise `stream`, then return and clear the device status word

@@ -202,3 +202,10 @@ def test_decode_workspace_size(L):
     assert so.attn_workspace_size(6, 2, 8, 2, 128, 96, None) == 0      # d = 64 or 128
     docm = L.Mods(L.MOD_DOC, 0, 0.0, A, None)
     assert so.attn_workspace_size(6, 2, 8, 2, 128, 128, ctypes.byref(docm)) == 0
+
+
+def test_test_hooks_validate_and_reset(L):
+    so = L.lib()
+    assert so.attn_test_hooks(0, 4) == 1  # unknown stall bit
+    assert so.attn_test_hooks(5_000_000, L.STALL_FWD | L.STALL_BWD) == 0
+    assert so.attn_test_hooks(0, 0) == 0  # defaults back

@@ -32,3 +32,18 @@ def test_gqa_8k_flops():
     fwd, bwd = bench.flops(gen.WORKLOADS["gqa_causal_8k"])
     assert fwd == 4 * 64 * 128 * 8192 * 8193 // 2
     assert bwd == 2.5 * fwd
+
+
+def test_peak_follows_the_clock_record():
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+    at_max = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    p, why = bench.bf16_peak(peaks, "measured", at_max)
+    assert p == 1900.0 and "burst" in why
+    slow = {"sm_mhz": 1485.0, "sm_max_mhz": 2070.0, "reasons": []}
+    p, why = bench.bf16_peak(peaks, "measured", slow)
+    assert abs(p - 1900.0 * 1485.0 / 2070.0) < 1e-9 and "1485" in why
+    capped = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    p, why = bench.bf16_peak(peaks, "measured", capped)
+    assert p == 1900.0 and "sw_power_cap" in why
+    p, _ = bench.bf16_peak(peaks, "measured", {"sm_mhz": None, "sm_max_mhz": None, "reasons": []})
+    assert p == 1900.0
