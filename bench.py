@@ -269,6 +269,21 @@ def traffic_record(kernel: str):
     return rec["bytes_per_launch"] if h == rec.get("source_sha") else None
 
 
+def computed_pairs(ea, cfg, mods, dev) -> int:
+    """(query, key) pairs inside the 128 x 128 tiles the kernels compute (the
+    non-skipped tiles of the block map), summed over the batch, per query
+    head: the same unit as allowed_pairs."""
+    B, N = cfg["B"], cfg["N"]
+    nT = (N + 127) // 128
+    if cfg.get("window") or cfg.get("doc"):
+        tiles = int((ea.block_map(B, N, mods, device=dev) > 0).sum().item())
+    elif cfg.get("causal"):
+        tiles = B * nT * (nT + 1) // 2
+    else:
+        tiles = B * nT * nT
+    return tiles * 128 * 128
+
+
 def workload_mods(ea, cfg, x, dev):
     docs = x.get("doc_ids")
     ddocs = torch.from_numpy(docs).to(dev) if docs is not None else None
@@ -372,6 +387,7 @@ def run_ours(args, world, rank, local):
     ws = torch.empty(nws, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     with_map = bool(cfg.get("window") or cfg.get("doc"))
+    fused_bwd = bool(cfg.get("causal")) and with_map and d == 128  # the library's one-kernel backward
 
     def mk_events(n):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -454,6 +470,8 @@ def run_ours(args, world, rank, local):
     ea.attn_status(stream)
 
     fwd_f, bwd_f = flops(cfg, docs)
+    allowed = allowed_pairs(cfg, docs)
+    computed = computed_pairs(ea, cfg, mods, dev)
     if fwd_only:
         bwd_f = 0.0
     ms = total_ms / args.steps
@@ -463,10 +481,16 @@ def run_ours(args, world, rank, local):
     fwd_t = fwd_f / (mean(k_fwd) * 1e-3) / 1e12
     bwd_ms = mean(k_pre) + mean(k_kv) + mean(k_dq)
     bwd_t = bwd_f / (bwd_ms * 1e-3) / 1e12 if not fwd_only else 0.0
-    # dominant kernel: the dK/dV kernel; its algorithmic work is 4 of the 5
-    # backward GEMMs (S recompute, dP, dV, dK) = 2x the forward FLOPs.
+    # Causal masks with window / document parts at d = 128 run the one-kernel
+    # backward: all 5 GEMMs (S and dP recomputed, dV, dK, dQ) in one kernel,
+    # between the bounds / row-statistics kernels and the dQ conversion.
+    # Otherwise the dK/dV kernel does 4 of the 5 (= 2x the forward FLOPs) and
+    # the dQ kernel the fifth (S and dP recomputed again, 2 more GEMMs).
     kernels = {"fwd_bf16": (mean(k_fwd), fwd_f)}
-    if not fwd_only:
+    if not fwd_only and fused_bwd:
+        kernels.update({"bwd_fused": (mean(k_kv), bwd_f), "bwd_pre": (mean(k_pre), 0.0),
+                        "bwd_dq_convert": (mean(k_dq), 0.0)})
+    elif not fwd_only:
         kernels.update({"bwd_dkdv": (mean(k_kv), 0.8 * bwd_f), "bwd_dq": (mean(k_dq), 0.2 * bwd_f),
                         "bwd_pre": (mean(k_pre), 0.0)})
     dom = max(kernels, key=lambda n: kernels[n][0])
@@ -484,7 +508,9 @@ def run_ours(args, world, rank, local):
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 5),
                     "traffic": None, "bytes_per_launch": nbytes,
                     "peak_source": f"{src} hbm_gbs (inputs stay in L2 between steps: warm)"}
-    launches = (2 if with_map else 1) + (0 if fwd_only else (4 if with_map else 3))
+    map_launches = (3 if cfg.get("doc") else 2) if with_map else 0  # document runs, block map, tile ranges
+    bwd_launches = 0 if fwd_only else (4 if fused_bwd else 3) + map_launches
+    launches = 1 + map_launches + bwd_launches
     line = {
         "metric": METRIC if name == WORKLOAD else f"attention TFLOPS fwd{'' if fwd_only else '/bwd'} ({name})",
         "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -498,6 +524,10 @@ def run_ours(args, world, rank, local):
         "fwd_frac_peak": round(fwd_t / peak, 4), "bwd_frac_peak": round(bwd_t / peak, 4),
         "kernel_ms": {n: round(t, 4) for n, (t, _) in kernels.items()},
         "roofline": roofline,
+        "tile_efficiency": {
+            "allowed_pairs": allowed, "computed_pairs": computed, "ratio": round(allowed / computed, 4),
+            "note": "allowed (i, j) pairs / pairs inside the non-skipped 128 x 128 tiles; the rest of the "
+                    "gap to the peak is kernel time"},
         "e2e": None if not e2e_steps else {
             "value": round(job_throughput(world, fwd_f + bwd_f, e2e_ms) / 1e12, 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),

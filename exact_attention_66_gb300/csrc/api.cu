@@ -204,6 +204,26 @@ size_t bwd_rowstat_bytes(int B, int Hq, int N) {
   return round_up((size_t)B * Hq * ((N + 127) / 128) * 128 * sizeof(float2), 256);
 }
 
+// The one-kernel backward runs causal masks with window / document parts at
+// d = 128 (measured on GB300: 20 % faster than the two kernels on the flex
+// workload, whose KV tiles meet few, mostly partial Q tiles; 7-10 % slower on
+// plain causal masks, where its dQ reductions slow the MMA pipe by more than
+// the two saved GEMMs).  Its workspace, after the row statistics and the mods
+// region: the per-row dQ quanta, the K/V bounds, the work-item counter and the
+// int32 dQ accumulator.
+bool bwd_fused(uint32_t flags, int d) {
+  return (flags & ATTN_MOD_CAUSAL) != 0 && needs_map(flags) && d == 128;
+}
+size_t bwd_qscale_bytes(int B, int Hq, int N) { return round_up((size_t)B * Hq * n_tiles(N) * TILE * sizeof(float), 256); }
+size_t bwd_kvb_bytes(int B, int Hkv) { return round_up((size_t)B * Hkv * sizeof(float2), 256); }
+size_t bwd_dqacc_bytes(int B, int Hq, int N, int d) {
+  return round_up((size_t)B * Hq * n_tiles(N) * TILE * d * sizeof(int), 256);
+}
+size_t bwd_fused_bytes(int B, int Hq, int Hkv, int N, int d, uint32_t flags) {
+  return bwd_fused(flags, d) ? bwd_qscale_bytes(B, Hq, N) + bwd_kvb_bytes(B, Hkv) + 256 + bwd_dqacc_bytes(B, Hq, N, d)
+                             : 0;
+}
+
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
 // Varlen workspace head: the sequence id of every packed row.
@@ -324,7 +344,7 @@ size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int N, int d, const a
     case ATTN_OP_FWD_FP8:
       return mods_bytes(B, N, f);
     case ATTN_OP_BWD:
-      return bwd_rowstat_bytes(B, Hq, N) + mods_bytes(B, N, f);
+      return bwd_rowstat_bytes(B, Hq, N) + mods_bytes(B, N, f) + bwd_fused_bytes(B, Hq, Hkv, N, d, f);
     case ATTN_OP_QUANT_FP8:
       return round_up((size_t)(B * Hq + 2 * B * Hkv) * sizeof(unsigned), 256);
     case ATTN_OP_FWD_VARLEN:
@@ -332,7 +352,9 @@ size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int N, int d, const a
       if (B != 1 || (f & ATTN_MOD_DOC)) return 0;
       const uint32_t fd = f | ATTN_MOD_DOC;  // the sequences are the documents
       return varlen_ids_bytes(N) +
-             (op == ATTN_OP_FWD_VARLEN ? mods_bytes(1, N, fd) : bwd_rowstat_bytes(1, Hq, N) + mods_bytes(1, N, fd));
+             (op == ATTN_OP_FWD_VARLEN ? mods_bytes(1, N, fd)
+                                       : bwd_rowstat_bytes(1, Hq, N) + mods_bytes(1, N, fd) +
+                                             bwd_fused_bytes(1, Hq, Hkv, N, d, fd));
     }
     default:
       return 0;
@@ -401,10 +423,24 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   L.dv = dv;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   L.rowstat = reinterpret_cast<float2*>(wsb);
-  if ((st = prepare_mods(L.p, wsb + bwd_rowstat_bytes(B, Hq, N), s)) != ATTN_OK) return st;
+  uint8_t* mregion = wsb + bwd_rowstat_bytes(B, Hq, N);
+  if ((st = prepare_mods(L.p, mregion, s)) != ATTN_OK) return st;
   if (events != nullptr)
     for (int e = 0; e < 4; ++e) L.events[e] = static_cast<cudaEvent_t>(events[e]);
-  return cuda_status(launch_bwd(L, d, has_score_mods(L.p.flags), needs_map(L.p.flags), s));
+  if (!bwd_fused(L.p.flags, d))
+    return cuda_status(launch_bwd(L, d, has_score_mods(L.p.flags), needs_map(L.p.flags), s));
+  uint8_t* fregion = mregion + mods_bytes(B, N, L.p.flags);
+  L.k = k;
+  L.v = v;
+  L.qscale = reinterpret_cast<float*>(fregion);
+  fregion += bwd_qscale_bytes(B, Hq, N);
+  L.kvb = reinterpret_cast<float2*>(fregion);
+  fregion += bwd_kvb_bytes(B, Hkv);
+  L.ticket = reinterpret_cast<int*>(fregion);
+  L.dqacc = reinterpret_cast<int*>(fregion + 256);
+  L.sms = sm_count();
+  if (L.sms < 1) return ATTN_ERR_CUDA;
+  return cuda_status(launch_bwd_fused(L, d, has_score_mods(L.p.flags), needs_map(L.p.flags), s));
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,

@@ -271,8 +271,6 @@ __global__ void __launch_bounds__(384, 1)
     bool doc_runs = false;
     const int2 run_j = doc ? doc_run(p, b, j, doc_runs) : make_int2(0, p.N);
     const bool doc_each = doc && !doc_runs;  // ids tested element by element
-    const uint64_t sc_in2 = f2_pack(sc_in, sc_in), sc_out2 = f2_pack(sc_out, sc_out);
-    const uint64_t one2 = f2_pack(1.f, 1.f);
     bool ok = true;
     // Test hook: warpgroup 0 waits on a phase nothing completes (attn_test_hooks).
     if ((p.stall & STALL_BWD) && w == 0) ok = wait_warp(&S.never, 0, ab);
@@ -299,61 +297,27 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(&S.xs_free);
 
         // P = exp2(x - LSE) (0 where masked); s[] keeps P (times the
-        // soft-cap derivative) for dS.  fp32 arithmetic in pairs.
-        int lo = causal ? j - i0 : -0x7fffffff;   // valid iff c >= lo
-        int hi = win ? p.window + j - i0 : 0x7fffffff;  // valid iff c < hi
+        // soft-cap derivative) for dS.
+        KvStep a;
+        a.scale_log2 = p.scale_log2;
+        a.sc_in = sc_in;
+        a.sc_out = sc_out;
+        a.al2 = al2;
+        a.al_base = al2 * (float)(j - i0);
+        a.lo = causal ? j - i0 : -0x7fffffff;
+        a.hi = win ? p.window + j - i0 : 0x7fffffff;
         if (doc_runs) {  // the query rows of this KV row's document: one interval
-          lo = max(lo, run_j.x - i0);
-          hi = min(hi, run_j.y - i0);
+          a.lo = max(a.lo, run_j.x - i0);
+          a.hi = min(a.hi, run_j.y - i0);
         }
-        const float al_base = al2 * (float)(j - i0);
-        const uint64_t al_base2 = f2_pack(al_base, al_base), nal2 = f2_pack(-al2, -al2);
-        const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
+        a.doc_cols = doc_each ? p.doc_ids + (size_t)b * p.N + i0 : nullptr;
+        a.doc_j = doc_j;
+        a.n_cols = p.N - i0;
+        a.sc = sc;
+        a.al = al;
+        a.partial = cls == CLS_PARTIAL;
         uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const uint64_t nl2 = f2_pack(__shfl_sync(0xffffffffu, my_nl2[c >> 5], c & 31),
-                                       __shfl_sync(0xffffffffu, my_nl2[(c + 1) >> 5], (c + 1) & 31));
-          const float s0 = __uint_as_float(s[c]), s1 = __uint_as_float(s[c + 1]);
-          uint64_t x2, dmul2 = 0;
-          if (sc || al) {
-            uint64_t y2 = f2_pack(s0, s1);
-            if (sc) {
-              const uint64_t t2 = tanh2_exp(f2_mul(y2, sc_in2));
-              y2 = f2_mul(t2, sc_out2);
-              dmul2 = f2_fma(t2, f2_neg(t2), one2);  // 1 - t^2
-            } else {
-              y2 = f2_mul(y2, sl2);
-            }
-            if (al) y2 = f2_fma(f2_pack((float)c, (float)(c + 1)), nal2, f2_add(y2, al_base2));
-            x2 = f2_add(y2, nl2);
-          } else {
-            x2 = f2_fma(f2_pack(s0, s1), sl2, nl2);
-          }
-          float x0, x1;
-          f2_unpack(x2, x0, x1);
-          float pe[2] = {ex2(x0), ex2(x1)};
-          if (cls == CLS_PARTIAL) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int cc = c + e;
-              bool valid = (cc >= lo) && (cc < hi);
-              if (doc_each && valid)
-                valid = (i0 + cc < p.N) && (__ldg(p.doc_ids + (size_t)b * p.N + i0 + cc) == doc_j);
-              if (!valid) pe[e] = 0.f;
-            }
-          }
-          pk[c / 2] = pack_bf16(pe[0], pe[1]);
-          if (sc) {
-            float q0, q1;
-            f2_unpack(f2_mul(f2_pack(pe[0], pe[1]), dmul2), q0, q1);
-            s[c] = __float_as_uint(q0);
-            s[c + 1] = __float_as_uint(q1);
-          } else {
-            s[c] = __float_as_uint(pe[0]);
-            s[c + 1] = __float_as_uint(pe[1]);
-          }
-        }
+        kv_row_p<MODS>(s, pk, my_nl2, a);
         // P^T(n) into TMEM once dV(n-1) has read P^T(n-1).
         if (n > 0) {
           if (!(ok = wait_warp(&S.pt_free, (n - 1) & 1, ab))) break;
@@ -374,15 +338,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_arrive(&S.xd_free);
 
         // dS = P (dP - D) (times the soft-cap derivative), in pairs.
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const uint64_t ndd = f2_pack(__shfl_sync(0xffffffffu, my_ndd[c >> 5], c & 31),
-                                       __shfl_sync(0xffffffffu, my_ndd[(c + 1) >> 5], (c + 1) & 31));
-          const uint64_t g2 = f2_add(f2_pack(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), ndd);
-          float ds0, ds1;
-          f2_unpack(f2_mul(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), g2), ds0, ds1);
-          pk[c / 2] = pack_bf16(ds0, ds1);
-        }
+        kv_row_ds<64>(s, dp, 0, my_ndd, pk);
         // dS^T(n) into TMEM once dK(n-1) has read dS^T(n-1).
         if (n > 0) {
           if (!(ok = wait_warp(&S.ds_free, (n - 1) & 1, ab))) break;

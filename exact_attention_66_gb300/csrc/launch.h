@@ -36,8 +36,20 @@ struct BwdLaunch {
   void* dv;
   AttnParams p;
   cudaEvent_t events[4];  // optional: recorded before pre / dkdv / dq and after dq
+  // One-kernel backward (causal masks, d = 128) only, all workspace:
+  const void* k;   // K, V (for the fixed-point bounds)
+  const void* v;
+  float2* kvb;     // [B, Hkv] {max |K|, max_j ||V_j||}
+  float* qscale;   // [B, Hq, nT*128] quantum multiplier of each query row's dQ
+  int* dqacc;      // [B, Hq, nT*128, d] int32 dQ sums in those quanta
+  int* ticket;     // work-item counter
+  int sms;         // persistent CTAs
 };
+// Two kernels after the row statistics (dK/dV kv-stationary, dQ q-stationary).
 cudaError_t launch_bwd(const BwdLaunch& L, int d, bool mods, bool masks, cudaStream_t st);
+// One main kernel (plus bounds, row statistics and a dQ conversion); needs
+// MOD_CAUSAL and d = 128.
+cudaError_t launch_bwd_fused(const BwdLaunch& L, int d, bool mods, bool masks, cudaStream_t st);
 
 // Decode step over a paged K/V cache (d = 64 or 128): q_len new tokens per sequence.
 struct DecodeParams {

@@ -123,14 +123,23 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  * V, the forward's O and LSE, and dO.  P is recomputed from LSE (the
  * FlashAttention-3 digest, "Rappel du fonctionnement": tiling and
  * recomputation).  The result is bitwise reproducible from run to run: no
- * floating-point atomics; every dQ, dK and dV tile is accumulated by one CTA
- * over its partner tiles in ascending order (contrast the FlexAttention/FA4
- * page, "Limitations actuelles": nondeterministic backward with block
- * sparsity).  dK/dV of a KV head sum over its query heads (GQA).
+ * floating-point atomics (contrast the FlexAttention/FA4 page, "Limitations
+ * actuelles": nondeterministic backward with block sparsity).  dK/dV of a KV
+ * head sum over its query heads (GQA).  Two implementations, chosen by the
+ * mods:
+ *  - causal with window / document parts, d = 128: one kernel computes dK, dV
+ *    and the dQ partials of every tile pair (5 GEMMs); each dQ partial is
+ *    rounded to an integer multiple of its row's quantum -- a power of two
+ *    chosen from a bound on |dQ| -- and summed as int32, so the sum does not
+ *    depend on the order the partials arrive in;
+ *  - otherwise: every dQ, dK and dV tile is accumulated by one CTA over its
+ *    partner tiles in ascending order (two kernels, 7 GEMMs per tile pair).
  * ws : workspace of attn_workspace_size(ATTN_OP_BWD, ...) bytes: the row
- *      statistics {LSE log2(e), D = rowsum(dO * O)} of every query row, and,
+ *      statistics {LSE log2(e), D = rowsum(dO * O)} of every query row;
  *      with window/document mods, the block map, its per-tile ranges and
- *      (documents) the document run of every position.
+ *      (documents) the document run of every position; for the one-kernel
+ *      form, the dQ quanta, K/V bounds and the int32 dQ sums (4 d bytes per
+ *      query row, rows padded to whole 128-row tiles).
  */
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
@@ -139,10 +148,12 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 
 /*
  * attn_bwd, plus timing: events[0..3] are cudaEvent_t handles created by the
- * caller; events[0] is recorded on `stream` before the row-sum kernel,
- * events[1] before the dK/dV kernel, events[2] before the dQ kernel and
- * events[3] after it (the block-map kernel, when the mods need one, runs
- * before events[0]).  Measurement aid for "profiler l'exécution" (the kernel
+ * caller, recorded on `stream`.  Two-kernel form: events[0] before the
+ * row-sum kernel, events[1] before the dK/dV kernel, events[2] before the dQ
+ * kernel, events[3] after it.  One-kernel form: events[0] before the bound and
+ * row-sum kernels, events[1] before the main kernel, events[2] before the dQ
+ * conversion, events[3] after it.  (The block-map kernels, when the mods need
+ * them, run before events[0].)  Measurement aid for "profiler l'exécution" (the kernel
  * fusion page, "Fusion et CUDA Graphs avec torch.compile"); results are
  * identical to attn_bwd.  events must not be NULL.
  */
@@ -172,7 +183,8 @@ attn_status_t attn_bwd_profiled(const void* q, const void* k, const void* v, con
  * Arguments, layout and errors are those of attn_bwd, without ws/ws_bytes.
  * Limit: the workspace attn_bwd would need, attn_workspace_size(ATTN_OP_BWD,
  * ...) (8 bytes per query row with rows padded to whole 128-row tiles, plus
- * the window / document mask data), must fit in ATTN_NOALLOC_SCRATCH_BYTES;
+ * the window / document mask data, plus 4 d + 4 bytes per padded query row
+ * when the one-kernel form runs), must fit in ATTN_NOALLOC_SCRATCH_BYTES;
  * otherwise the call returns ATTN_ERR_WORKSPACE before touching the device.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current).  Because CUDA loads

@@ -95,8 +95,18 @@ def test_workspace_sizes(L):
     m = L.make_mods(causal=True, window=64)
     # block map (B*nT*nT bytes) + per-Q-tile and per-KV-tile ranges (2 x B*nT int2), each 256-aligned
     assert ws(L.OP_FWD, 4, 16, 16, 4096, 128, m) == 4 * 32 * 32 + 2 * 1024
-    # one {LSE, D} float pair per query row, rows padded to whole 128-row tiles
+    # one {LSE, D} float pair per query row, rows padded to whole 128-row tiles ...
+    assert ws(L.OP_BWD, 1, 64, 8, 8192, 128, None) == 64 * 8192 * 8
     assert ws(L.OP_BWD, 1, 64, 8, 8192, 128, L.make_mods(causal=True)) == 64 * 8192 * 8
+    # ... and, for the one-kernel backward (causal with window / document parts,
+    # d = 128), a dQ quantum per padded query row, the K/V bounds (8 bytes per
+    # KV head, 256-aligned), the work-item counter (256 bytes) and the int32 dQ
+    # accumulator, after the mods region
+    mw = L.make_mods(causal=True, window=1024)
+    mods_region = 64 * 64 + 2 * 512  # block map, tile ranges (1 x 64 int2 each, 256-aligned)
+    fused = 64 * 8192 * 4 + 256 + 256 + 64 * 8192 * 128 * 4
+    assert ws(L.OP_BWD, 1, 64, 8, 8192, 128, mw) == 64 * 8192 * 8 + mods_region + fused
+    # d = 64 runs the two-kernel backward: no extra workspace
     assert ws(L.OP_BWD, 2, 2, 2, 1000, 64, m) == 2 * 2 * 1024 * 8 + 256 + 2 * 256
     assert ws(L.OP_QUANT_FP8, 2, 16, 16, 16384, 128, None) == 512  # 96 fp32 amax words
     assert ws(L.OP_FWD, 1, 3, 2, 128, 128, None) == 0  # invalid shape -> 0

@@ -47,3 +47,13 @@ def test_peak_follows_the_clock_record():
     assert p == 1900.0 and "sw_power_cap" in why
     p, _ = bench.bf16_peak(peaks, "measured", {"sm_mhz": None, "sm_max_mhz": None, "reasons": []})
     assert p == 1900.0
+
+
+def test_computed_pairs_of_analytic_masks():
+    # causal: the nT (nT + 1) / 2 non-skipped tiles of every batch entry
+    cfg = dict(B=2, N=1000, causal=True)
+    assert bench.computed_pairs(None, cfg, None, None) == 2 * 8 * 9 // 2 * 128 * 128
+    assert bench.computed_pairs(None, dict(B=1, N=300), None, None) == 9 * 128 * 128
+    # the computed area always covers the allowed pairs
+    full = dict(B=1, Hq=1, Hkv=1, N=8192, d=128, causal=True)
+    assert bench.allowed_pairs(full) <= bench.computed_pairs(None, full, None, None)

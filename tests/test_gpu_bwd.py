@@ -30,6 +30,15 @@ CASES = [
 ]
 
 
+# More work items (batch x KV head x KV tile) than SMs: each CTA of the
+# persistent causal backward takes several items in turn.
+MANY = [
+    (2, 16, 16, 2048, 128, dict(causal=True)),
+    (4, 8, 2, 1536, 64, dict(causal=True, window=700)),
+    (3, 8, 4, 1300, 128, dict(causal=True, doc=True, softcap=30.0, alibi=True)),
+]
+
+
 def _ids(c):
     B, Hq, Hkv, N, d, m = c
     return f"B{B}_H{Hq}x{Hkv}_N{N}_d{d}_" + ("-".join(m) or "none")
@@ -52,7 +61,7 @@ def _run(case, seed):
     return x, om, s, (dq, dk, dv), (o, lse, dev, m)
 
 
-@pytest.mark.parametrize("case", CASES, ids=_ids)
+@pytest.mark.parametrize("case", CASES + MANY, ids=_ids)
 def test_backward_parity(case):
     x, om, s, (dq, dk, dv), _ = _run(case, seed=300 + case[3] + case[4])
     dQ, dK, dV = attn64.backward(x["q"], x["k"], x["v"], x["do"], s, om)
@@ -61,11 +70,17 @@ def test_backward_parity(case):
         assert e <= GRAD_TOL, (name, e)
 
 
-@pytest.mark.parametrize("case", [CASES[2], CASES[11]], ids=_ids)
+# MHA with many short work items per CTA (item boundaries in every CTA), plain
+# causal (two-kernel backward) and with a window (one-kernel backward)
+REPRO = [CASES[2], CASES[11], MANY[0], (8, 16, 16, 1024, 128, dict(causal=True)),
+         (8, 16, 16, 1024, 128, dict(causal=True, window=300))]
+
+
+@pytest.mark.parametrize("case", REPRO, ids=_ids)
 def test_backward_is_bitwise_reproducible(case):
     ea = lib()
     x, om, s, g1, (o, lse, dev, m) = _run(case, seed=9)
-    for _ in range(2):
+    for _ in range(6):
         g2 = ea.backward(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], s, m)
         ea.attn_status()
         for a, b in zip(g1, g2):
