@@ -378,10 +378,22 @@ __global__ void __launch_bounds__(384, 1)
       };
       int J = union_next(p, b, I0, J_begin, J_end);
       int c = CLS_SKIP;
+      // Half-period offset of Q tile 1 in long CTAs: its first S waits until
+      // Q tile 0's softmax has produced its first P, so that tile 1's GEMMs run
+      // while tile 0's exponentials do.  Left alone, the two tiles share every
+      // K/V slot and run in lockstep: both softmax warpgroups compute at once
+      // while the tensor pipe idles (clock stamps on the GQA 8K workload:
+      // both S issued within 2 cycles of each other, 3950 cycles per KV tile
+      // for 2048 of MMA).  The offset decays over some 25 KV tiles as the
+      // shared ring pulls the tiles together again, and costs half a period at
+      // the start, so short CTAs keep the plain start (measured: GQA 8K
+      // forward -4.0 %, MHA 2K and flex workloads unchanged).
       if (ok && J < J_end) {
         int ks;
         ok = slot(ks);
         c = tile_class(p, b, I, J);
+        if (ok && t == 1 && J_end - J_begin >= 24 && c != CLS_SKIP && tile_class(p, b, I0, J) != CLS_SKIP)
+          ok = mbar_wait(&S.p_full[0], 0, ab);
         if (ok) {
           if (c != CLS_SKIP) issue_S(sR + ks * C::TILE_BYTES);
           mma_commit(&S.empty[ks]);
