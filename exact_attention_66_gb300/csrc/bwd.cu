@@ -12,10 +12,10 @@
 //  * bwd_dkdv: one CTA per (batch, KV head, 128-row KV tile).  K_J and V_J stay
 //    in shared memory; Q tiles (3-slot TMA ring) and dO tiles (2-slot ring) of
 //    every query head of the GQA group and every needed Q tile stream past
-//    them.  S^T = K Q^T and dP^T = V dO^T land in one shared TMEM region; two
-//    softmax warpgroups (a thread per KV row, 64 query columns each) turn them
-//    into P^T and dS^T, packed bf16 in TMEM; dV += P^T dO and dK += dS^T Q
-//    read their A operand from TMEM.
+//    them.  S^T = K Q^T and dP^T = V dO^T land in TMEM regions of their own;
+//    two softmax warpgroups (a thread per KV row, 64 query columns each) turn
+//    them into P^T and dS^T, packed bf16 into the dP^T region; dV += P^T dO
+//    and dK += dS^T Q read their A operand from TMEM.
 //  * bwd_dq:   one CTA per (batch, query head, 128-row Q tile), streaming K/V
 //    tiles: S = Q K^T and dP = dO V^T in TMEM, dS to shared memory,
 //    dQ += dS K.
@@ -34,13 +34,19 @@ namespace attn {
 
 // ================================================================== dK, dV
 // Shared memory: K_J, V_J, a 3-slot Q ring and a 2-slot dO ring.  TMEM (512 columns):
-//   X   [0, 128)        S^T(n), then dP^T(n) once the softmax has copied S^T out
-//   P^T [128, 192)      packed bf16, A operand of dV += P^T dO
-//   dS^T [192, 256)     packed bf16, A operand of dK += dS^T Q
+//   XS  [0, 128)        S^T(n), copied to registers and handed back at once
+//   XD  [128, 256)      dP^T(n); then, per softmax warpgroup w (query columns
+//                       [64 w, 64 w + 64)), packed bf16 dS^T(n) at columns
+//                       [64 w, 64 w + 32) (A of dK += dS^T Q) and P^T(n) at
+//                       [64 w + 32, 64 w + 64) (A of dV += P^T dO)
 //   dV  [256, 256 + D), dK [256 + D, 256 + 2D)  fp32 accumulators
-// Sharing X between S^T and dP^T leaves room for P^T and dS^T in TMEM, so no
-// GEMM of the next step waits for an accumulation of this one, and dV / dK
-// read their A operand from TMEM instead of shared memory.
+// A warpgroup writes only columns it has already loaded, so it overwrites
+// nothing the other has yet to read.  The tensor pipe runs one CTA's MMAs in
+// issue order, so dP^T(n+1) may be issued right behind dK(n), the last reader
+// of the region.  Because P^T does not stay in XS, S^T(n+1) is computed while
+// the softmax works on P(n); per step the softmax waits for one GEMM only,
+// dP^T.  (P^T in place over S^T kept S^T(n+1) waiting for the exponentials of
+// P(n): 3660 cycles a step against 2048 of MMA.)
 template <int D>
 struct KvCfg {
   static constexpr int CH = D / 64;
@@ -62,15 +68,13 @@ struct KvBars {
   uint64_t in_full;              // K_J, V_J
   uint64_t qfull[3], qempty[3];  // Q ring
   uint64_t dfull[2], dempty[2];  // dO ring
-  uint64_t s_full;             // S^T(n) in X                (MMA commit)
-  uint64_t xs_free;            // S^T(n) copied out of X     (256 softmax threads)
-  uint64_t dp_full;            // dP^T(n) in X               (MMA commit)
-  uint64_t xd_free;            // dP^T(n) copied out of X    (256)
-  uint64_t p_full;             // P^T(n) stored in TMEM      (256)
-  uint64_t pt_free;            // dV(n) done reading P^T     (MMA commit)
-  uint64_t ds_full;            // dS^T(n) stored in TMEM     (256)
-  uint64_t ds_free;            // dK(n) done reading dS^T    (MMA commit)
-  uint64_t fin;                // every MMA done
+  uint64_t s_full;             // S^T(n) in XS               (MMA commit)
+  uint64_t xs_free;            // S^T(n) copied out of XS    (256 softmax threads)
+  uint64_t dp_full;            // dP^T(n) in XD              (MMA commit)
+  uint64_t p_full;             // P^T(n) stored in XD        (256)
+  uint64_t ds_full;            // dS^T(n) stored in XD       (256)
+  uint64_t fin;                // every MMA of the dV / dK / dP^T issuer done
+  uint64_t fin_s;              // every MMA of the S^T issuer done
   uint64_t never;              // test hook: a phase that nothing completes
   uint32_t tmem_base;
   int abort;
@@ -136,12 +140,10 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&S.s_full, 1);
     mbar_init(&S.xs_free, 256);
     mbar_init(&S.dp_full, 1);
-    mbar_init(&S.xd_free, 256);
     mbar_init(&S.p_full, 256);
-    mbar_init(&S.pt_free, 1);
     mbar_init(&S.ds_full, 256);
-    mbar_init(&S.ds_free, 1);
     mbar_init(&S.fin, 1);
+    mbar_init(&S.fin_s, 1);
     mbar_init(&S.never, 1);
     fence_mbar_init();
   }
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sV = smem_u32(smem + C::V_OFF);
   const uint32_t sQ = smem_u32(smem + C::Q_OFF);
   const uint32_t sDO = smem_u32(smem + C::DO_OFF);
-  const uint32_t tX = tmem, tPT = tmem + 128, tDS = tmem + 192;
+  const uint32_t tXS = tmem, tXD = tmem + 128;
   const uint32_t tdV = tmem + 256, tdK = tmem + 256 + D;
 
   if (warp < 4) regs_dec<BWD_REGS_LOW>();
@@ -196,12 +198,14 @@ __global__ void __launch_bounds__(384, 1)
         if (nd > s) mbar_wait_drain(&S.dfull[s], ((nd - 1 - s) / C::DOS) & 1);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // One thread issues every GEMM, in the order in which the softmax releases
-    // X and fills P^T / dS^T, so it never waits on an event that comes after
-    // one it could already act on: per step n, dP(n), dV(n), S(n+1), dK(n).
-    // (Putting the X chain ahead of the accumulations -- S(n+1), dV(n),
-    // dP(n+1), dK(n) -- measured slower.)
+    // ---------------------------------------------- MMA issuer: dV, dK, dP^T
+    // Per step n: dV(n) once P^T(n) is stored, then dK(n) and dP(n+1) once
+    // dS^T(n) is.  dP^T(n+1) overwrites XD behind the two GEMMs that read it
+    // (issue order), and one thread issuing every accumulation fixes their
+    // order.  The S^T chain has a thread of its own (warp 2): the tensor pipe
+    // queues few MMAs, and one thread issuing both chains answered each
+    // softmax hand-off only after issuing the other chain's GEMMs (4000 cycles
+    // a step, 3050 of them spent issuing).
     if (lane == 0) {
       bool ok = mbar_wait(&S.in_full, 0, ab);
       tc_fence_after();
@@ -209,50 +213,59 @@ __global__ void __launch_bounds__(384, 1)
         int g = 0, I = steps.I_first, n = 0;
         auto q_at = [&](int m) { return sQ + (uint32_t)((m % C::QS) * C::TB); };
         auto do_at = [&](int m) { return sDO + (uint32_t)((m % C::DOS) * C::TB); };
-        // S^T(m) = K Q(m)^T into X once dP^T(m-1) has been copied out.
-        auto issue_s = [&](int m) -> bool {
-          if (m > 0 && !mbar_wait(&S.xd_free, (m - 1) & 1, ab)) return false;
-          if (!mbar_wait(&S.qfull[m % C::QS], (m / C::QS) & 1, ab)) return false;
-          tc_fence_after();
-          issue_nt<D * 2>(tX, sK, q_at(m));
-          mma_commit(&S.s_full);
-          return true;
-        };
-        // dP^T(m) = V dO(m)^T into X once S^T(m) has been copied out.
+        // dP^T(m) = V dO(m)^T into XD.
         auto issue_dp = [&](int m) -> bool {
-          if (!mbar_wait(&S.xs_free, m & 1, ab)) return false;
           if (!mbar_wait(&S.dfull[m % C::DOS], (m / C::DOS) & 1, ab)) return false;
           tc_fence_after();
-          issue_nt<D * 2>(tX, sV, do_at(m));
+          issue_nt<D * 2>(tXD, sV, do_at(m));
           mma_commit(&S.dp_full);
           return true;
         };
-        ok = issue_s(0);
+        ok = issue_dp(0);
         while (ok) {
-          int g2 = g, I2 = I;
-          const bool has_next = steps.advance(p, b, g2, I2);
-          if (!(ok = issue_dp(n))) break;
+          const bool has_next = steps.advance(p, b, g, I);
           // dV += P^T(n) dO(n); dO(n) is free after it.
           if (!(ok = mbar_wait(&S.p_full, n & 1, ab))) break;
           tc_fence_after();
-          issue_acc<D, true>(tdV, 0, tPT, do_at(n), n == 0);
-          mma_commit(&S.pt_free);
+          issue_acc_inplace<D>(tdV, tXD + 32, do_at(n), n == 0);
           mma_commit(&S.dempty[n % C::DOS]);
-          if (has_next && !(ok = issue_s(n + 1))) break;
-          // dK += dS^T(n) Q(n); Q(n) is free after it.
+          // dK += dS^T(n) Q(n); Q(n) is free after it (S^T(n) completed
+          // before the softmax stored dS^T(n)).
           if (!(ok = mbar_wait(&S.ds_full, n & 1, ab))) break;
           tc_fence_after();
-          issue_acc<D, true>(tdK, 0, tDS, q_at(n), n == 0);
-          mma_commit(&S.ds_free);
+          issue_acc_inplace<D>(tdK, tXD, q_at(n), n == 0);
           mma_commit(&S.qempty[n % C::QS]);
           if (!has_next) break;
-          g = g2;
-          I = I2;
+          if (!(ok = issue_dp(n + 1))) break;
           ++n;
         }
       }
       mma_commit(&S.fin);
       mbar_wait_drain(&S.fin, 0);
+    }
+  } else if (warp == 2) {
+    // --------------------------------------------------- MMA issuer: S^T
+    // S^T(n) = K Q(n)^T into XS once the softmax has copied S^T(n-1) out.
+    // Each S^T(n) completes before the softmax goes on with step n, so none is
+    // in flight when the other issuer's last commit (fin) completes.
+    if (lane == 0) {
+      bool ok = mbar_wait(&S.in_full, 0, ab);
+      tc_fence_after();
+      if (ok && any) {
+        int g = 0, I = steps.I_first, n = 0;
+        do {
+          if (n > 0 && !(ok = mbar_wait(&S.xs_free, (n - 1) & 1, ab))) break;
+          if (!(ok = mbar_wait(&S.qfull[n % C::QS], (n / C::QS) & 1, ab))) break;
+          tc_fence_after();
+          issue_nt<D * 2>(tXS, sK, sQ + (uint32_t)((n % C::QS) * C::TB));
+          mma_commit(&S.s_full);
+          ++n;
+        } while (steps.advance(p, b, g, I));
+      }
+      // On an early exit S^T(n) may still be running: let it finish before
+      // the CTA frees its TMEM.
+      mma_commit(&S.fin_s);
+      mbar_wait_drain(&S.fin_s, 0);
     }
   } else if (warp >= 4) {
     // ---------------------------------------------- softmax / dS warpgroups
@@ -287,11 +300,11 @@ __global__ void __launch_bounds__(384, 1)
         const float2 rs0 = rs[lane], rs1 = rs[32 + lane];
         const float my_nl2[2] = {-rs0.x, -rs1.x}, my_ndd[2] = {-rs0.y, -rs1.y};
 
-        // S^T(n) -> registers, X back to the MMA pipe.
+        // S^T(n) -> registers, XS back to the MMA pipe (S^T(n+1)).
         if (!(ok = wait_warp(&S.s_full, n & 1, ab))) break;
         tc_fence_after();
         uint32_t s[64];
-        tmem_ld64(tX + lane_off + 64 * w, s);
+        tmem_ld64(tXS + lane_off + 64 * w, s);
         tmem_wait64(s);
         tc_fence_before();
         mbar_arrive(&S.xs_free);
@@ -316,35 +329,34 @@ __global__ void __launch_bounds__(384, 1)
         a.sc = sc;
         a.al = al;
         a.partial = cls == CLS_PARTIAL;
-        uint32_t pk[32];
+        // P as packed bf16 (pk, the A operand of dV) and the factor of dS
+        // (pd: P times the soft-cap derivative, else P), also bf16, which
+        // keeps the registers live across the dP^T loads to pk, pd, dp and o.
+        uint32_t pk[32], pd[32];
         kv_row_p<MODS>(s, pk, my_nl2, a);
-        // P^T(n) into TMEM once dV(n-1) has read P^T(n-1).
-        if (n > 0) {
-          if (!(ok = wait_warp(&S.pt_free, (n - 1) & 1, ab))) break;
-          tc_fence_after();
-        }
-        tmem_st32(tPT + lane_off + 32 * w, pk);
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          pd[q] = sc ? pack_bf16(__uint_as_float(s[2 * q]), __uint_as_float(s[2 * q + 1])) : pk[q];
+
+        // dS = P (dP - D) (times the soft-cap derivative), in pairs, from the
+        // two 32-column halves of this warpgroup's dP^T columns: the second
+        // half first, so that P^T(n) can go there at once (dV(n-1) and
+        // dK(n-1) read XD before dP^T(n) overwrote it), then the first half,
+        // which dS^T(n) replaces.
+        if (!(ok = wait_warp(&S.dp_full, n & 1, ab))) break;
+        tc_fence_after();
+        uint32_t dp[32], o[32];
+        tmem_ld32(tXD + lane_off + 64 * w + 32, dp);
+        tmem_wait_ld(dp);
+        kv_row_ds_bf16<32>(pd + 16, dp, 32, my_ndd, o + 16);
+        tmem_st32(tXD + lane_off + 64 * w + 32, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&S.p_full);
-
-        // dP^T(n) -> registers, X back to the MMA pipe.
-        if (!(ok = wait_warp(&S.dp_full, n & 1, ab))) break;
-        tc_fence_after();
-        uint32_t dp[64];
-        tmem_ld64(tX + lane_off + 64 * w, dp);
-        tmem_wait64(dp);
-        tc_fence_before();
-        mbar_arrive(&S.xd_free);
-
-        // dS = P (dP - D) (times the soft-cap derivative), in pairs.
-        kv_row_ds<64>(s, dp, 0, my_ndd, pk);
-        // dS^T(n) into TMEM once dK(n-1) has read dS^T(n-1).
-        if (n > 0) {
-          if (!(ok = wait_warp(&S.ds_free, (n - 1) & 1, ab))) break;
-          tc_fence_after();
-        }
-        tmem_st32(tDS + lane_off + 32 * w, pk);
+        tmem_ld32(tXD + lane_off + 64 * w, dp);
+        tmem_wait_ld(dp);
+        kv_row_ds_bf16<32>(pd, dp, 0, my_ndd, o);
+        tmem_st32(tXD + lane_off + 64 * w, o);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&S.ds_full);
@@ -519,7 +531,7 @@ __global__ void __launch_bounds__(384, 1)
         } else {
           if (!(ok = mbar_wait(&S.p_full, n & 1, ab))) break;
           tc_fence_after();
-          issue_acc<D, false>(tdQ, sDS, 0, k_sm, n == 0);
+          issue_acc<D>(tdQ, sDS, k_sm, n == 0);
           mma_commit(&S.acc_done);
           mma_commit(&S.kempty[ks]);
         }

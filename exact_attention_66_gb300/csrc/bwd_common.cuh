@@ -195,23 +195,31 @@ __device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int r, uin
   }
 }
 
-// D(tmem, 128 x D) += A(128 x 128 keys) B(128 keys x D, MN-major in shared
-// memory).  A is a K-major shared-memory tile (A_TMEM false; a_tmem ignored)
-// or packed bf16 in TMEM (A_TMEM true; a_smem ignored).
-template <int D, bool A_TMEM>
-__device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_smem, uint32_t a_tmem,
-                                          uint32_t b_smem, bool first) {
+// D(tmem, 128 x D) (+)= A(128 x 128 keys) B(128 keys x D, MN-major in shared
+// memory), A a K-major shared-memory tile.
+template <int D>
+__device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, bool first) {
   constexpr uint32_t id = idesc_bf16(128, D, false, true);
   const uint64_t ad = opaque(sdesc_sw128(a_smem, 16, 1024)), bd = opaque(sdesc_sw128(b_smem, 16384, 1024));
 #pragma unroll
-  for (int kk = 0; kk < TILE / 16; ++kk) {
-    const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-    const uint64_t b = sdesc_add(bd, kk * 16 * 128);
-    if (A_TMEM)
-      mma_f16_ts(d_tmem, a_tmem + kk * 8, b, id, acc);
-    else
-      mma_f16_ss(d_tmem, sdesc_add(ad, (kk / 4) * 16384 + (kk % 4) * 32), b, id, acc);
-  }
+  for (int kk = 0; kk < TILE / 16; ++kk)
+    mma_f16_ss(d_tmem, sdesc_add(ad, (kk / 4) * 16384 + (kk % 4) * 32), sdesc_add(bd, kk * 16 * 128), id,
+               (first && kk == 0) ? 0u : 1u);
+}
+
+// The same with A packed bf16 in TMEM, written in place over a 128-column
+// fp32 tile by the two softmax warpgroups: keys [64 h, 64 h + 64) at TMEM
+// columns [64 h, 64 h + 32) of a_tmem, each warpgroup inside the columns it
+// read, so neither overwrites values the other has still to load.
+template <int D>
+__device__ __forceinline__ void issue_acc_inplace(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
+                                                  bool first) {
+  constexpr uint32_t id = idesc_bf16(128, D, false, true);
+  const uint64_t bd = opaque(sdesc_sw128(b_smem, 16384, 1024));
+#pragma unroll
+  for (int kk = 0; kk < TILE / 16; ++kk)
+    mma_f16_ts(d_tmem, a_tmem + (kk / 4) * 64 + (kk % 4) * 8, sdesc_add(bd, kk * 16 * 128), id,
+               (first && kk == 0) ? 0u : 1u);
 }
 
 // Store 32 packed bf16 words (64 consecutive columns starting at 64 * w) of
@@ -342,27 +350,11 @@ __device__ __forceinline__ void kv_row_p(uint32_t (&s)[64], uint32_t (&pk)[32], 
   kv_row_p_cols<MODS, 64>(s, pk, 0, nl2, a);
 }
 
-// dS^T(j, i0 + c) = P (dP - D) (times the soft-cap derivative, folded into s
-// by kv_row_p) for NC columns starting at column c0, packed bf16 into pk;
-// ndd[e] = -D of query rows i0 + e * 32 + lane, broadcast by shuffles.
-template <int NC>
-__device__ __forceinline__ void kv_row_ds(const uint32_t (&s)[64], const uint32_t* dp, int c0,
-                                          const float (&ndd)[2], uint32_t* pk) {
-#pragma unroll
-  for (int k = 0; k < NC; k += 2) {
-    const int c = c0 + k;
-    const uint64_t nd = f2_pack(__shfl_sync(0xffffffffu, ndd[c >> 5], c & 31),
-                                __shfl_sync(0xffffffffu, ndd[(c + 1) >> 5], (c + 1) & 31));
-    const uint64_t g2 = f2_add(f2_pack(__uint_as_float(dp[k]), __uint_as_float(dp[k + 1])), nd);
-    float ds0, ds1;
-    f2_unpack(f2_mul(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), g2), ds0, ds1);
-    pk[k / 2] = pack_bf16(ds0, ds1);
-  }
-}
-
-// dS^T as kv_row_ds, with P (times the soft-cap derivative) given as packed
-// bf16: pd[k] holds columns c0 + 2k, c0 + 2k + 1.  Keeps the caller's
-// register footprint to half of the fp32 form.
+// dS^T(j, i0 + c) = P (dP - D) (times the soft-cap derivative) for NC
+// columns starting at column c0, packed bf16 into pk; P (times the
+// derivative) given as packed bf16, pd[k] holding columns c0 + 2k, c0 + 2k + 1
+// (half the registers of fp32); ndd[e] = -D of query rows i0 + e * 32 + lane,
+// broadcast by shuffles.
 template <int NC>
 __device__ __forceinline__ void kv_row_ds_bf16(const uint32_t* pd, const uint32_t* dp, int c0,
                                                const float (&ndd)[2], uint32_t* pk) {

@@ -134,19 +134,6 @@ __device__ __forceinline__ void red_add_s32(int* a, int v) {
   asm volatile("red.global.add.s32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
 }
 
-// D(tmem, 128 x D) (+)= P^T(TMEM) dO: P^T packed bf16 in X, query columns
-// [64 h, 64 h + 64) at TMEM columns [64 h, 64 h + 32) (each softmax
-// warpgroup packs its half in place of its own S^T columns).
-template <int D>
-__device__ __forceinline__ void issue_dv(uint32_t d_tmem, uint32_t x_tmem, uint32_t b_smem, bool first) {
-  constexpr uint32_t id = idesc_bf16(128, D, false, true);
-  const uint64_t bd = opaque(sdesc_sw128(b_smem, 16384, 1024));
-#pragma unroll
-  for (int kk = 0; kk < TILE / 16; ++kk)
-    mma_f16_ts(d_tmem, x_tmem + (kk / 4) * 64 + (kk % 4) * 8, sdesc_add(bd, kk * 16 * 128), id,
-               (first && kk == 0) ? 0u : 1u);
-}
-
 // The dQ partial of a step, dQ^T(tmem, 128 head-dimension lanes x 128 query
 // columns) = K^T dS^T, with K and the dS^T tile both read MN-major (the
 // head-dimension, resp. query, columns contiguous in 64-column chunks of the
@@ -314,7 +301,7 @@ __global__ void __launch_bounds__(FU_THREADS, 1)
             if (!(ok = mbar_wait(&S.p_full, m & 1, ab))) break;
             if (c > 0 && !(ok = mbar_wait(&S.acc_free, (c - 1) & 1, ab))) break;
             tc_fence_after();
-            issue_dv<D>(tdV, tX, do_at(m), true);
+            issue_acc_inplace<D>(tdV, tX, do_at(m), true);
           }
           mma_commit(&S.dempty[m & 1]);  // dO(m): read by dV(m) and dP(m)
           if (has_next) {
@@ -325,7 +312,7 @@ __global__ void __launch_bounds__(FU_THREADS, 1)
           }
           if (!(ok = mbar_wait(&S.ds_full, m & 1, ab))) break;
           tc_fence_after();
-          issue_acc<D, false>(tdK, sDS, 0, q_at(m), first);
+          issue_acc<D>(tdK, sDS, q_at(m), first);
           mma_commit(&S.qempty[m & 1]);  // Q(m): read by S(m) and dK(m)
           issue_dq(tY, sDS, sK);
           mma_commit(&S.dq_full);
@@ -340,7 +327,7 @@ __global__ void __launch_bounds__(FU_THREADS, 1)
           if (!(ok = mbar_wait(&S.p_full, (m + 1) & 1, ab))) break;
           if (!(ok = mbar_wait(&S.dfull[(m + 1) & 1], ((m + 1) >> 1) & 1, ab))) break;
           tc_fence_after();
-          issue_dv<D>(tdV, tX, do_at(m + 1), false);
+          issue_acc_inplace<D>(tdV, tX, do_at(m + 1), false);
           I = I2;
           g = g2;
           first = false;
