@@ -261,12 +261,22 @@ def traffic_record(kernel: str):
         return None
     if not rec:
         return None
-    src = os.path.join(ROOT, "exact_attention_66_gb300", "csrc", rec["source"])
+    h = sources_sha(rec["source"])
+    return rec["bytes_per_launch"] if h is not None and h == rec.get("source_sha") else None
+
+
+def sources_sha(names) -> str | None:
+    """First 16 hex digits of the SHA-256 of the named kernel sources (one file
+    name or a list, concatenated in the given order)."""
+    names = [names] if isinstance(names, str) else list(names)
+    m = hashlib.sha256()
     try:
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for n in names:
+            with open(os.path.join(ROOT, "exact_attention_66_gb300", "csrc", n), "rb") as f:
+                m.update(f.read())
     except OSError:
         return None
-    return rec["bytes_per_launch"] if h == rec.get("source_sha") else None
+    return m.hexdigest()[:16]
 
 
 def computed_pairs(ea, cfg, mods, dev) -> int:
