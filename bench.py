@@ -393,7 +393,10 @@ def run_ours(args, world, rank, local):
     mods, docs = workload_mods(ea, cfg, x, dev)
     nws_f = ea.attn_workspace_size(ea.OP_FWD, B, Hq, Hkv, N, d, mods)
     ws_f = torch.empty(max(nws_f, 1), dtype=torch.uint8, device=dev)
-    nws = ea.attn_workspace_size(ea.OP_BWD, B, Hq, Hkv, N, d, mods)
+    # --bwd-fp8: the opt-in mixed e4m3 backward (d = 128, at most the causal mask)
+    bwd_fp8 = bool(args.bwd_fp8) and not fwd_only
+    bmods = ea.make_mods(causal=cfg.get("causal", False), bwd_fp8=True) if bwd_fp8 else mods
+    nws = ea.attn_workspace_size(ea.OP_BWD, B, Hq, Hkv, N, d, bmods)
     ws = torch.empty(nws, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     with_map = bool(cfg.get("window") or cfg.get("doc"))
@@ -412,13 +415,13 @@ def run_ours(args, world, rank, local):
         if ev is None:
             fwd()
             if not fwd_only:
-                ea.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods, ws, nws, stream)
+                ea.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, bmods, ws, nws, stream)
         else:
             ev[0].record(stream)
             fwd()
             ev[1].record(stream)
             if not fwd_only:
-                ea.attn_bwd_profiled(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, mods,
+                ea.attn_bwd_profiled(q, k, v, o, do, lse, dq, dk, dv, B, Hq, Hkv, N, d, scale, bmods,
                                      ws, nws, stream, ev[2:6])
 
     for _ in range(args.warmup):
@@ -472,7 +475,7 @@ def run_ours(args, world, rank, local):
             ob, lb, dqb, dkb, dvb = (dev_out[n][b] for n in ("o", "lse", "dq", "dk", "dv"))
             fo, fl = ea.forward(qb, kb, vb, scale, mods, out=ob, lse=lb, stream=stream)
             if not fwd_only:
-                ea.attn_bwd(qb, kb, vb, fo, dob, fl, dqb, dkb, dvb, B, Hq, Hkv, N, d, scale, mods, ws, nws, stream)
+                ea.attn_bwd(qb, kb, vb, fo, dob, fl, dqb, dkb, dvb, B, Hq, Hkv, N, d, scale, bmods, ws, nws, stream)
 
         e2e_ms = pipelined_e2e(dev, stream, [(host[n], dev_in[n]) for n in in_names],
                                [(dev_out[n], host_out[n]) for n in out_names], compute, e2e_steps, world)
@@ -501,8 +504,9 @@ def run_ours(args, world, rank, local):
         kernels.update({"bwd_fused": (mean(k_kv), bwd_f), "bwd_pre": (mean(k_pre), 0.0),
                         "bwd_dq_convert": (mean(k_dq), 0.0)})
     elif not fwd_only:
-        kernels.update({"bwd_dkdv": (mean(k_kv), 0.8 * bwd_f), "bwd_dq": (mean(k_dq), 0.2 * bwd_f),
-                        "bwd_pre": (mean(k_pre), 0.0)})
+        kernels.update({"bwd_dkdv_e4m3" if bwd_fp8 else "bwd_dkdv": (mean(k_kv), 0.8 * bwd_f),
+                        "bwd_dq": (mean(k_dq), 0.2 * bwd_f),
+                        "bwd_quant_and_pre" if bwd_fp8 else "bwd_pre": (mean(k_pre), 0.0)})
     dom = max(kernels, key=lambda n: kernels[n][0])
     dom_ms, dom_flops = kernels[dom]
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
@@ -519,13 +523,16 @@ def run_ours(args, world, rank, local):
                     "traffic": None, "bytes_per_launch": nbytes,
                     "peak_source": f"{src} hbm_gbs (inputs stay in L2 between steps: warm)"}
     map_launches = (3 if cfg.get("doc") else 2) if with_map else 0  # document runs, block map, tile ranges
-    bwd_launches = 0 if fwd_only else (4 if fused_bwd else 3) + map_launches
+    bwd_launches = 0 if fwd_only else (4 if fused_bwd else 3) + map_launches + (3 if bwd_fp8 else 0)
     launches = 1 + map_launches + bwd_launches
     line = {
-        "metric": METRIC if name == WORKLOAD else f"attention TFLOPS fwd{'' if fwd_only else '/bwd'} ({name})",
+        "metric": (METRIC if name == WORKLOAD and not bwd_fp8 else
+                   f"attention TFLOPS fwd{'' if fwd_only else '/bwd'} ({name}"
+                   + (", mixed e4m3 backward: e4m3 dP and dV GEMMs)" if bwd_fp8 else ")")),
         "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 + e4m3 (dP, dV)" if bwd_fp8 else "bf16",
         "data": "synthetic",
         "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
                    "mask": mods_label(cfg), "parallelism": f"replicas{world}" if world > 1 else "single",
@@ -967,6 +974,8 @@ def main():
                     help="workload to time; the default is the one the metric is quoted on")
     ap.add_argument("--batch", type=int, default=0,
                     help="paged decode workloads only: this many sequences instead of the workload's (profiling)")
+    ap.add_argument("--bwd-fp8", action="store_true",
+                    help="time the opt-in mixed e4m3 backward (ATTN_MOD_BWD_FP8; d = 128, at most a causal mask)")
     ap.add_argument("--heads", type=int, default=0,
                     help="query heads for a smaller profiling case (8 per KV head; fp8_outliers_16k: as many KV "
                          "heads); default: the workload's")

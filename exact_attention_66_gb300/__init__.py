@@ -12,7 +12,7 @@ from __future__ import annotations
 import math
 
 from ._lib import (  # noqa: F401
-    AttnError, Mods, EXPORTS, MOD_ALIBI, MOD_CAUSAL, MOD_DOC, MOD_SOFTCAP, MOD_WINDOW, OP_BWD,
+    AttnError, Mods, EXPORTS, MOD_ALIBI, MOD_BWD_FP8, MOD_CAUSAL, MOD_DOC, MOD_SOFTCAP, MOD_WINDOW, OP_BWD,
     OP_BWD_VARLEN, OP_DECODE_PAGED, OP_FWD, OP_FWD_FP8, OP_FWD_VARLEN, OP_QUANT_FP8, TILE_FULL, TILE_PARTIAL,
     TILE_SKIP, attn_block_map, attn_bwd, attn_bwd_profiled, attn_bwd_noalloc, attn_bwd_varlen,
     NOALLOC_SCRATCH_BYTES, attn_fwd, attn_fwd_fp8, attn_fwd_varlen, attn_hadamard_quant_fp8,

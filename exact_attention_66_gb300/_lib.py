@@ -20,7 +20,7 @@ STATUS_NAMES = {
     4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_DEVICE", 6: "ATTN_ERR_TIMEOUT", 7: "ATTN_ERR_BOUNDS",
 }
 
-MOD_CAUSAL, MOD_WINDOW, MOD_DOC, MOD_SOFTCAP, MOD_ALIBI = 1, 2, 4, 8, 16
+MOD_CAUSAL, MOD_WINDOW, MOD_DOC, MOD_SOFTCAP, MOD_ALIBI, MOD_BWD_FP8 = 1, 2, 4, 8, 16, 32
 OP_FWD, OP_BWD, OP_FWD_FP8, OP_QUANT_FP8, OP_FWD_VARLEN, OP_BWD_VARLEN, OP_DECODE_PAGED = 0, 1, 2, 3, 4, 5, 6
 TILE_SKIP, TILE_PARTIAL, TILE_FULL = 0, 1, 2
 
@@ -109,12 +109,13 @@ def _check(st: int, where: str) -> None:
 
 
 def make_mods(causal=False, window=None, doc_ids=None, softcap=None, alibi=False,
-              alibi_slopes=None) -> Mods:
-    """attn_mods_t from Python values (doc_ids / alibi_slopes: device tensors)."""
+              alibi_slopes=None, bwd_fp8=False) -> Mods:
+    """attn_mods_t from Python values (doc_ids / alibi_slopes: device tensors;
+    bwd_fp8: the mixed e4m3 backward)."""
     m = Mods()
     m.flags = ((MOD_CAUSAL if causal else 0) | (MOD_WINDOW if window is not None else 0)
                | (MOD_DOC if doc_ids is not None else 0) | (MOD_SOFTCAP if softcap is not None else 0)
-               | (MOD_ALIBI if alibi else 0))
+               | (MOD_ALIBI if alibi else 0) | (MOD_BWD_FP8 if bwd_fp8 else 0))
     m.window = int(window) if window is not None else 0
     m.softcap = float(softcap) if softcap is not None else 0.0
     m.doc_ids = _ptr(doc_ids)

@@ -52,7 +52,7 @@ size_t mods_bytes(int B, int N, uint32_t flags) {
 attn_status_t check_mods(const attn_mods_t* m) {
   if (!m) return ATTN_OK;
   const uint32_t known = ATTN_MOD_CAUSAL | ATTN_MOD_WINDOW | ATTN_MOD_DOC | ATTN_MOD_SOFTCAP |
-                         ATTN_MOD_ALIBI;
+                         ATTN_MOD_ALIBI | ATTN_MOD_BWD_FP8;
   if (m->flags & ~known) return ATTN_ERR_INVALID_ARG;
   if ((m->flags & ATTN_MOD_WINDOW) && m->window < 1) return ATTN_ERR_INVALID_ARG;
   if ((m->flags & ATTN_MOD_DOC) && (m->doc_ids == nullptr || !aligned(m->doc_ids, 4)))
@@ -224,6 +224,20 @@ size_t bwd_fused_bytes(int B, int Hq, int Hkv, int N, int d, uint32_t flags) {
                              : 0;
 }
 
+// Mixed e4m3 backward (ATTN_MOD_BWD_FP8): d = 128 and no mod but the causal
+// mask.  Its workspace, after the row statistics: e4m3 dO and V, their scales
+// (2 B Hkv floats) and the amax scratch of the quantisation (2 B Hkv words).
+bool bwd_fp8(uint32_t flags) { return (flags & ATTN_MOD_BWD_FP8) != 0; }
+bool bwd_fp8_supported(uint32_t flags, int d) {
+  return d == 128 && (flags & ~(uint32_t)(ATTN_MOD_CAUSAL | ATTN_MOD_BWD_FP8)) == 0;
+}
+size_t bwd_do8_bytes(int B, int Hq, int N, int d) { return round_up((size_t)B * Hq * N * d, 256); }
+size_t bwd_v8_bytes(int B, int Hkv, int N, int d) { return round_up((size_t)B * Hkv * N * d, 256); }
+size_t bwd_fp8s_bytes(int B, int Hkv) { return round_up((size_t)2 * B * Hkv * sizeof(float), 256); }
+size_t bwd_fp8_bytes(int B, int Hq, int Hkv, int N, int d, uint32_t flags) {
+  return bwd_fp8(flags) ? bwd_do8_bytes(B, Hq, N, d) + bwd_v8_bytes(B, Hkv, N, d) + 2 * bwd_fp8s_bytes(B, Hkv) : 0;
+}
+
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
 // Varlen workspace head: the sequence id of every packed row.
@@ -344,7 +358,8 @@ size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int N, int d, const a
     case ATTN_OP_FWD_FP8:
       return mods_bytes(B, N, f);
     case ATTN_OP_BWD:
-      return bwd_rowstat_bytes(B, Hq, N) + mods_bytes(B, N, f) + bwd_fused_bytes(B, Hq, Hkv, N, d, f);
+      return bwd_rowstat_bytes(B, Hq, N) + mods_bytes(B, N, f) + bwd_fused_bytes(B, Hq, Hkv, N, d, f) +
+             bwd_fp8_bytes(B, Hq, Hkv, N, d, f);
     case ATTN_OP_QUANT_FP8:
       return round_up((size_t)(B * Hq + 2 * B * Hkv) * sizeof(unsigned), 256);
     case ATTN_OP_FWD_VARLEN:
@@ -402,6 +417,7 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   if (!aligned(lse, 4)) return ATTN_ERR_UNSUPPORTED;
   if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if ((st = check_mods(mods)) != ATTN_OK) return st;
+  if (bwd_fp8(mod_flags(mods)) && !bwd_fp8_supported(mod_flags(mods), d)) return ATTN_ERR_UNSUPPORTED;
   const size_t need = attn_workspace_size(ATTN_OP_BWD, B, Hq, Hkv, N, d, mods);
   if ((st = check_ws(ws, ws_bytes, need)) != ATTN_OK) return st;
   int* status = nullptr;
@@ -427,6 +443,20 @@ static attn_status_t bwd_impl(const void* q, const void* k, const void* v, const
   if ((st = prepare_mods(L.p, mregion, s)) != ATTN_OK) return st;
   if (events != nullptr)
     for (int e = 0; e < 4; ++e) L.events[e] = static_cast<cudaEvent_t>(events[e]);
+  if (bwd_fp8(L.p.flags)) {  // no mods region, no one-kernel region
+    uint8_t* r8 = mregion;
+    L.fp8 = true;
+    L.v = v;
+    L.do8 = r8;
+    r8 += bwd_do8_bytes(B, Hq, N, d);
+    L.v8 = r8;
+    r8 += bwd_v8_bytes(B, Hkv, N, d);
+    L.fp8s = reinterpret_cast<float*>(r8);
+    L.fp8amax = reinterpret_cast<unsigned*>(r8 + bwd_fp8s_bytes(B, Hkv));
+    if (!make_map(&L.tdo8, L.do8, true, d, N, (long long)B * Hq) ||
+        !make_map(&L.tv8, L.v8, true, d, N, (long long)B * Hkv))
+      return ATTN_ERR_CUDA;
+  }
   if (!bwd_fused(L.p.flags, d))
     return cuda_status(launch_bwd(L, d, has_score_mods(L.p.flags), needs_map(L.p.flags), s));
   uint8_t* fregion = mregion + mods_bytes(B, N, L.p.flags);

@@ -33,6 +33,10 @@
 namespace attn {
 
 // ================================================================== dK, dV
+// e4m3 P^T of the mixed backward is P * P8_MUL: P <= 1 stays below the e4m3
+// maximum (448), and P down to 2^-17 stays above its smallest subnormal.
+constexpr float P8_MUL = 256.f;
+
 // Shared memory: K_J, V_J, a 3-slot Q ring and a 2-slot dO ring.  TMEM (512 columns):
 //   XS  [0, 128)        S^T(n), copied to registers and handed back at once
 //   XD  [128, 256)      dP^T(n); then, per softmax warpgroup w (query columns
@@ -47,22 +51,28 @@ namespace attn {
 // the softmax works on P(n); per step the softmax waits for one GEMM only,
 // dP^T.  (P^T in place over S^T kept S^T(n+1) waiting for the exponentials of
 // P(n): 3660 cycles a step against 2048 of MMA.)
-template <int D>
+// FP8 (the mixed e4m3 backward): V and dO tiles are e4m3 (128-byte rows, one
+// TMA box each), and P^T goes to an e4m3 shared-memory tile, the A operand of
+// the e4m3 dV GEMM.
+template <int D, bool FP8 = false>
 struct KvCfg {
   static constexpr int CH = D / 64;
   static constexpr int TB = TILE * D * 2;
+  static constexpr int VB = FP8 ? TILE * D : TB;  // one V or dO tile
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = TB;
   // Q tiles in a 3-slot ring (last read by dK, the step's final GEMM) and dO
   // tiles in a 2-slot ring (last read by dV): the load of Q(n+1) never waits
   // for dK(n-1), which runs late in step n.
   static constexpr int QS = 3, DOS = 2;
-  static constexpr int Q_OFF = 2 * TB;
+  static constexpr int Q_OFF = TB + VB;
   static constexpr int DO_OFF = Q_OFF + QS * TB;
-  static constexpr int BAR_OFF = DO_OFF + DOS * TB;
+  static constexpr int P8_OFF = DO_OFF + DOS * VB;             // e4m3 P^T tile (FP8 only)
+  static constexpr int BAR_OFF = P8_OFF + (FP8 ? TILE * TILE : 0);
   static constexpr int SMEM_BYTES = smem_one_cta(BAR_OFF + 256 + 1024);
 };
 static_assert(KvCfg<128>::SMEM_BYTES <= 232448, "dK/dV shared memory exceeds 227 KB");
+static_assert(KvCfg<128, true>::SMEM_BYTES <= 232448, "dK/dV shared memory exceeds 227 KB");
 
 struct KvBars {
   uint64_t in_full;              // K_J, V_J
@@ -101,14 +111,19 @@ struct KvSteps {
   }
 };
 
-// MODS: soft-cap / ALiBi compiled in; MASKS: window / document masks.
-template <int D, bool MODS, bool MASKS>
+// MODS: soft-cap / ALiBi compiled in; MASKS: window / document masks.  FP8:
+// the mixed e4m3 backward (d = 128, no score mods, no window / document
+// masks): tv and tdo map the e4m3 V and dO, fp8s holds their dequantisation
+// scales ([B * Hkv] of dO, then [B * Hkv] of V); dP^T and dV run as e4m3 GEMMs,
+// P^T rounded to e4m3 after scaling by P8_MUL, dS and dK stay bf16.
+template <int D, bool MODS, bool MASKS, bool FP8 = false>
 __global__ void __launch_bounds__(384, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                     const float2* __restrict__ rowstat, __nv_bfloat16* __restrict__ dk,
-                    __nv_bfloat16* __restrict__ dv, const AttnParams p) {
-  using C = KvCfg<D>;
+                    __nv_bfloat16* __restrict__ dv, const AttnParams p, const float* __restrict__ fp8s) {
+  static_assert(!FP8 || (D == 128 && !MODS && !MASKS), "the e4m3 backward has d = 128 and no mods");
+  using C = KvCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   KvBars& S = *reinterpret_cast<KvBars*>(smem + C::BAR_OFF);
@@ -159,17 +174,20 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sQ = smem_u32(smem + C::Q_OFF);
   const uint32_t sDO = smem_u32(smem + C::DO_OFF);
   const uint32_t tXS = tmem, tXD = tmem + 128;
+  const uint32_t sP8 = smem_u32(smem + C::P8_OFF);
   const uint32_t tdV = tmem + 256, tdK = tmem + 256 + D;
 
   if (warp < 4) regs_dec<BWD_REGS_LOW>();
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
-      mbar_arrive_tx(&S.in_full, 2 * C::TB);
+      mbar_arrive_tx(&S.in_full, C::TB + C::VB);
       for (int ch = 0; ch < C::CH; ++ch) {
         tma_load_3d(smem + C::K_OFF + ch * 16384, &tk, &S.in_full, ch * 64, J * TILE, b * p.Hkv + hk);
-        tma_load_3d(smem + C::V_OFF + ch * 16384, &tv, &S.in_full, ch * 64, J * TILE, b * p.Hkv + hk);
+        if (!FP8)
+          tma_load_3d(smem + C::V_OFF + ch * 16384, &tv, &S.in_full, ch * 64, J * TILE, b * p.Hkv + hk);
       }
+      if (FP8) tma_load_3d(smem + C::V_OFF, &tv, &S.in_full, 0, J * TILE, b * p.Hkv + hk);
       int nq = 0, nd = 0;  // Q / dO loads issued
       if (any) {
         int g = 0, I = steps.I_first;
@@ -183,10 +201,13 @@ __global__ void __launch_bounds__(384, 1)
                         b * p.Hq + hq);
           ++nq;
           if (!mbar_wait(&S.dempty[ds], ((nd / C::DOS) & 1) ^ 1, ab)) break;
-          mbar_arrive_tx(&S.dfull[ds], C::TB);
-          for (int ch = 0; ch < C::CH; ++ch)
-            tma_load_3d(smem + C::DO_OFF + ds * C::TB + ch * 16384, &tdo, &S.dfull[ds], ch * 64, I * TILE,
-                        b * p.Hq + hq);
+          mbar_arrive_tx(&S.dfull[ds], C::VB);
+          if (FP8)
+            tma_load_3d(smem + C::DO_OFF + ds * C::VB, &tdo, &S.dfull[ds], 0, I * TILE, b * p.Hq + hq);
+          else
+            for (int ch = 0; ch < C::CH; ++ch)
+              tma_load_3d(smem + C::DO_OFF + ds * C::TB + ch * 16384, &tdo, &S.dfull[ds], ch * 64, I * TILE,
+                          b * p.Hq + hq);
           ++nd;
         } while (steps.advance(p, b, g, I));
       }
@@ -212,12 +233,15 @@ __global__ void __launch_bounds__(384, 1)
       if (ok && any) {
         int g = 0, I = steps.I_first, n = 0;
         auto q_at = [&](int m) { return sQ + (uint32_t)((m % C::QS) * C::TB); };
-        auto do_at = [&](int m) { return sDO + (uint32_t)((m % C::DOS) * C::TB); };
+        auto do_at = [&](int m) { return sDO + (uint32_t)((m % C::DOS) * C::VB); };
         // dP^T(m) = V dO(m)^T into XD.
         auto issue_dp = [&](int m) -> bool {
           if (!mbar_wait(&S.dfull[m % C::DOS], (m / C::DOS) & 1, ab)) return false;
           tc_fence_after();
-          issue_nt<D * 2>(tXD, sV, do_at(m));
+          if (FP8)
+            issue_nt_e4m3(tXD, sV, do_at(m));
+          else
+            issue_nt<D * 2>(tXD, sV, do_at(m));
           mma_commit(&S.dp_full);
           return true;
         };
@@ -227,7 +251,10 @@ __global__ void __launch_bounds__(384, 1)
           // dV += P^T(n) dO(n); dO(n) is free after it.
           if (!(ok = mbar_wait(&S.p_full, n & 1, ab))) break;
           tc_fence_after();
-          issue_acc_inplace<D>(tdV, tXD + 32, do_at(n), n == 0);
+          if (FP8)
+            issue_acc_e4m3<D>(tdV, sP8, do_at(n), n == 0);
+          else
+            issue_acc_inplace<D>(tdV, tXD + 32, do_at(n), n == 0);
           mma_commit(&S.dempty[n % C::DOS]);
           // dK += dS^T(n) Q(n); Q(n) is free after it (S^T(n) completed
           // before the softmax stored dS^T(n)).
@@ -281,6 +308,9 @@ __global__ void __launch_bounds__(384, 1)
     const bool doc = MASKS && (p.flags & MOD_DOC) != 0;
     const float sc_in = p.scale / p.softcap, sc_out = p.softcap * LOG2E;
     const int doc_j = (doc && j < p.N) ? p.doc_ids[(size_t)b * p.N + j] : 0;
+    // e4m3: dP = dP8 * sdo * sv; dV = dV8 * sdo / P8_MUL.
+    const float sdo = FP8 ? fp8s[b * p.Hkv + hk] : 1.f;
+    const float dps = FP8 ? sdo * fp8s[p.B * p.Hkv + b * p.Hkv + hk] : 1.f;
     bool doc_runs = false;
     const int2 run_j = doc ? doc_run(p, b, j, doc_runs) : make_int2(0, p.N);
     const bool doc_each = doc && !doc_runs;  // ids tested element by element
@@ -332,11 +362,16 @@ __global__ void __launch_bounds__(384, 1)
         // P as packed bf16 (pk, the A operand of dV) and the factor of dS
         // (pd: P times the soft-cap derivative, else P), also bf16, which
         // keeps the registers live across the dP^T loads to pk, pd, dp and o.
-        uint32_t pk[32], pd[32];
+        uint32_t pk[32], pd[32], p8[16];
         kv_row_p<MODS>(s, pk, my_nl2, a);
 #pragma unroll
         for (int q = 0; q < 32; ++q)
           pd[q] = sc ? pack_bf16(__uint_as_float(s[2 * q]), __uint_as_float(s[2 * q + 1])) : pk[q];
+        if (FP8)
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            p8[q] = pack_e4m3x4(__uint_as_float(s[4 * q]) * P8_MUL, __uint_as_float(s[4 * q + 1]) * P8_MUL,
+                                __uint_as_float(s[4 * q + 2]) * P8_MUL, __uint_as_float(s[4 * q + 3]) * P8_MUL);
 
         // dS = P (dP - D) (times the soft-cap derivative), in pairs, from the
         // two 32-column halves of this warpgroup's dP^T columns: the second
@@ -345,17 +380,27 @@ __global__ void __launch_bounds__(384, 1)
         // which dS^T(n) replaces.
         if (!(ok = wait_warp(&S.dp_full, n & 1, ab))) break;
         tc_fence_after();
+        if (FP8) {
+          // e4m3 P^T into its shared-memory tile: dV(n-1), its last reader,
+          // completed before the commit of dP^T(n) that was just seen.
+          store_half_row_e4m3(smem + C::P8_OFF, r, w, p8);
+          fence_async_smem();
+          tc_fence_before();
+          mbar_arrive(&S.p_full);
+        }
         uint32_t dp[32], o[32];
         tmem_ld32(tXD + lane_off + 64 * w + 32, dp);
         tmem_wait_ld(dp);
-        kv_row_ds_bf16<32>(pd + 16, dp, 32, my_ndd, o + 16);
-        tmem_st32(tXD + lane_off + 64 * w + 32, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&S.p_full);
+        kv_row_ds_bf16<32, FP8>(pd + 16, dp, 32, my_ndd, o + 16, dps);
+        if (!FP8) {
+          tmem_st32(tXD + lane_off + 64 * w + 32, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&S.p_full);
+        }
         tmem_ld32(tXD + lane_off + 64 * w, dp);
         tmem_wait_ld(dp);
-        kv_row_ds_bf16<32>(pd, dp, 0, my_ndd, o);
+        kv_row_ds_bf16<32, FP8>(pd, dp, 0, my_ndd, o, dps);
         tmem_st32(tXD + lane_off + 64 * w, o);
         tmem_wait_st();
         tc_fence_before();
@@ -367,7 +412,8 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     if (ok) {
       const size_t row = ((size_t)b * p.Hkv + hk) * p.N + j;
-      store_cols<D / 2>(tdV + lane_off + w * (D / 2), any, 1.0f, dv + row * D + w * (D / 2), j < p.N);
+      store_cols<D / 2>(tdV + lane_off + w * (D / 2), any, FP8 ? sdo / P8_MUL : 1.0f, dv + row * D + w * (D / 2),
+                        j < p.N);
       store_cols<D / 2>(tdK + lane_off + w * (D / 2), any, p.scale, dk + row * D + w * (D / 2), j < p.N);
     }
   }
@@ -652,26 +698,31 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ------------------------------------------------------------------ launch
-template <int D, bool MODS, bool MASKS>
+template <int D, bool MODS, bool MASKS, bool FP8 = false>
 static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
   const AttnParams& p = L.p;
   const long long rows = (long long)p.B * p.Hq * p.nT * TILE;
   const long long threads = rows * (D / 8);
   if (L.events[0]) cudaEventRecord(L.events[0], st);
+  cudaError_t e;
+  if (FP8 && (e = launch_quant_bwd_fp8(L.dout, L.v, L.do8, L.v8, L.fp8s, p.B, p.Hq, p.Hkv, p.N, L.fp8amax, st)) !=
+                 cudaSuccess)
+    return e;
   bwd_pre_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
       (const __nv_bfloat16*)L.o, (const __nv_bfloat16*)L.dout, L.lse, L.rowstat, p.N, rows, PreExtra{});
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
   static int kv_regs = -1, dq_regs = -1;
-  auto kv = bwd_dkdv_kernel<D, MODS, MASKS>;
+  using KC = KvCfg<D, FP8>;
+  auto kv = bwd_dkdv_kernel<D, MODS, MASKS, FP8>;
   if ((e = check_regs(kv, kv_regs)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KvCfg<D>::SMEM_BYTES)) !=
-      cudaSuccess)
+  if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, KC::SMEM_BYTES)) != cudaSuccess)
     return e;
   if (L.events[1]) cudaEventRecord(L.events[1], st);
-  kv<<<(unsigned)(p.nT * p.B * p.Hkv), 384, KvCfg<D>::SMEM_BYTES, st>>>(
-      L.tq, L.tk, L.tv, L.tdo, L.rowstat, (__nv_bfloat16*)L.dk, (__nv_bfloat16*)L.dv, p);
+  kv<<<(unsigned)(p.nT * p.B * p.Hkv), 384, KC::SMEM_BYTES, st>>>(
+      L.tq, L.tk, FP8 ? L.tv8 : L.tv, FP8 ? L.tdo8 : L.tdo, L.rowstat, (__nv_bfloat16*)L.dk, (__nv_bfloat16*)L.dv, p,
+      L.fp8s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   auto dqk = bwd_dq_kernel<D, MODS, MASKS>;
@@ -688,6 +739,7 @@ static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd(const BwdLaunch& L, int d, bool mods, bool masks, cudaStream_t st) {
+  if (L.fp8) return (d == 128 && !mods && !masks) ? launch_bwd_t<128, false, false, true>(L, st) : cudaErrorInvalidValue;
   if (d == 128)
     return mods ? launch_bwd_t<128, true, true>(L, st)
                 : masks ? launch_bwd_t<128, false, true>(L, st) : launch_bwd_t<128, false, false>(L, st);

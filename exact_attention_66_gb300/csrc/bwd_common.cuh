@@ -222,6 +222,37 @@ __device__ __forceinline__ void issue_acc_inplace(uint32_t d_tmem, uint32_t a_tm
                (first && kk == 0) ? 0u : 1u);
 }
 
+// e4m3 forms for the mixed backward (kind::f8f6f4, 32 keys per MMA, twice the
+// bf16 rate).  D(tmem, 128 x 128) = A B^T, A and B e4m3 K-major 128-byte
+// swizzled tiles of 128-byte rows (K = 128).
+__device__ __forceinline__ void issue_nt_e4m3(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+  constexpr uint32_t id = idesc_e4m3(128, 128, false, false);
+  const uint64_t ad = opaque(sdesc_sw128(a_smem, 16, 1024)), bd = opaque(sdesc_sw128(b_smem, 16, 1024));
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    mma_f8_ss(d_tmem, sdesc_add(ad, kk * 32), sdesc_add(bd, kk * 32), id, kk > 0 ? 1u : 0u);
+}
+// D(tmem, 128 x D) (+)= A(128 x 128 keys, e4m3 K-major) B(128 keys x D, e4m3
+// MN-major, 128-byte rows: 32 keys = 4 KB per MMA).
+template <int D>
+__device__ __forceinline__ void issue_acc_e4m3(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, bool first) {
+  constexpr uint32_t id = idesc_e4m3(128, D, false, true);
+  const uint64_t ad = opaque(sdesc_sw128(a_smem, 16, 1024)), bd = opaque(sdesc_sw128(b_smem, 16384, 1024));
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    mma_f8_ss(d_tmem, sdesc_add(ad, kk * 32), sdesc_add(bd, kk * 32 * 128), id, (first && kk == 0) ? 0u : 1u);
+}
+
+// Store 16 words of e4m3 codes (64 consecutive columns starting at 64 * w)
+// of row r into a 128 x 128 e4m3 K-major swizzled tile (128-byte rows).
+__device__ __forceinline__ void store_half_row_e4m3(uint8_t* tile, int r, int w, const uint32_t (&v)[16]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t addr = (uint32_t)(r * 128 + (((4 * w + c) ^ (r & 7)) << 4));
+    *reinterpret_cast<uint4*>(tile + addr) = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+  }
+}
+
 // Store 32 packed bf16 words (64 consecutive columns starting at 64 * w) of
 // row r into a 128 x 128 bf16 K-major swizzled tile.
 __device__ __forceinline__ void store_half_row(uint8_t* tile, int r, int w, const uint32_t (&v)[32]) {
@@ -355,15 +386,18 @@ __device__ __forceinline__ void kv_row_p(uint32_t (&s)[64], uint32_t (&pk)[32], 
 // derivative) given as packed bf16, pd[k] holding columns c0 + 2k, c0 + 2k + 1
 // (half the registers of fp32); ndd[e] = -D of query rows i0 + e * 32 + lane,
 // broadcast by shuffles.
-template <int NC>
+// SCALED: dP is dp * dps (the dequantisation factor of an e4m3 dP).
+template <int NC, bool SCALED = false>
 __device__ __forceinline__ void kv_row_ds_bf16(const uint32_t* pd, const uint32_t* dp, int c0,
-                                               const float (&ndd)[2], uint32_t* pk) {
+                                               const float (&ndd)[2], uint32_t* pk, float dps = 1.f) {
+  const uint64_t dps2 = f2_pack(dps, dps);
 #pragma unroll
   for (int k = 0; k < NC; k += 2) {
     const int c = c0 + k;
     const uint64_t nd = f2_pack(__shfl_sync(0xffffffffu, ndd[c >> 5], c & 31),
                                 __shfl_sync(0xffffffffu, ndd[(c + 1) >> 5], (c + 1) & 31));
-    const uint64_t g2 = f2_add(f2_pack(__uint_as_float(dp[k]), __uint_as_float(dp[k + 1])), nd);
+    const uint64_t dp2 = f2_pack(__uint_as_float(dp[k]), __uint_as_float(dp[k + 1]));
+    const uint64_t g2 = SCALED ? f2_fma(dp2, dps2, nd) : f2_add(dp2, nd);
     float ds0, ds1;
     f2_unpack(f2_mul(f2_pack(bf16lo_f32(pd[k / 2]), bf16hi_f32(pd[k / 2])), g2), ds0, ds1);
     pk[k / 2] = pack_bf16(ds0, ds1);

@@ -35,7 +35,8 @@ struct QuantTensors {
   const __nv_bfloat16* x[3];  // Q, K, V
   uint8_t* out[3];            // e4m3 codes
   long long rows[3];          // B * H * N
-  int heads[3];               // H of each tensor
+  int heads[3];               // scales of each tensor per batch entry (its H, or Hkv for dO)
+  long long rps[3];           // rows per scale: N, or G * N for dO (one scale per query-head group)
   unsigned* amax[3];          // [B * H] float bits (workspace)
   float* scale[3];            // [B * H] dequantisation scales (output)
   const int8_t* signs;        // [Hkv, 128] or nullptr (no rotation)
@@ -219,7 +220,8 @@ __global__ void __launch_bounds__(256) quant_pass_kernel(const QuantTensors t) {
     if (hn) load_group(t, nxt, l8, q, rawn);
     const int ti = cur.ti;
     const float norm = out_norm(t, ti);
-    const bool one_head = cur.r0 / t.N == (cur.r1 - 1) / t.N;
+    const long long rps = t.rps[ti];
+    const bool one_head = cur.r0 / rps == (cur.r1 - 1) / rps;
     float mx = 0.f;
 #pragma unroll
     for (int s = 0; s < SLABS; ++s) {
@@ -229,7 +231,7 @@ __global__ void __launch_bounds__(256) quant_pass_kernel(const QuantTensors t) {
       transform16<ROPE>(t, ti, row, l8, raw[s], inv_freq, v);
       if (WRITE) {
         if (row_raw >= cur.r1) continue;
-        const float a = __uint_as_float(t.amax[ti][row / t.N]);
+        const float a = __uint_as_float(t.amax[ti][row / rps]);
         const float mul = a > 0.f ? (448.0f / a) * norm : 1.0f;
         uint4 codes;
         codes.x = pack_e4m3x4(v[0] * mul, v[1] * mul, v[2] * mul, v[3] * mul);
@@ -247,13 +249,13 @@ __global__ void __launch_bounds__(256) quant_pass_kernel(const QuantTensors t) {
         } else {  // rows of two heads in this group (short sequences): one atomic per row
 #pragma unroll
           for (int o = 1; o < 8; o <<= 1) rm = fmaxf(rm, __shfl_xor_sync(0xffffffffu, rm, o));
-          if (l8 == 0 && row_raw < cur.r1) atomicMax(t.amax[ti] + row / t.N, __float_as_uint(rm * norm));
+          if (l8 == 0 && row_raw < cur.r1) atomicMax(t.amax[ti] + row / rps, __float_as_uint(rm * norm));
         }
       }
     }
     if (!WRITE && one_head) {
       mx = warp_max(mx);
-      if (lane == 0) atomicMax(t.amax[ti] + cur.r0 / t.N, __float_as_uint(mx * norm));
+      if (lane == 0) atomicMax(t.amax[ti] + cur.r0 / rps, __float_as_uint(mx * norm));
     }
     cur = nxt;
 #pragma unroll
@@ -272,6 +274,8 @@ __global__ void quant_scale_kernel(const QuantTensors t, int B) {
   }
 }
 
+static cudaError_t run_quant(const QuantTensors& t, int B, unsigned* amax_ws, size_t n_amax, cudaStream_t st);
+
 cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, void* q8, void* k8,
                                   void* v8, float* scales, const int8_t* signs, int B, int Hq,
                                   int Hkv, int N, float rope_base, unsigned* amax_ws, cudaStream_t st) {
@@ -285,7 +289,10 @@ cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, v
   t.out[2] = (uint8_t*)v8;
   t.heads[0] = Hq;
   t.heads[1] = t.heads[2] = Hkv;
-  for (int i = 0; i < 3; ++i) t.rows[i] = (long long)B * t.heads[i] * N;
+  for (int i = 0; i < 3; ++i) {
+    t.rows[i] = (long long)B * t.heads[i] * N;
+    t.rps[i] = N;
+  }
   t.amax[0] = amax_ws;
   t.amax[1] = amax_ws + B * Hq;
   t.amax[2] = amax_ws + B * Hq + B * Hkv;
@@ -296,7 +303,12 @@ cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, v
   t.N = N;
   t.Hkv = Hkv;
   t.G = Hq / Hkv;
-  cudaError_t e = cudaMemsetAsync(amax_ws, 0, sizeof(unsigned) * (size_t)(B * Hq + 2 * B * Hkv), st);
+  return run_quant(t, B, amax_ws, (size_t)(B * Hq + 2 * B * Hkv), st);
+}
+
+// The three passes of a quantisation: amax, scales, codes.
+static cudaError_t run_quant(const QuantTensors& t, int B, unsigned* amax_ws, size_t n_amax, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(amax_ws, 0, sizeof(unsigned) * n_amax, st);
   if (e != cudaSuccess) return e;
   long long groups = 0;
   for (int i = 0; i < 3; ++i) groups += (t.rows[i] + ROWS_PER_WARP - 1) / ROWS_PER_WARP;
@@ -312,6 +324,35 @@ cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, v
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   (rope ? quant_pass_kernel<true, true> : quant_pass_kernel<true, false>)<<<(unsigned)blocks, 256, 0, st>>>(t);
   return cudaGetLastError();
+}
+
+// Operands of the mixed e4m3 backward: dO with one scale per (batch, KV head)
+// -- the query heads of a group are consecutive in [B, Hq, N, d], so a
+// group's rows are one run of G * N rows -- and V per (batch, KV head).  No
+// rotation (the dV GEMM contracts over rows, not over the rotated columns).
+// scales: [B * Hkv] of dO, then [B * Hkv] of V.
+cudaError_t launch_quant_bwd_fp8(const void* dout, const void* v, void* do8, void* v8, float* scales, int B,
+                                 int Hq, int Hkv, int N, unsigned* amax_ws, cudaStream_t st) {
+  QuantTensors t{};
+  t.x[0] = (const __nv_bfloat16*)dout;
+  t.x[2] = (const __nv_bfloat16*)v;
+  t.out[0] = (uint8_t*)do8;
+  t.out[2] = (uint8_t*)v8;
+  t.heads[0] = t.heads[2] = Hkv;
+  t.rows[0] = (long long)B * Hq * N;
+  t.rows[2] = (long long)B * Hkv * N;
+  t.rps[0] = (long long)(Hq / Hkv) * N;
+  t.rps[1] = t.rps[2] = N;
+  t.amax[0] = amax_ws;
+  t.amax[1] = amax_ws + B * Hkv;
+  t.amax[2] = amax_ws + B * Hkv;
+  t.scale[0] = scales;
+  t.scale[1] = scales + B * Hkv;
+  t.scale[2] = scales + B * Hkv;
+  t.N = N;
+  t.Hkv = Hkv;
+  t.G = Hq / Hkv;
+  return run_quant(t, B, amax_ws, (size_t)(2 * B * Hkv), st);
 }
 
 }  // namespace attn

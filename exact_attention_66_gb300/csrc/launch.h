@@ -44,6 +44,13 @@ struct BwdLaunch {
   int* dqacc;      // [B, Hq, nT*128, d] int32 dQ sums in those quanta
   int* ticket;     // work-item counter
   int sms;         // persistent CTAs
+  // Mixed e4m3 backward (d = 128, causal or no mask) only, all workspace:
+  bool fp8;                // dP^T and dV GEMMs in e4m3
+  CUtensorMap tdo8, tv8;   // e4m3 maps of do8, v8
+  void* do8;               // e4m3 [B, Hq, N, d]: dO / its scale
+  void* v8;                // e4m3 [B, Hkv, N, d]: V / its scale
+  float* fp8s;             // [B * Hkv] dO scales, then [B * Hkv] V scales (amax / 448)
+  unsigned* fp8amax;       // [2 * B * Hkv] amax scratch
 };
 // Two kernels after the row statistics (dK/dV kv-stationary, dQ q-stationary).
 cudaError_t launch_bwd(const BwdLaunch& L, int d, bool mods, bool masks, cudaStream_t st);
@@ -95,5 +102,7 @@ cudaError_t launch_seq_ids(const int* cu, int n_seqs, int total, int* ids, cudaS
 cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, void* q8, void* k8,
                                   void* v8, float* scales, const int8_t* signs, int B, int Hq,
                                   int Hkv, int N, float rope_base, unsigned* amax_ws, cudaStream_t st);
+cudaError_t launch_quant_bwd_fp8(const void* dout, const void* v, void* do8, void* v8, float* scales, int B,
+                                 int Hq, int Hkv, int N, unsigned* amax_ws, cudaStream_t st);
 
 }  // namespace attn

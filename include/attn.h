@@ -64,7 +64,8 @@ enum {
   ATTN_MOD_WINDOW = 1u << 1,  /* allowed iff i - j < window */
   ATTN_MOD_DOC = 1u << 2,     /* allowed iff doc_ids[b][i] == doc_ids[b][j] */
   ATTN_MOD_SOFTCAP = 1u << 3, /* score x -> softcap * tanh(x / softcap), applied to scale*q.k */
-  ATTN_MOD_ALIBI = 1u << 4    /* score x -> x - slope[hq] * (i - j), after the soft-cap */
+  ATTN_MOD_ALIBI = 1u << 4,   /* score x -> x - slope[hq] * (i - j), after the soft-cap */
+  ATTN_MOD_BWD_FP8 = 1u << 5  /* attn_bwd only: mixed e4m3 backward (see attn_bwd); ignored elsewhere */
 };
 
 /* FlexAttention variants as a fixed set of flags plus runtime scalars
@@ -134,12 +135,23 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  *    depend on the order the partials arrive in;
  *  - otherwise: every dQ, dK and dV tile is accumulated by one CTA over its
  *    partner tiles in ascending order (two kernels, 7 GEMMs per tile pair).
+ * ATTN_MOD_BWD_FP8 selects a mixed-precision form of the second one (the
+ * FlashAttention-3 digest, "Basse précision FP8 et incoherent processing",
+ * describes FP8 for the forward; this extends it to the two backward GEMMs
+ * whose operands behave like the forward's): dO and V are rounded to e4m3
+ * with one scale amax/448 per (batch, KV head) each, and in the dK/dV kernel
+ * dP = dO V^T and dV = P^T dO run as e4m3 GEMMs (P scaled by 256 before
+ * rounding); dS, dK = dS^T Q and the whole dQ kernel stay bf16.  Less
+ * accurate than the bf16 backward (tests/test_gpu_bwd_fp8.py bounds the
+ * error).  Needs d = 128 and no mod other than ATTN_MOD_CAUSAL, else
+ * ATTN_ERR_UNSUPPORTED.  Also bitwise reproducible.
  * ws : workspace of attn_workspace_size(ATTN_OP_BWD, ...) bytes: the row
  *      statistics {LSE log2(e), D = rowsum(dO * O)} of every query row;
  *      with window/document mods, the block map, its per-tile ranges and
  *      (documents) the document run of every position; for the one-kernel
  *      form, the dQ quanta, K/V bounds and the int32 dQ sums (4 d bytes per
- *      query row, rows padded to whole 128-row tiles).
+ *      query row, rows padded to whole 128-row tiles); with ATTN_MOD_BWD_FP8,
+ *      the e4m3 copies of dO and V (d bytes per row) and their scales.
  */
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
                        const void* dout, const float* lse, void* dq, void* dk, void* dv,

@@ -112,6 +112,20 @@ def test_workspace_sizes(L):
     assert ws(L.OP_FWD, 1, 3, 2, 128, 128, None) == 0  # invalid shape -> 0
 
 
+def test_fp8_backward_workspace_and_limits(L):
+    ws = L.attn_workspace_size
+    m = L.make_mods(causal=True, bwd_fp8=True)
+    # row statistics, then e4m3 dO and V (d bytes per row), then the dO / V scales and the
+    # quantisation's amax words (2 * B * Hkv 4-byte entries each, 256-aligned)
+    assert ws(L.OP_BWD, 1, 64, 8, 8192, 128, m) == 64 * 8192 * 8 + 64 * 8192 * 128 + 8 * 8192 * 128 + 2 * 256
+    so = L.lib()
+    rejected = [L.make_mods(causal=True, window=64, bwd_fp8=True), L.make_mods(softcap=30.0, bwd_fp8=True),
+                L.make_mods(alibi=True, bwd_fp8=True)]
+    for mm in rejected:  # ATTN_ERR_UNSUPPORTED before any other check of the workspace
+        assert so.attn_bwd(A, A, A, A, A, A, A, A, A, 1, 2, 2, 256, 128, 0.1, ctypes.byref(mm), A, 16, None) == 2
+    assert so.attn_bwd(A, A, A, A, A, A, A, A, A, 1, 2, 2, 256, 64, 0.1, ctypes.byref(m), A, 16, None) == 2
+
+
 def test_status_strings(L):
     for c in range(8):
         assert L.status_string(c)
