@@ -77,7 +77,7 @@ static_assert(KvCfg<128, true>::SMEM_BYTES <= 232448, "dK/dV shared memory excee
 struct KvBars {
   uint64_t in_full;              // K_J, V_J
   uint64_t qfull[3], qempty[3];  // Q ring
-  uint64_t dfull[2], dempty[2];  // dO ring
+  uint64_t dfull[2];             // dO ring (a slot is free once qempty shows its step's dK done)
   uint64_t s_full;             // S^T(n) in XS               (MMA commit)
   uint64_t xs_free;            // S^T(n) copied out of XS    (256 softmax threads)
   uint64_t dp_full;            // dP^T(n) in XD              (MMA commit)
@@ -148,10 +148,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&S.qfull[s], 1);
       mbar_init(&S.qempty[s], 1);
     }
-    for (int s = 0; s < C::DOS; ++s) {
-      mbar_init(&S.dfull[s], 1);
-      mbar_init(&S.dempty[s], 1);
-    }
+    for (int s = 0; s < C::DOS; ++s) mbar_init(&S.dfull[s], 1);
     mbar_init(&S.s_full, 1);
     mbar_init(&S.xs_free, 256);
     mbar_init(&S.dp_full, 1);
@@ -200,7 +197,9 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_3d(smem + C::Q_OFF + qs * C::TB + ch * 16384, &tq, &S.qfull[qs], ch * 64, I * TILE,
                         b * p.Hq + hq);
           ++nq;
-          if (!mbar_wait(&S.dempty[ds], ((nd / C::DOS) & 1) ^ 1, ab)) break;
+          // dO(nd) goes over dO(nd - 2): read by dP^T and dV of step nd - 2,
+          // both done once that step's dK is (issue order; one commit fewer a step).
+          if (nd >= C::DOS && !mbar_wait(&S.qempty[(nd - C::DOS) % C::QS], ((nd - C::DOS) / C::QS) & 1, ab)) break;
           mbar_arrive_tx(&S.dfull[ds], C::VB);
           if (FP8)
             tma_load_3d(smem + C::DO_OFF + ds * C::VB, &tdo, &S.dfull[ds], 0, I * TILE, b * p.Hq + hq);
@@ -248,16 +247,15 @@ __global__ void __launch_bounds__(384, 1)
         ok = issue_dp(0);
         while (ok) {
           const bool has_next = steps.advance(p, b, g, I);
-          // dV += P^T(n) dO(n); dO(n) is free after it.
+          // dV += P^T(n) dO(n).
           if (!(ok = mbar_wait(&S.p_full, n & 1, ab))) break;
           tc_fence_after();
           if (FP8)
             issue_acc_e4m3<D>(tdV, sP8, do_at(n), n == 0);
           else
             issue_acc_inplace<D>(tdV, tXD + 32, do_at(n), n == 0);
-          mma_commit(&S.dempty[n % C::DOS]);
-          // dK += dS^T(n) Q(n); Q(n) is free after it (S^T(n) completed
-          // before the softmax stored dS^T(n)).
+          // dK += dS^T(n) Q(n); Q(n) and dO(n) are free after it (S^T(n)
+          // completed before the softmax stored dS^T(n); dV(n) ran before dK(n)).
           if (!(ok = mbar_wait(&S.ds_full, n & 1, ab))) break;
           tc_fence_after();
           issue_acc_inplace<D>(tdK, tXD, q_at(n), n == 0);
