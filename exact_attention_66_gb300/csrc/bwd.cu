@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   KvBars& S = *reinterpret_cast<KvBars*>(smem + C::BAR_OFF);
-  const Abort ab{&S.abort, p.status, p.wait_ns};
+  const Abort ab{&S.abort, p.status};
   const int warp = warp_id(), lane = lane_id();
 
   const int BHk = p.B * p.Hkv;
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(384, 1)
     const bool doc_each = doc && !doc_runs;  // ids tested element by element
     bool ok = true;
     // Test hook: warpgroup 0 waits on a phase nothing completes (attn_test_hooks).
-    if ((p.stall & STALL_BWD) && w == 0) ok = wait_warp(&S.never, 0, ab);
+    if ((p.stall & STALL_BWD) && w == 0) ok = wait_warp(&S.never, 0, ab, p.wait_ns);
     if (ok && any) {
       int g = 0, I = steps.I_first, n = 0;
       do {
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   DqBars& S = *reinterpret_cast<DqBars*>(smem + C::BAR_OFF);
-  const Abort ab{&S.abort, p.status, p.wait_ns};
+  const Abort ab{&S.abort, p.status};
   const int warp = warp_id(), lane = lane_id();
 
   const int BH = p.B * p.Hq;

@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(FU_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   FuBars& S = *reinterpret_cast<FuBars*>(smem + C::BAR_OFF);
-  const Abort ab{&S.abort, p.status, p.wait_ns};
+  const Abort ab{&S.abort, p.status};
   const int warp = warp_id(), lane = lane_id();
   const int G = p.Hq / p.Hkv;
   const int n_items = p.nT * p.B * p.Hkv;
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(FU_THREADS, 1)
     uint8_t* ds_tile = smem + C::DS_OFF;
     bool ok = true;
     // Test hook: warpgroup 0 waits on a phase nothing completes (attn_test_hooks).
-    if ((p.stall & STALL_BWD) && w == 0) ok = wait_warp(&S.never, 0, ab);
+    if ((p.stall & STALL_BWD) && w == 0) ok = wait_warp(&S.never, 0, ab, p.wait_ns);
     int k = 0, c = 0, m = 0;  // items read, items with steps, steps
     while (ok) {
       const int s = k & 1;

@@ -59,7 +59,7 @@ struct AttnParams {
   const int2* row_range;
   const int2* col_range;
   int* status;          // device status word
-  unsigned long long wait_ns;  // time limit of a pipeline wait (ns)
+  unsigned long long wait_ns;  // time limit of the test hooks' stalled wait (ns)
   int stall;                   // STALL_* test hook bits, 0 normally
 };
 
@@ -128,8 +128,9 @@ __device__ __forceinline__ int2 doc_run(const AttnParams& p, int b, int pos, boo
 
 // Every lane of the warp waits; the warp proceeds only if all of them saw the
 // phase complete (keeps the warp converged for the .sync.aligned tcgen05 ops).
-__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const Abort& ab) {
-  const bool ok = mbar_wait(bar, parity, ab);
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const Abort& ab,
+                                          unsigned long long limit = ATTN_WAIT_TIMEOUT_NS) {
+  const bool ok = mbar_wait(bar, parity, ab, limit);
   return __all_sync(0xffffffffu, ok);
 }
 

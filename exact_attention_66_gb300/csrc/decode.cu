@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   DecBars& S = *reinterpret_cast<DecBars*>(smem + C::BAR_OFF);
-  const Abort ab{&S.abort, p.status, p.wait_ns};
+  const Abort ab{&S.abort, p.status};
   const int warp = warp_id(), lane = lane_id();
   const int G = p.G;
   const int R = G * p.q_len;      // tile rows in use: (query head, token) pairs

@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   FwdBars& S = *reinterpret_cast<FwdBars*>(smem + C::BAR_OFF);
-  const Abort ab{&S.abort, p.status, p.wait_ns};
+  const Abort ab{&S.abort, p.status};
   const int warp = warp_id(), lane = lane_id();
 
   // Work item, heaviest Q blocks first (longest-processing-time order).
@@ -476,9 +476,10 @@ __global__ void __launch_bounds__(384, 1)
     int ns = 0;
     bool ok = true;
     // Test hook: the first tile's warpgroup waits on a phase nothing completes,
-    // runs into the wait limit, and the whole grid drains (attn_test_hooks).
-    if ((p.stall & STALL_FWD) && t == 0) ok = wait_warp(&S.never, 0, ab);
-    for (int J = J_begin; ok && J < J_end; ++J) {
+    // runs into the launch's limit and raises the abort word; every later wait
+    // of the grid then gives up, and the kernel drains (attn_test_hooks).
+    if ((p.stall & STALL_FWD) && t == 0) ok = wait_warp(&S.never, 0, ab, p.wait_ns);
+    for (int J = J_begin; J < J_end; ++J) {
       const int cls = tile_class(p, b, I, J);
       if (cls == CLS_SKIP) continue;
       const bool partial = cls == CLS_PARTIAL;

@@ -379,8 +379,10 @@ enum { ATTN_STALL_FWD = 1, ATTN_STALL_BWD = 2 };
  * context stays usable (the FlashAttention-3 digest's asynchronous
  * producer/consumer pipeline, "Fonctionnalités des GPU Hopper", is what these
  * waits belong to; the bound itself is this library's own).
- * wait_limit_ns : time limit of each pipeline wait in kernels launched after
- *                 this call; 0 restores the default (1 s).
+ * wait_limit_ns : time limit of the stalled wait (below) in kernels launched
+ *                 after this call; 0 restores the default (1 s).  Every other
+ *                 wait keeps the default, and gives up as soon as the stalled
+ *                 one has.
  * stall         : 0, or an OR of ATTN_STALL_FWD (forward kernels: the first
  *                 query tile's compute warpgroup of every CTA first waits on a
  *                 barrier that nothing completes) and ATTN_STALL_BWD (the
