@@ -15,6 +15,7 @@ CASES = [
     (2, 4, 2, 384, 128, dict(causal=True)),
     (1, 8, 1, 1000, 128, dict(causal=True)),
     (1, 2, 2, 200, 64, {}),
+    (1, 4, 2, 600, 128, {}),   # no mask, odd tile count
     (1, 2, 2, 1, 128, dict(causal=True)),
     (1, 2, 2, 129, 64, dict(causal=True)),
     (2, 2, 2, 640, 128, dict(causal=True, window=300)),
