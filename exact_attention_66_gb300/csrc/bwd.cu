@@ -450,7 +450,7 @@ struct DqBars {
   uint64_t vfull[2], vempty[2];  // V ring
   uint64_t s_full, s_free, p_full, acc_done;
   uint64_t a_ready;              // Q and dO copied into TMEM: their slots are free
-  uint64_t fin[2];               // per issuer: all its MMAs done
+  uint64_t fin[3];               // per issuer: all its MMAs done
   uint32_t tmem_base;
   int abort;
 };
@@ -493,13 +493,12 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&S.vfull[s], 1);
       mbar_init(&S.vempty[s], 1);  // read by dP (issuer A)
     }
-    mbar_init(&S.s_full, 1);
+    mbar_init(&S.s_full, 2);       // S(n) and dP(n), one commit each
     mbar_init(&S.s_free, 256);
     mbar_init(&S.p_full, 256);
     mbar_init(&S.acc_done, 1);     // dQ(n) done: dS buffer free
     mbar_init(&S.a_ready, 256);    // Q / dO in TMEM: slots 4 and 5 free
-    mbar_init(&S.fin[0], 1);
-    mbar_init(&S.fin[1], 1);
+    for (int i = 0; i < 3; ++i) mbar_init(&S.fin[i], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -551,28 +550,39 @@ __global__ void __launch_bounds__(384, 1)
       for (int s = 0; s < C::VS; ++s)
         if (nv > s) mbar_wait_drain(&S.vfull[s], ((nv - 1 - s) / C::VS) & 1);
     }
-  } else if (warp == 1 || warp == 2) {
-    // Issuer A (warp 1): S = Q K^T and dP = dO V^T.  Issuer B (warp 2): dQ += dS K.
+  } else if (warp < 4) {
+    // Three issuing threads, one per warp of warps 1-3, so that each SM
+    // sub-partition carries at most one of them: S = Q K^T (warp 1), dP = dO V^T
+    // (warp 3), dQ += dS K (warp 2).  A thread whose MMAs wait for room in the
+    // tensor pipe slows the softmax warps of its sub-partition, and every
+    // hand-off waits for the slowest warp: with S and dP on one thread, the
+    // softmax warps beside it trailed the others by 250-400 cycles a step.
     if (lane == 0) {
-      const bool A = warp == 1;
+      const int role = warp == 1 ? 0 : warp == 3 ? 1 : 2;  // 0: S, 1: dP, 2: dQ
       bool ok = mbar_wait(&S.in_full, 0, ab);
       tc_fence_after();
       int n = 0;
       for (int J = J_first; ok && J < J_end; J = next_J(J + 1), ++n) {
         const int ks = n % C::KS, vs = n % C::VS;
         const uint32_t k_sm = sKr + ks * C::TB, v_sm = sVr + vs * C::TB;
-        if (!(ok = mbar_wait(&S.kfull[ks], (n / C::KS) & 1, ab))) break;
-        if (A) {
-          if (!(ok = mbar_wait(&S.vfull[vs], (n / C::VS) & 1, ab))) break;
+        if (role < 2) {
+          // S(n) / dP(n) once the softmax has copied S(n-1) and dP(n-1) out.
+          if (role == 0 && !(ok = mbar_wait(&S.kfull[ks], (n / C::KS) & 1, ab))) break;
+          if (role == 1 && !(ok = mbar_wait(&S.vfull[vs], (n / C::VS) & 1, ab))) break;
           if (n == 0 && !(ok = mbar_wait(&S.a_ready, 0, ab))) break;
           if (n > 0 && !(ok = mbar_wait(&S.s_free, (n - 1) & 1, ab))) break;
           tc_fence_after();
-          issue_nt_tmem_a<D>(tS, tQa, k_sm);
-          issue_nt_tmem_a<D>(tdP, tDOa, v_sm);
-          mma_commit(&S.s_full);
-          mma_commit(&S.vempty[vs]);
-          mma_commit(&S.kempty[ks]);
+          if (role == 0) {
+            issue_nt_tmem_a<D>(tS, tQa, k_sm);
+            mma_commit(&S.s_full);
+            mma_commit(&S.kempty[ks]);
+          } else {
+            issue_nt_tmem_a<D>(tdP, tDOa, v_sm);
+            mma_commit(&S.s_full);
+            mma_commit(&S.vempty[vs]);
+          }
         } else {
+          if (!(ok = mbar_wait(&S.kfull[ks], (n / C::KS) & 1, ab))) break;
           if (!(ok = mbar_wait(&S.p_full, n & 1, ab))) break;
           tc_fence_after();
           issue_acc<D>(tdQ, sDS, k_sm, n == 0);
@@ -580,8 +590,8 @@ __global__ void __launch_bounds__(384, 1)
           mma_commit(&S.kempty[ks]);
         }
       }
-      mma_commit(&S.fin[A ? 0 : 1]);
-      mbar_wait_drain(&S.fin[A ? 0 : 1], 0);
+      mma_commit(&S.fin[role]);
+      mbar_wait_drain(&S.fin[role], 0);
     }
   } else if (warp >= 4) {
     regs_inc<BWD_REGS_HIGH>();
@@ -682,7 +692,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(&S.p_full);
     }
-    if (ok) ok = wait_warp(&S.fin[1], 0, ab);
+    if (ok) ok = wait_warp(&S.fin[2], 0, ab);
     tc_fence_after();
     if (ok) store_cols<D / 2>(tdQ + lane_off + w * (D / 2), n > 0, p.scale, dq + row * D + w * (D / 2), i < p.N);
   }
