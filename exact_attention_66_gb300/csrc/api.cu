@@ -506,7 +506,7 @@ static attn_status_t quant_impl(const void* q, const void* k, const void* v, voi
   int* status = nullptr;
   if ((st = device_state(&status)) != ATTN_OK) return st;
   return cuda_status(launch_hadamard_quant(q, k, v, q8, k8, v8, scales, signs, B, Hq, Hkv, N, rope_base,
-                                           static_cast<unsigned*>(ws),
+                                           static_cast<unsigned*>(ws), status,
                                            static_cast<cudaStream_t>(stream)));
 }
 

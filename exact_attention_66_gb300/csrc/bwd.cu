@@ -713,7 +713,7 @@ static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
   const long long threads = rows * (D / 8);
   if (L.events[0]) cudaEventRecord(L.events[0], st);
   cudaError_t e;
-  if (FP8 && (e = launch_quant_bwd_fp8(L.dout, L.v, L.do8, L.v8, L.fp8s, p.B, p.Hq, p.Hkv, p.N, L.fp8amax, st)) !=
+  if (FP8 && (e = launch_quant_bwd_fp8(L.dout, L.v, L.do8, L.v8, L.fp8s, p.B, p.Hq, p.Hkv, p.N, L.fp8amax, p.status, st)) !=
                  cudaSuccess)
     return e;
   bwd_pre_kernel<D><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(

@@ -12,10 +12,10 @@
 // Two bandwidth-bound passes over Q, K, V: pass 1 finds the amax of every
 // (batch, head) of the rotated tensors (integer atomic max of the non-negative
 // float bits, so the result does not depend on the order), pass 2 recomputes
-// the rotation and writes e4m3 codes scaled by 448 / amax.  Layout: eight
-// lanes per 128-element row, lane l8 holding elements 16 l8 .. 16 l8 + 15, so
-// a warp works on four rows at once; it walks groups of 16 consecutive rows
-// and loads the next group before transforming the current one.  The
+// the rotation and writes e4m3 codes scaled by 448 / amax.  Rows reach
+// shared memory in 64-row stages by bulk copy (one producer thread per CTA,
+// a 6-slot ring); eight lanes per 128-element row, lane l8 holding elements
+// 16 l8 .. 16 l8 + 15, so a compute warp takes four rows of a stage.  The
 // butterflies of distance 1..8 stay in registers (two lanes of fp32 per
 // instruction from distance 2 on), 16..64 go through three warp shuffles; the
 // signs are applied to the bf16 bits while converting, and 1 / sqrt(128)
@@ -42,11 +42,26 @@ struct QuantTensors {
   const int8_t* signs;        // [Hkv, 128] or nullptr (no rotation)
   float rope_k;               // RoPE: inv_freq(c) = exp2(-c * rope_k), rope_k = 2 log2(base) / 128; 0 = off
   int N, Hkv, G;              // G = Hq / Hkv
+  int* status;                // device status word (bounded waits report a timeout there)
 };
 
-constexpr int ROWS_PER_WARP = 16;
-constexpr int SLABS = ROWS_PER_WARP / 4;       // four rows per warp instruction
+constexpr int STAGE_ROWS = 256;                 // rows per shared-memory stage
+constexpr int STAGE_BYTES = STAGE_ROWS * 256;    // 64 KB of bf16 rows (d = 128)
+constexpr int QSTAGES = 3;                       // ring slots per CTA
+constexpr int QWARPS = 16;                       // compute warps
+constexpr int WROWS = STAGE_ROWS / QWARPS;       // rows of a stage per compute warp (16)
+constexpr int SLABS = WROWS / 4;                 // four rows per warp instruction
+constexpr int QTHREADS = (QWARPS + 1) * 32;      // plus one producer warp
 constexpr float HAD_NORM = 0.08838834764831845f;  // 1 / sqrt(128)
+
+// Untiled bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from global to shared memory, completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -63,11 +78,18 @@ __device__ __forceinline__ Raw16 load16(const QuantTensors& t, int ti, long long
   return Raw16{__ldg(p), __ldg(p + 1)};
 }
 
+// KV head whose signs rotate rows of head plane n (= b * H + h) of tensor ti.
+__device__ __forceinline__ int sign_head(const QuantTensors& t, int ti, long long n) {
+  const int head = (int)(n % t.heads[ti]);
+  return ti == 0 ? head / t.G : head;
+}
+
 // This lane's 16 values of the row: RoPE (when on), then the signed
 // Walsh-Hadamard transform without its 1 / sqrt(128) (Q and K with signs), or
 // the plain values.  Every lane of the warp must call it (warp shuffles).
+// hk: the row's sign head (sign_head), pos: its position in its sequence.
 template <bool ROPE>
-__device__ __forceinline__ void transform16(const QuantTensors& t, int ti, long long row, int l8, const Raw16& raw,
+__device__ __forceinline__ void transform16(const QuantTensors& t, int ti, int hk, int pos, int l8, const Raw16& raw,
                                             const float (&inv_freq)[16], float (&v)[16]) {
   const uint32_t w[8] = {raw.a.x, raw.a.y, raw.a.z, raw.a.w, raw.b.x, raw.b.y, raw.b.z, raw.b.w};
   if (ti == 2 || (!ROPE && t.signs == nullptr)) {
@@ -80,8 +102,6 @@ __device__ __forceinline__ void transform16(const QuantTensors& t, int ti, long 
   }
   uint32_t sgn[4] = {0u, 0u, 0u, 0u};  // sign bytes of elements 4 j .. 4 j + 3
   if (t.signs != nullptr) {
-    const int head = (int)((row / t.N) % t.heads[ti]);
-    const int hk = ti == 0 ? head / t.G : head;
     const uint4 sg = __ldg(reinterpret_cast<const uint4*>(t.signs + hk * 128 + 16 * l8));
     sgn[0] = sg.x;
     sgn[1] = sg.y;
@@ -94,7 +114,7 @@ __device__ __forceinline__ void transform16(const QuantTensors& t, int ti, long 
       v[2 * k] = bf16lo_f32(w[k]);
       v[2 * k + 1] = bf16hi_f32(w[k]);
     }
-    const float pos = (float)(row % t.N);
+    const float fpos = (float)pos;
     const bool first = l8 < 4;
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
@@ -103,7 +123,7 @@ __device__ __forceinline__ void transform16(const QuantTensors& t, int ti, long 
       // 2 pi = C1 - C2 with C1 = fl(2 pi) and C2 = 1.7484556e-7 its excess;
       // both steps are fused multiply-adds, so k C1 enters exactly.  Then the
       // fast sine / cosine, accurate to a few 1e-7 on that interval.
-      const float ang = pos * inv_freq[e];
+      const float ang = fpos * inv_freq[e];
       const float kf = rintf(ang * 0.15915494309189535f);  // 1 / (2 pi)
       const float red = fmaf(kf, 1.7484556e-07f, fmaf(-kf, 6.28318548f, ang));
       float sn, cs;
@@ -170,68 +190,148 @@ __device__ __forceinline__ float out_norm(const QuantTensors& t, int ti) {
   return (ti != 2 && t.signs != nullptr) ? HAD_NORM : 1.0f;
 }
 
-// Work: groups of 16 consecutive rows of Q, then K, then V; a warp walks the
-// groups gi, gi + stride, ... and loads the next group before transforming
-// the current one, so its loads stay in flight for the whole pass.
+// Work: stages of 256 consecutive rows (64 KB) of Q, then K, then V.  One
+// producer thread per CTA streams a CTA's stages (stage g = blockIdx.x +
+// k * gridDim.x) into a ring of shared-memory slots with bulk copies, with the
+// stage's indices (tensor, first row, scale and head of its rows) in a record
+// beside each slot; sixteen compute warps take 16 rows each per stage, copy
+// them to registers and hand the slot back before transforming them.  With
+// the rows staged through registers instead (one 16-row group in flight per
+// warp), too few bytes were in flight to keep HBM busy: a third of its
+// bandwidth at 59 % issue.
 struct Group {
   int ti;
   long long r0, r1;
 };
-__device__ __forceinline__ bool group_of(const QuantTensors& t, long long gi, Group& g) {
+__device__ __forceinline__ bool stage_of(const QuantTensors& t, long long g, Group& gr) {
 #pragma unroll
   for (int ti = 0; ti < 3; ++ti) {
-    const long long n = (t.rows[ti] + ROWS_PER_WARP - 1) / ROWS_PER_WARP;
-    if (gi < n) {
-      g.ti = ti;
-      g.r0 = gi * ROWS_PER_WARP;
-      g.r1 = min(g.r0 + ROWS_PER_WARP, t.rows[ti]);
+    const long long n = (t.rows[ti] + STAGE_ROWS - 1) / STAGE_ROWS;
+    if (g < n) {
+      gr.ti = ti;
+      gr.r0 = g * STAGE_ROWS;
+      gr.r1 = min(gr.r0 + STAGE_ROWS, t.rows[ti]);
       return true;
     }
-    gi -= n;
+    g -= n;
   }
   return false;
 }
-__device__ __forceinline__ void load_group(const QuantTensors& t, const Group& g, int l8, int q, Raw16 (&raw)[SLABS]) {
-#pragma unroll
-  for (int s = 0; s < SLABS; ++s) {
-    const long long row = g.r0 + 4 * s + q;
-    raw[s] = row < g.r1 ? load16(t, g.ti, row, l8) : Raw16{make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
-  }
-}
+
+// A stage's indices, computed once by the producer (64-bit divisions per row
+// cost more instructions than the transform).
+struct StageInfo {
+  long long r0, r1;  // rows [r0, r1) of tensor ti
+  long long h0, n0;  // scale index and head plane of row r0
+  int ti;
+  int one_head;      // every row has scale h0
+  int one_n;         // every row is in head plane n0
+  int hk0;           // sign head of plane n0
+};
+
+struct QuantBars {
+  uint64_t full[QSTAGES], empty[QSTAGES];
+  StageInfo info[QSTAGES];
+  int abort;
+  int done[QSTAGES];  // the producer found no further stage
+};
+constexpr int QSMEM = QSTAGES * STAGE_BYTES + (int)sizeof(QuantBars) + 128;
 
 // Pass 1 (WRITE false): amax of every (batch, head).  Pass 2 (WRITE true):
 // e4m3 codes scaled by 448 / amax.  ROPE: rotary embedding in front (its 16
 // inverse frequencies per lane are only kept in registers when it is on).
 template <bool WRITE, bool ROPE>
-__global__ void __launch_bounds__(256) quant_pass_kernel(const QuantTensors t) {
-  const int lane = lane_id(), l8 = lane & 7, q = lane >> 3;
+__global__ void __launch_bounds__(QTHREADS, 1) quant_pass_kernel(const QuantTensors t) {
+  extern __shared__ uint8_t qsm_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)qsm_raw + 127) & ~(uintptr_t)127);
+  QuantBars& S = *reinterpret_cast<QuantBars*>(sm + QSTAGES * STAGE_BYTES);
+  const Abort ab{&S.abort, t.status};
+  const int warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    S.abort = 0;
+    for (int s = 0; s < QSTAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], QWARPS);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == QWARPS) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      long long k = 0;
+      bool ok = true;
+      for (long long g = blockIdx.x;; g += gridDim.x, ++k) {
+        const int s = (int)(k % QSTAGES);
+        if (!(ok = mbar_wait(&S.empty[s], (uint32_t)((k / QSTAGES) & 1) ^ 1u, ab))) break;
+        Group gr;
+        StageInfo& in = S.info[s];
+        if (!stage_of(t, g, gr)) {  // tell the compute warps, with no copy
+          S.done[s] = 1;
+          mbar_arrive(&S.full[s]);
+          break;
+        }
+        const long long rps = t.rps[gr.ti];
+        in.r0 = gr.r0;
+        in.r1 = gr.r1;
+        in.ti = gr.ti;
+        in.h0 = gr.r0 / rps;
+        in.one_head = gr.r1 - 1 < (in.h0 + 1) * rps;
+        in.n0 = gr.r0 / t.N;
+        in.one_n = gr.r1 - 1 < (in.n0 + 1) * t.N;
+        in.hk0 = t.signs != nullptr ? sign_head(t, gr.ti, in.n0) : 0;
+        S.done[s] = 0;
+        const uint32_t bytes = (uint32_t)(gr.r1 - gr.r0) * 256u;
+        mbar_arrive_tx(&S.full[s], bytes);
+        bulk_load(sm + s * STAGE_BYTES, t.x[gr.ti] + gr.r0 * 128, bytes, &S.full[s]);
+      }
+      // Copies still in flight (the compute warps stopped early) must land
+      // before the CTA exits: the last phase armed in each slot completes
+      // ((phases armed in it - 1) & 1).
+      const long long armed = ok ? k + 1 : k;
+      for (int s = 0; s < QSTAGES; ++s)
+        if (armed > s) mbar_wait_drain(&S.full[s], (uint32_t)(((armed - 1 - s) / QSTAGES) & 1));
+    }
+    return;
+  }
+  // -------------------------------------------------------- compute warps
+  const int l8 = lane & 7, qr = lane >> 3;
   float inv_freq[16];
   if (ROPE) rope_freqs(t, l8, inv_freq);
-  const long long stride = (long long)gridDim.x * 8;
-  long long gi = (long long)blockIdx.x * 8 + warp_id();
-  Group cur;
-  bool have = group_of(t, gi, cur);
-  Raw16 raw[SLABS];
-  if (have) load_group(t, cur, l8, q, raw);
-  while (have) {
-    Group nxt;
-    const bool hn = group_of(t, gi + stride, nxt);
-    Raw16 rawn[SLABS];
-    if (hn) load_group(t, nxt, l8, q, rawn);
-    const int ti = cur.ti;
+  for (long long k = 0;; ++k) {
+    const int s = (int)(k % QSTAGES);
+    if (!wait_warp(&S.full[s], (uint32_t)((k / QSTAGES) & 1), ab)) break;
+    if (S.done[s]) break;
+    const StageInfo in = S.info[s];
+    Raw16 raw[SLABS];
+#pragma unroll
+    for (int sl = 0; sl < SLABS; ++sl) {
+      const int lr = WROWS * warp + 4 * sl + qr;
+      if (in.r0 + lr < in.r1) {
+        const uint4* src = reinterpret_cast<const uint4*>(sm + s * STAGE_BYTES + lr * 256 + l8 * 32);
+        raw[sl] = Raw16{src[0], src[1]};
+      } else {
+        raw[sl] = Raw16{make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[s]);
+
+    const int ti = in.ti;
     const float norm = out_norm(t, ti);
     const long long rps = t.rps[ti];
-    const bool one_head = cur.r0 / rps == (cur.r1 - 1) / rps;
     float mx = 0.f;
 #pragma unroll
-    for (int s = 0; s < SLABS; ++s) {
-      const long long row_raw = cur.r0 + 4 * s + q;
-      const long long row = min(row_raw, cur.r1 - 1);
+    for (int sl = 0; sl < SLABS; ++sl) {
+      const long long row_raw = in.r0 + WROWS * warp + 4 * sl + qr;
+      const long long row = min(row_raw, in.r1 - 1);
+      const long long n = in.one_n ? in.n0 : row / t.N;
+      const int hk = t.signs == nullptr ? 0 : in.one_n ? in.hk0 : sign_head(t, ti, n);
       float v[16];
-      transform16<ROPE>(t, ti, row, l8, raw[s], inv_freq, v);
+      transform16<ROPE>(t, ti, hk, (int)(row - n * t.N), l8, raw[sl], inv_freq, v);
       if (WRITE) {
-        if (row_raw >= cur.r1) continue;
-        const float a = __uint_as_float(t.amax[ti][row / rps]);
+        if (row_raw >= in.r1) continue;
+        const float a = __uint_as_float(t.amax[ti][in.one_head ? in.h0 : row / rps]);
         const float mul = a > 0.f ? (448.0f / a) * norm : 1.0f;
         uint4 codes;
         codes.x = pack_e4m3x4(v[0] * mul, v[1] * mul, v[2] * mul, v[3] * mul);
@@ -243,25 +343,20 @@ __global__ void __launch_bounds__(256) quant_pass_kernel(const QuantTensors t) {
         float rm = 0.f;
 #pragma unroll
         for (int e = 0; e < 16; ++e) rm = fmaxf(rm, fabsf(v[e]));
-        if (row_raw >= cur.r1) rm = 0.f;
-        if (one_head) {
+        if (row_raw >= in.r1) rm = 0.f;
+        if (in.one_head) {
           mx = fmaxf(mx, rm);
-        } else {  // rows of two heads in this group (short sequences): one atomic per row
+        } else {  // rows of two heads in this stage (short sequences): one atomic per row
 #pragma unroll
           for (int o = 1; o < 8; o <<= 1) rm = fmaxf(rm, __shfl_xor_sync(0xffffffffu, rm, o));
-          if (l8 == 0 && row_raw < cur.r1) atomicMax(t.amax[ti] + row / rps, __float_as_uint(rm * norm));
+          if (l8 == 0 && row_raw < in.r1) atomicMax(t.amax[ti] + row / rps, __float_as_uint(rm * norm));
         }
       }
     }
-    if (!WRITE && one_head) {
+    if (!WRITE && in.one_head) {
       mx = warp_max(mx);
-      if (lane == 0) atomicMax(t.amax[ti] + cur.r0 / rps, __float_as_uint(mx * norm));
+      if (lane == 0) atomicMax(t.amax[ti] + in.h0, __float_as_uint(mx * norm));
     }
-    cur = nxt;
-#pragma unroll
-    for (int s = 0; s < SLABS; ++s) raw[s] = rawn[s];
-    gi += stride;
-    have = hn;
   }
 }
 
@@ -278,8 +373,10 @@ static cudaError_t run_quant(const QuantTensors& t, int B, unsigned* amax_ws, si
 
 cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, void* q8, void* k8,
                                   void* v8, float* scales, const int8_t* signs, int B, int Hq,
-                                  int Hkv, int N, float rope_base, unsigned* amax_ws, cudaStream_t st) {
+                                  int Hkv, int N, float rope_base, unsigned* amax_ws, int* status,
+                                  cudaStream_t st) {
   QuantTensors t{};
+  t.status = status;
   t.rope_k = rope_base > 0.f ? 2.0f * log2f(rope_base) / 128.0f : 0.f;
   t.x[0] = (const __nv_bfloat16*)q;
   t.x[1] = (const __nv_bfloat16*)k;
@@ -310,19 +407,24 @@ cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, v
 static cudaError_t run_quant(const QuantTensors& t, int B, unsigned* amax_ws, size_t n_amax, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(amax_ws, 0, sizeof(unsigned) * n_amax, st);
   if (e != cudaSuccess) return e;
-  long long groups = 0;
-  for (int i = 0; i < 3; ++i) groups += (t.rows[i] + ROWS_PER_WARP - 1) / ROWS_PER_WARP;
+  long long stages = 0;
+  for (int i = 0; i < 3; ++i) stages += (t.rows[i] + STAGE_ROWS - 1) / STAGE_ROWS;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  // Two 8-warp blocks per SM stay resident (register-limited); each warp walks many groups.
-  const long long blocks = min((groups + 7) / 8, (long long)sms * 2);
+  // One CTA per SM, each walking many stages.
+  const long long blocks = min(stages, (long long)sms);
   const bool rope = t.rope_k != 0.f;
-  (rope ? quant_pass_kernel<false, true> : quant_pass_kernel<false, false>)<<<(unsigned)blocks, 256, 0, st>>>(t);
+  auto p1 = rope ? quant_pass_kernel<false, true> : quant_pass_kernel<false, false>;
+  auto p2 = rope ? quant_pass_kernel<true, true> : quant_pass_kernel<true, false>;
+  if ((e = cudaFuncSetAttribute(p1, cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(p2, cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM)) != cudaSuccess) return e;
+  if (blocks == 0) return cudaSuccess;
+  p1<<<(unsigned)blocks, QTHREADS, QSMEM, st>>>(t);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   quant_scale_kernel<<<dim3(1, 3), 256, 0, st>>>(t, B);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  (rope ? quant_pass_kernel<true, true> : quant_pass_kernel<true, false>)<<<(unsigned)blocks, 256, 0, st>>>(t);
+  p2<<<(unsigned)blocks, QTHREADS, QSMEM, st>>>(t);
   return cudaGetLastError();
 }
 
@@ -332,8 +434,9 @@ static cudaError_t run_quant(const QuantTensors& t, int B, unsigned* amax_ws, si
 // rotation (the dV GEMM contracts over rows, not over the rotated columns).
 // scales: [B * Hkv] of dO, then [B * Hkv] of V.
 cudaError_t launch_quant_bwd_fp8(const void* dout, const void* v, void* do8, void* v8, float* scales, int B,
-                                 int Hq, int Hkv, int N, unsigned* amax_ws, cudaStream_t st) {
+                                 int Hq, int Hkv, int N, unsigned* amax_ws, int* status, cudaStream_t st) {
   QuantTensors t{};
+  t.status = status;
   t.x[0] = (const __nv_bfloat16*)dout;
   t.x[2] = (const __nv_bfloat16*)v;
   t.out[0] = (uint8_t*)do8;

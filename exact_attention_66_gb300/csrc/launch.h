@@ -101,8 +101,9 @@ cudaError_t launch_seq_ids(const int* cu, int n_seqs, int total, int* ids, cudaS
 // rope_base > 0: RoPE (rotate-half, position = row index) applied first.
 cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, void* q8, void* k8,
                                   void* v8, float* scales, const int8_t* signs, int B, int Hq,
-                                  int Hkv, int N, float rope_base, unsigned* amax_ws, cudaStream_t st);
+                                  int Hkv, int N, float rope_base, unsigned* amax_ws, int* status,
+                                  cudaStream_t st);
 cudaError_t launch_quant_bwd_fp8(const void* dout, const void* v, void* do8, void* v8, float* scales, int B,
-                                 int Hq, int Hkv, int N, unsigned* amax_ws, cudaStream_t st);
+                                 int Hq, int Hkv, int N, unsigned* amax_ws, int* status, cudaStream_t st);
 
 }  // namespace attn
