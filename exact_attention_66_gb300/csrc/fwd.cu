@@ -565,9 +565,14 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t lo[64];
       if (FP8)
         l += exp_e4m3(s, mul, mu);
-      else if (partial)
+      else if (partial) {
         l += exp_bf16<true>(s, lo, mul, mu);
-      else
+        // The residual of P into the S columns (this warpgroup's until it
+        // releases them below), for the TS MMA: stored now, so that it is not
+        // live in registers across the wait and the rescale.
+        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&lo[0]));
+        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&lo[32]));
+      } else
         l += exp_bf16<false>(s, lo, mul, mu);
 
       // The previous P V must be done before O is rescaled or P overwritten.
@@ -590,10 +595,6 @@ __global__ void __launch_bounds__(384, 1)
         store_p_smem<32>(p_tile, r, s);
       } else {
         store_p_smem<64>(p_tile, r, s);
-        if (partial) {  // residual of P into the (now unused) S columns, for the TS MMA
-          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&lo[0]));
-          tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&lo[32]));
-        }
       }
       tmem_wait_st();
       fence_async_smem();
