@@ -63,10 +63,12 @@ struct FwdCfg {
   static constexpr int THREADS = 384;
   // Register split: launched at 168 per thread (65536 / 384, rounded down to
   // a multiple of 8); warpgroup 0 (TMA, MMA, two idle warps) gives up
-  // registers to the two softmax warpgroups: 128 * 56 + 256 * 224 = 384 * 168
-  // for bf16.  The e4m3 kernel runs 5 % faster at 40 / 232 (measured on the
-  // 16K FP8 workload; bf16 is 1.6 % slower there), where ptxas spills less.
-  static constexpr int LAUNCH_REGS = 168, REGS_LOW = FP8 ? 40 : 56, REGS_HIGH = FP8 ? 232 : 224;
+  // registers to the two softmax warpgroups.  bf16: 64 / 216 (the softmax
+  // fits in 216 once the P residual is stored as soon as it is formed; the
+  // issuing warps spilled at 56: 64 / 216 was 0.6-5.3 % faster than 56 / 224
+  // on the GQA 8K, MHA 2K, flex and paged workloads).  e4m3: 40 / 232, 5 %
+  // faster than 56 / 224 on the 16K FP8 workload, where ptxas spills less.
+  static constexpr int LAUNCH_REGS = 168, REGS_LOW = FP8 ? 40 : 64, REGS_HIGH = FP8 ? 232 : 216;
   static_assert(128 * REGS_LOW + 256 * REGS_HIGH <= 384 * LAUNCH_REGS, "register split exceeds the launch allocation");
 };
 static_assert(FwdCfg<128, false>::SMEM_BYTES <= 232448, "forward shared memory exceeds 227 KB");
