@@ -36,17 +36,21 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                       const float* __restrict__ lse,
                                                       float2* __restrict__ rowstat, int N,
                                                       long long rows_padded, const PreExtra x) {
-  constexpr int TPR = D / 8;  // threads per row, 8 bf16 each
-  const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long row = gt / TPR;
-  const int part = (int)(gt % TPR);
-  const long long np = (long long)((N + TILE - 1) / TILE) * TILE;
-  const long long bh = row / np;
-  const int i = (int)(row - bh * np);
+  constexpr int TPR = D / 8;           // threads per row, 8 bf16 each
+  constexpr int RPB = 256 / TPR;       // rows per block (blocks of 256 threads)
+  // A block holds RPB rows of one (batch, head): one 32-bit division per
+  // block index instead of a 64-bit one per thread (which cost about half the
+  // kernel's issue slots).
+  const int np = (N + TILE - 1) / TILE * TILE;
+  const unsigned bph = (unsigned)(np / RPB);  // blocks per (batch, head)
+  const unsigned bh = blockIdx.x / bph;
+  const int i = (int)(blockIdx.x - bh * bph) * RPB + (int)(threadIdx.x / TPR);
+  const int part = (int)(threadIdx.x % TPR);
+  const long long row = (long long)bh * np + i;
   const bool real = row < rows_padded && i < N;
   float acc = 0.f, ss = 0.f;  // rowsum(dO * O), ||dO||^2
   if (real) {
-    const long long src = bh * N + i;
+    const long long src = (long long)bh * N + i;
     const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + src * D) + part);
     const uint4 g = __ldg(reinterpret_cast<const uint4*>(dout + src * D) + part);
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
@@ -67,7 +71,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   if (row < rows_padded && part == 0) {
     float l2 = INFINITY;
     if (real) {
-      const float v = lse[bh * N + i];
+      const float v = lse[(long long)bh * N + i];
       l2 = v == -INFINITY ? INFINITY : v * LOG2E;
     }
     rowstat[row] = make_float2(l2, acc);
@@ -83,7 +87,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
       x.qscale[row] = q;
     }
   }
-  if (x.ticket != nullptr && gt == 0) *x.ticket = 0;
+  if (x.ticket != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *x.ticket = 0;
   if (x.dqacc != nullptr && row < rows_padded) {
     uint4* z = reinterpret_cast<uint4*>(x.dqacc + row * D + part * 8);
     z[0] = make_uint4(0u, 0u, 0u, 0u);
