@@ -710,7 +710,7 @@ template <int D, bool MODS, bool MASKS, bool FP8 = false>
 static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
   const AttnParams& p = L.p;
   const long long rows = (long long)p.B * p.Hq * p.nT * TILE;
-  const long long threads = rows * (D / 8);
+  const long long threads = rows * (D / 16);  // bwd_pre: 16 elements of a row per thread
   if (L.events[0]) cudaEventRecord(L.events[0], st);
   cudaError_t e;
   if (FP8 && (e = launch_quant_bwd_fp8(L.dout, L.v, L.do8, L.v8, L.fp8s, p.B, p.Hq, p.Hkv, p.N, L.fp8amax, p.status, st)) !=

@@ -538,7 +538,7 @@ static cudaError_t launch_fused_t(const BwdLaunch& L, cudaStream_t st) {
   constexpr int D = 128;
   const AttnParams& p = L.p;
   const long long rows = (long long)p.B * p.Hq * p.nT * TILE;
-  const long long threads = rows * (D / 8);
+  const long long threads = rows * (D / 16);  // bwd_pre: 16 elements of a row per thread
   if (L.events[0]) cudaEventRecord(L.events[0], st);
   cudaError_t e = cudaMemsetAsync(L.kvb, 0, (size_t)p.B * p.Hkv * sizeof(float2), st);
   if (e != cudaSuccess) return e;
