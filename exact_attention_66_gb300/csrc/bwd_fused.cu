@@ -511,22 +511,27 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const int* __restrict__
                                                          const float* __restrict__ qscale,
                                                          __nv_bfloat16* __restrict__ dq, int N, int nT,
                                                          float scale, long long rows) {
-  constexpr int TPR = D / 8;
+  constexpr int TPR = D / 16;  // threads per row, 16 elements each
   const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = gt / TPR;  // row of dq, [B * Hq * N]
   const int part = (int)(gt % TPR);
   if (row >= rows) return;
-  const long long bh = row / N;
-  const long long prow = bh * nT * TILE + (row - bh * N);  // padded row
+  // rows < 2^31 (a dQ of 2^31 rows would not fit in device memory): 32-bit division
+  const unsigned bh = (unsigned)row / (unsigned)N;
+  const long long prow = (long long)bh * nT * TILE + (row - (long long)bh * N);  // padded row
   const float mul = scale / qscale[prow];
-  const int4* src = reinterpret_cast<const int4*>(dqacc + prow * D + part * 8);
-  const int4 a = src[0], b = src[1];
-  uint4 o;
-  o.x = pack_bf16((float)a.x * mul, (float)a.y * mul);
-  o.y = pack_bf16((float)a.z * mul, (float)a.w * mul);
-  o.z = pack_bf16((float)b.x * mul, (float)b.y * mul);
-  o.w = pack_bf16((float)b.z * mul, (float)b.w * mul);
-  reinterpret_cast<uint4*>(dq + row * D)[part] = o;
+  const int4* src = reinterpret_cast<const int4*>(dqacc + prow * D + part * 16);
+  uint4* dst = reinterpret_cast<uint4*>(dq + row * D) + 2 * part;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int4 a = src[2 * h], b = src[2 * h + 1];
+    uint4 o;
+    o.x = pack_bf16((float)a.x * mul, (float)a.y * mul);
+    o.y = pack_bf16((float)a.z * mul, (float)a.w * mul);
+    o.z = pack_bf16((float)b.x * mul, (float)b.y * mul);
+    o.w = pack_bf16((float)b.z * mul, (float)b.w * mul);
+    dst[h] = o;
+  }
 }
 
 // ------------------------------------------------------------------ launch
@@ -572,7 +577,7 @@ static cudaError_t launch_fused_t(const BwdLaunch& L, cudaStream_t st) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (L.events[2]) cudaEventRecord(L.events[2], st);
   const long long dq_rows = (long long)p.B * p.Hq * p.N;
-  dq_convert_kernel<D><<<(unsigned)((dq_rows * (D / 8) + 255) / 256), 256, 0, st>>>(
+  dq_convert_kernel<D><<<(unsigned)((dq_rows * (D / 16) + 255) / 256), 256, 0, st>>>(
       L.dqacc, L.qscale, (__nv_bfloat16*)L.dq, p.N, p.nT, p.scale, dq_rows);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (L.events[3]) cudaEventRecord(L.events[3], st);
