@@ -360,6 +360,207 @@ __global__ void __launch_bounds__(QTHREADS, 1) quant_pass_kernel(const QuantTens
   }
 }
 
+// Whole rows per thread (every prologue without RoPE).  A stage of 256 rows
+// reaches shared memory as two tensor copies (columns 0-63 and 64-127) with
+// the 128-byte swizzle: 16-byte chunk c of row r sits in slot c ^ (r % 8) of
+// the row's 128 bytes, so a thread reading its own row chunk by chunk meets
+// eight different bank groups across any eight consecutive rows.  Each of
+// eight compute warps takes 32 rows of a stage, one per thread, and runs all
+// seven butterfly stages in registers with no shuffle: distance 1 in scalar
+// fp32 on the two halves of a bf16 pair word, distances 2..64 two lanes per
+// instruction.  The butterflies, their order and the sign and scale steps are
+// those of the lane-split form above, so both give the same bits.  Codes
+// leave through a per-warp transposition in shared memory (row r, chunk c in
+// slot c ^ (r % 8) again), so each store instruction writes four whole rows.
+constexpr int RWARPS = 8;                          // compute warps (two warpgroups)
+constexpr int RTHREADS = (RWARPS + 4) * 32;        // plus a producer warpgroup (one thread works)
+// Register split: launched at 168 a thread (ptxas' bound for 384 threads), the
+// producer warpgroup gives registers back so a compute thread can hold its
+// 128 rotated values, the sign words and the code words without spilling.
+constexpr int R_LAUNCH = 168, R_LOW = 56, R_HIGH = 224;
+static_assert(128 * R_LOW + 256 * R_HIGH <= RTHREADS * R_LAUNCH, "register split over the launch's allocation");
+constexpr int XPOSE_BYTES = RWARPS * 32 * 128;     // one 32-row block of codes per compute warp
+constexpr int RSMEM = QSTAGES * STAGE_BYTES + XPOSE_BYTES + (int)sizeof(QuantBars) + 1024;
+static_assert(RWARPS * 32 == STAGE_ROWS, "one row of a stage per compute thread");
+
+struct QuantMaps {
+  CUtensorMap m[3];  // [rows, 128] bf16 of each tensor, 64 x 256 boxes, 128-byte swizzle
+};
+
+// XOR masks that negate halves of bf16 pair words: bit 15 (low half) and bit
+// 31 (high half) from the sign bits of int8 signs.  sw holds the signs of four
+// consecutive elements 4 j .. 4 j + 3; lo: the word of elements 4 j, 4 j + 1,
+// hi: the word of 4 j + 2, 4 j + 3.
+__device__ __forceinline__ uint32_t sign_mask_lo(uint32_t sw) { return __byte_perm(sw, 0u, 0x1404) & 0x80008000u; }
+__device__ __forceinline__ uint32_t sign_mask_hi(uint32_t sw) { return __byte_perm(sw, 0u, 0x3424) & 0x80008000u; }
+
+template <bool WRITE>
+__global__ void __launch_bounds__(RTHREADS, 1) quant_rows_kernel(const QuantTensors t,
+                                                                 const __grid_constant__ QuantMaps maps) {
+  extern __shared__ uint8_t qsm_raw[];
+  // The 128-byte swizzle repeats every 1024 bytes: slots start on that boundary.
+  uint8_t* sm = (uint8_t*)(((uintptr_t)qsm_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* xpose = sm + QSTAGES * STAGE_BYTES;
+  QuantBars& S = *reinterpret_cast<QuantBars*>(xpose + XPOSE_BYTES);
+  const Abort ab{&S.abort, t.status};
+  const int warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    S.abort = 0;
+    for (int s = 0; s < QSTAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], RWARPS);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp >= RWARPS) {
+    // ------------------------------------------------------------ producer
+    regs_dec<R_LOW>();
+    if (warp == RWARPS && lane == 0) {
+      for (int i = 0; i < 3; ++i)
+        if (t.rows[i] > 0) tma_prefetch_desc(&maps.m[i]);
+      long long k = 0;
+      bool ok = true;
+      for (long long g = blockIdx.x;; g += gridDim.x, ++k) {
+        const int s = (int)(k % QSTAGES);
+        if (!(ok = mbar_wait(&S.empty[s], (uint32_t)((k / QSTAGES) & 1) ^ 1u, ab))) break;
+        Group gr;
+        StageInfo& in = S.info[s];
+        if (!stage_of(t, g, gr)) {
+          S.done[s] = 1;
+          mbar_arrive(&S.full[s]);
+          break;
+        }
+        const long long rps = t.rps[gr.ti];
+        in.r0 = gr.r0;
+        in.r1 = gr.r1;
+        in.ti = gr.ti;
+        in.h0 = gr.r0 / rps;
+        in.one_head = gr.r1 - 1 < (in.h0 + 1) * rps;
+        in.n0 = gr.r0 / t.N;
+        in.one_n = gr.r1 - 1 < (in.n0 + 1) * t.N;
+        in.hk0 = t.signs != nullptr ? sign_head(t, gr.ti, in.n0) : 0;
+        S.done[s] = 0;
+        // Both boxes count in full: rows past the tensor's end arrive as zeros.
+        mbar_arrive_tx(&S.full[s], STAGE_BYTES);
+        tma_load_2d(sm + s * STAGE_BYTES, &maps.m[gr.ti], &S.full[s], 0, (int)gr.r0);
+        tma_load_2d(sm + s * STAGE_BYTES + STAGE_BYTES / 2, &maps.m[gr.ti], &S.full[s], 64, (int)gr.r0);
+      }
+      const long long armed = ok ? k + 1 : k;
+      for (int s = 0; s < QSTAGES; ++s)
+        if (armed > s) mbar_wait_drain(&S.full[s], (uint32_t)(((armed - 1 - s) / QSTAGES) & 1));
+    }
+    return;
+  }
+  // -------------------------------------------------------- compute warps
+  regs_inc<R_HIGH>();
+  const int lr = warp * 32 + lane;  // this thread's row of every stage
+  uint8_t* xw = xpose + warp * (32 * 128);
+  const uint64_t m1 = f2_pack(-1.f, -1.f);
+  for (long long k = 0;; ++k) {
+    const int s = (int)(k % QSTAGES);
+    if (!wait_warp(&S.full[s], (uint32_t)((k / QSTAGES) & 1), ab)) break;
+    if (S.done[s]) break;
+    const StageInfo in = S.info[s];
+    uint32_t w[64];  // bf16 pair words: w[j] = elements 2 j, 2 j + 1
+    {
+      const uint8_t* src = sm + s * STAGE_BYTES + lr * 128;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 q = *reinterpret_cast<const uint4*>(src + (c >> 3) * (STAGE_BYTES / 2) +
+                                                         (((c & 7) ^ (lr & 7)) << 4));
+        w[4 * c] = q.x;
+        w[4 * c + 1] = q.y;
+        w[4 * c + 2] = q.z;
+        w[4 * c + 3] = q.w;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[s]);
+
+    const int ti = in.ti;
+    const long long row = in.r0 + lr;
+    const bool valid = row < in.r1;
+    const long long rowc = valid ? row : in.r1 - 1;
+    const float norm = out_norm(t, ti);
+    uint64_t P[64];  // P[j] = (y[2 j], y[2 j + 1])
+    if (ti != 2 && t.signs != nullptr) {
+      const int hk = in.one_n ? in.hk0 : sign_head(t, ti, rowc / t.N);
+      const uint4* sg = reinterpret_cast<const uint4*>(t.signs + hk * 128);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {  // elements 16 i .. 16 i + 15
+        const uint4 q = __ldg(sg + i);
+        const uint32_t sw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int wi = 8 * i + 2 * j + e;
+            const uint32_t x = w[wi] ^ (e == 0 ? sign_mask_lo(sw[j]) : sign_mask_hi(sw[j]));
+            const float a = bf16lo_f32(x), b = bf16hi_f32(x);
+            P[wi] = f2_pack(a + b, a - b);  // distance 1
+          }
+        }
+      }
+#pragma unroll
+      for (int hb = 1; hb < 64; hb <<= 1) {  // distances 2 .. 64: pair index bit hb
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          if (j & hb) continue;
+          const uint64_t a2 = P[j], b2 = P[j | hb];
+          P[j] = f2_add(a2, b2);
+          P[j | hb] = f2_fma(b2, m1, a2);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 64; ++j) P[j] = f2_pack(bf16lo_f32(w[j]), bf16hi_f32(w[j]));
+    }
+
+    if (!WRITE) {
+      float r4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        float y0, y1;
+        f2_unpack(P[j], y0, y1);
+        r4[j & 3] = max3(r4[j & 3], fabsf(y0), fabsf(y1));
+      }
+      float rm = valid ? fmaxf(fmaxf(r4[0], r4[1]), fmaxf(r4[2], r4[3])) : 0.f;
+      if (in.one_head) {
+        rm = warp_max(rm);
+        if (lane == 0) atomicMax(t.amax[ti] + in.h0, __float_as_uint(rm * norm));
+      } else if (valid) {  // rows of two scales in this stage (short sequences): one atomic per row
+        atomicMax(t.amax[ti] + row / t.rps[ti], __float_as_uint(rm * norm));
+      }
+    } else {
+      const float a = __uint_as_float(t.amax[ti][in.one_head ? in.h0 : rowc / t.rps[ti]]);
+      const float mul = a > 0.f ? (448.0f / a) * norm : 1.0f;
+      const uint64_t mul2 = f2_pack(mul, mul);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {  // code bytes 16 c .. 16 c + 15 of the row
+        uint32_t cw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float y0, y1, y2, y3;
+          f2_unpack(f2_mul(P[8 * c + 2 * j], mul2), y0, y1);
+          f2_unpack(f2_mul(P[8 * c + 2 * j + 1], mul2), y2, y3);
+          cw[j] = pack_e4m3x4(y0, y1, y2, y3);
+        }
+        *reinterpret_cast<uint4*>(xw + lane * 128 + ((c ^ (lane & 7)) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {  // rows 4 i .. 4 i + 3 of the warp's block, eight lanes a row
+        const int rr = 4 * i + (lane >> 3), ch = lane & 7;
+        const uint4 val = *reinterpret_cast<const uint4*>(xw + rr * 128 + ((ch ^ (rr & 7)) << 4));
+        const long long grow = in.r0 + warp * 32 + rr;
+        if (grow < in.r1) reinterpret_cast<uint4*>(t.out[ti] + grow * 128)[ch] = val;
+      }
+      __syncwarp();
+    }
+  }
+}
+
 __global__ void quant_scale_kernel(const QuantTensors t, int B) {
   const int ti = blockIdx.y;
   const int n = B * t.heads[ti];
@@ -414,17 +615,43 @@ static cudaError_t run_quant(const QuantTensors& t, int B, unsigned* amax_ws, si
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   // One CTA per SM, each walking many stages.
   const long long blocks = min(stages, (long long)sms);
-  const bool rope = t.rope_k != 0.f;
-  auto p1 = rope ? quant_pass_kernel<false, true> : quant_pass_kernel<false, false>;
-  auto p2 = rope ? quant_pass_kernel<true, true> : quant_pass_kernel<true, false>;
-  if ((e = cudaFuncSetAttribute(p1, cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(p2, cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM)) != cudaSuccess) return e;
+  if (t.rope_k != 0.f) {  // RoPE: lane-split rows
+    auto p1 = quant_pass_kernel<false, true>;
+    auto p2 = quant_pass_kernel<true, true>;
+    if ((e = cudaFuncSetAttribute(p1, cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(p2, cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM)) != cudaSuccess) return e;
+    if (blocks == 0) return cudaSuccess;
+    p1<<<(unsigned)blocks, QTHREADS, QSMEM, st>>>(t);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    quant_scale_kernel<<<dim3(1, 3), 256, 0, st>>>(t, B);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    p2<<<(unsigned)blocks, QTHREADS, QSMEM, st>>>(t);
+    return cudaGetLastError();
+  }
+  QuantMaps maps{};
+  for (int i = 0; i < 3; ++i)
+    if (t.rows[i] > 0 && !make_rows_map(&maps.m[i], t.x[i], t.rows[i], STAGE_ROWS)) return cudaErrorInvalidValue;
+  auto p1 = quant_rows_kernel<false>;
+  auto p2 = quant_rows_kernel<true>;
+  // The register split inside the kernels assumes R_LAUNCH registers a thread
+  // at launch: with fewer, the compute warps' increase could never be granted.
+  static int regs[2] = {-1, -1};
+  for (int w = 0; w < 2; ++w) {
+    if (regs[w] < 0) {
+      cudaFuncAttributes fa;
+      if ((e = cudaFuncGetAttributes(&fa, w ? p2 : p1)) != cudaSuccess) return e;
+      regs[w] = fa.numRegs;
+    }
+    if (regs[w] != R_LAUNCH) return cudaErrorInvalidConfiguration;
+  }
+  if ((e = cudaFuncSetAttribute(p1, cudaFuncAttributeMaxDynamicSharedMemorySize, RSMEM)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(p2, cudaFuncAttributeMaxDynamicSharedMemorySize, RSMEM)) != cudaSuccess) return e;
   if (blocks == 0) return cudaSuccess;
-  p1<<<(unsigned)blocks, QTHREADS, QSMEM, st>>>(t);
+  p1<<<(unsigned)blocks, RTHREADS, RSMEM, st>>>(t, maps);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   quant_scale_kernel<<<dim3(1, 3), 256, 0, st>>>(t, B);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  p2<<<(unsigned)blocks, QTHREADS, QSMEM, st>>>(t);
+  p2<<<(unsigned)blocks, RTHREADS, RSMEM, st>>>(t, maps);
   return cudaGetLastError();
 }
 

@@ -98,6 +98,10 @@ cudaError_t launch_tile_ranges(const AttnParams& p, const uint8_t* map, int2* ro
 cudaError_t launch_doc_bounds(const AttnParams& p, int2* bounds, int* unsorted, cudaStream_t st);
 cudaError_t launch_seq_ids(const int* cu, int n_seqs, int total, int* ids, cudaStream_t st);
 
+// TMA descriptor of a [rows, 128] bf16 tensor: 64-column x box_rows-row boxes,
+// 128-byte swizzle (api.cu).
+bool make_rows_map(CUtensorMap* m, const void* ptr, long long rows, int box_rows);
+
 // rope_base > 0: RoPE (rotate-half, position = row index) applied first.
 cudaError_t launch_hadamard_quant(const void* q, const void* k, const void* v, void* q8, void* k8,
                                   void* v8, float* scales, const int8_t* signs, int B, int Hq,
