@@ -12,20 +12,18 @@
 // Two bandwidth-bound passes over Q, K, V: pass 1 finds the amax of every
 // (batch, head) of the rotated tensors (integer atomic max of the non-negative
 // float bits, so the result does not depend on the order), pass 2 recomputes
-// the rotation and writes e4m3 codes scaled by 448 / amax.  Rows reach
-// shared memory in 64-row stages by bulk copy (one producer thread per CTA,
-// a 6-slot ring); eight lanes per 128-element row, lane l8 holding elements
-// 16 l8 .. 16 l8 + 15, so a compute warp takes four rows of a stage.  The
-// butterflies of distance 1..8 stay in registers (two lanes of fp32 per
-// instruction from distance 2 on), 16..64 go through three warp shuffles; the
-// signs are applied to the bf16 bits while converting, and 1 / sqrt(128)
-// is folded into the amax and the quantisation multiplier.
+// the rotation and writes e4m3 codes scaled by 448 / amax.  Each compute
+// thread holds one whole 128-element row and runs the seven butterfly stages
+// in registers with no shuffle: distance 1 in scalar fp32 on the two halves
+// of a bf16 pair word, distances 2..64 two lanes per instruction.  The signs
+// are applied to the bf16 bits while converting, and 1 / sqrt(128) is folded
+// into the amax and the quantisation multiplier.
 //
 // Optionally RoPE is fused in front of the rotation (the digest's "fused with
 // RoPE at no extra cost"): the row at position n of its head has its element
 // pairs (c, c + 64) turned by n * base^(-2c/128) before the signs and the
-// Hadamard butterflies, in the same registers -- lane l8 pairs with lane
-// l8 ^ 4 -- so RoPE costs no extra pass over memory.
+// Hadamard butterflies, in the same registers, so RoPE costs no extra pass
+// over memory.
 #include "common.cuh"
 #include "launch.h"
 
@@ -45,37 +43,24 @@ struct QuantTensors {
   int* status;                // device status word (bounded waits report a timeout there)
 };
 
-constexpr int STAGE_ROWS = 256;                 // rows per shared-memory stage
-constexpr int STAGE_BYTES = STAGE_ROWS * 256;    // 64 KB of bf16 rows (d = 128)
-constexpr int QSTAGES = 3;                       // ring slots per CTA
-constexpr int QWARPS = 16;                       // compute warps
-constexpr int WROWS = STAGE_ROWS / QWARPS;       // rows of a stage per compute warp (16)
-constexpr int SLABS = WROWS / 4;                 // four rows per warp instruction
-constexpr int QTHREADS = (QWARPS + 1) * 32;      // plus one producer warp
-constexpr float HAD_NORM = 0.08838834764831845f;  // 1 / sqrt(128)
-
-// Untiled bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
-// aligned) from global to shared memory, completing on an mbarrier.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
+constexpr int STAGE_ROWS = 256;                   // rows per shared-memory stage
+constexpr int STAGE_BYTES = STAGE_ROWS * 256;      // 64 KB of bf16 rows (d = 128)
+constexpr int QSTAGES = 3;                         // ring slots per CTA
+constexpr int RWARPS = 8;                          // compute warps (two warpgroups)
+constexpr int RTHREADS = (RWARPS + 4) * 32;        // plus a producer warpgroup (one thread works)
+constexpr int XPOSE_BYTES = RWARPS * 32 * 128;     // one 32-row block of codes per compute warp
+constexpr float HAD_NORM = 0.08838834764831845f;   // 1 / sqrt(128)
+static_assert(RWARPS * 32 == STAGE_ROWS, "one row of a stage per compute thread");
+// Register split: launched at 168 a thread (ptxas' bound for 384 threads), the
+// producer warpgroup gives registers back so a compute thread can hold its
+// 128 rotated values, the sign words and the code words without spilling.
+constexpr int R_LAUNCH = 168, R_LOW = 56, R_HIGH = 224;
+static_assert(128 * R_LOW + 256 * R_HIGH <= RTHREADS * R_LAUNCH, "register split over the launch's allocation");
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
   return x;
-}
-
-// This lane's 16 bf16 elements of a row.
-struct Raw16 {
-  uint4 a, b;
-};
-__device__ __forceinline__ Raw16 load16(const QuantTensors& t, int ti, long long row, int l8) {
-  const uint4* p = reinterpret_cast<const uint4*>(t.x[ti] + row * 128 + 16 * l8);
-  return Raw16{__ldg(p), __ldg(p + 1)};
 }
 
 // KV head whose signs rotate rows of head plane n (= b * H + h) of tensor ti.
@@ -84,121 +69,17 @@ __device__ __forceinline__ int sign_head(const QuantTensors& t, int ti, long lon
   return ti == 0 ? head / t.G : head;
 }
 
-// This lane's 16 values of the row: RoPE (when on), then the signed
-// Walsh-Hadamard transform without its 1 / sqrt(128) (Q and K with signs), or
-// the plain values.  Every lane of the warp must call it (warp shuffles).
-// hk: the row's sign head (sign_head), pos: its position in its sequence.
-template <bool ROPE>
-__device__ __forceinline__ void transform16(const QuantTensors& t, int ti, int hk, int pos, int l8, const Raw16& raw,
-                                            const float (&inv_freq)[16], float (&v)[16]) {
-  const uint32_t w[8] = {raw.a.x, raw.a.y, raw.a.z, raw.a.w, raw.b.x, raw.b.y, raw.b.z, raw.b.w};
-  if (ti == 2 || (!ROPE && t.signs == nullptr)) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      v[2 * k] = bf16lo_f32(w[k]);
-      v[2 * k + 1] = bf16hi_f32(w[k]);
-    }
-    return;
-  }
-  uint32_t sgn[4] = {0u, 0u, 0u, 0u};  // sign bytes of elements 4 j .. 4 j + 3
-  if (t.signs != nullptr) {
-    const uint4 sg = __ldg(reinterpret_cast<const uint4*>(t.signs + hk * 128 + 16 * l8));
-    sgn[0] = sg.x;
-    sgn[1] = sg.y;
-    sgn[2] = sg.z;
-    sgn[3] = sg.w;
-  }
-  if (ROPE) {  // RoPE first (before the signs), rotate-half pairs (c, c + 64)
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      v[2 * k] = bf16lo_f32(w[k]);
-      v[2 * k + 1] = bf16hi_f32(w[k]);
-    }
-    const float fpos = (float)pos;
-    const bool first = l8 < 4;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const float partner = __shfl_xor_sync(0xffffffffu, v[e], 4);
-      // Angle reduced to [-pi, pi] by Cody and Waite's two-constant method:
-      // 2 pi = C1 - C2 with C1 = fl(2 pi) and C2 = 1.7484556e-7 its excess;
-      // both steps are fused multiply-adds, so k C1 enters exactly.  Then the
-      // fast sine / cosine, accurate to a few 1e-7 on that interval.
-      const float ang = fpos * inv_freq[e];
-      const float kf = rintf(ang * 0.15915494309189535f);  // 1 / (2 pi)
-      const float red = fmaf(kf, 1.7484556e-07f, fmaf(-kf, 6.28318548f, ang));
-      float sn, cs;
-      __sincosf(red, &sn, &cs);
-      v[e] = first ? fmaf(v[e], cs, -partner * sn) : fmaf(v[e], cs, partner * sn);
-    }
-    if (t.signs == nullptr) return;
-#pragma unroll
-    for (int e = 0; e < 16; ++e)
-      v[e] = __uint_as_float(__float_as_uint(v[e]) ^ (((sgn[e >> 2] >> (8 * (e & 3) + 7)) & 1u) << 31));
-  } else {  // signs applied to the bf16 bits while converting
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t sb = sgn[k >> 1] >> (16 * (k & 1));  // sign bytes of elements 2 k, 2 k + 1
-      v[2 * k] = __uint_as_float((w[k] << 16) ^ ((sb & 0x80u) << 24));
-      v[2 * k + 1] = __uint_as_float((w[k] & 0xFFFF0000u) ^ ((sb & 0x8000u) << 16));
-    }
-  }
-  // Butterflies (a, b) -> (a + b, a - b) on index pairs (j, j ^ h).  h = 1: scalar.
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float a0 = v[2 * k], b0 = v[2 * k + 1];
-    v[2 * k] = a0 + b0;
-    v[2 * k + 1] = a0 - b0;
-  }
-  uint64_t P[8];  // pairs (v[2 k], v[2 k + 1])
-#pragma unroll
-  for (int k = 0; k < 8; ++k) P[k] = f2_pack(v[2 * k], v[2 * k + 1]);
-  const uint64_t m1 = f2_pack(-1.f, -1.f);
-#pragma unroll
-  for (int hb = 1; hb < 8; hb <<= 1) {  // h = 2, 4, 8: pair index bit hb
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (k & hb) continue;
-      const uint64_t a2 = P[k], b2 = P[k | hb];
-      P[k] = f2_add(a2, b2);
-      P[k | hb] = f2_fma(b2, m1, a2);
-    }
-  }
-#pragma unroll
-  for (int m = 1; m < 8; m <<= 1) {  // h = 16, 32, 64: lane bit m of l8
-    const float sgn_self = (l8 & m) ? -1.f : 1.f;
-    const uint64_t s2 = f2_pack(sgn_self, sgn_self);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      float x0, x1;
-      f2_unpack(P[k], x0, x1);
-      const float o0 = __shfl_xor_sync(0xffffffffu, x0, m), o1 = __shfl_xor_sync(0xffffffffu, x1, m);
-      P[k] = f2_fma(P[k], s2, f2_pack(o0, o1));  // lower index: a + b; upper: a' - b'
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < 8; ++k) f2_unpack(P[k], v[2 * k], v[2 * k + 1]);
-}
-
-// RoPE inverse frequencies of this lane's 16 elements (c mod 64 = 16 (l8 & 3) + e).
-__device__ __forceinline__ void rope_freqs(const QuantTensors& t, int l8, float (&f)[16]) {
-#pragma unroll
-  for (int e = 0; e < 16; ++e) f[e] = t.rope_k != 0.f ? exp2f(-(float)(16 * (l8 & 3) + e) * t.rope_k) : 0.f;
-}
-
-// Scale of the values transform16 returns for tensor ti (1 / sqrt(128) when rotated).
+// Scale of the transformed values of tensor ti (1 / sqrt(128) when rotated).
 __device__ __forceinline__ float out_norm(const QuantTensors& t, int ti) {
   return (ti != 2 && t.signs != nullptr) ? HAD_NORM : 1.0f;
 }
 
 // Work: stages of 256 consecutive rows (64 KB) of Q, then K, then V.  One
 // producer thread per CTA streams a CTA's stages (stage g = blockIdx.x +
-// k * gridDim.x) into a ring of shared-memory slots with bulk copies, with the
-// stage's indices (tensor, first row, scale and head of its rows) in a record
-// beside each slot; sixteen compute warps take 16 rows each per stage, copy
-// them to registers and hand the slot back before transforming them.  With
-// the rows staged through registers instead (one 16-row group in flight per
-// warp), too few bytes were in flight to keep HBM busy: a third of its
-// bandwidth at 59 % issue.
+// k * gridDim.x) into a ring of shared-memory slots, with the stage's indices
+// (tensor, first row, scale and head of its rows) in a record beside each
+// slot; each of eight compute warps takes 32 rows of a stage, one per thread,
+// copies them to registers and hands the slot back before transforming them.
 struct Group {
   int ti;
   long long r0, r1;
@@ -232,33 +113,77 @@ struct StageInfo {
 struct QuantBars {
   uint64_t full[QSTAGES], empty[QSTAGES];
   StageInfo info[QSTAGES];
+  float rope_f[64];   // RoPE inverse frequencies base^(-2c/128), c = 0..63
   int abort;
   int done[QSTAGES];  // the producer found no further stage
 };
-constexpr int QSMEM = QSTAGES * STAGE_BYTES + (int)sizeof(QuantBars) + 128;
+constexpr int RSMEM = QSTAGES * STAGE_BYTES + XPOSE_BYTES + (int)sizeof(QuantBars) + 1024;
+
+struct QuantMaps {
+  CUtensorMap m[3];  // [rows, 128] bf16 of each tensor, 64 x 256 boxes, 128-byte swizzle
+};
+
+// XOR masks that negate halves of bf16 pair words: bit 15 (low half) and bit
+// 31 (high half) from the sign bits of int8 signs.  sw holds the signs of four
+// consecutive elements 4 j .. 4 j + 3; lo: the word of elements 4 j, 4 j + 1,
+// hi: the word of 4 j + 2, 4 j + 3.
+__device__ __forceinline__ uint32_t sign_mask_lo(uint32_t sw) { return __byte_perm(sw, 0u, 0x1404) & 0x80008000u; }
+__device__ __forceinline__ uint32_t sign_mask_hi(uint32_t sw) { return __byte_perm(sw, 0u, 0x3424) & 0x80008000u; }
+
+// Butterflies of distances 2 .. 64 on the pairs P[j] = (y[2 j], y[2 j + 1]):
+// (a, b) -> (a + b, a - b) on pair indices (j, j ^ hb).
+__device__ __forceinline__ void butterflies_2_64(uint64_t (&P)[64]) {
+  const uint64_t m1 = f2_pack(-1.f, -1.f);
+#pragma unroll
+  for (int hb = 1; hb < 64; hb <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      if (j & hb) continue;
+      const uint64_t a2 = P[j], b2 = P[j | hb];
+      P[j] = f2_add(a2, b2);
+      P[j | hb] = f2_fma(b2, m1, a2);
+    }
+  }
+}
 
 // Pass 1 (WRITE false): amax of every (batch, head).  Pass 2 (WRITE true):
-// e4m3 codes scaled by 448 / amax.  ROPE: rotary embedding in front (its 16
-// inverse frequencies per lane are only kept in registers when it is on).
+// e4m3 codes scaled by 448 / amax.  ROPE: rotary embedding in front.
+//
+// A stage of 256 rows reaches shared memory as two tensor copies (columns
+// 0-63 and 64-127) with the 128-byte swizzle: 16-byte chunk c of row r sits in
+// slot c ^ (r % 8) of the row's 128 bytes, so a thread reading its own row
+// chunk by chunk meets eight different bank groups across any eight
+// consecutive rows.  Codes leave through a per-warp transposition in shared
+// memory (row r, chunk c in slot c ^ (r % 8) again), so each store
+// instruction writes four whole rows.  With sixteen warps of eight lanes per
+// row instead (three butterfly stages through warp shuffles), the passes were
+// held back by their instruction count: 0.27 ms where this form takes 0.21.
 template <bool WRITE, bool ROPE>
-__global__ void __launch_bounds__(QTHREADS, 1) quant_pass_kernel(const QuantTensors t) {
+__global__ void __launch_bounds__(RTHREADS, 1) quant_rows_kernel(const QuantTensors t,
+                                                                 const __grid_constant__ QuantMaps maps) {
   extern __shared__ uint8_t qsm_raw[];
-  uint8_t* sm = (uint8_t*)(((uintptr_t)qsm_raw + 127) & ~(uintptr_t)127);
-  QuantBars& S = *reinterpret_cast<QuantBars*>(sm + QSTAGES * STAGE_BYTES);
+  // The 128-byte swizzle repeats every 1024 bytes: slots start on that boundary.
+  uint8_t* sm = (uint8_t*)(((uintptr_t)qsm_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* xpose = sm + QSTAGES * STAGE_BYTES;
+  QuantBars& S = *reinterpret_cast<QuantBars*>(xpose + XPOSE_BYTES);
   const Abort ab{&S.abort, t.status};
   const int warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     S.abort = 0;
     for (int s = 0; s < QSTAGES; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], QWARPS);
+      mbar_init(&S.empty[s], RWARPS);
     }
     fence_mbar_init();
   }
+  if (ROPE && threadIdx.x < 64) S.rope_f[threadIdx.x] = exp2f(-(float)threadIdx.x * t.rope_k);
   __syncthreads();
-  if (warp == QWARPS) {
+  if (warp >= RWARPS) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    regs_dec<R_LOW>();
+    if (warp == RWARPS && lane == 0) {
+      for (int i = 0; i < 3; ++i)
+        if (t.rows[i] > 0) tma_prefetch_desc(&maps.m[i]);
       long long k = 0;
       bool ok = true;
       for (long long g = blockIdx.x;; g += gridDim.x, ++k) {
@@ -281,9 +206,10 @@ __global__ void __launch_bounds__(QTHREADS, 1) quant_pass_kernel(const QuantTens
         in.one_n = gr.r1 - 1 < (in.n0 + 1) * t.N;
         in.hk0 = t.signs != nullptr ? sign_head(t, gr.ti, in.n0) : 0;
         S.done[s] = 0;
-        const uint32_t bytes = (uint32_t)(gr.r1 - gr.r0) * 256u;
-        mbar_arrive_tx(&S.full[s], bytes);
-        bulk_load(sm + s * STAGE_BYTES, t.x[gr.ti] + gr.r0 * 128, bytes, &S.full[s]);
+        // Both boxes count in full: rows past the tensor's end arrive as zeros.
+        mbar_arrive_tx(&S.full[s], STAGE_BYTES);
+        tma_load_2d(sm + s * STAGE_BYTES, &maps.m[gr.ti], &S.full[s], 0, (int)gr.r0);
+        tma_load_2d(sm + s * STAGE_BYTES + STAGE_BYTES / 2, &maps.m[gr.ti], &S.full[s], 64, (int)gr.r0);
       }
       // Copies still in flight (the compute warps stopped early) must land
       // before the CTA exits: the last phase armed in each slot completes
@@ -295,168 +221,9 @@ __global__ void __launch_bounds__(QTHREADS, 1) quant_pass_kernel(const QuantTens
     return;
   }
   // -------------------------------------------------------- compute warps
-  const int l8 = lane & 7, qr = lane >> 3;
-  float inv_freq[16];
-  if (ROPE) rope_freqs(t, l8, inv_freq);
-  for (long long k = 0;; ++k) {
-    const int s = (int)(k % QSTAGES);
-    if (!wait_warp(&S.full[s], (uint32_t)((k / QSTAGES) & 1), ab)) break;
-    if (S.done[s]) break;
-    const StageInfo in = S.info[s];
-    Raw16 raw[SLABS];
-#pragma unroll
-    for (int sl = 0; sl < SLABS; ++sl) {
-      const int lr = WROWS * warp + 4 * sl + qr;
-      if (in.r0 + lr < in.r1) {
-        const uint4* src = reinterpret_cast<const uint4*>(sm + s * STAGE_BYTES + lr * 256 + l8 * 32);
-        raw[sl] = Raw16{src[0], src[1]};
-      } else {
-        raw[sl] = Raw16{make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[s]);
-
-    const int ti = in.ti;
-    const float norm = out_norm(t, ti);
-    const long long rps = t.rps[ti];
-    float mx = 0.f;
-#pragma unroll
-    for (int sl = 0; sl < SLABS; ++sl) {
-      const long long row_raw = in.r0 + WROWS * warp + 4 * sl + qr;
-      const long long row = min(row_raw, in.r1 - 1);
-      const long long n = in.one_n ? in.n0 : row / t.N;
-      const int hk = t.signs == nullptr ? 0 : in.one_n ? in.hk0 : sign_head(t, ti, n);
-      float v[16];
-      transform16<ROPE>(t, ti, hk, (int)(row - n * t.N), l8, raw[sl], inv_freq, v);
-      if (WRITE) {
-        if (row_raw >= in.r1) continue;
-        const float a = __uint_as_float(t.amax[ti][in.one_head ? in.h0 : row / rps]);
-        const float mul = a > 0.f ? (448.0f / a) * norm : 1.0f;
-        uint4 codes;
-        codes.x = pack_e4m3x4(v[0] * mul, v[1] * mul, v[2] * mul, v[3] * mul);
-        codes.y = pack_e4m3x4(v[4] * mul, v[5] * mul, v[6] * mul, v[7] * mul);
-        codes.z = pack_e4m3x4(v[8] * mul, v[9] * mul, v[10] * mul, v[11] * mul);
-        codes.w = pack_e4m3x4(v[12] * mul, v[13] * mul, v[14] * mul, v[15] * mul);
-        reinterpret_cast<uint4*>(t.out[ti] + row * 128)[l8] = codes;
-      } else {
-        float rm = 0.f;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) rm = fmaxf(rm, fabsf(v[e]));
-        if (row_raw >= in.r1) rm = 0.f;
-        if (in.one_head) {
-          mx = fmaxf(mx, rm);
-        } else {  // rows of two heads in this stage (short sequences): one atomic per row
-#pragma unroll
-          for (int o = 1; o < 8; o <<= 1) rm = fmaxf(rm, __shfl_xor_sync(0xffffffffu, rm, o));
-          if (l8 == 0 && row_raw < in.r1) atomicMax(t.amax[ti] + row / rps, __float_as_uint(rm * norm));
-        }
-      }
-    }
-    if (!WRITE && in.one_head) {
-      mx = warp_max(mx);
-      if (lane == 0) atomicMax(t.amax[ti] + in.h0, __float_as_uint(mx * norm));
-    }
-  }
-}
-
-// Whole rows per thread (every prologue without RoPE).  A stage of 256 rows
-// reaches shared memory as two tensor copies (columns 0-63 and 64-127) with
-// the 128-byte swizzle: 16-byte chunk c of row r sits in slot c ^ (r % 8) of
-// the row's 128 bytes, so a thread reading its own row chunk by chunk meets
-// eight different bank groups across any eight consecutive rows.  Each of
-// eight compute warps takes 32 rows of a stage, one per thread, and runs all
-// seven butterfly stages in registers with no shuffle: distance 1 in scalar
-// fp32 on the two halves of a bf16 pair word, distances 2..64 two lanes per
-// instruction.  The butterflies, their order and the sign and scale steps are
-// those of the lane-split form above, so both give the same bits.  Codes
-// leave through a per-warp transposition in shared memory (row r, chunk c in
-// slot c ^ (r % 8) again), so each store instruction writes four whole rows.
-constexpr int RWARPS = 8;                          // compute warps (two warpgroups)
-constexpr int RTHREADS = (RWARPS + 4) * 32;        // plus a producer warpgroup (one thread works)
-// Register split: launched at 168 a thread (ptxas' bound for 384 threads), the
-// producer warpgroup gives registers back so a compute thread can hold its
-// 128 rotated values, the sign words and the code words without spilling.
-constexpr int R_LAUNCH = 168, R_LOW = 56, R_HIGH = 224;
-static_assert(128 * R_LOW + 256 * R_HIGH <= RTHREADS * R_LAUNCH, "register split over the launch's allocation");
-constexpr int XPOSE_BYTES = RWARPS * 32 * 128;     // one 32-row block of codes per compute warp
-constexpr int RSMEM = QSTAGES * STAGE_BYTES + XPOSE_BYTES + (int)sizeof(QuantBars) + 1024;
-static_assert(RWARPS * 32 == STAGE_ROWS, "one row of a stage per compute thread");
-
-struct QuantMaps {
-  CUtensorMap m[3];  // [rows, 128] bf16 of each tensor, 64 x 256 boxes, 128-byte swizzle
-};
-
-// XOR masks that negate halves of bf16 pair words: bit 15 (low half) and bit
-// 31 (high half) from the sign bits of int8 signs.  sw holds the signs of four
-// consecutive elements 4 j .. 4 j + 3; lo: the word of elements 4 j, 4 j + 1,
-// hi: the word of 4 j + 2, 4 j + 3.
-__device__ __forceinline__ uint32_t sign_mask_lo(uint32_t sw) { return __byte_perm(sw, 0u, 0x1404) & 0x80008000u; }
-__device__ __forceinline__ uint32_t sign_mask_hi(uint32_t sw) { return __byte_perm(sw, 0u, 0x3424) & 0x80008000u; }
-
-template <bool WRITE>
-__global__ void __launch_bounds__(RTHREADS, 1) quant_rows_kernel(const QuantTensors t,
-                                                                 const __grid_constant__ QuantMaps maps) {
-  extern __shared__ uint8_t qsm_raw[];
-  // The 128-byte swizzle repeats every 1024 bytes: slots start on that boundary.
-  uint8_t* sm = (uint8_t*)(((uintptr_t)qsm_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* xpose = sm + QSTAGES * STAGE_BYTES;
-  QuantBars& S = *reinterpret_cast<QuantBars*>(xpose + XPOSE_BYTES);
-  const Abort ab{&S.abort, t.status};
-  const int warp = warp_id(), lane = lane_id();
-  if (threadIdx.x == 0) {
-    S.abort = 0;
-    for (int s = 0; s < QSTAGES; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], RWARPS);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (warp >= RWARPS) {
-    // ------------------------------------------------------------ producer
-    regs_dec<R_LOW>();
-    if (warp == RWARPS && lane == 0) {
-      for (int i = 0; i < 3; ++i)
-        if (t.rows[i] > 0) tma_prefetch_desc(&maps.m[i]);
-      long long k = 0;
-      bool ok = true;
-      for (long long g = blockIdx.x;; g += gridDim.x, ++k) {
-        const int s = (int)(k % QSTAGES);
-        if (!(ok = mbar_wait(&S.empty[s], (uint32_t)((k / QSTAGES) & 1) ^ 1u, ab))) break;
-        Group gr;
-        StageInfo& in = S.info[s];
-        if (!stage_of(t, g, gr)) {
-          S.done[s] = 1;
-          mbar_arrive(&S.full[s]);
-          break;
-        }
-        const long long rps = t.rps[gr.ti];
-        in.r0 = gr.r0;
-        in.r1 = gr.r1;
-        in.ti = gr.ti;
-        in.h0 = gr.r0 / rps;
-        in.one_head = gr.r1 - 1 < (in.h0 + 1) * rps;
-        in.n0 = gr.r0 / t.N;
-        in.one_n = gr.r1 - 1 < (in.n0 + 1) * t.N;
-        in.hk0 = t.signs != nullptr ? sign_head(t, gr.ti, in.n0) : 0;
-        S.done[s] = 0;
-        // Both boxes count in full: rows past the tensor's end arrive as zeros.
-        mbar_arrive_tx(&S.full[s], STAGE_BYTES);
-        tma_load_2d(sm + s * STAGE_BYTES, &maps.m[gr.ti], &S.full[s], 0, (int)gr.r0);
-        tma_load_2d(sm + s * STAGE_BYTES + STAGE_BYTES / 2, &maps.m[gr.ti], &S.full[s], 64, (int)gr.r0);
-      }
-      const long long armed = ok ? k + 1 : k;
-      for (int s = 0; s < QSTAGES; ++s)
-        if (armed > s) mbar_wait_drain(&S.full[s], (uint32_t)(((armed - 1 - s) / QSTAGES) & 1));
-    }
-    return;
-  }
-  // -------------------------------------------------------- compute warps
   regs_inc<R_HIGH>();
   const int lr = warp * 32 + lane;  // this thread's row of every stage
   uint8_t* xw = xpose + warp * (32 * 128);
-  const uint64_t m1 = f2_pack(-1.f, -1.f);
   for (long long k = 0;; ++k) {
     const int s = (int)(k % QSTAGES);
     if (!wait_warp(&S.full[s], (uint32_t)((k / QSTAGES) & 1), ab)) break;
@@ -483,10 +250,56 @@ __global__ void __launch_bounds__(RTHREADS, 1) quant_rows_kernel(const QuantTens
     const bool valid = row < in.r1;
     const long long rowc = valid ? row : in.r1 - 1;
     const float norm = out_norm(t, ti);
+    const bool signed_rows = ti != 2 && t.signs != nullptr;
+    const uint4* sg = nullptr;  // the row's 128 sign bytes
+    if (signed_rows) sg = reinterpret_cast<const uint4*>(t.signs + (in.one_n ? in.hk0 : sign_head(t, ti, rowc / t.N)) * 128);
     uint64_t P[64];  // P[j] = (y[2 j], y[2 j + 1])
-    if (ti != 2 && t.signs != nullptr) {
-      const int hk = in.one_n ? in.hk0 : sign_head(t, ti, rowc / t.N);
-      const uint4* sg = reinterpret_cast<const uint4*>(t.signs + hk * 128);
+    if (ROPE && ti != 2) {
+      float v[128];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        v[2 * j] = bf16lo_f32(w[j]);
+        v[2 * j + 1] = bf16hi_f32(w[j]);
+      }
+      const long long n = in.one_n ? in.n0 : rowc / t.N;
+      const float fpos = (float)(int)(rowc - n * t.N);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {  // rotate-half pairs (c, c + 64), frequency index c
+        // Angle reduced to [-pi, pi] by Cody and Waite's two-constant method:
+        // 2 pi = C1 - C2 with C1 = fl(2 pi) and C2 = 1.7484556e-7 its excess;
+        // both steps are fused multiply-adds, so k C1 enters exactly.  Then
+        // the fast sine / cosine, accurate to a few 1e-7 on that interval.
+        const float ang = fpos * S.rope_f[c];
+        const float kf = rintf(ang * 0.15915494309189535f);  // 1 / (2 pi)
+        const float red = fmaf(kf, 1.7484556e-07f, fmaf(-kf, 6.28318548f, ang));
+        float sn, cs;
+        __sincosf(red, &sn, &cs);
+        const float x1 = v[c], x2 = v[c + 64];
+        v[c] = fmaf(x1, cs, -x2 * sn);
+        v[c + 64] = fmaf(x2, cs, x1 * sn);
+      }
+      if (signed_rows) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {  // elements 16 i .. 16 i + 15
+          const uint4 q = __ldg(sg + i);
+          const uint32_t sw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = 16 * i + e;
+            v[c] = __uint_as_float(__float_as_uint(v[c]) ^ ((sw[e >> 2] << (24 - 8 * (e & 3))) & 0x80000000u));
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const float a = v[2 * j], b = v[2 * j + 1];
+          P[j] = f2_pack(a + b, a - b);  // distance 1
+        }
+        butterflies_2_64(P);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) P[j] = f2_pack(v[2 * j], v[2 * j + 1]);
+      }
+    } else if (signed_rows) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {  // elements 16 i .. 16 i + 15
         const uint4 q = __ldg(sg + i);
@@ -502,16 +315,7 @@ __global__ void __launch_bounds__(RTHREADS, 1) quant_rows_kernel(const QuantTens
           }
         }
       }
-#pragma unroll
-      for (int hb = 1; hb < 64; hb <<= 1) {  // distances 2 .. 64: pair index bit hb
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          if (j & hb) continue;
-          const uint64_t a2 = P[j], b2 = P[j | hb];
-          P[j] = f2_add(a2, b2);
-          P[j | hb] = f2_fma(b2, m1, a2);
-        }
-      }
+      butterflies_2_64(P);
     } else {
 #pragma unroll
       for (int j = 0; j < 64; ++j) P[j] = f2_pack(bf16lo_f32(w[j]), bf16hi_f32(w[j]));
@@ -615,34 +419,23 @@ static cudaError_t run_quant(const QuantTensors& t, int B, unsigned* amax_ws, si
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   // One CTA per SM, each walking many stages.
   const long long blocks = min(stages, (long long)sms);
-  if (t.rope_k != 0.f) {  // RoPE: lane-split rows
-    auto p1 = quant_pass_kernel<false, true>;
-    auto p2 = quant_pass_kernel<true, true>;
-    if ((e = cudaFuncSetAttribute(p1, cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(p2, cudaFuncAttributeMaxDynamicSharedMemorySize, QSMEM)) != cudaSuccess) return e;
-    if (blocks == 0) return cudaSuccess;
-    p1<<<(unsigned)blocks, QTHREADS, QSMEM, st>>>(t);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    quant_scale_kernel<<<dim3(1, 3), 256, 0, st>>>(t, B);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    p2<<<(unsigned)blocks, QTHREADS, QSMEM, st>>>(t);
-    return cudaGetLastError();
-  }
   QuantMaps maps{};
   for (int i = 0; i < 3; ++i)
     if (t.rows[i] > 0 && !make_rows_map(&maps.m[i], t.x[i], t.rows[i], STAGE_ROWS)) return cudaErrorInvalidValue;
-  auto p1 = quant_rows_kernel<false>;
-  auto p2 = quant_rows_kernel<true>;
+  const bool rope = t.rope_k != 0.f;
+  auto p1 = rope ? quant_rows_kernel<false, true> : quant_rows_kernel<false, false>;
+  auto p2 = rope ? quant_rows_kernel<true, true> : quant_rows_kernel<true, false>;
   // The register split inside the kernels assumes R_LAUNCH registers a thread
   // at launch: with fewer, the compute warps' increase could never be granted.
-  static int regs[2] = {-1, -1};
+  static int regs[4] = {-1, -1, -1, -1};
   for (int w = 0; w < 2; ++w) {
-    if (regs[w] < 0) {
+    int& r = regs[2 * rope + w];
+    if (r < 0) {
       cudaFuncAttributes fa;
       if ((e = cudaFuncGetAttributes(&fa, w ? p2 : p1)) != cudaSuccess) return e;
-      regs[w] = fa.numRegs;
+      r = fa.numRegs;
     }
-    if (regs[w] != R_LAUNCH) return cudaErrorInvalidConfiguration;
+    if (r != R_LAUNCH) return cudaErrorInvalidConfiguration;
   }
   if ((e = cudaFuncSetAttribute(p1, cudaFuncAttributeMaxDynamicSharedMemorySize, RSMEM)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(p2, cudaFuncAttributeMaxDynamicSharedMemorySize, RSMEM)) != cudaSuccess) return e;
