@@ -517,6 +517,7 @@ static attn_status_t quant_impl(const void* q, const void* k, const void* v, voi
   if ((st = check_tensors({q, k, v, q8, k8, v8})) != ATTN_OK) return st;
   if (scales == nullptr) return ATTN_ERR_INVALID_ARG;
   if (!aligned(scales, 4)) return ATTN_ERR_UNSUPPORTED;
+  if (signs != nullptr && !aligned(signs, 16)) return ATTN_ERR_UNSUPPORTED;  // read in 16-byte words
   const size_t need = attn_workspace_size(ATTN_OP_QUANT_FP8, B, Hq, Hkv, N, d, nullptr);
   if ((st = check_ws(ws, ws_bytes, need)) != ATTN_OK) return st;
   int* status = nullptr;

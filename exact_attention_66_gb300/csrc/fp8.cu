@@ -57,6 +57,15 @@ static_assert(RWARPS * 32 == STAGE_ROWS, "one row of a stage per compute thread"
 constexpr int R_LAUNCH = 168, R_LOW = 56, R_HIGH = 224;
 static_assert(128 * R_LOW + 256 * R_HIGH <= RTHREADS * R_LAUNCH, "register split over the launch's allocation");
 
+// 2-D tile load (coordinates innermost first) completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
@@ -184,6 +193,8 @@ __global__ void __launch_bounds__(RTHREADS, 1) quant_rows_kernel(const QuantTens
     if (warp == RWARPS && lane == 0) {
       for (int i = 0; i < 3; ++i)
         if (t.rows[i] > 0) tma_prefetch_desc(&maps.m[i]);
+      long long total = 0;
+      for (int i = 0; i < 3; ++i) total += (t.rows[i] + STAGE_ROWS - 1) / STAGE_ROWS;
       long long k = 0;
       bool ok = true;
       for (long long g = blockIdx.x;; g += gridDim.x, ++k) {
@@ -191,7 +202,9 @@ __global__ void __launch_bounds__(RTHREADS, 1) quant_rows_kernel(const QuantTens
         if (!(ok = mbar_wait(&S.empty[s], (uint32_t)((k / QSTAGES) & 1) ^ 1u, ab))) break;
         Group gr;
         StageInfo& in = S.info[s];
-        if (!stage_of(t, g, gr)) {  // tell the compute warps, with no copy
+        // Pass 2 walks the stages backwards: it starts on the rows pass 1
+        // read last, which are still in L2.
+        if (g >= total || !stage_of(t, WRITE ? total - 1 - g : g, gr)) {  // tell the compute warps, with no copy
           S.done[s] = 1;
           mbar_arrive(&S.full[s]);
           break;

@@ -315,8 +315,8 @@ attn_status_t attn_bwd_varlen(const void* q, const void* k, const void* v, const
  * sign vector of the row's KV head (query head hq uses signs[hq/(Hq/Hkv)]);
  * V is not rotated.  Each (b, head) tensor is then scaled by 448/amax and
  * rounded to e4m3 (nearest even, saturating).
- * signs  : device int8 [Hkv, d] of +-1, or NULL to skip the rotation (the
- *          plain-FP8 variant).
+ * signs  : device int8 [Hkv, d] of +-1, 16-byte aligned (ATTN_ERR_UNSUPPORTED
+ *          otherwise), or NULL to skip the rotation (the plain-FP8 variant).
  * q8     : e4m3 [B,Hq,N,d];  k8, v8 : e4m3 [B,Hkv,N,d].
  * scales : device fp32, B*Hq + 2*B*Hkv entries: the dequantisation scales
  *          amax/448 of Q [B,Hq], then K [B,Hkv], then V [B,Hkv] (1 where a

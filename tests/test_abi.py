@@ -86,6 +86,8 @@ def test_other_entry_points_validate(L):
     assert so.attn_fwd_fp8(A, A, A, A, A, A, 1, 2, 2, 64, 64, 0.1, None, None, 0, None) == 2
     assert so.attn_hadamard_quant_fp8(A, A, A, A, A, A, A, None, 1, 2, 2, 64, 64, A, 4096, None) == 2
     assert so.attn_hadamard_quant_fp8(A, A, A, A, A, A, None, None, 1, 2, 2, 64, 128, A, 4096, None) == 1
+    # signs are read in 16-byte words
+    assert so.attn_hadamard_quant_fp8(A, A, A, A, A, A, A, A + 8, 1, 2, 2, 64, 128, A, 1 << 20, None) == 2
     assert so.attn_block_map(None, 1, 100, None, None) == 1
 
 
