@@ -224,10 +224,20 @@ __global__ void __launch_bounds__(384, 1)
   const Abort ab{&S.abort, p.status};
   const int warp = warp_id(), lane = lane_id();
 
-  // Work item, heaviest Q blocks first (longest-processing-time order).
+  // Work item.  Causal or masked launches: heaviest Q blocks first
+  // (longest-processing-time order), heads interleaved.  Otherwise every Q
+  // block costs the same, and the Q blocks of a head -- and the query heads of
+  // a KV head -- run one after another, so the CTAs in flight share few heads'
+  // K and V and L2 keeps them (32 heads of 16K keys are 128 MB of e4m3 K/V).
   const int BH = p.B * p.Hq;
-  const int qblk = p.n_qblk - 1 - (int)(blockIdx.x / BH);
-  const int bh = (int)(blockIdx.x % BH);
+  int qblk, bh;
+  if (MASKS || (p.flags & MOD_CAUSAL)) {
+    qblk = p.n_qblk - 1 - (int)(blockIdx.x / BH);
+    bh = (int)(blockIdx.x % BH);
+  } else {
+    bh = (int)(blockIdx.x / p.n_qblk);
+    qblk = (int)(blockIdx.x % p.n_qblk);
+  }
   const int b = bh / p.Hq, hq = bh - b * p.Hq;
   const int hk = hq / (p.Hq / p.Hkv);
   const int I0 = 2 * qblk;
