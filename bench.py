@@ -314,6 +314,23 @@ def l2_note(cfg):
     return f"inputs fit in L2 (Q {q_bytes / 2**10:.0f} KiB): warm-cache timing"
 
 
+def link_gbs(stream, host_src, dev_dst, dev_src, host_dst) -> dict:
+    """Host link bandwidth right after the end-to-end steps: one pinned
+    host -> device copy and one device -> host copy, each timed alone with
+    CUDA events (GB/s).  The machine's host link is shared, and the end-to-end
+    figure follows it."""
+    out = {}
+    for name, dst, src in (("h2d", dev_dst, host_src), ("d2h", host_dst, dev_src)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        out[name] = round(src.numel() * src.element_size() / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+    return out
+
+
 def pipelined_e2e(dev, compute_stream, ins, outs, compute, steps, world):
     """Time ``steps`` end-to-end steps through the public API, pipelined.
 
@@ -464,6 +481,7 @@ def run_ours(args, world, rank, local):
     h2d = sum(host[n].numel() * host[n].element_size() for n in in_names)
     d2h = sum(t.numel() * t.element_size() for t in (o, lse, dq, dk, dv)[:len(out_names)])
     e2e_ms = float("nan")
+    link = None
     if e2e_steps:
         dev_in = {n: (t, torch.empty_like(t)) for n, t in zip(("q", "k", "v", "do"), (q, k, v, do))}
         dev_out = {n: (t, torch.empty_like(t)) for n, t in zip(("o", "lse", "dq", "dk", "dv"), (o, lse, dq, dk, dv))}
@@ -480,6 +498,8 @@ def run_ours(args, world, rank, local):
         e2e_ms = pipelined_e2e(dev, stream, [(host[n], dev_in[n]) for n in in_names],
                                [(dev_out[n], host_out[n]) for n in out_names], compute, e2e_steps, world)
         e2e_ms = allmax(world, e2e_ms)
+        link = link_gbs(stream, host[in_names[0]], dev_in[in_names[0]][0], dev_out[out_names[0]][0],
+                        host_out[out_names[0]][0])
     ea.attn_status(stream)
 
     fwd_f, bwd_f = flops(cfg, docs)
@@ -548,7 +568,8 @@ def run_ours(args, world, rank, local):
         "e2e": None if not e2e_steps else {
             "value": round(job_throughput(world, fwd_f + bwd_f, e2e_ms) / 1e12, 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-            "pipelined": "copies in and out on their own streams, two device buffer sets"},
+            "pipelined": "copies in and out on their own streams, two device buffer sets",
+            "link_gbs": link},
         "gpu_launches": launches * args.steps,
         "clocks": clk,
     }

@@ -45,7 +45,9 @@ def _prologue(B, Hq, Hkv, N, seed, rotate):
 
 
 @pytest.mark.parametrize("rotate", [True, False], ids=["hadamard", "plain"])
-@pytest.mark.parametrize("shape", [(1, 4, 2, 300), (2, 2, 2, 1000)], ids=str)
+# N < 256 and N = 1: one 256-row stage holds rows of many heads (per-row
+# sign heads and amax atomics); N = 300, 1000: stages straddle two heads.
+@pytest.mark.parametrize("shape", [(1, 4, 2, 300), (2, 2, 2, 1000), (1, 6, 3, 100), (2, 6, 3, 1)], ids=str)
 def test_prologue_matches_oracle(rotate, shape):
     B, Hq, Hkv, N = shape
     x, signs, (q8, k8, v8, sc) = _prologue(B, Hq, Hkv, N, 7 + N, rotate)
@@ -73,7 +75,7 @@ ROPE_REL = 1e-3
 
 
 @pytest.mark.parametrize("rotate", [True, False], ids=["hadamard", "plain"])
-@pytest.mark.parametrize("shape", [(1, 4, 2, 300), (2, 2, 1, 2100)], ids=str)
+@pytest.mark.parametrize("shape", [(1, 4, 2, 300), (2, 2, 1, 2100), (1, 6, 3, 100)], ids=str)
 def test_rope_prologue_matches_oracle(rotate, shape):
     """RoPE fused in front of the Hadamard rotation and the quantiser."""
     ea = lib()
