@@ -43,22 +43,28 @@ namespace {
 constexpr int DEC_THREADS = 256;
 
 // Shared-memory layout.  The MMAs read Q and P as 128-row tiles, of which only
-// the R = G T rows of the query heads and tokens matter.  With R <= 8 (SMALL) a Q or P tile is
-// a single 8-row swizzle group per 64-column half (1 KB) and the MMA
-// descriptor's stride between 8-row groups is 0, so its other fifteen groups
-// re-read the same eight rows (the S and O rows they produce are never read);
-// the room saved goes to deeper K and V rings, i.e. more bytes in flight.
-template <int D, bool SMALL>
+// the R = G T rows of the query heads and tokens matter.  A Q or P tile keeps
+// QG 8-row swizzle groups (QG KB) per 64-column chunk:
+//  * QG = 1 (R <= 8): the MMA descriptor's stride between 8-row groups is 0,
+//    so its other fifteen groups re-read the same eight rows;
+//  * QG = 4 (R <= 32): the stride is 1 KB and groups 4..15 read the 12 KB
+//    after the chunk -- the next chunk, P or the K ring, always inside the
+//    CTA's shared memory, since the rings follow Q and P;
+//  * QG = 16: whole 128-row tiles.
+// The S and O rows that rows >= 8 QG produce are never read, and neither are
+// the S / O rows >= R: one softmax thread per row < R.  The room saved goes to
+// deeper K and V rings, i.e. more bytes in flight.
+template <int D, int QG>
 struct DecCfg {
   static constexpr int CH = D / 64;                     // 64-column chunks of a Q / K / V row
   static constexpr int TB = TILE * D * 2;               // one bf16 K or V tile of 128 rows
-  static constexpr int QCH = SMALL ? 1024 : 16384;      // one 64-column chunk of a Q / P tile
+  static constexpr int QCH = QG * 1024;                 // one 64-column chunk of a Q / P tile
   static constexpr int QTB = CH * QCH;                  // one Q tile
   static constexpr int PTB = 2 * QCH;                   // the P tile (128 keys)
-  static constexpr uint32_t QSBO = SMALL ? 0u : 1024u;  // MMA stride between 8-row groups
+  static constexpr uint32_t QSBO = QG == 1 ? 0u : 1024u;  // MMA stride between 8-row groups
   // K ring and V ring slots (shared memory left after Q and P; twice as many
   // of the half-size tiles of d = 64)
-  static constexpr int KS = (SMALL ? 3 : 2) * (D == 64 ? 2 : 1), VS = KS;
+  static constexpr int KS = (QG < 16 ? 3 : 2) * (D == 64 ? 2 : 1), VS = KS;
   static constexpr int Q_OFF = 0;                       // two Q tiles (item parity)
   static constexpr int P_OFF = 2 * QTB;
   static constexpr int K_OFF = P_OFF + PTB;
@@ -67,6 +73,9 @@ struct DecCfg {
   static constexpr int SMEM = smem_one_cta(BAR_OFF + 512 + 1024);
   static_assert(SMEM <= 232448, "decode shared memory exceeds 227 KB");
   static_assert(K_OFF % 1024 == 0, "swizzled tiles need 1 KB alignment");
+  // Reads of groups QG..15 past the last Q / P chunk stay inside the K ring.
+  static_assert(QG == 1 || QG == 16 || P_OFF + PTB - QCH + 16 * 1024 <= V_OFF + VS * TB,
+                "partial Q / P tiles must be followed by 16 KB of shared memory");
 };
 constexpr int DEC_MAX_SLOTS = 6;
 
@@ -232,12 +241,12 @@ __device__ __forceinline__ void dec_issue_pv(uint32_t o_tmem, uint32_t p_smem, u
 }
 
 // MODS: soft-cap / ALiBi compiled in (the window is a column interval and
-// runs in both variants); SMALL: at most 8 query heads per KV head.
-template <int D, bool MODS, bool SMALL>
+// runs in both variants); QG: 8-row groups of the Q / P tiles (8 QG >= R).
+template <int D, bool MODS, int QG>
 __global__ void __launch_bounds__(DEC_THREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const DecodeParams p) {
-  using C = DecCfg<D, SMALL>;
+  using C = DecCfg<D, QG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   DecBars& S = *reinterpret_cast<DecBars*>(smem + C::BAR_OFF);
@@ -689,10 +698,11 @@ static cudaError_t launch_pdl(void (*kern)(Args...), unsigned grid, unsigned thr
 
 template <int D>
 static cudaError_t launch_decode_d(const DecodeLaunch& L, bool mods, cudaStream_t st) {
-  const bool small = L.p.G * L.p.q_len <= 8;
-  auto kern = mods ? (small ? decode_kernel<D, true, true> : decode_kernel<D, true, false>)
-                   : (small ? decode_kernel<D, false, true> : decode_kernel<D, false, false>);
-  const int smem = small ? DecCfg<D, true>::SMEM : DecCfg<D, false>::SMEM;
+  const int R = L.p.G * L.p.q_len;
+  const int qg = R <= 8 ? 1 : R <= 32 ? 4 : 16;
+  auto kern = mods ? (qg == 1 ? decode_kernel<D, true, 1> : qg == 4 ? decode_kernel<D, true, 4> : decode_kernel<D, true, 16>)
+                   : (qg == 1 ? decode_kernel<D, false, 1> : qg == 4 ? decode_kernel<D, false, 4> : decode_kernel<D, false, 16>);
+  const int smem = qg == 1 ? DecCfg<D, 1>::SMEM : qg == 4 ? DecCfg<D, 4>::SMEM : DecCfg<D, 16>::SMEM;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
   if ((e = launch_pdl(kern, (unsigned)L.grid, DEC_THREADS, (size_t)smem, st, L.tq, L.tk, L.tv, L.p)) != cudaSuccess)

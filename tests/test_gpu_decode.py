@@ -26,6 +26,8 @@ CASES = [
     (4, 32, 8, 900, None, {}, 4),                                  # 4 tokens: 16 rows per item
     (3, 16, 8, 600, [600, 2, 130], dict(window=50, alibi=True), 3),  # 6 rows; a token before the cache start
     (2, 32, 2, 300, [300, 257], dict(softcap=20.0), 8),           # 128 rows: all four softmax warps
+    (2, 16, 2, 800, None, {}, 2, 64),                              # d = 64, 16 rows: four-group tiles
+    (3, 32, 4, 1000, [1000, 5, 640], dict(window=300), 4),         # 32 rows: four-group tiles, full
 ]
 
 
