@@ -83,27 +83,52 @@ __device__ __forceinline__ float out_norm(const QuantTensors& t, int ti) {
   return (ti != 2 && t.signs != nullptr) ? HAD_NORM : 1.0f;
 }
 
-// Work: stages of 256 consecutive rows (64 KB) of Q, then K, then V.  One
-// producer thread per CTA streams a CTA's stages (stage g = blockIdx.x +
-// k * gridDim.x) into a ring of shared-memory slots, with the stage's indices
-// (tensor, first row, scale and head of its rows) in a record beside each
-// slot; each of eight compute warps takes 32 rows of a stage, one per thread,
-// copies them to registers and hands the slot back before transforming them.
+// Work: stages of 256 consecutive rows (64 KB) of Q, K and V, interleaved
+// round by round (stage r of Q, of K, of V, then stage r + 1 ...) while the
+// tensors have stages left, so that the rotated rows (bound by their
+// instructions) and the plain V rows (bound by memory) are in flight at the
+// same time.  One producer thread per CTA streams a CTA's stages (stage g =
+// blockIdx.x + k * gridDim.x) into a ring of shared-memory slots, with the
+// stage's indices (tensor, first row, scale and head of its rows) in a record
+// beside each slot; the compute warps copy their rows to registers and hand
+// the slot back before transforming them.
 struct Group {
   int ti;
   long long r0, r1;
 };
 __device__ __forceinline__ bool stage_of(const QuantTensors& t, long long g, Group& gr) {
+  long long n[3];
 #pragma unroll
-  for (int ti = 0; ti < 3; ++ti) {
-    const long long n = (t.rows[ti] + STAGE_ROWS - 1) / STAGE_ROWS;
-    if (g < n) {
-      gr.ti = ti;
-      gr.r0 = g * STAGE_ROWS;
-      gr.r1 = min(gr.r0 + STAGE_ROWS, t.rows[ti]);
-      return true;
+  for (int ti = 0; ti < 3; ++ti) n[ti] = (t.rows[ti] + STAGE_ROWS - 1) / STAGE_ROWS;
+  // Rounds [prev, next) have cnt tensors with stages left; at most three phases.
+  long long prev = 0;
+#pragma unroll 1
+  for (int ph = 0; ph < 3; ++ph) {
+    long long next = 0x7fffffffffffffffll;
+    int cnt = 0;
+#pragma unroll
+    for (int ti = 0; ti < 3; ++ti)
+      if (n[ti] > prev) {
+        ++cnt;
+        next = min(next, n[ti]);
+      }
+    if (cnt == 0) return false;
+    const long long span = (next - prev) * cnt;
+    if (g < span) {
+      const long long round = prev + g / cnt;
+      int k = (int)(g % cnt);
+#pragma unroll
+      for (int ti = 0; ti < 3; ++ti)
+        if (n[ti] > prev && k-- == 0) {
+          gr.ti = ti;
+          gr.r0 = round * STAGE_ROWS;
+          gr.r1 = min(gr.r0 + STAGE_ROWS, t.rows[ti]);
+          return true;
+        }
+      return false;
     }
-    g -= n;
+    g -= span;
+    prev = next;
   }
   return false;
 }
