@@ -348,11 +348,13 @@ def pipelined_e2e(dev, compute_stream, ins, outs, compute, steps, world):
     ev_comp = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def one(i):
+    def one(i, t=None):
         b = i & 1
         with torch.cuda.stream(s_in):
             if i >= 2:
                 s_in.wait_event(ev_comp[b])  # step i - 2 has read buffer set b
+            if t is not None:
+                t[0].record(s_in)
             for host, bufs in ins:
                 bufs[b].copy_(host, non_blocking=True)
             ev_in[b].record(s_in)
@@ -363,9 +365,14 @@ def pipelined_e2e(dev, compute_stream, ins, outs, compute, steps, world):
         ev_comp[b].record(compute_stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[b])
+            if t is not None:
+                t[2].record(s_out)
             for bufs, hosts in outs:
                 hosts[b].copy_(bufs[b], non_blocking=True)
             ev_out[b].record(s_out)
+        if t is not None:
+            t[1].record(s_in)
+            t[3].record(s_out)
 
     for i in range(2):  # warm-up
         one(i)
@@ -373,12 +380,21 @@ def pipelined_e2e(dev, compute_stream, ins, outs, compute, steps, world):
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s_in)
+    ts = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     for i in range(steps):
-        one(i)
+        one(i, ts[i])
     s_out.wait_stream(compute_stream)
     e1.record(s_out)
     torch.cuda.synchronize(dev)
+    pipelined_e2e.copy_ms = (sum(t[0].elapsed_time(t[1]) for t in ts) / steps,
+                             sum(t[2].elapsed_time(t[3]) for t in ts) / steps)
     return e0.elapsed_time(e1) / steps
+
+
+def copy_gbs_in_pipeline(ms_in, ms_out, h2d, d2h) -> dict:
+    """Bandwidth the pipelined copies got inside the timed end-to-end steps
+    (bytes of a step's copies / the mean time its copy group took), rounded."""
+    return {"h2d": round(h2d / (ms_in * 1e-3) / 1e9, 1), "d2h": round(d2h / (ms_out * 1e-3) / 1e9, 1)}
 
 
 def run_ours(args, world, rank, local):
@@ -481,7 +497,7 @@ def run_ours(args, world, rank, local):
     h2d = sum(host[n].numel() * host[n].element_size() for n in in_names)
     d2h = sum(t.numel() * t.element_size() for t in (o, lse, dq, dk, dv)[:len(out_names)])
     e2e_ms = float("nan")
-    link = None
+    link = in_pipe = None
     if e2e_steps:
         dev_in = {n: (t, torch.empty_like(t)) for n, t in zip(("q", "k", "v", "do"), (q, k, v, do))}
         dev_out = {n: (t, torch.empty_like(t)) for n, t in zip(("o", "lse", "dq", "dk", "dv"), (o, lse, dq, dk, dv))}
@@ -498,6 +514,7 @@ def run_ours(args, world, rank, local):
         e2e_ms = pipelined_e2e(dev, stream, [(host[n], dev_in[n]) for n in in_names],
                                [(dev_out[n], host_out[n]) for n in out_names], compute, e2e_steps, world)
         e2e_ms = allmax(world, e2e_ms)
+        in_pipe = copy_gbs_in_pipeline(*pipelined_e2e.copy_ms, h2d, d2h)
         link = link_gbs(stream, host[in_names[0]], dev_in[in_names[0]][0], dev_out[out_names[0]][0],
                         host_out[out_names[0]][0])
     ea.attn_status(stream)
@@ -569,7 +586,7 @@ def run_ours(args, world, rank, local):
             "value": round(job_throughput(world, fwd_f + bwd_f, e2e_ms) / 1e12, 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
             "pipelined": "copies in and out on their own streams, two device buffer sets",
-            "link_gbs": link},
+            "link_gbs": link, "copy_gbs_in_steps": in_pipe},
         "gpu_launches": launches * args.steps,
         "clocks": clk,
     }
