@@ -462,7 +462,11 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     ea.attn_status(stream)
 
-    evs = [mk_events(6) for _ in range(args.steps)]
+    # The timed steps are the public calls a user makes (attn_fwd, attn_bwd),
+    # events only around the loop; the per-kernel times come from a separate
+    # pass through attn_bwd_profiled afterwards (its events between the
+    # kernels cost about 1 % and keep the dQ kernel from starting in the dK/dV
+    # kernel's tail).
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -472,7 +476,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     t_start.record(stream)
     for s in range(args.steps):
-        step(evs[s])
+        step()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
@@ -480,6 +484,11 @@ def run_ours(args, world, rank, local):
     ea.attn_status(stream)
     total_ms = t_start.elapsed_time(t_end)
     total_ms = allmax(world, total_ms)
+    evs = [mk_events(6) for _ in range(max(3, min(args.steps, 20)))]
+    for ev in evs:
+        step(ev)
+    torch.cuda.synchronize(dev)
+    ea.attn_status(stream)
     mean = lambda a: sum(a) / len(a)  # noqa: E731
     k_fwd = [e[0].elapsed_time(e[1]) for e in evs]
     if fwd_only:
@@ -640,7 +649,6 @@ def run_varlen(args, world, rank, local):
         step()
     torch.cuda.synchronize(dev)
     ea.attn_status(stream)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     clocks = ClockSampler(local)
@@ -649,15 +657,20 @@ def run_varlen(args, world, rank, local):
     torch.cuda.synchronize(dev)
     t0.record(stream)
     for s in range(args.steps):
-        step(evs[s])
+        step()
     t1.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     barrier(world)
     ea.attn_status(stream)
     ms = allmax(world, t0.elapsed_time(t1)) / args.steps
-    k_fwd = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
-    k_bwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    # per-call times from a separate pass with events between the calls
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(max(3, min(args.steps, 20)))]
+    for ev in evs:
+        step(ev)
+    torch.cuda.synchronize(dev)
+    k_fwd = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)
+    k_bwd = sum(e[1].elapsed_time(e[2]) for e in evs) / len(evs)
     peaks, src = load_peaks()
     peak, peak_src = bf16_peak(peaks, src, clk)
     fwd_f, bwd_f = flops(cfg, x["doc_ids"])
@@ -898,7 +911,6 @@ def run_fp8(args, world, rank, local):
         step()
     torch.cuda.synchronize(dev)
     ea.attn_status(stream)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     clocks = ClockSampler(local)
@@ -907,15 +919,20 @@ def run_fp8(args, world, rank, local):
     torch.cuda.synchronize(dev)
     t0.record(stream)
     for s in range(args.steps):
-        step(evs[s])
+        step()
     t1.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     barrier(world)
     ea.attn_status(stream)
     ms = allmax(world, t0.elapsed_time(t1)) / args.steps
-    k_pro = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
-    k_fwd = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    # per-call times from a separate pass with events between the calls
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(max(3, min(args.steps, 20)))]
+    for ev in evs:
+        step(ev)
+    torch.cuda.synchronize(dev)
+    k_pro = sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs)
+    k_fwd = sum(e[1].elapsed_time(e[2]) for e in evs) / len(evs)
     # the same prologue with RoPE fused in front of the rotation
     r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for rep in range(2):

@@ -124,6 +124,10 @@ __global__ void __launch_bounds__(384, 1)
                     __nv_bfloat16* __restrict__ dv, const AttnParams p, const float* __restrict__ fp8s) {
   static_assert(!FP8 || (D == 128 && !MODS && !MASKS), "the e4m3 backward has d = 128 and no mods");
   using C = KvCfg<D, FP8>;
+  // The dQ kernel that follows reads nothing this kernel writes: once every
+  // CTA of this grid has started, its CTAs may take the SMs this grid's last
+  // CTAs leave idle.
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   KvBars& S = *reinterpret_cast<KvBars*>(smem + C::BAR_OFF);
@@ -703,6 +707,10 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // Launched as a programmatic dependent of the dK/dV kernel (it may start
+  // before that grid ends): no CTA of this grid completes before the dK/dV
+  // grid has, so work after this kernel in the stream sees dK and dV too.
+  pdl_wait();
 }
 
 // ------------------------------------------------------------------ launch
@@ -739,8 +747,23 @@ static cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t st) {
       cudaSuccess)
     return e;
   if (L.events[2]) cudaEventRecord(L.events[2], st);
-  dqk<<<(unsigned)(p.nT * p.B * p.Hq), 384, DqCfg<D>::SMEM_BYTES, st>>>(
-      L.tq, L.tk, L.tv, L.tdo, L.rowstat, (__nv_bfloat16*)L.dq, p);
+  {
+    // Programmatic dependent launch: dQ's CTAs may start on the SMs the
+    // dK/dV grid's tail leaves idle (each waits for that grid before exiting).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.nT * p.B * p.Hq));
+    cfg.blockDim = dim3(384);
+    cfg.dynamicSmemBytes = DqCfg<D>::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, dqk, L.tq, L.tk, L.tv, L.tdo, L.rowstat, (__nv_bfloat16*)L.dq, p)) !=
+        cudaSuccess)
+      return e;
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (L.events[3]) cudaEventRecord(L.events[3], st);
   return cudaGetLastError();
