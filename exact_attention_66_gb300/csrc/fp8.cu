@@ -19,8 +19,8 @@
 // are applied to the bf16 bits while converting, and 1 / sqrt(128) is folded
 // into the amax and the quantisation multiplier.
 //
-// Optionally RoPE is fused in front of the rotation (the digest's "fused with
-// RoPE at no extra cost"): the row at position n of its head has its element
+// Optionally RoPE is fused in front of the rotation (the digest notes that the
+// rotation can ride along with RoPE for free): the row at position n of its head has its element
 // pairs (c, c + 64) turned by n * base^(-2c/128) before the signs and the
 // Hadamard butterflies, in the same registers, so RoPE costs no extra pass
 // over memory.
